@@ -1,0 +1,324 @@
+"""Pins for the CPU oracle: it is checked against things other than itself.
+
+* hand-worked examples and chunk offsets written out from the pages' rules
+  (tests/golden/, each with its citation);
+* brute force in exact integer arithmetic (numpy int64) on tiny inputs;
+* the tp = 1 special case, which is a textbook GEMM (numpy float64 matmul);
+* the shard-concatenation identity of the reduce-scatter sum;
+* "active shape == buffer allocated at exactly T" and the untouched capacity tail;
+* the five active-shape constraints, each violated on its own.
+
+Every check is also run once against a planted mistake (a shard dropped, an operand
+transposed, offsets taken from the capacity...) to show that it can fail.
+"""
+import itertools
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gemm_overlap_gemms_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+SENTINEL = 0xFFFF
+
+
+def bf16_bits(a) -> np.ndarray:
+    """Exact small values (or float arrays) -> bf16 bit patterns."""
+    t = torch.as_tensor(np.asarray(a, dtype=np.float32)).to(torch.bfloat16)
+    return synth.to_u16(t)
+
+
+def bits_to_f64(a: np.ndarray) -> np.ndarray:
+    return synth.from_u16(a).to(torch.float64).numpy()
+
+
+# ---------------------------------------------------------------- bf16 rounding
+
+def test_round_bf16_special_values():
+    one = 0x3F80
+    assert oracle.round_bf16(1.0) == one
+    assert oracle.round_bf16(1.0 + 2.0 ** -8) == one          # tie -> even (down)
+    assert oracle.round_bf16(1.0 + 3 * 2.0 ** -8) == one + 2  # tie -> even (up)
+    assert oracle.round_bf16(1.0 + 2.0 ** -8 + 2.0 ** -30) == one + 1  # above the tie
+    assert oracle.round_bf16(-2.0) == 0xC000
+    assert oracle.round_bf16(0.0) == 0x0000
+    assert oracle.round_bf16(3.5e38) == 0x7F80                # past max finite -> inf
+    assert oracle.round_bf16(float("nan")) == 0x7FC0
+
+
+def test_round_bf16_matches_library_on_fp32_values():
+    # For values that are exact in fp32, one-step rounding from double must agree
+    # with the library's fp32 -> bf16 conversion (round to nearest even).
+    g = torch.Generator().manual_seed(1)
+    x = torch.randn(4000, generator=g, dtype=torch.float32) * 10.0
+    x = torch.cat([x, torch.tensor([1e-39, -3e-40, 6e-39], dtype=torch.float32)])
+    want = synth.to_u16(x.to(torch.bfloat16))
+    got = np.array([oracle.round_bf16(float(v)) for v in x.tolist()], dtype=np.uint16)
+    np.testing.assert_array_equal(got, want)
+
+
+# ---------------------------------------------------------------- chunk layout
+
+def test_chunk_offsets_golden():
+    cases = json.load(open(os.path.join(GOLDEN, "chunk_offsets.json")))["cases"]
+    for case in cases:
+        T, tp, H = case["T"], case["tp"], case["hidden"]
+        assert oracle.chunk_rows(T, tp) == case["rows_per_chunk"]
+        offs = [oracle.chunk_offset(T, tp, r) for r in range(tp)]
+        assert offs == case["row_offsets"]
+        assert [o * H * 2 for o in offs] == case["byte_offsets"]
+        if case["T"] != case["capacity"]:
+            assert offs != case["capacity_reading"]
+
+
+def check_gather(G, shards, T):
+    """Pin: rows [r*c, (r+1)*c) of G hold shard r; rows >= T hold the sentinel."""
+    tp = len(shards)
+    c = T // tp
+    for r, s in enumerate(shards):
+        if not np.array_equal(G[r * c:(r + 1) * c], s):
+            return False
+    return bool(np.all(G[T:] == SENTINEL))
+
+
+@pytest.mark.parametrize("T,tp,cap", [(6, 3, 12), (8, 2, 8), (4, 4, 16), (12, 4, 20)])
+def test_allgather_prefix_and_tail(T, tp, cap):
+    H = 5
+    g = synth.generator()
+    shards = [synth.to_u16(synth.small_int_bf16((T // tp, H), -9, 9, g)) for _ in range(tp)]
+    G = np.full((cap, H), SENTINEL, dtype=np.uint16)
+    oracle.allgather(shards, G, T)
+    assert check_gather(G, shards, T)
+    # planted mistake: offsets from the capacity instead of T
+    if cap != T:
+        bad = np.full((cap, H), SENTINEL, dtype=np.uint16)
+        cc = cap // tp
+        for r, s in enumerate(shards):
+            bad[r * cc:r * cc + T // tp] = s
+        assert not check_gather(bad, shards, T)
+
+
+# ---------------------------------------------------------------- worked examples
+
+def test_worked_example_ag():
+    ex = json.load(open(os.path.join(GOLDEN, "worked_examples.json")))["ag_gemm"]
+    assert np.array_equal(np.array(ex["Wt_stored_NxH"]), np.array(ex["W_math_HxN"]).T)
+    shards = [bf16_bits(s) for s in ex["shards"]]
+    Wt = bf16_bits(ex["Wt_stored_NxH"])
+    G = np.full((ex["capacity"], ex["H"]), SENTINEL, dtype=np.uint16)
+    G, Y = oracle.ag_gemm(shards, Wt, G=G, T=ex["T"])
+    np.testing.assert_array_equal(bits_to_f64(G[:ex["T"]]), np.array(ex["G_active_rows"]))
+    assert np.all(G[ex["T"]:] == SENTINEL)
+    np.testing.assert_array_equal(Y, np.array(ex["Y"], dtype=np.float64))
+
+
+def test_worked_example_rs():
+    ex = json.load(open(os.path.join(GOLDEN, "worked_examples.json")))["gemm_rs"]
+    for bm, bt in zip(ex["B_math_KxH"], ex["Bt_stored_HxK"]):
+        assert np.array_equal(np.array(bt), np.array(bm).T)
+    A = [bf16_bits(a) for a in ex["A"]]
+    Bt = [bf16_bits(b) for b in ex["Bt_stored_HxK"]]
+    S, Y = oracle.gemm_rs(A, Bt)
+    np.testing.assert_array_equal(S, np.array(ex["S"], dtype=np.float64))
+    for r in range(ex["tp"]):
+        np.testing.assert_array_equal(Y[r], np.array(ex["Y_blocks"][r], dtype=np.float64))
+
+
+# ---------------------------------------------------------------- brute force (exact ints)
+
+def ag_exact_int(shards, Wt):
+    """Independent statement in exact integers: concatenate, then matmul in int64."""
+    X = np.concatenate([bits_to_f64(s) for s in shards]).astype(np.int64)
+    return X @ bits_to_f64(Wt).astype(np.int64).T
+
+
+def rs_exact_int(A, Bt):
+    S = np.zeros((A[0].shape[0], Bt[0].shape[0]), dtype=np.int64)
+    for a, b in zip(A, Bt):
+        S += bits_to_f64(a).astype(np.int64) @ bits_to_f64(b).astype(np.int64).T
+    return S
+
+
+def _int_cases():
+    for tp in (1, 2, 3, 4):
+        for T in range(tp, 17, tp):
+            for H in (1, 3, 8, 16):
+                yield T, H, tp
+
+
+def test_ag_bruteforce_integer():
+    g = synth.generator(seed=7)
+    n = 0
+    for T, H, tp in _int_cases():
+        N = 1 + (T + H) % 5
+        shards = [synth.to_u16(synth.small_int_bf16((T // tp, H), -8, 8, g)) for _ in range(tp)]
+        Wt = synth.to_u16(synth.small_int_bf16((N, H), -8, 8, g))
+        G = np.full((T + 3, H), SENTINEL, dtype=np.uint16)
+        G, Y = oracle.ag_gemm(shards, Wt, G=G, T=T)
+        np.testing.assert_array_equal(Y, ag_exact_int(shards, Wt).astype(np.float64))
+        assert check_gather(G, shards, T)
+        n += 1
+    assert n > 100
+
+
+def test_rs_bruteforce_integer():
+    g = synth.generator(seed=8)
+    for T, H, tp in _int_cases():
+        K = 1 + (3 * T + H) % 7
+        A = [synth.to_u16(synth.small_int_bf16((T, K), -8, 8, g)) for _ in range(tp)]
+        Bt = [synth.to_u16(synth.small_int_bf16((H, K), -8, 8, g)) for _ in range(tp)]
+        S, Y = oracle.gemm_rs(A, Bt)
+        want = rs_exact_int(A, Bt).astype(np.float64)
+        np.testing.assert_array_equal(S, want)
+        c = T // tp
+        for r in range(tp):
+            np.testing.assert_array_equal(Y[r], want[r * c:(r + 1) * c])
+
+
+def test_bruteforce_detects_planted_mistakes():
+    g = synth.generator(seed=9)
+    T, H, tp, N, K = 8, 6, 2, 5, 4
+    shards = [synth.to_u16(synth.small_int_bf16((T // tp, H), -8, 8, g)) for _ in range(tp)]
+    Wt = synth.to_u16(synth.small_int_bf16((N, H), -8, 8, g))
+    want = ag_exact_int(shards, Wt)
+    # shards in the wrong order
+    _, Y = oracle.ag_gemm(shards[::-1], Wt)
+    assert not np.array_equal(Y, want)
+    # a square weight passed transposed
+    Wsq = synth.to_u16(synth.small_int_bf16((H, H), -8, 8, g))
+    _, Y = oracle.ag_gemm(shards, np.ascontiguousarray(Wsq.T))
+    assert not np.array_equal(Y, ag_exact_int(shards, Wsq))
+    # a dropped shard term in the reduce-scatter sum
+    A = [synth.to_u16(synth.small_int_bf16((T, K), 1, 8, g)) for _ in range(tp)]
+    Bt = [synth.to_u16(synth.small_int_bf16((H, K), 1, 8, g)) for _ in range(tp)]
+    S1, _ = oracle.gemm_rs(A[:1], Bt[:1])
+    assert not np.array_equal(S1, rs_exact_int(A, Bt))
+    # a flipped sign
+    neg = synth.to_u16(-synth.from_u16(A[1]))
+    S2, _ = oracle.gemm_rs([A[0], neg], Bt)
+    assert not np.array_equal(S2, rs_exact_int(A, Bt))
+
+
+# ---------------------------------------------------------------- closed forms
+
+def test_rs_all_ones_closed_form():
+    tp, T, K, H = 4, 8, 7, 3
+    A = [bf16_bits(np.ones((T, K))) for _ in range(tp)]
+    Bt = [bf16_bits(np.ones((H, K))) for _ in range(tp)]
+    S, Y = oracle.gemm_rs(A, Bt)
+    assert np.all(S == tp * K)
+
+
+def test_rs_row_ownership_encoded():
+    # A_j[t][0] = t, everything else 0; Bt_j[n][0] = 1 for j == 0 only.
+    # Then S[t][n] = t, so block r row i must hold r*c + i.
+    tp, T, K, H = 4, 12, 2, 3
+    A = [bf16_bits(np.stack([np.arange(T), np.zeros(T)], 1)) for _ in range(tp)]
+    Bt = [bf16_bits(np.stack([np.full(H, 1.0 if j == 0 else 0.0), np.zeros(H)], 1))
+          for j in range(tp)]
+    S, Y = oracle.gemm_rs(A, Bt)
+    c = T // tp
+    for r in range(tp):
+        assert np.all(Y[r] == (r * c + np.arange(c))[:, None])
+
+
+def test_ag_one_hot_selects_weight_columns():
+    # X row t is the unit vector e_{t mod H}; then Y[t] = W[t mod H, :] = Wt[:, t mod H].
+    tp, T, H, N = 2, 8, 4, 3
+    X = np.zeros((T, H))
+    X[np.arange(T), np.arange(T) % H] = 1.0
+    shards = [bf16_bits(X[r * (T // tp):(r + 1) * (T // tp)]) for r in range(tp)]
+    Wt = bf16_bits(np.arange(N * H).reshape(N, H) - 5.0)
+    _, Y = oracle.ag_gemm(shards, Wt)
+    Wf = bits_to_f64(Wt)
+    for t in range(T):
+        np.testing.assert_array_equal(Y[t], Wf[:, t % H])
+
+
+# ---------------------------------------------------------------- library special cases
+
+def test_tp1_is_a_textbook_gemm():
+    g = synth.generator(seed=3)
+    for T, H, N in [(37, 64, 29), (128, 256, 96)]:
+        shards, W = synth.ag_inputs(T, H, N, 1, g)
+        s = synth.to_u16(shards[0])
+        Wt = synth.to_u16(W)
+        _, Y = oracle.ag_gemm([s], Wt)
+        ref = bits_to_f64(s) @ bits_to_f64(Wt).T
+        # both are double sums of exact products; only the summation order differs
+        bound = H * 2.0 ** -52 * (np.abs(bits_to_f64(s)) @ np.abs(bits_to_f64(Wt)).T)
+        assert np.all(np.abs(Y - ref) <= bound)
+        S, Yb = oracle.gemm_rs([s], [Wt])
+        assert np.all(np.abs(S - ref) <= bound)
+        np.testing.assert_array_equal(Yb[0], S)
+
+
+def test_rs_equals_gemm_on_concatenated_shards():
+    g = synth.generator(seed=4)
+    tp, T, K, H = 4, 24, 40, 48
+    A, Bt = synth.rs_inputs(T, K, H, tp, g)
+    A = [synth.to_u16(a) for a in A]
+    Bt = [synth.to_u16(b) for b in Bt]
+    S, Y = oracle.gemm_rs(A, Bt)
+    Acat = np.concatenate(A, axis=1)           # [T, tp*K]
+    Btcat = np.concatenate(Bt, axis=1)         # [H, tp*K]
+    S1, _ = oracle.gemm_rs([Acat], [Btcat])
+    ref = bits_to_f64(Acat) @ bits_to_f64(Btcat).T
+    bound = tp * K * 2.0 ** -52 * (np.abs(bits_to_f64(Acat)) @ np.abs(bits_to_f64(Btcat)).T)
+    assert np.all(np.abs(S - S1) <= 2 * bound)
+    assert np.all(np.abs(S - ref) <= 2 * bound)
+    np.testing.assert_array_equal(np.concatenate(Y), S)
+
+
+# ---------------------------------------------------------------- active shape
+
+def test_active_shape_equals_exact_allocation():
+    g = synth.generator(seed=5)
+    tp, H, N, cap = 4, 32, 24, 64
+    for T in (4, 20, 36, 64):
+        shards, W = synth.ag_inputs(T, H, N, tp, g)
+        shards = [synth.to_u16(s) for s in shards]
+        Wt = synth.to_u16(W)
+        Gcap = np.full((cap, H), SENTINEL, dtype=np.uint16)
+        Gcap, Ycap = oracle.ag_gemm(shards, Wt, G=Gcap, T=T)
+        Gex = np.full((T, H), SENTINEL, dtype=np.uint16)
+        Gex, Yex = oracle.ag_gemm(shards, Wt, G=Gex, T=T)
+        np.testing.assert_array_equal(Gcap[:T], Gex)
+        np.testing.assert_array_equal(Ycap.view(np.uint64), Yex.view(np.uint64))
+        assert np.all(Gcap[T:] == SENTINEL)
+
+
+def test_rows_helpers_agree_with_full_products():
+    g = synth.generator(seed=6)
+    tp, T, H, N, K = 2, 10, 16, 12, 8
+    shards, W = synth.ag_inputs(T, H, N, tp, g)
+    shards = [synth.to_u16(s) for s in shards]
+    Wt = synth.to_u16(W)
+    G, Y = oracle.ag_gemm(shards, Wt)
+    rows = np.array([0, 4, 5, 9])
+    np.testing.assert_array_equal(oracle.gemm_rows(G, Wt, rows), Y[rows])
+    A, Bt = synth.rs_inputs(T, K, H, tp, g)
+    A = [synth.to_u16(a) for a in A]
+    Bt = [synth.to_u16(b) for b in Bt]
+    S, Yb = oracle.gemm_rs(A, Bt)
+    out, owner, local = oracle.gemm_rs_rows(A, Bt, rows)
+    np.testing.assert_array_equal(out, S[rows])
+    np.testing.assert_array_equal(owner, rows // (T // tp))
+    np.testing.assert_array_equal(local, rows % (T // tp))
+
+
+@pytest.mark.parametrize("shape,expect", [
+    ([8, 16], 0),
+    ([8], 1), ([8, 16, 1], 1),          # not two-dimensional
+    ([0, 16], 2), ([8, 0], 2),          # zero
+    ([40, 16], 3),                      # beyond capacity
+    ([8, 32], 4),                       # hidden changed
+    ([6, 16], 5),                       # not divisible by tp
+    ([32, 16], 0), ([4, 16], 0),
+])
+def test_active_shape_constraints(shape, expect):
+    assert oracle.check_active_shape(shape, cap_tokens=32, cap_hidden=16, tp=4) == expect
