@@ -1,0 +1,497 @@
+#!/usr/bin/env python
+"""Benchmark of the active-shape AG-GEMM / GEMM-RS path on one GB300 per rank.
+
+One step = one pass of the whole hot path over the 16 packed-sequence microbatches
+of the SwiGLU MLP workload (tp=4 virtual ranks, hidden=4096, ffn=14336, capacity
+8192 tokens, T ~ U{1024..8192 step 4}): per microbatch, set the active shape, then
+  fc1  AG-GEMM  Y1 = concat_r X_r @ W1^T       (X_r [T/4, 4096], W1 [7168, 4096])
+  fc2  GEMM-RS  Y_r = rows_r sum_j A_j @ B_j^T (A_j [T, 3584],   B_j [4096, 3584])
+with every activation distinct per microbatch (2.7 GB per step, far larger than L2)
+and the weights shared. FLOPs are algorithmic: 2*T*H*N for AG, 2*T*K*H*tp for RS.
+
+  python bench.py [--steps K] [--warmup W] [--gpus N] [--impl ours|reference] [--sweep]
+
+Prints one JSON line (rank 0). ``--impl reference`` times the CPU oracle instead, on a
+bounded row sample of the same workload. ``--sweep`` additionally prints one JSON line
+per (op, T) point of the active-T sweep.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import shutil
+import signal
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gemm_overlap_gemms_gb300 import synth  # noqa: E402
+
+METRIC = "AG-GEMM / GEMM-RS TFLOP/s and % of GB300 bf16 peak vs active token count T"
+WORKLOAD = "swiglu"
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            return d, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK), "fallback"
+
+
+def _peak_value(d, *keys):
+    for k in keys:
+        v = d.get(k)
+        if isinstance(v, (int, float)):
+            return float(v)
+        if isinstance(v, dict):
+            for kk in ("value", "median", "tflops", "gbs"):
+                if isinstance(v.get(kk), (int, float)):
+                    return float(v[kk])
+    return None
+
+
+def step_flops(Ts, w):
+    H, N, K, tp = w.hidden, w.ag_n[0], w.rs_k[0], w.tp
+    ag = sum(2.0 * T * H * N for T in Ts)
+    rs = sum(2.0 * T * K * H * tp for T in Ts)
+    return ag, rs
+
+
+# ---------------------------------------------------------------- distributed plumbing
+
+def dist_init(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        smi = shutil.which("nvidia-smi")
+        if not smi:
+            return
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.proc = subprocess.Popen([smi, "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                                      "--format=csv,noheader,nounits", "-lms", "200"],
+                                     stdout=self.out, stderr=subprocess.DEVNULL)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.send_signal(signal.SIGTERM)
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.flush()
+        self.out.seek(0)
+        lines = [l.strip() for l in self.out.read().splitlines() if l.strip()]
+        self.out.close()
+        os.unlink(self.out.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- our arm
+
+class SwigluWorkload:
+    """Device-resident inputs of the 16 microbatches plus the shared weights."""
+
+    def __init__(self, device, seed=synth.SEED):
+        from gemm_overlap_gemms_gb300 import ub
+        self.w = w = synth.WORKLOADS[WORKLOAD]
+        self.Ts = synth.token_counts(WORKLOAD, seed)
+        g = synth.generator(device, seed)
+        H, N, K, tp = w.hidden, w.ag_n[0], w.rs_k[0], w.tp
+        self.W1 = synth.normal_bf16((N, H), 1.0 / math.sqrt(H), g, device)
+        self.B = [synth.normal_bf16((H, K), 1.0 / math.sqrt(K), g, device) for _ in range(tp)]
+        self.X, self.A = [], []
+        for T in self.Ts:
+            self.X.append(synth.normal_bf16((T, H), 1.0, g, device))
+            self.A.append([synth.normal_bf16((T, K), 1.0, g, device) for _ in range(tp)])
+        cap = w.max_tokens
+        self.Y1 = torch.empty((cap, N), dtype=torch.bfloat16, device=device)
+        self.Yrs = torch.empty((cap, H), dtype=torch.bfloat16, device=device)
+        self.buf = ub.UserBuffer([cap, H], tp)
+
+    def shards(self, i):
+        T, tp = self.Ts[i], self.w.tp
+        c = T // tp
+        return [self.X[i][r * c:(r + 1) * c] for r in range(tp)]
+
+    def out_shards(self, i):
+        T, tp = self.Ts[i], self.w.tp
+        c = T // tp
+        return [self.Yrs[r * c:(r + 1) * c] for r in range(tp)]
+
+    def run_mb(self, i, stream):
+        T = self.Ts[i]
+        self.buf.set_active_shape([T, self.w.hidden])
+        self.buf.ag_gemm(self.shards(i), self.W1, self.Y1, stream=stream)
+        self.buf.gemm_rs(self.A[i], self.B, self.out_shards(i), stream=stream)
+
+    def step(self, stream):
+        for i in range(len(self.Ts)):
+            self.run_mb(i, stream)
+
+
+def time_steps(fn, steps, warmup, stream, world):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    return e0.elapsed_time(e1)  # ms
+
+
+def e2e_measure(wl, steps, warmup, stream, world):
+    """Same step, with each microbatch's activations copied in from pinned host memory
+    and its outputs copied back, inside the timed region."""
+    hX = [x.cpu().pin_memory() for x in wl.X]
+    hA = [[a.cpu().pin_memory() for a in As] for As in wl.A]
+    N, H = wl.w.ag_n[0], wl.w.hidden
+    hY1 = [torch.empty((T, N), dtype=torch.bfloat16).pin_memory() for T in wl.Ts]
+    hY2 = [torch.empty((T, H), dtype=torch.bfloat16).pin_memory() for T in wl.Ts]
+    h2d = sum(x.numel() * 2 for x in hX) + sum(a.numel() * 2 for As in hA for a in As)
+    d2h = sum(y.numel() * 2 for y in hY1) + sum(y.numel() * 2 for y in hY2)
+
+    def step():
+        with torch.cuda.stream(stream):
+            for i, T in enumerate(wl.Ts):
+                wl.X[i].copy_(hX[i], non_blocking=True)
+                for j in range(wl.w.tp):
+                    wl.A[i][j].copy_(hA[i][j], non_blocking=True)
+                wl.run_mb(i, stream)
+                hY1[i].copy_(wl.Y1[:T], non_blocking=True)
+                hY2[i].copy_(wl.Yrs[:T], non_blocking=True)
+
+    ms = time_steps(step, steps, warmup, stream, world)
+    return ms, h2d, d2h
+
+
+def cpu_baseline(wl, seconds):
+    """The oracle as it stands, on a row sample of one microbatch of the workload."""
+    import oracle
+    i = len(wl.Ts) // 2
+    T, w = wl.Ts[i], wl.w
+    H, N, K, tp = w.hidden, w.ag_n[0], w.rs_k[0], w.tp
+    X = synth.to_u16(wl.X[i])
+    W1 = synth.to_u16(wl.W1)
+    B = [synth.to_u16(b) for b in wl.B]
+    A = [synth.to_u16(a) for a in wl.A[i]]
+    rng = np.random.default_rng(0)
+    G = np.full((T, H), 0xFFFF, dtype=np.uint16)
+    c = T // tp
+    oracle.allgather([X[r * c:(r + 1) * c] for r in range(tp)], G, T)
+
+    def run(nrows):
+        rows = np.sort(rng.choice(T, size=nrows, replace=False))
+        t0 = time.perf_counter()
+        oracle.gemm_rows(G, W1, rows)
+        oracle.gemm_rs_rows([a[rows] for a in A], B, rows, T)
+        return time.perf_counter() - t0, nrows * (2.0 * H * N + 2.0 * K * H * tp)
+
+    dt, _ = run(4)
+    per_row = max(dt / 4, 1e-4)
+    n = int(min(T, max(4, seconds / per_row)))
+    dt, flops = run(n)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.threads(),
+            "kind": "oracle",
+            "sample": "%d of %d rows of microbatch %d (T=%d): fc1 AG-GEMM rows plus fc2 GEMM-RS "
+                      "rows, fp64 loops, %.1f s" % (n, T, i, T, dt)}
+
+
+def run_ours(args):
+    from gemm_overlap_gemms_gb300 import ub
+    rank, world, local = dist_init(args)
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device)
+    wl = SwigluWorkload(device)
+    w = wl.w
+    ag_flops, rs_flops = step_flops(wl.Ts, w)
+    flops = ag_flops + rs_flops
+
+    with torch.cuda.stream(stream):
+        pass
+    clocks = ClockSampler(local)
+    wl.buf.set_option("profile", 1)
+
+    def step():
+        wl.step(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    wl.buf.kernel_time("ag")
+    wl.buf.kernel_time("rs")
+    clocks.start()
+    ms = time_steps(step, args.steps, 0, stream, world)
+    clk = clocks.stop()
+    ag_ms, ag_n = wl.buf.kernel_time("ag")
+    rs_ms, rs_n = wl.buf.kernel_time("rs")
+    wl.buf.set_option("profile", 0)
+    assert wl.buf.query_status() == ub.UB_OK, "device status %d" % wl.buf.query_status()
+    ms = max_over_ranks(ms, world)
+    total_flops = flops * args.steps * world
+    value = total_flops / (ms / 1e3) / 1e12
+
+    pk, src = peaks()
+    tensor_peak = _peak_value(pk, "bf16_tflops_sustained", "bf16_tflops") or FALLBACK["bf16_tflops_sustained"]
+    kernels = {
+        "ag": {"launches": ag_n, "avg_us": 1e3 * ag_ms / max(ag_n, 1),
+               "tflops": (ag_flops * args.steps) / (ag_ms / 1e3) / 1e12 if ag_ms > 0 else None},
+        "rs": {"launches": rs_n, "avg_us": 1e3 * rs_ms / max(rs_n, 1),
+               "tflops": (rs_flops * args.steps) / (rs_ms / 1e3) / 1e12 if rs_ms > 0 else None},
+    }
+    dom = "rs" if rs_ms >= ag_ms else "ag"
+    achieved = kernels[dom]["tflops"]
+    roofline = {"bound": "tensor", "kernel": "ub_gemm_kernel<%s>" % ("MODE_RS" if dom == "rs" else "MODE_AG"),
+                "achieved": achieved, "peak": tensor_peak, "unit": "TFLOP/s",
+                "frac": achieved / tensor_peak if achieved else None, "traffic": None,
+                "peak_source": "%s bf16 sustained" % src}
+
+    e2e = None
+    if not args.no_e2e:
+        e_ms, h2d, d2h = e2e_measure(wl, max(2, min(args.steps, 5)), 1, stream, world)
+        e_steps = max(2, min(args.steps, 5))
+        e_ms = max_over_ranks(e_ms, world)
+        e2e = {"value": flops * e_steps * world / (e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e_ms / e_steps}
+
+    sweep = sweep_points(wl, stream) if args.sweep and rank == 0 else None
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, args.cpu_seconds)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; packed-sequence token counts, N(0,1) activations, "
+                "N(0,1/fan_in) weights)",
+        "config": {"workload": "SwiGLU MLP: tp=4 virtual shards, hidden=4096, ffn=14336, "
+                               "max_tokens=8192, 16 microbatches T~U{1024..8192 step 4}; "
+                               "fc1 AG-GEMM N=7168 + fc2 GEMM-RS K=3584",
+                   "tp": w.tp, "hidden": w.hidden, "max_tokens": w.max_tokens,
+                   "microbatches": len(wl.Ts), "tokens_per_step": int(sum(wl.Ts)),
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2: 2.7 GB of distinct activations per step; "
+                         "weights shared across microbatches"},
+        "gpu_launches": ag_n + rs_n,
+        "kernels": kernels,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "clocks": clk,
+        "flops_per_step": {"ag": ag_flops, "rs": rs_flops},
+    }
+    if rank == 0:
+        if sweep:
+            for p in sweep:
+                print(json.dumps(p))
+        print(json.dumps(line))
+    wl.buf.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def sweep_points(wl, stream):
+    """TFLOP/s of each op at a ladder of active T on the benchmark's handle."""
+    w = wl.w
+    H, N, K, tp = w.hidden, w.ag_n[0], w.rs_k[0], w.tp
+    out = []
+    Xmax = wl.X[int(np.argmax(wl.Ts))]
+    Amax = wl.A[int(np.argmax(wl.Ts))]
+    Tmax = max(wl.Ts)
+    pk, src = peaks()
+    tensor_peak = _peak_value(pk, "bf16_tflops_sustained", "bf16_tflops") or FALLBACK["bf16_tflops_sustained"]
+    for T in (4, 64, 256, 512, 1024, 2048, 4096, 6144, 8192):
+        if T > Tmax:
+            X = synth.normal_bf16((T, H), 1.0, synth.generator(Xmax.device, 5), Xmax.device)
+            A = [synth.normal_bf16((T, K), 1.0, synth.generator(Xmax.device, 6 + j), Xmax.device)
+                 for j in range(tp)]
+        else:
+            X, A = Xmax[:T], [a[:T].contiguous() for a in Amax]
+        c = T // tp
+        shards = [X[r * c:(r + 1) * c] for r in range(tp)]
+        outs = [wl.Yrs[r * c:(r + 1) * c] for r in range(tp)]
+        wl.buf.set_active_shape([T, H])
+        for op in ("ag", "rs"):
+            fn = (lambda: wl.buf.ag_gemm(shards, wl.W1, wl.Y1, stream=stream)) if op == "ag" else \
+                 (lambda: wl.buf.gemm_rs(A, wl.B, outs, stream=stream))
+            reps = 20
+            ms = time_steps(fn, reps, 3, stream, 1) / reps
+            fl = 2.0 * T * H * N if op == "ag" else 2.0 * T * K * H * tp
+            tf = fl / (ms / 1e3) / 1e12
+            out.append({"sweep": op, "T": T, "us": ms * 1e3, "tflops": tf,
+                        "frac_of_peak": tf / tensor_peak, "note": "includes the copy-engine gather" if op == "ag" else ""})
+    return out
+
+
+# ---------------------------------------------------------------- reference arm (the oracle)
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    w = synth.WORKLOADS[WORKLOAD]
+    Ts = synth.token_counts(WORKLOAD)
+    H, N, K, tp = w.hidden, w.ag_n[0], w.rs_k[0], w.tp
+    g = synth.generator("cpu")
+    W1 = synth.to_u16(synth.normal_bf16((N, H), 1.0 / math.sqrt(H), g))
+    B = [synth.to_u16(synth.normal_bf16((H, K), 1.0 / math.sqrt(K), g)) for _ in range(tp)]
+    rng = np.random.default_rng(0)
+    nrows = oracle.threads()          # one sampled row per oracle thread
+
+    def one_mb(i):
+        T = Ts[i]
+        x = synth.to_u16(synth.normal_bf16((nrows, H), 1.0, g))
+        a = [synth.to_u16(synth.normal_bf16((nrows, K), 1.0, g)) for _ in range(tp)]
+        rows = np.sort(rng.choice(T, size=nrows, replace=False))
+        t0 = time.perf_counter()
+        oracle.gemm_rows(x, W1, np.arange(nrows))
+        oracle.gemm_rs_rows(a, B, rows, T)
+        return time.perf_counter() - t0, nrows * (2.0 * H * N + 2.0 * K * H * tp)
+
+    t_mb, _ = one_mb(0)
+    budget = 150.0 / max(1, args.steps + args.warmup)    # whole run within a few minutes
+    per_step = int(max(1, min(len(Ts), budget / max(t_mb, 1e-3))))
+    cursor = [0]
+
+    def one_step():
+        # a bounded sample of one step: `nrows` rows of fc1 and fc2 in `per_step`
+        # microbatches, cycling through all of them across steps
+        dt = fl = 0.0
+        for _ in range(per_step):
+            d, f = one_mb(cursor[0] % len(Ts))
+            cursor[0] += 1
+            dt += d
+            fl += f
+        return dt, fl
+
+    for _ in range(args.warmup):
+        one_step()
+    tot_dt = tot_fl = 0.0
+    for _ in range(args.steps):
+        dt, fl = one_step()
+        tot_dt += dt
+        tot_fl += fl
+    value = tot_fl / tot_dt / 1e12
+    sample = ("per step %d rows (one per thread) of fc1 AG-GEMM and fc2 GEMM-RS in each of %d "
+              "of the %d microbatches, cycling; fp64 loops" % (nrows, per_step, len(Ts)))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * tot_dt / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "SwiGLU MLP: tp=4 virtual shards, hidden=4096, ffn=14336, "
+                               "max_tokens=8192, 16 microbatches T~U{1024..8192 step 4}; "
+                               "fc1 AG-GEMM N=7168 + fc2 GEMM-RS K=3584"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

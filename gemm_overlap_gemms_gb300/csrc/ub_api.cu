@@ -1,0 +1,617 @@
+// Host runtime of libubgemm: the C ABI declared in include/ub.h.
+//
+// A handle is the registered user buffer of "Support dynamic token counts in TP
+// communication/GEMM overlap" (TransformerEngine issue #3564): one allocation at
+// capacity [max_tokens, hidden], an active shape that is only a logical view (nothing
+// allocated, freed or re-registered per microbatch), and chunk offsets computed from
+// the active first dimension. The all-gather is the copy-engine ("use_ce") variant of
+// the "ring_exchange" method of "How to setup TP Overlap configs" (TransformerEngine
+// issue #1344), collapsed onto one GPU: each virtual rank's chunk is a device-to-device
+// cudaMemcpyAsync on a side stream, followed by a stream memory write of the call's
+// epoch into the chunk's readiness flag, which the persistent GEMM polls.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "ub_internal.h"
+
+using ubk::GemmParams;
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(UB_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+#define UB_CUDA(call)                                   \
+    do {                                                \
+        cudaError_t e_ = (call);                        \
+        if (e_ != cudaSuccess) return cuda_fail(e_, #call); \
+    } while (0)
+
+// ---------------------------------------------------------------- driver entry points
+
+typedef CUresult (*PFN_encodeTiled)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+typedef CUresult (*PFN_writeValue32)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
+
+struct DriverFns {
+    PFN_encodeTiled encode = nullptr;
+    PFN_writeValue32 write_value32 = nullptr;
+    int status = -1;  // -1 unresolved, 0 ok, else error
+};
+
+DriverFns &driver()
+{
+    static DriverFns fns;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q1, q2;
+        void *f1 = nullptr, *f2 = nullptr;
+        cudaError_t e1 = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f1, 12000, cudaEnableDefault, &q1);
+        cudaError_t e2 = cudaGetDriverEntryPointByVersion("cuStreamWriteValue32", &f2, 12000, cudaEnableDefault, &q2);
+        if (e1 == cudaSuccess && e2 == cudaSuccess && q1 == cudaDriverEntryPointSuccess &&
+            q2 == cudaDriverEntryPointSuccess && f1 && f2) {
+            fns.encode = reinterpret_cast<PFN_encodeTiled>(f1);
+            fns.write_value32 = reinterpret_cast<PFN_writeValue32>(f2);
+            fns.status = 0;
+        } else {
+            fns.status = 1;
+        }
+    });
+    return fns;
+}
+
+// ---------------------------------------------------------------- tensor maps
+
+// 2-D row-major bf16 tensor [outer, inner] with row pitch `pitch_bytes`, moved in boxes
+// of [box_outer, box_inner] with the 128-byte swizzle (box_inner * 2 == 128).
+int encode_2d(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t outer, uint64_t pitch_bytes,
+              uint32_t box_inner, uint32_t box_outer)
+{
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {pitch_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = driver().encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides,
+                                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(UB_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for [%llu x %llu], pitch %llu", (int)r,
+                    (unsigned long long)outer, (unsigned long long)inner, (unsigned long long)pitch_bytes);
+    return UB_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Kernel parameters are cached by everything that determines them (mode, shape,
+// pointers, ring start), so a repeated call encodes no tensor map.
+struct CacheEntry {
+    std::vector<const void *> key;
+    GemmParams params;
+    uint64_t last_use;
+};
+
+constexpr int kCacheEntries = 64;
+constexpr int kMaxProfiled = 4096;
+
+struct ProfileRing {
+    std::vector<cudaEvent_t> start, stop;
+    int count = 0;
+};
+
+}  // namespace
+
+struct ub_handle {
+    int device = 0;
+    int sm_count = 0;
+    int64_t max_tokens = 0, hidden = 0;
+    int tp = 1;
+    int64_t T = 0;  // active tokens
+    void *ub = nullptr;      // [max_tokens, hidden] bf16
+    uint32_t *ctrl = nullptr;  // flags[UB_MAX_TP] | abort | status
+    cudaStream_t side = nullptr;
+    cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+    uint32_t epoch = 0;
+    // options
+    int64_t sm_margin = 0;
+    int64_t timeout_ns = 1000000000;
+    int64_t self_rank = 0;
+    int64_t drop_flag = -1;
+    int64_t profile = 0;
+    ub_counters_t counters{};
+    std::vector<CacheEntry> cache;
+    uint64_t use_clock = 0;
+    ProfileRing prof[2];
+};
+
+namespace {
+
+uint32_t *flags_of(ub_handle *h) { return h->ctrl; }
+uint32_t *abort_of(ub_handle *h) { return h->ctrl + UB_MAX_TP; }
+int32_t *status_of(ub_handle *h) { return reinterpret_cast<int32_t *>(h->ctrl + UB_MAX_TP + 1); }
+
+// Makes the handle's device current for the duration of a call.
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = true;
+    explicit DeviceGuard(int dev)
+    {
+        if (cudaGetDevice(&prev) != cudaSuccess) {
+            ok = false;
+            return;
+        }
+        if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+    }
+    ~DeviceGuard()
+    {
+        if (ok && prev >= 0) cudaSetDevice(prev);
+    }
+};
+
+int grid_for(ub_handle *h, int num_tiles)
+{
+    int g = h->sm_count - static_cast<int>(h->sm_margin);
+    if (g < 1) g = 1;
+    return g < num_tiles ? g : num_tiles;
+}
+
+GemmParams *cache_lookup(ub_handle *h, const std::vector<const void *> &key)
+{
+    for (auto &e : h->cache)
+        if (e.key == key) {
+            e.last_use = ++h->use_clock;
+            return &e.params;
+        }
+    return nullptr;
+}
+
+GemmParams *cache_insert(ub_handle *h, std::vector<const void *> key, const GemmParams &p)
+{
+    if (static_cast<int>(h->cache.size()) < kCacheEntries) {
+        h->cache.push_back(CacheEntry{std::move(key), p, ++h->use_clock});
+        return &h->cache.back().params;
+    }
+    size_t victim = 0;
+    for (size_t i = 1; i < h->cache.size(); ++i)
+        if (h->cache[i].last_use < h->cache[victim].last_use) victim = i;
+    h->cache[victim] = CacheEntry{std::move(key), p, ++h->use_clock};
+    return &h->cache[victim].params;
+}
+
+int launch(ub_handle *h, const GemmParams &p, int mode, cudaStream_t s)
+{
+    const int grid = grid_for(h, p.num_tiles);
+    ProfileRing &ring = h->prof[mode];
+    const bool timed = h->profile != 0 && ring.count < kMaxProfiled;
+    if (timed) {
+        if (static_cast<int>(ring.start.size()) <= ring.count) {
+            cudaEvent_t a, b;
+            UB_CUDA(cudaEventCreate(&a));
+            UB_CUDA(cudaEventCreate(&b));
+            ring.start.push_back(a);
+            ring.stop.push_back(b);
+        }
+        UB_CUDA(cudaEventRecord(ring.start[ring.count], s));
+    }
+    cudaError_t e = ubk::launch_gemm(p, mode, grid, s);
+    if (e != cudaSuccess) return cuda_fail(e, "GEMM kernel launch");
+    if (timed) {
+        UB_CUDA(cudaEventRecord(ring.stop[ring.count], s));
+        ++ring.count;
+    }
+    return UB_OK;
+}
+
+int check_handle(ub_handle *h)
+{
+    if (!h) return fail(UB_ERR_ARG, "null handle");
+    return UB_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *ub_last_error(void) { return g_err; }
+
+int ub_validate_active_shape(int ndim, const int64_t *dims, int64_t max_tokens, int64_t hidden, int tp)
+{
+    if (ndim != 2) return fail(UB_ERR_RANK, "active shape must be two-dimensional, got %d dims", ndim);
+    if (!dims) return fail(UB_ERR_ARG, "null shape");
+    if (dims[0] <= 0 || dims[1] <= 0)
+        return fail(UB_ERR_ZERO, "active shape [%lld, %lld] has a zero extent", (long long)dims[0],
+                    (long long)dims[1]);
+    if (dims[0] > max_tokens)
+        return fail(UB_ERR_CAPACITY, "active tokens %lld exceed the registered capacity %lld", (long long)dims[0],
+                    (long long)max_tokens);
+    if (dims[1] != hidden)
+        return fail(UB_ERR_HIDDEN, "hidden %lld differs from the registered hidden %lld", (long long)dims[1],
+                    (long long)hidden);
+    if (tp < 1 || dims[0] % tp != 0)
+        return fail(UB_ERR_DIVISIBLE, "active tokens %lld not divisible by tp %d", (long long)dims[0], tp);
+    return UB_OK;
+}
+
+int ub_create(int64_t max_tokens, int64_t hidden, int tp, ub_dtype_t dtype, ub_handle_t *out)
+{
+    if (!out) return fail(UB_ERR_ARG, "null output handle pointer");
+    *out = nullptr;
+    if (tp < 1 || tp > UB_MAX_TP) return fail(UB_ERR_ARG, "tp %d outside [1, %d]", tp, UB_MAX_TP);
+    if (max_tokens <= 0 || hidden <= 0)
+        return fail(UB_ERR_ZERO, "capacity [%lld, %lld] has a zero extent", (long long)max_tokens, (long long)hidden);
+    if (dtype != UB_BF16) return fail(UB_ERR_DTYPE, "only UB_BF16 user buffers are supported");
+    if (hidden % 8 != 0) return fail(UB_ERR_ALIGN, "hidden %lld is not a multiple of 8", (long long)hidden);
+    if (max_tokens % tp != 0)
+        return fail(UB_ERR_DIVISIBLE, "max_tokens %lld not divisible by tp %d", (long long)max_tokens, tp);
+    if (max_tokens > (int64_t(1) << 31) - 1 || hidden > (int64_t(1) << 24))
+        return fail(UB_ERR_ARG, "capacity [%lld, %lld] too large", (long long)max_tokens, (long long)hidden);
+
+    int dev = 0;
+    UB_CUDA(cudaGetDevice(&dev));
+    if (driver().status != 0)
+        return fail(UB_ERR_CUDA, "driver entry points cuTensorMapEncodeTiled / cuStreamWriteValue32 unavailable");
+    ub_handle *h = new (std::nothrow) ub_handle();
+    if (!h) return fail(UB_ERR_ARG, "out of host memory");
+    h->device = dev;
+    h->max_tokens = max_tokens;
+    h->hidden = hidden;
+    h->tp = tp;
+    h->T = max_tokens;
+    auto cleanup = [&](int code) {
+        ub_destroy(h);
+        return code;
+    };
+    cudaError_t e = cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cleanup(cuda_fail(e, "cudaDeviceGetAttribute"));
+    e = cudaMalloc(&h->ub, static_cast<size_t>(max_tokens) * hidden * 2);
+    if (e != cudaSuccess) return cleanup(cuda_fail(e, "cudaMalloc(user buffer)"));
+    ++h->counters.device_allocations;
+    e = cudaMalloc(reinterpret_cast<void **>(&h->ctrl), 256);
+    if (e != cudaSuccess) return cleanup(cuda_fail(e, "cudaMalloc(control block)"));
+    ++h->counters.device_allocations;
+    e = cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return cleanup(cuda_fail(e, "cudaStreamCreateWithFlags"));
+    e = cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming);
+    if (e != cudaSuccess) return cleanup(cuda_fail(e, "cudaEventCreateWithFlags"));
+    e = cudaMemsetAsync(h->ctrl, 0, 256, h->side);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(h->side);
+    if (e != cudaSuccess) return cleanup(cuda_fail(e, "clearing the control block"));
+    *out = h;
+    return UB_OK;
+}
+
+int ub_destroy(ub_handle_t h)
+{
+    if (!h) return fail(UB_ERR_ARG, "null handle");
+    DeviceGuard g(h->device);
+    if (h->side) cudaStreamSynchronize(h->side);
+    for (auto &ring : h->prof) {
+        for (auto ev : ring.start) cudaEventDestroy(ev);
+        for (auto ev : ring.stop) cudaEventDestroy(ev);
+    }
+    if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+    if (h->ev_join) cudaEventDestroy(h->ev_join);
+    if (h->side) cudaStreamDestroy(h->side);
+    if (h->ctrl) cudaFree(h->ctrl);
+    if (h->ub) cudaFree(h->ub);
+    delete h;
+    return UB_OK;
+}
+
+int ub_set_active_shape_nd(ub_handle_t h, int ndim, const int64_t *dims)
+{
+    if (int rc = check_handle(h)) return rc;
+    int rc = ub_validate_active_shape(ndim, dims, h->max_tokens, h->hidden, h->tp);
+    if (rc != UB_OK) return rc;
+    h->T = dims[0];
+    return UB_OK;
+}
+
+int ub_set_active_shape(ub_handle_t h, int64_t T, int64_t hidden)
+{
+    const int64_t dims[2] = {T, hidden};
+    return ub_set_active_shape_nd(h, 2, dims);
+}
+
+int ub_get_active_shape(ub_handle_t h, int64_t *T, int64_t *hidden)
+{
+    if (int rc = check_handle(h)) return rc;
+    if (T) *T = h->T;
+    if (hidden) *hidden = h->hidden;
+    return UB_OK;
+}
+
+int ub_get_capacity(ub_handle_t h, int64_t *max_tokens, int64_t *hidden)
+{
+    if (int rc = check_handle(h)) return rc;
+    if (max_tokens) *max_tokens = h->max_tokens;
+    if (hidden) *hidden = h->hidden;
+    return UB_OK;
+}
+
+int ub_get_tp(ub_handle_t h, int *tp)
+{
+    if (int rc = check_handle(h)) return rc;
+    if (tp) *tp = h->tp;
+    return UB_OK;
+}
+
+int ub_buffer(ub_handle_t h, void **dev_ptr, size_t *bytes)
+{
+    if (int rc = check_handle(h)) return rc;
+    if (dev_ptr) *dev_ptr = h->ub;
+    if (bytes) *bytes = static_cast<size_t>(h->max_tokens) * h->hidden * 2;
+    return UB_OK;
+}
+
+int ub_grid_ctas(ub_handle_t h, int *ctas)
+{
+    if (int rc = check_handle(h)) return rc;
+    if (ctas) *ctas = grid_for(h, 1 << 30);
+    return UB_OK;
+}
+
+int ag_gemm(ub_handle_t h, const void *const *shards, const void *Wt, int64_t N, void *Y, void *stream)
+{
+    if (int rc = check_handle(h)) return rc;
+    if (!shards || !Wt || !Y) return fail(UB_ERR_ARG, "ag_gemm: null pointer argument");
+    if (N <= 0) return fail(UB_ERR_ZERO, "ag_gemm: N = %lld", (long long)N);
+    if (N % 8 != 0) return fail(UB_ERR_ALIGN, "ag_gemm: N = %lld is not a multiple of 8", (long long)N);
+    if (N > (int64_t(1) << 24)) return fail(UB_ERR_ARG, "ag_gemm: N = %lld too large", (long long)N);
+    if (!aligned16(Wt) || !aligned16(Y)) return fail(UB_ERR_ALIGN, "ag_gemm: Wt / Y not 16-byte aligned");
+    const int tp = h->tp;
+    for (int r = 0; r < tp; ++r) {
+        if (!shards[r]) return fail(UB_ERR_ARG, "ag_gemm: shard %d is null", r);
+        if (!aligned16(shards[r])) return fail(UB_ERR_ALIGN, "ag_gemm: shard %d not 16-byte aligned", r);
+    }
+    DeviceGuard g(h->device);
+    if (!g.ok) return fail(UB_ERR_CUDA, "ag_gemm: cannot select the handle's device");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t T = h->T, H = h->hidden, c = T / tp;
+    const int self = static_cast<int>(h->self_rank);
+    char *ub = static_cast<char *>(h->ub);
+
+    std::vector<const void *> key;
+    key.reserve(tp + 6);
+    key.push_back(reinterpret_cast<const void *>(uintptr_t(ubk::MODE_AG)));
+    key.push_back(reinterpret_cast<const void *>(uintptr_t(T)));
+    key.push_back(reinterpret_cast<const void *>(uintptr_t(N)));
+    key.push_back(reinterpret_cast<const void *>(uintptr_t(self)));
+    key.push_back(Wt);
+    key.push_back(Y);
+    for (int r = 0; r < tp; ++r) key.push_back(shards[r]);
+    GemmParams *pp = cache_lookup(h, key);
+    if (!pp) {
+        GemmParams p;
+        memset(&p, 0, sizeof p);
+        for (int r = 0; r < tp; ++r) {
+            // Chunk r is read from the user buffer, except the self chunk, which the
+            // kernel reads in place from its shard while the copy engine stages it.
+            const void *src = r == self ? shards[r] : static_cast<const void *>(ub + r * c * H * 2);
+            if (int rc = encode_2d(&p.tmA[r], src, H, c, H * 2, ubk::BK, ubk::BM)) return rc;
+            if (int rc = encode_2d(&p.tmY[r], static_cast<char *>(Y) + r * c * N * 2, N, c, N * 2,
+                                   ubk::STORE_COLS, 32))
+                return rc;
+        }
+        if (int rc = encode_2d(&p.tmB[0], Wt, H, N, H * 2, ubk::BK, ubk::BN)) return rc;
+        h->counters.tensor_map_encodes += 2 * tp + 1;
+        p.tp = tp;
+        p.c = static_cast<int>(c);
+        p.n_out = static_cast<int>(N);
+        p.k_blocks = static_cast<int>((H + ubk::BK - 1) / ubk::BK);
+        p.k_blocks_per_shard = p.k_blocks;
+        p.m_tiles = static_cast<int>((c + ubk::BM - 1) / ubk::BM);
+        p.n_tiles = static_cast<int>((N + ubk::BN - 1) / ubk::BN);
+        p.num_tiles = tp * p.m_tiles * p.n_tiles;
+        p.self_rank = self;
+        pp = cache_insert(h, std::move(key), p);
+    }
+    GemmParams &p = *pp;
+    p.flags = flags_of(h);
+    p.abort_word = abort_of(h);
+    p.status = status_of(h);
+    p.timeout_ns = static_cast<uint64_t>(h->timeout_ns);
+    const uint32_t epoch = ++h->epoch;
+    p.epoch = epoch;
+    const int64_t drop = h->drop_flag;
+    h->drop_flag = -1;
+
+    // Fork the copy-engine stream off `s`: it starts once the work already queued on
+    // `s` (which may still read the buffer) is done.
+    UB_CUDA(cudaEventRecord(h->ev_fork, s));
+    UB_CUDA(cudaStreamWaitEvent(h->side, h->ev_fork, 0));
+    // Ring order after the self rank; the self chunk (read in place by the GEMM) last.
+    for (int q = 1; q <= tp; ++q) {
+        const int r = (self + q) % tp;
+        UB_CUDA(cudaMemcpyAsync(ub + r * c * H * 2, shards[r], static_cast<size_t>(c * H * 2),
+                                cudaMemcpyDeviceToDevice, h->side));
+        if (r != drop) {
+            CUresult cr = driver().write_value32(reinterpret_cast<CUstream>(h->side),
+                                                 reinterpret_cast<CUdeviceptr>(flags_of(h) + r), epoch,
+                                                 CU_STREAM_WRITE_VALUE_DEFAULT);
+            if (cr != CUDA_SUCCESS) return fail(UB_ERR_CUDA, "cuStreamWriteValue32 failed (%d)", (int)cr);
+        }
+    }
+    int rc = launch(h, p, ubk::MODE_AG, s);
+    // Join the side stream back into `s` even if the launch failed.
+    UB_CUDA(cudaEventRecord(h->ev_join, h->side));
+    UB_CUDA(cudaStreamWaitEvent(s, h->ev_join, 0));
+    if (rc != UB_OK) return rc;
+    ++h->counters.ag_calls;
+    h->counters.last_T = T;
+    return UB_OK;
+}
+
+int gemm_rs(ub_handle_t h, const void *const *A, const void *const *Bt, int64_t K, void *const *Y_shards,
+            void *stream)
+{
+    if (int rc = check_handle(h)) return rc;
+    if (!A || !Bt || !Y_shards) return fail(UB_ERR_ARG, "gemm_rs: null pointer argument");
+    if (K <= 0) return fail(UB_ERR_ZERO, "gemm_rs: K = %lld", (long long)K);
+    if (K % 8 != 0) return fail(UB_ERR_ALIGN, "gemm_rs: K = %lld is not a multiple of 8", (long long)K);
+    if (K > (int64_t(1) << 24)) return fail(UB_ERR_ARG, "gemm_rs: K = %lld too large", (long long)K);
+    const int tp = h->tp;
+    for (int j = 0; j < tp; ++j) {
+        if (!A[j] || !Bt[j] || !Y_shards[j]) return fail(UB_ERR_ARG, "gemm_rs: pointer %d is null", j);
+        if (!aligned16(A[j]) || !aligned16(Bt[j]) || !aligned16(Y_shards[j]))
+            return fail(UB_ERR_ALIGN, "gemm_rs: pointer %d not 16-byte aligned", j);
+    }
+    DeviceGuard g(h->device);
+    if (!g.ok) return fail(UB_ERR_CUDA, "gemm_rs: cannot select the handle's device");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t T = h->T, H = h->hidden, c = T / tp;
+
+    std::vector<const void *> key;
+    key.reserve(3 * tp + 3);
+    key.push_back(reinterpret_cast<const void *>(uintptr_t(ubk::MODE_RS)));
+    key.push_back(reinterpret_cast<const void *>(uintptr_t(T)));
+    key.push_back(reinterpret_cast<const void *>(uintptr_t(K)));
+    for (int j = 0; j < tp; ++j) {
+        key.push_back(A[j]);
+        key.push_back(Bt[j]);
+        key.push_back(Y_shards[j]);
+    }
+    GemmParams *pp = cache_lookup(h, key);
+    if (!pp) {
+        GemmParams p;
+        memset(&p, 0, sizeof p);
+        for (int j = 0; j < tp; ++j) {
+            if (int rc = encode_2d(&p.tmA[j], A[j], K, T, K * 2, ubk::BK, ubk::BM)) return rc;
+            if (int rc = encode_2d(&p.tmB[j], Bt[j], K, H, K * 2, ubk::BK, ubk::BN)) return rc;
+            if (int rc = encode_2d(&p.tmY[j], Y_shards[j], H, c, H * 2, ubk::STORE_COLS, 32)) return rc;
+        }
+        h->counters.tensor_map_encodes += 3 * tp;
+        p.tp = tp;
+        p.c = static_cast<int>(c);
+        p.n_out = static_cast<int>(H);
+        p.k_blocks_per_shard = static_cast<int>((K + ubk::BK - 1) / ubk::BK);
+        p.k_blocks = tp * p.k_blocks_per_shard;
+        p.m_tiles = static_cast<int>((c + ubk::BM - 1) / ubk::BM);
+        p.n_tiles = static_cast<int>((H + ubk::BN - 1) / ubk::BN);
+        p.num_tiles = tp * p.m_tiles * p.n_tiles;
+        p.self_rank = 0;
+        pp = cache_insert(h, std::move(key), p);
+    }
+    GemmParams &p = *pp;
+    p.flags = flags_of(h);
+    p.abort_word = abort_of(h);
+    p.status = status_of(h);
+    p.timeout_ns = static_cast<uint64_t>(h->timeout_ns);
+    p.epoch = ++h->epoch;
+    if (int rc = launch(h, p, ubk::MODE_RS, s)) return rc;
+    ++h->counters.rs_calls;
+    h->counters.last_T = T;
+    return UB_OK;
+}
+
+int ub_set_option(ub_handle_t h, int key, int64_t val)
+{
+    if (int rc = check_handle(h)) return rc;
+    switch (key) {
+    case UB_OPT_SM_MARGIN:
+        if (val < 0 || val >= h->sm_count) return fail(UB_ERR_ARG, "sm_margin %lld outside [0, %d)", (long long)val, h->sm_count);
+        h->sm_margin = val;
+        return UB_OK;
+    case UB_OPT_TIMEOUT_NS:
+        if (val < 1000) return fail(UB_ERR_ARG, "timeout %lld ns below 1 us", (long long)val);
+        h->timeout_ns = val;
+        return UB_OK;
+    case UB_OPT_SELF_RANK:
+        if (val < 0 || val >= h->tp) return fail(UB_ERR_ARG, "self rank %lld outside [0, %d)", (long long)val, h->tp);
+        h->self_rank = val;
+        return UB_OK;
+    case UB_OPT_DROP_FLAG:
+        if (val < -1 || val >= h->tp) return fail(UB_ERR_ARG, "drop_flag %lld outside [-1, %d)", (long long)val, h->tp);
+        h->drop_flag = val;
+        return UB_OK;
+    case UB_OPT_PROFILE:
+        if (val != 0 && val != 1) return fail(UB_ERR_ARG, "profile must be 0 or 1");
+        h->profile = val;
+        return UB_OK;
+    default:
+        return fail(UB_ERR_ARG, "unknown option %d", key);
+    }
+}
+
+int ub_get_option(ub_handle_t h, int key, int64_t *val)
+{
+    if (int rc = check_handle(h)) return rc;
+    if (!val) return fail(UB_ERR_ARG, "null output");
+    switch (key) {
+    case UB_OPT_SM_MARGIN: *val = h->sm_margin; return UB_OK;
+    case UB_OPT_TIMEOUT_NS: *val = h->timeout_ns; return UB_OK;
+    case UB_OPT_SELF_RANK: *val = h->self_rank; return UB_OK;
+    case UB_OPT_DROP_FLAG: *val = h->drop_flag; return UB_OK;
+    case UB_OPT_PROFILE: *val = h->profile; return UB_OK;
+    default: return fail(UB_ERR_ARG, "unknown option %d", key);
+    }
+}
+
+int ub_query_status(ub_handle_t h)
+{
+    if (int rc = check_handle(h)) return rc;
+    DeviceGuard g(h->device);
+    int32_t st = 0;
+    UB_CUDA(cudaMemcpyAsync(&st, status_of(h), sizeof st, cudaMemcpyDeviceToHost, h->side));
+    UB_CUDA(cudaStreamSynchronize(h->side));
+    return st;
+}
+
+int ub_clear_status(ub_handle_t h)
+{
+    if (int rc = check_handle(h)) return rc;
+    DeviceGuard g(h->device);
+    UB_CUDA(cudaMemsetAsync(status_of(h), 0, sizeof(int32_t), h->side));
+    UB_CUDA(cudaStreamSynchronize(h->side));
+    return UB_OK;
+}
+
+int ub_get_counters(ub_handle_t h, ub_counters_t *out)
+{
+    if (int rc = check_handle(h)) return rc;
+    if (!out) return fail(UB_ERR_ARG, "null output");
+    *out = h->counters;
+    return UB_OK;
+}
+
+int ub_kernel_time(ub_handle_t h, int op, double *total_ms, int64_t *launches)
+{
+    if (int rc = check_handle(h)) return rc;
+    if (op != UB_OP_AG && op != UB_OP_RS) return fail(UB_ERR_ARG, "unknown op %d", op);
+    DeviceGuard g(h->device);
+    ProfileRing &ring = h->prof[op];
+    double sum = 0.0;
+    if (ring.count > 0) UB_CUDA(cudaEventSynchronize(ring.stop[ring.count - 1]));
+    for (int i = 0; i < ring.count; ++i) {
+        float ms = 0.f;
+        UB_CUDA(cudaEventElapsedTime(&ms, ring.start[i], ring.stop[i]));
+        sum += ms;
+    }
+    if (total_ms) *total_ms = sum;
+    if (launches) *launches = ring.count;
+    ring.count = 0;
+    return UB_OK;
+}
+
+}  // extern "C"

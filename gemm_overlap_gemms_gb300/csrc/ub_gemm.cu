@@ -1,0 +1,521 @@
+// Persistent tcgen05 / TMEM BF16 GEMM for the active-shape AG-GEMM and GEMM-RS.
+//
+// One kernel, two modes:
+//  * MODE_AG -- the column-parallel linear after the all-gather (QKV / fc1 diagrams of
+//    "Do tp overlap support thd..."): Y[chunk r rows] = UB[chunk r rows] * Wt^T. Tiles
+//    are walked chunk by chunk in ring order from the self rank ("ring_exchange" of
+//    "How to setup TP Overlap configs", with the chunk loop on the device as in its
+//    "atomic_gemm"); the producer waits for a chunk's readiness flag, written by the
+//    copy engine's stream after it lands the chunk, before loading any of its rows.
+//  * MODE_RS -- the row-parallel linear followed by the reduce-scatter (MLP diagram):
+//    the K loop runs over (shard j, k-block), so sum_j A_j * Bt_j^T accumulates in
+//    TMEM, and the epilogue writes the rows of block r straight into Y_shards[r].
+//
+// M tiles never straddle a chunk: tile rows are counted inside chunk r, and every
+// tensor map of an output block (and, for AG, of an input chunk) has exactly c = T/tp
+// rows, so the tensor memory accelerator zero-fills loads and drops stores past the
+// chunk end. No byte past the active prefix is read or written ("Support dynamic
+// token counts in TP communication/GEMM overlap", "Implementation approach").
+//
+// Warp roles (192 threads, one CTA per SM):
+//   warp 0      TMA producer: flag waits, A/B tiles into a 4-stage smem ring
+//   warp 1      TMEM owner and MMA issuer: tcgen05.mma 128x256x16, fp32 in TMEM
+//   warps 2..5  epilogue: tcgen05.ld -> bf16 -> swizzled smem -> TMA store
+// The accumulator is double-buffered (2 x 256 TMEM columns), so the epilogue of one
+// tile overlaps the main loop of the next.
+//
+// Every wait is bounded (%globaltimer): when one runs out the CTA records
+// UB_ERR_TIMEOUT in the status word, publishes the call's epoch in the abort word so
+// the other CTAs stop too, drains its own outstanding copies and MMAs, frees its TMEM
+// and returns. Nothing traps.
+#include <cuda_bf16.h>
+
+#include "ub_internal.h"
+
+namespace ubk {
+namespace {
+
+// ------------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int x, int y)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int x, int y)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(x), "r"(y)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void bulk_wait_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+__device__ __forceinline__ void fence_proxy_async_shared()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+// fp32 pair -> packed bf16x2 (round to nearest even); `lo` lands at the lower address.
+__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo, uint32_t hi)
+{
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(__uint_as_float(hi)), "f"(__uint_as_float(lo)));
+    return d;
+}
+
+// ---- tcgen05
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand tile written by TMA with the
+// 128-byte swizzle: rows of 128 bytes (64 bf16 of K), 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address      [0,14)
+    d |= static_cast<uint64_t>(16u >> 4) << 16;           // leading offset     [16,30) (unused: K fits one row)
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;         // stride offset      [32,46)
+    d |= static_cast<uint64_t>(1u) << 46;                 // descriptor version [46,48)
+    d |= static_cast<uint64_t>(2u) << 61;                 // swizzle: 128 B     [61,64)
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both K-major,
+// N = BN, M = BM.
+constexpr uint32_t kIdesc = (1u << 4)                           // D format: f32
+                            | (1u << 7)                         // A format: bf16
+                            | (1u << 10)                        // B format: bf16
+                            | (static_cast<uint32_t>(BN >> 3) << 17)  // N / 8
+                            | (static_cast<uint32_t>(BM >> 4) << 24); // M / 16
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on `bar` once every tcgen05 operation this thread issued so far has completed.
+__device__ __forceinline__ void umma_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t *v)
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
+          "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),
+          "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]),
+          "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ------------------------------------------------------------------ bounded waits
+
+struct WaitCtx {
+    uint32_t *abort_word;
+    int32_t *status;
+    uint64_t timeout_ns;
+    uint32_t epoch;
+};
+
+__device__ __forceinline__ bool call_aborted(const WaitCtx &w)
+{
+    return *reinterpret_cast<volatile uint32_t *>(w.abort_word) == w.epoch;
+}
+
+__device__ void raise_error(const WaitCtx &w, int code)
+{
+    atomicCAS(reinterpret_cast<int *>(w.status), 0, code);
+    __threadfence();
+    atomicExch(w.abort_word, w.epoch);
+}
+
+// Wait for phase `parity` of an mbarrier. False when this call was aborted or the
+// wait ran past the timeout (which then raises UB_ERR_TIMEOUT).
+__device__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtx &w)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 31u) == 0) {
+            if (call_aborted(w)) return false;
+            if (global_timer() - t0 > w.timeout_ns) {
+                raise_error(w, UB_ERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// Wait used while draining at exit: ignores the abort word, still bounded in time.
+__device__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns)
+{
+    const uint64_t t0 = global_timer();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer() - t0 > timeout_ns) return false;
+    }
+    return true;
+}
+
+// Wait until the readiness flag of a chunk has reached this call's epoch (wrap-safe),
+// then order the tensor-memory-accelerator reads that follow after it.
+__device__ bool wait_flag(const uint32_t *flag, const WaitCtx &w)
+{
+    uint64_t t0 = 0;
+    for (uint32_t n = 0;; ++n) {
+        uint32_t v;
+        asm volatile("ld.acquire.sys.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+        if (static_cast<int32_t>(v - w.epoch) >= 0) {
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            return true;
+        }
+        if (n == 0) {
+            t0 = global_timer();
+        } else if ((n & 7u) == 0) {
+            if (call_aborted(w)) return false;
+            if (global_timer() - t0 > w.timeout_ns) {
+                raise_error(w, UB_ERR_TIMEOUT);
+                return false;
+            }
+        }
+        __nanosleep(256);
+    }
+}
+
+// ------------------------------------------------------------------ tile walk
+
+struct Tile {
+    int r;  // chunk (AG) / output row block (RS)
+    int m;  // M tile inside the chunk
+    int n;  // N tile
+};
+
+template <int MODE>
+__device__ __forceinline__ Tile tile_at(int t, const GemmParams &p)
+{
+    const int per_chunk = p.m_tiles * p.n_tiles;
+    const int q = t / per_chunk;  // position in the ring
+    const int rem = t - q * per_chunk;
+    Tile x;
+    if (MODE == MODE_AG) {
+        int r = p.self_rank + q;
+        x.r = r >= p.tp ? r - p.tp : r;
+    } else {
+        x.r = q;
+    }
+    x.m = rem / p.n_tiles;
+    x.n = rem - x.m * p.n_tiles;
+    return x;
+}
+
+// ------------------------------------------------------------------ the kernel
+
+template <int MODE>
+__global__ void __launch_bounds__(THREADS, 1) ub_gemm_kernel(const __grid_constant__ GemmParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *smA = base;
+    uint8_t *smB = smA + STAGES * A_STAGE_BYTES;
+    uint8_t *smE = smB + STAGES * B_STAGE_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smE + EPI_WARPS * 2 * EPI_BUF_BYTES);
+    // barrier slots: full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2], drain
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
+    const uint32_t bar0 = smem_u32(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const WaitCtx w{p.abort_word, p.status, p.timeout_ns, p.epoch};
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), EPI_WARPS);
+        }
+        mbar_init(drain_bar, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------------------------------------------------- producer
+        const int nmaps = MODE == MODE_AG ? 1 : p.tp;
+        for (int i = 0; i < nmaps; ++i) prefetch_tmap(&p.tmB[i]);
+        uint32_t stage = 0, phase = 0, ready = 0;
+        int issued = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+            const Tile x = tile_at<MODE>(t, p);
+            if (MODE == MODE_AG && x.r != p.self_rank && !((ready >> x.r) & 1u)) {
+                if (!wait_flag(p.flags + x.r, w)) {
+                    ok = false;
+                    break;
+                }
+                ready |= 1u << x.r;
+            }
+            const int arow = MODE == MODE_AG ? x.m * BM : x.r * p.c + x.m * BM;
+            const int brow = x.n * BN;
+            for (int kb = 0; kb < p.k_blocks; ++kb) {
+                if (!mbar_wait(empty_bar(stage), phase ^ 1u, w)) {
+                    ok = false;
+                    break;
+                }
+                const CUtensorMap *ma;
+                const CUtensorMap *mb;
+                int kx;
+                if (MODE == MODE_AG) {
+                    ma = &p.tmA[x.r];
+                    mb = &p.tmB[0];
+                    kx = kb * BK;
+                } else {
+                    const int j = kb / p.k_blocks_per_shard;
+                    kx = (kb - j * p.k_blocks_per_shard) * BK;
+                    ma = &p.tmA[j];
+                    mb = &p.tmB[j];
+                }
+                mbar_arrive_expect_tx(full_bar(stage), A_STAGE_BYTES + B_STAGE_BYTES);
+                tma_load_2d(smem_u32(smA + stage * A_STAGE_BYTES), ma, full_bar(stage), kx, arow);
+                tma_load_2d(smem_u32(smB + stage * B_STAGE_BYTES), mb, full_bar(stage), kx, brow);
+                ++issued;
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        // Drain: the last STAGES loads must have landed before the CTA may exit.
+        for (int i = issued > STAGES ? issued - STAGES : 0; i < issued; ++i)
+            mbar_wait_drain(full_bar(i % STAGES), static_cast<uint32_t>(i / STAGES) & 1u, p.timeout_ns);
+    } else if (warp == 1 && lane == 0) {
+        // ---------------------------------------------------------- MMA issuer
+        uint32_t stage = 0, phase = 0;
+        int local = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++local) {
+            const uint32_t acc = local & 1;
+            const uint32_t acc_phase = (local >> 1) & 1;
+            if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, w)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + acc * BN;
+            for (int kb = 0; kb < p.k_blocks; ++kb) {
+                if (!mbar_wait(full_bar(stage), phase, w)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a0 = smem_u32(smA + stage * A_STAGE_BYTES);
+                const uint32_t b0 = smem_u32(smB + stage * B_STAGE_BYTES);
+#pragma unroll
+                for (int k = 0; k < BK / 16; ++k)
+                    umma_bf16(d_tmem, smem_desc_sw128(a0 + 32u * k), smem_desc_sw128(b0 + 32u * k),
+                              (kb | k) != 0 ? 1u : 0u);
+                umma_commit(empty_bar(stage));
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            umma_commit(tfull_bar(acc));
+        }
+        // Drain: every MMA issued must be complete before TMEM is released.
+        umma_commit(drain_bar);
+        mbar_wait_drain(drain_bar, 0, p.timeout_ns);
+    } else if (warp >= 2) {
+        // ---------------------------------------------------------- epilogue
+        const int quarter = warp & 3;  // TMEM lanes this warp may read: 32*quarter ...
+        uint8_t *ebuf = smE + (warp - 2) * 2 * EPI_BUF_BYTES;
+        const uint32_t ebuf0 = smem_u32(ebuf);
+        int local = 0, nstore = 0;
+        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++local) {
+            const Tile x = tile_at<MODE>(t, p);
+            const uint32_t acc = local & 1;
+            const uint32_t acc_phase = (local >> 1) & 1;
+            // One lane waits and the warp follows its verdict, so the warp never splits
+            // around the warp-wide tcgen05.ld below.
+            int live = 0;
+            if (lane == 0) live = mbar_wait(tfull_bar(acc), acc_phase, w) ? 1 : 0;
+            if (!__shfl_sync(0xffffffffu, live, 0)) break;
+            tc_fence_after();
+            const int row0 = x.m * BM + quarter * 32;  // first row of this warp's slab, inside block r
+            const bool rows_live = row0 < p.c;
+            const uint32_t trow = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
+#pragma unroll 1
+            for (int sub = 0; sub < BN / STORE_COLS; ++sub) {
+                uint32_t v[STORE_COLS];
+                tmem_ld32(trow + sub * STORE_COLS, v);
+                tmem_ld32(trow + sub * STORE_COLS + 32, v + 32);
+                tmem_wait_ld();
+                if (sub == BN / STORE_COLS - 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(tempty_bar(acc));
+                }
+                const int col = x.n * BN + sub * STORE_COLS;
+                if (!rows_live || col >= p.n_out) continue;
+                const uint32_t buf = ebuf0 + (nstore & 1) * EPI_BUF_BYTES;
+                if (lane == 0) bulk_wait_read<1>();  // the store that last used `buf` has read it
+                __syncwarp();
+                const uint32_t rowaddr = buf + lane * 128u;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    st_shared_v4(rowaddr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4),
+                                 pack_bf16x2(v[8 * j + 0], v[8 * j + 1]), pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                                 pack_bf16x2(v[8 * j + 4], v[8 * j + 5]), pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+                }
+                fence_proxy_async_shared();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&p.tmY[x.r], buf, col, row0);
+                    bulk_commit();
+                }
+                ++nstore;
+            }
+        }
+        if (lane == 0) bulk_wait_all();
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmParams &p, int mode, int grid, cudaStream_t stream)
+{
+    cudaError_t e;
+    if (mode == MODE_AG) {
+        e = cudaFuncSetAttribute(ub_gemm_kernel<MODE_AG>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        ub_gemm_kernel<MODE_AG><<<grid, THREADS, SMEM_BYTES, stream>>>(p);
+    } else {
+        e = cudaFuncSetAttribute(ub_gemm_kernel<MODE_RS>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        ub_gemm_kernel<MODE_RS><<<grid, THREADS, SMEM_BYTES, stream>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace ubk

@@ -1,0 +1,58 @@
+// Internal interface between the host runtime (ub_api.cu) and the GEMM kernel
+// (ub_gemm.cu). Not installed; the public ABI is include/ub.h.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ub.h"
+
+namespace ubk {
+
+// Tile shape of the persistent kernel: one CTA owns a 128 x 256 output tile at a
+// time, accumulating in TMEM (128 lanes x 256 fp32 columns, double-buffered), with a
+// 4-stage shared-memory ring of 128x64 (A) and 256x64 (B) BF16 tiles in the 128-byte
+// swizzled layout the tensor memory accelerator writes.
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;          // 64 bf16 = 128 bytes = one swizzle row
+constexpr int STAGES = 4;
+constexpr int EPI_WARPS = 4;
+constexpr int THREADS = 64 + 32 * EPI_WARPS;  // producer warp, MMA warp, epilogue warps
+constexpr int STORE_COLS = 64;  // epilogue store box: 64 columns x 32 rows
+constexpr int A_STAGE_BYTES = BM * BK * 2;
+constexpr int B_STAGE_BYTES = BN * BK * 2;
+constexpr int EPI_BUF_BYTES = 32 * STORE_COLS * 2;  // 4 KiB per warp per buffer
+constexpr int SMEM_BYTES = 1024 /* alignment slack */ + STAGES * (A_STAGE_BYTES + B_STAGE_BYTES) +
+                           EPI_WARPS * 2 * EPI_BUF_BYTES + 256 /* barriers */;
+constexpr int TMEM_COLS = 2 * BN;  // two accumulators
+
+enum Mode : int { MODE_AG = 0, MODE_RS = 1 };
+
+// Kernel parameters, passed by value as a __grid_constant__ (tensor maps must live
+// in parameter, constant or global memory).
+struct GemmParams {
+    CUtensorMap tmA[UB_MAX_TP];  // AG: chunk r ([c, hidden] view); RS: A_j ([T, K])
+    CUtensorMap tmB[UB_MAX_TP];  // AG: [0] = Wt ([N, hidden]); RS: Bt_j ([hidden, K])
+    CUtensorMap tmY[UB_MAX_TP];  // output block r: AG [c, N] of Y; RS Y_shards[r] [c, hidden]
+    const uint32_t *flags;       // AG readiness flag per chunk (device)
+    uint32_t *abort_word;        // epoch of an aborted call (device)
+    int32_t *status;             // sticky UB_ERR_* (device)
+    uint64_t timeout_ns;
+    uint32_t epoch;
+    int tp;
+    int c;                       // rows per chunk = T / tp
+    int n_out;                   // N (AG) or hidden (RS)
+    int k_blocks;                // BK-blocks per tile (RS: over all tp shards)
+    int k_blocks_per_shard;      // RS: BK-blocks of one shard's K
+    int m_tiles;                 // per chunk: ceil(c / BM)
+    int n_tiles;                 // ceil(n_out / BN)
+    int num_tiles;               // tp * m_tiles * n_tiles
+    int self_rank;               // AG: chunk read in place, no flag wait
+};
+
+// Launch the persistent GEMM (mode MODE_AG or MODE_RS) with `grid` CTAs on `stream`.
+cudaError_t launch_gemm(const GemmParams &p, int mode, int grid, cudaStream_t stream);
+
+}  // namespace ubk

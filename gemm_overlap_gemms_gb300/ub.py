@@ -1,0 +1,316 @@
+"""ctypes binding of libubgemm (include/ub.h): argument marshalling only.
+
+Every step of the AG-GEMM and GEMM-RS path runs in the library's kernels and copy
+engine calls; this module checks tensor dtypes, devices and shapes, passes raw
+device pointers and the current CUDA stream, and turns error codes into exceptions.
+There is no fallback: if ``libubgemm.so`` is missing, the first call raises.
+
+API modelled on "Support dynamic token counts in TP communication/GEMM overlap"
+(TransformerEngine issue #3564), "Proposed API": ``initialize_ub([max_tokens,
+hidden], tp_size, dtype=torch.bfloat16)`` registers a buffer at capacity, and
+``set_ub_active_shape([T, hidden])`` sets the active shape before each microbatch.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libubgemm.so")
+_lib = None
+
+UB_OK = 0
+ERRORS = {
+    -1: "UB_ERR_ARG", -2: "UB_ERR_DTYPE", -3: "UB_ERR_RANK", -4: "UB_ERR_ZERO",
+    -5: "UB_ERR_CAPACITY", -6: "UB_ERR_HIDDEN", -7: "UB_ERR_DIVISIBLE", -8: "UB_ERR_ALIGN",
+    -9: "UB_ERR_CUDA", -10: "UB_ERR_TIMEOUT",
+}
+CODES = {v: k for k, v in ERRORS.items()}
+OPTIONS = {"sm_margin": 1, "timeout_ns": 2, "self_rank": 3, "drop_flag": 4, "profile": 5}
+OPS = {"ag": 0, "rs": 1}
+MAX_TP = 8
+EXPORTS = [
+    "ub_create", "ub_destroy", "ub_set_active_shape", "ub_set_active_shape_nd",
+    "ub_validate_active_shape", "ub_get_active_shape", "ub_get_capacity", "ub_get_tp",
+    "ub_buffer", "ag_gemm", "gemm_rs", "ub_set_option", "ub_get_option", "ub_query_status",
+    "ub_clear_status", "ub_get_counters", "ub_kernel_time", "ub_grid_ctas", "ub_last_error",
+]
+
+
+class UbError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__("%s (%d): %s" % (ERRORS.get(code, "UB_ERR?"), code, msg))
+        self.code = code
+        self.name = ERRORS.get(code, "UB_ERR?")
+
+
+class Counters(ctypes.Structure):
+    _fields_ = [("ag_calls", ctypes.c_int64), ("rs_calls", ctypes.c_int64),
+                ("device_allocations", ctypes.c_int64), ("last_T", ctypes.c_int64),
+                ("tensor_map_encodes", ctypes.c_int64)]
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load libubgemm.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError("libubgemm.so is not built (%s); run __graft_entry__.build()" % _LIB_PATH)
+    L = ctypes.CDLL(_LIB_PATH)
+    P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    PP = ctypes.POINTER(ctypes.c_void_p)
+    sig = {
+        "ub_create": [I64, I64, I, I, ctypes.POINTER(P)],
+        "ub_destroy": [P],
+        "ub_set_active_shape": [P, I64, I64],
+        "ub_set_active_shape_nd": [P, I, ctypes.POINTER(I64)],
+        "ub_validate_active_shape": [I, ctypes.POINTER(I64), I64, I64, I],
+        "ub_get_active_shape": [P, ctypes.POINTER(I64), ctypes.POINTER(I64)],
+        "ub_get_capacity": [P, ctypes.POINTER(I64), ctypes.POINTER(I64)],
+        "ub_get_tp": [P, ctypes.POINTER(I)],
+        "ub_buffer": [P, PP, ctypes.POINTER(ctypes.c_size_t)],
+        "ag_gemm": [P, PP, P, I64, P, P],
+        "gemm_rs": [P, PP, PP, I64, PP, P],
+        "ub_set_option": [P, I, I64],
+        "ub_get_option": [P, I, ctypes.POINTER(I64)],
+        "ub_query_status": [P],
+        "ub_clear_status": [P],
+        "ub_get_counters": [P, ctypes.POINTER(Counters)],
+        "ub_kernel_time": [P, I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I64)],
+        "ub_grid_ctas": [P, ctypes.POINTER(I)],
+        "ub_last_error": [],
+    }
+    for name, args in sig.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_char_p if name == "ub_last_error" else ctypes.c_int
+    _lib = L
+    return L
+
+
+def last_error() -> str:
+    return load().ub_last_error().decode(errors="replace")
+
+
+def _check(rc: int):
+    if rc != UB_OK:
+        raise UbError(rc, last_error())
+    return rc
+
+
+def validate_active_shape(shape, max_tokens: int, hidden: int, tp: int) -> int:
+    """UB_OK or the UB_ERR_* code of the first violated active-shape constraint."""
+    dims = (ctypes.c_int64 * max(1, len(shape)))(*[int(d) for d in shape])
+    return load().ub_validate_active_shape(len(shape), dims, max_tokens, hidden, tp)
+
+
+def _stream_ptr(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptrs(tensors):
+    return (ctypes.c_void_p * len(tensors))(*[t.data_ptr() for t in tensors])
+
+
+def _bf16_cuda(t: torch.Tensor, name: str, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.dtype != torch.bfloat16 or not t.is_cuda:
+        raise TypeError("%s must be a CUDA bfloat16 tensor, got %s on %s" % (name, t.dtype, t.device))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+
+
+class _DeviceArray:
+    """Exposes the registered buffer to torch through __cuda_array_interface__."""
+
+    def __init__(self, owner, ptr: int, shape):
+        self._owner = owner
+        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": "<i2",
+                                         "data": (ptr, False), "version": 3, "strides": None}
+
+
+class UserBuffer:
+    """A user buffer registered at capacity [max_tokens, hidden] for tp virtual ranks."""
+
+    def __init__(self, shape, tp_size: int, dtype=torch.bfloat16):
+        if len(shape) != 2:
+            raise UbError(CODES["UB_ERR_RANK"], "capacity shape must be [max_tokens, hidden]")
+        if dtype != torch.bfloat16:
+            raise UbError(CODES["UB_ERR_DTYPE"], "only torch.bfloat16 user buffers are supported")
+        L = load()
+        h = ctypes.c_void_p()
+        _check(L.ub_create(int(shape[0]), int(shape[1]), int(tp_size), 0, ctypes.byref(h)))
+        self._h = h
+        self.max_tokens, self.hidden, self.tp = int(shape[0]), int(shape[1]), int(tp_size)
+        self.device = torch.device("cuda", torch.cuda.current_device())
+
+    # -- lifetime
+    def close(self):
+        if getattr(self, "_h", None):
+            load().ub_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    # -- shapes
+    def set_active_shape(self, shape):
+        dims = (ctypes.c_int64 * max(1, len(shape)))(*[int(d) for d in shape])
+        _check(load().ub_set_active_shape_nd(self._h, len(shape), dims))
+
+    @property
+    def active_shape(self):
+        T, H = ctypes.c_int64(), ctypes.c_int64()
+        _check(load().ub_get_active_shape(self._h, ctypes.byref(T), ctypes.byref(H)))
+        return (T.value, H.value)
+
+    @property
+    def capacity_shape(self):
+        M, H = ctypes.c_int64(), ctypes.c_int64()
+        _check(load().ub_get_capacity(self._h, ctypes.byref(M), ctypes.byref(H)))
+        return (M.value, H.value)
+
+    def buffer(self) -> torch.Tensor:
+        """The whole registered buffer as a [max_tokens, hidden] bf16 CUDA tensor (a view)."""
+        p = ctypes.c_void_p()
+        n = ctypes.c_size_t()
+        _check(load().ub_buffer(self._h, ctypes.byref(p), ctypes.byref(n)))
+        arr = _DeviceArray(self, p.value, (self.max_tokens, self.hidden))
+        return torch.as_tensor(arr, device=self.device).view(torch.bfloat16)
+
+    def buffer_ptr(self) -> int:
+        p = ctypes.c_void_p()
+        _check(load().ub_buffer(self._h, ctypes.byref(p), None))
+        return p.value
+
+    # -- options / status
+    def set_option(self, key: str, value: int):
+        _check(load().ub_set_option(self._h, OPTIONS[key], int(value)))
+
+    def get_option(self, key: str) -> int:
+        v = ctypes.c_int64()
+        _check(load().ub_get_option(self._h, OPTIONS[key], ctypes.byref(v)))
+        return v.value
+
+    def query_status(self) -> int:
+        """Sticky device status (UB_OK or UB_ERR_*); synchronise the stream first."""
+        return load().ub_query_status(self._h)
+
+    def clear_status(self):
+        _check(load().ub_clear_status(self._h))
+
+    def counters(self) -> dict:
+        c = Counters()
+        _check(load().ub_get_counters(self._h, ctypes.byref(c)))
+        return {f: getattr(c, f) for f, _ in Counters._fields_}
+
+    def kernel_time(self, op: str):
+        """(total_ms, launches) of the GEMM kernels of ``op`` since the last query
+        (needs the ``profile`` option)."""
+        ms, n = ctypes.c_double(), ctypes.c_int64()
+        _check(load().ub_kernel_time(self._h, OPS[op], ctypes.byref(ms), ctypes.byref(n)))
+        return ms.value, n.value
+
+    def grid_ctas(self) -> int:
+        g = ctypes.c_int()
+        _check(load().ub_grid_ctas(self._h, ctypes.byref(g)))
+        return g.value
+
+    # -- the two operations
+    def ag_gemm(self, shards, Wt: torch.Tensor, Y: torch.Tensor | None = None, stream=None):
+        """Y[T, N] = concat_r(shards[r]) @ Wt.T; the gathered input stays in the buffer."""
+        T, H = self.active_shape
+        if len(shards) != self.tp:
+            raise ValueError("expected %d shards, got %d" % (self.tp, len(shards)))
+        c = T // self.tp
+        for r, s in enumerate(shards):
+            _bf16_cuda(s, "shards[%d]" % r, (c, H))
+        _bf16_cuda(Wt, "Wt")
+        if Wt.dim() != 2 or Wt.shape[1] != H:
+            raise ValueError("Wt must be [N, %d], got %s" % (H, tuple(Wt.shape)))
+        N = Wt.shape[0]
+        if Y is None:
+            Y = torch.empty((T, N), dtype=torch.bfloat16, device=Wt.device)
+        _bf16_cuda(Y, "Y")
+        if Y.dim() != 2 or Y.shape[0] < T or Y.shape[1] != N:
+            raise ValueError("Y must be [>=%d, %d], got %s" % (T, N, tuple(Y.shape)))
+        _check(load().ag_gemm(self._h, _ptrs(shards), ctypes.c_void_p(Wt.data_ptr()), N,
+                              ctypes.c_void_p(Y.data_ptr()), _stream_ptr(stream)))
+        return Y
+
+    def gemm_rs(self, A, Bt, Y_shards=None, stream=None):
+        """Y_shards[r] = rows [r*c, (r+1)*c) of sum_j A[j] @ Bt[j].T (c = T / tp)."""
+        T, H = self.active_shape
+        if len(A) != self.tp or len(Bt) != self.tp:
+            raise ValueError("expected %d A and Bt operands" % self.tp)
+        K = A[0].shape[1] if A[0].dim() == 2 else -1
+        for j in range(self.tp):
+            _bf16_cuda(A[j], "A[%d]" % j, (T, K))
+            _bf16_cuda(Bt[j], "Bt[%d]" % j, (H, K))
+        c = T // self.tp
+        if Y_shards is None:
+            Y_shards = [torch.empty((c, H), dtype=torch.bfloat16, device=A[0].device)
+                        for _ in range(self.tp)]
+        if len(Y_shards) != self.tp:
+            raise ValueError("expected %d output shards" % self.tp)
+        for r, y in enumerate(Y_shards):
+            _bf16_cuda(y, "Y_shards[%d]" % r)
+            if y.dim() != 2 or y.shape[0] < c or y.shape[1] != H:
+                raise ValueError("Y_shards[%d] must be [>=%d, %d]" % (r, c, H))
+        _check(load().gemm_rs(self._h, _ptrs(A), _ptrs(Bt), K, _ptrs(Y_shards),
+                              _stream_ptr(stream)))
+        return Y_shards
+
+
+# ---------------------------------------------------------------- module-level manager
+
+_default: UserBuffer | None = None
+
+
+def initialize_ub(shape, tp_size: int, dtype=torch.bfloat16) -> UserBuffer:
+    """Register the default user buffer at capacity ``shape`` = [max_tokens, hidden]."""
+    global _default
+    if _default is not None:
+        _default.close()
+    _default = UserBuffer(shape, tp_size, dtype)
+    return _default
+
+
+def set_ub_active_shape(shape):
+    """Set the active shape [T, hidden] of the default user buffer."""
+    if _default is None:
+        raise RuntimeError("initialize_ub() has not been called")
+    _default.set_active_shape(shape)
+
+
+def get_ub() -> UserBuffer:
+    if _default is None:
+        raise RuntimeError("initialize_ub() has not been called")
+    return _default
+
+
+def destroy_ub():
+    global _default
+    if _default is not None:
+        _default.close()
+        _default = None

@@ -1,0 +1,199 @@
+/*
+ * ub.h -- C ABI of libubgemm: active-shape tensor-parallel AG-GEMM and GEMM-RS on one
+ * GB300 (sm_103a), with the tp "ranks" as virtual shards resident in the same HBM.
+ *
+ * The operations follow three public pages on tensor-parallel communication/GEMM
+ * overlap:
+ *  [P1] "Do tp overlap support thd, whose sequence length is flexible?"
+ *       (Megatron-LM discussion #1240), answer: QKV and MLP diagrams
+ *       (ColumnParallelLinear after the all-gather of [S, H]; RowParallelLinear
+ *       whose [S, H] output is summed over ranks and split by rows); the user buffer
+ *       is sized by the communicated tensor [S, hidden], not the GEMM output.
+ *  [P2] "Support dynamic token counts in TP communication/GEMM overlap"
+ *       (TransformerEngine issue #3564): "Proposed API" (initialize at
+ *       [max_tokens, hidden], set an active shape per microbatch), "Implementation
+ *       approach in the prototype" (capacity and active shape kept apart; nothing
+ *       allocated, freed or re-registered; active data is a contiguous prefix; chunk
+ *       offsets and counts use the active first dimension) and "Constrain the initial
+ *       behavior" (2-D, nonzero, within capacity, hidden unchanged, T divisible by
+ *       tp; unquantized 2-byte BF16 only).
+ *  [P3] "How to setup TP Overlap configs" (TransformerEngine issue #1344): the
+ *       "ring_exchange" method with copy-engine send/recv ("use_ce"), "num_splits"
+ *       forced to the TP size, the on-device chunk loop of "atomic_gemm", and the
+ *       "num_sm" / "set_sm_margin" SM reservation.
+ *
+ * Conventions for every call:
+ *  - All matrices are row-major BF16. Linear weights are stored out x in, the layout
+ *    of a PyTorch nn.Linear weight: the column-parallel weight is Wt[N][hidden]
+ *    (Y = X * Wt^T), each row-parallel shard weight is Bt_j[hidden][K]
+ *    (S = sum_j A_j * Bt_j^T). Accumulation is fp32; outputs are rounded to BF16
+ *    (round to nearest even).
+ *  - Device pointers must be 16-byte aligned and N, K, hidden multiples of 8
+ *    (UB_ERR_ALIGN otherwise): rows are moved by the tensor memory accelerator.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream). Calls are
+ *    asynchronous on it; the caller keeps every buffer alive until the stream has
+ *    passed the call. Results are deterministic run to run (no split-K, no atomics).
+ *  - Every function returns UB_OK (0) or a negative UB_ERR_* code; on error the
+ *    state of the handle is unchanged and ub_last_error() describes the failure.
+ *  - A handle is used from one host thread at a time.
+ */
+#ifndef UB_H
+#define UB_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define UB_MAX_TP 8 /* virtual ranks per handle */
+
+typedef struct ub_handle *ub_handle_t; /* opaque; owned by the library */
+
+typedef enum { UB_BF16 = 0 } ub_dtype_t; /* [P2] "Constrain...": 2-byte BF16 only */
+
+enum {
+    UB_OK = 0,
+    UB_ERR_ARG = -1,       /* null pointer, tp out of [1, UB_MAX_TP], bad option */
+    UB_ERR_DTYPE = -2,     /* dtype other than UB_BF16 */
+    UB_ERR_RANK = -3,      /* active shape not two-dimensional */
+    UB_ERR_ZERO = -4,      /* a zero (or negative) extent */
+    UB_ERR_CAPACITY = -5,  /* T larger than the registered max_tokens */
+    UB_ERR_HIDDEN = -6,    /* hidden differs from the registered hidden */
+    UB_ERR_DIVISIBLE = -7, /* T (or max_tokens) not divisible by tp */
+    UB_ERR_ALIGN = -8,     /* pointer not 16-byte aligned, or N / K / hidden % 8 != 0 */
+    UB_ERR_CUDA = -9,      /* a CUDA runtime or driver call failed */
+    UB_ERR_TIMEOUT = -10   /* a bounded device-side wait expired (see ub_query_status) */
+};
+
+/* Options for ub_set_option / ub_get_option. */
+enum {
+    UB_OPT_SM_MARGIN = 1,  /* SMs left out of the GEMM grid ([P3] "num_sm"); default 0 */
+    UB_OPT_TIMEOUT_NS = 2, /* bound of every device-side wait, ns; default 1e9 */
+    UB_OPT_SELF_RANK = 3,  /* ring start of ag_gemm: the chunk read in place; default 0 */
+    UB_OPT_DROP_FLAG = 4,  /* fault injection on the host: the next ag_gemm skips the
+                              readiness-flag write of this chunk (-1 = off, one-shot) */
+    UB_OPT_PROFILE = 5     /* 1 = time every GEMM kernel launch with CUDA events */
+};
+
+/* Operation ids for ub_kernel_time. */
+enum { UB_OP_AG = 0, UB_OP_RS = 1 };
+
+/*
+ * Register a user buffer at capacity [max_tokens, hidden] for tp virtual ranks
+ * ([P2] "Proposed API", initialize_ub). Allocates, once, the buffer
+ * (max_tokens * hidden * 2 bytes) and a small control block (tp readiness flags, an
+ * abort word, a status word) on the current CUDA device, plus one side stream and two
+ * events. The active shape starts at capacity. Requires max_tokens % tp == 0 so that
+ * the initial active shape is itself valid. *out receives the handle.
+ * Errors: UB_ERR_ARG, UB_ERR_ZERO, UB_ERR_DTYPE, UB_ERR_ALIGN, UB_ERR_DIVISIBLE,
+ * UB_ERR_CUDA (no device, allocation failure).
+ */
+int ub_create(int64_t max_tokens, int64_t hidden, int tp, ub_dtype_t dtype, ub_handle_t *out);
+
+/* Release everything the handle owns. Synchronises the handle's side stream. */
+int ub_destroy(ub_handle_t h);
+
+/*
+ * Set the active shape [T, hidden] for the next calls ([P2] set_ub_active_shape,
+ * "Implementation approach": a logical shape only -- nothing is allocated, freed or
+ * re-registered, and no GPU work is issued). Constraints, checked in this order
+ * ([P2] "Constrain the initial behavior"): two-dimensional (UB_ERR_RANK), nonzero
+ * (UB_ERR_ZERO), T <= max_tokens (UB_ERR_CAPACITY), hidden unchanged
+ * (UB_ERR_HIDDEN), T % tp == 0 (UB_ERR_DIVISIBLE). A rejected shape leaves the
+ * previous active shape in place.
+ */
+int ub_set_active_shape(ub_handle_t h, int64_t T, int64_t hidden);
+/* The same with the shape given as ndim extents (the rank is checked too). */
+int ub_set_active_shape_nd(ub_handle_t h, int ndim, const int64_t *dims);
+
+/* The same five checks without a handle: 0 or the UB_ERR_* of the first violation. */
+int ub_validate_active_shape(int ndim, const int64_t *dims, int64_t max_tokens,
+                             int64_t hidden, int tp);
+
+/* Active and capacity shapes ([P2] "Proposed API": active/capacity shape getters). */
+int ub_get_active_shape(ub_handle_t h, int64_t *T, int64_t *hidden);
+int ub_get_capacity(ub_handle_t h, int64_t *max_tokens, int64_t *hidden);
+int ub_get_tp(ub_handle_t h, int *tp);
+
+/* Device address and byte size of the registered buffer. After ag_gemm its first T
+ * rows hold the gathered input concat_r X_r (rows >= T are never touched). */
+int ub_buffer(ub_handle_t h, void **dev_ptr, size_t *bytes);
+
+/*
+ * All-gather + GEMM for the column-parallel linear ([P1] QKV / fc1 diagrams; [P3]
+ * "ring_exchange" with "use_ce"): with T the active token count and c = T / tp,
+ *     UB[r*c + i][:] = shards[r][i][:]            for r < tp, i < c
+ *     Y[t][n]       = sum_h UB[t][h] * Wt[n][h]   for t < T, n < N.
+ * shards: host array of tp device pointers, each [c, hidden]. Wt: device [N, hidden].
+ * Y: device [T, N] (leading dimension N). The chunk copies run on the copy engine on
+ * the handle's side stream, each followed by a readiness-flag write; one persistent
+ * GEMM kernel on `stream` walks the chunks in ring order starting at
+ * UB_OPT_SELF_RANK (whose chunk it reads in place, without waiting), waits for each
+ * other chunk's flag, and never reads or writes rows >= T. The side stream is joined
+ * back into `stream` before return. A device wait that expires is reported by
+ * ub_query_status (UB_ERR_TIMEOUT), never by a trap.
+ * Errors: UB_ERR_ARG, UB_ERR_ZERO (N <= 0), UB_ERR_ALIGN, UB_ERR_CUDA.
+ */
+int ag_gemm(ub_handle_t h, const void *const *shards, const void *Wt, int64_t N, void *Y,
+            void *stream);
+
+/*
+ * GEMM + reduce-scatter for the row-parallel linear ([P1] MLP diagram, fc2; [P2]
+ * "Implementation approach": row blocks from the active first dimension):
+ *     S[t][n]        = sum_{j<tp} sum_{k<K} A_j[t][k] * Bt_j[n][k]   (fp32, in TMEM)
+ *     Y_shards[r][i] = bf16(S[r*c + i])                            for i < c = T / tp
+ * A: host array of tp device pointers, each [T, K]. Bt: tp device pointers, each
+ * [hidden, K]. Y_shards: tp device pointers, each [c, hidden]. The cross-shard sum
+ * never leaves the accumulator; each rank's block is written directly, and no byte of
+ * A_j beyond row T nor of Y_shards[r] beyond row c is touched.
+ * Errors: UB_ERR_ARG, UB_ERR_ZERO (K <= 0), UB_ERR_ALIGN, UB_ERR_CUDA.
+ */
+int gemm_rs(ub_handle_t h, const void *const *A, const void *const *Bt, int64_t K,
+            void *const *Y_shards, void *stream);
+
+/* Options (UB_OPT_*). UB_ERR_ARG for an unknown key or an out-of-range value. */
+int ub_set_option(ub_handle_t h, int key, int64_t val);
+int ub_get_option(ub_handle_t h, int key, int64_t *val);
+
+/*
+ * Sticky device status: UB_OK, or the first UB_ERR_* a kernel of this handle raised
+ * (UB_ERR_TIMEOUT when a readiness flag or pipeline barrier wait ran out). Reads the
+ * device word through the handle's side stream; call it after the stream of the
+ * calls of interest has been synchronised. Returns UB_ERR_CUDA if the read fails.
+ */
+int ub_query_status(ub_handle_t h);
+/* Reset the sticky device status to UB_OK (stream-ordered on the side stream). */
+int ub_clear_status(ub_handle_t h);
+
+/* Counters of the handle: calls made, device allocations made (constant after
+ * ub_create), last active T used by a GEMM call. */
+typedef struct {
+    int64_t ag_calls;
+    int64_t rs_calls;
+    int64_t device_allocations;
+    int64_t last_T;
+    int64_t tensor_map_encodes;
+} ub_counters_t;
+int ub_get_counters(ub_handle_t h, ub_counters_t *out);
+
+/*
+ * With UB_OPT_PROFILE = 1, every GEMM kernel launch of operation `op` (UB_OP_AG or
+ * UB_OP_RS) is bracketed by CUDA events on its launch stream (up to 4096 launches are
+ * kept). This call waits for the last recorded launch, returns the summed kernel time
+ * in milliseconds and the launch count, and clears the record.
+ */
+int ub_kernel_time(ub_handle_t h, int op, double *total_ms, int64_t *launches);
+
+/* Grid size a GEMM call of this handle launches (SM count minus the margin). */
+int ub_grid_ctas(ub_handle_t h, int *ctas);
+
+/* Message of the last failed call on this host thread ("" if none). */
+const char *ub_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* UB_H */

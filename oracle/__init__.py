@@ -180,18 +180,23 @@ def gemm_rs(A, Bt, with_S: bool = True):
     return S, Y
 
 
-def gemm_rs_rows(A, Bt, rows):
-    """For selected active rows t: (S[t], owner rank t // c, local row t - owner*c)."""
-    A = [_u16(a) for a in A]
+def gemm_rs_rows(A_rows, Bt, rows, T: int):
+    """For selected active rows t = rows[q] of a T-token GEMM-RS: (S[t], owner rank
+    t // c, local row t - owner*c). ``A_rows[j]`` holds only the selected rows of A_j
+    (``A_rows[j][q] = A_j[rows[q]]``), so full-size checks need not copy all of A_j."""
+    A_rows = [_u16(a) for a in A_rows]
     Bt = [_u16(b) for b in Bt]
-    tp = len(A)
-    T, K = A[0].shape
-    H = Bt[0].shape[0]
+    tp = len(A_rows)
     rows = np.ascontiguousarray(rows, dtype=np.int64)
+    K = Bt[0].shape[1]
+    H = Bt[0].shape[0]
+    for a in A_rows:
+        assert a.shape == (rows.size, K)
+    assert T % tp == 0
     assert rows.size == 0 or (rows.min() >= 0 and rows.max() < T)
     out = np.empty((rows.size, H), dtype=np.float64)
     owner = np.empty(rows.size, dtype=np.int32)
     local = np.empty(rows.size, dtype=np.int64)
-    _load().oracle_gemm_rs_rows(tp, T, K, H, _ptr_array(A), _ptr_array(Bt), _ptr(rows),
+    _load().oracle_gemm_rs_rows(tp, T, K, H, _ptr_array(A_rows), _ptr_array(Bt), _ptr(rows),
                                 rows.size, _ptr(out), _ptr(owner), _ptr(local))
     return out, owner, local

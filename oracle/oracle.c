@@ -177,10 +177,11 @@ void oracle_gemm_rs(int tp, int64_t T, int64_t K, int64_t H,
     }
 }
 
-/* GEMM-RS on selected rows of the active prefix (for full-size spot checks):
- * out[q][n] = S[rows[q]][n]; owner[q] = rows[q] / c and local[q] = rows[q] - owner*c. */
+/* GEMM-RS on selected rows of the active prefix (for full-size spot checks). The
+ * caller passes, per shard j, only the selected rows: A_rows[j][q][k] = A_j[rows[q]][k].
+ * out[q][n] = S[rows[q]][n]; owner[q] = rows[q] / c; local[q] = rows[q] - owner[q]*c. */
 void oracle_gemm_rs_rows(int tp, int64_t T, int64_t K, int64_t H,
-                         const uint16_t *const *A, const uint16_t *const *Bt,
+                         const uint16_t *const *A_rows, const uint16_t *const *Bt,
                          const int64_t *rows, int64_t nrows,
                          double *out, int32_t *owner, int64_t *local)
 {
@@ -193,7 +194,7 @@ void oracle_gemm_rs_rows(int tp, int64_t T, int64_t K, int64_t H,
         owner[q] = r;
         local[q] = t - oracle_chunk_offset(T, tp, r);
         for (int64_t n = 0; n < H; ++n)
-            out[q * H + n] = rs_element(tp, K, A, Bt, t, n);
+            out[q * H + n] = rs_element(tp, K, A_rows, Bt, q, n);
     }
 }
 

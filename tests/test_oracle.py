@@ -305,7 +305,7 @@ def test_rows_helpers_agree_with_full_products():
     A = [synth.to_u16(a) for a in A]
     Bt = [synth.to_u16(b) for b in Bt]
     S, Yb = oracle.gemm_rs(A, Bt)
-    out, owner, local = oracle.gemm_rs_rows(A, Bt, rows)
+    out, owner, local = oracle.gemm_rs_rows([a[rows] for a in A], Bt, rows, T)
     np.testing.assert_array_equal(out, S[rows])
     np.testing.assert_array_equal(owner, rows // (T // tp))
     np.testing.assert_array_equal(local, rows % (T // tp))
