@@ -230,6 +230,8 @@ int check_handle(ub_handle *h)
 
 }  // namespace
 
+void ubk::set_last_error(const char *msg) { snprintf(g_err, sizeof g_err, "%s", msg); }
+
 extern "C" {
 
 const char *ub_last_error(void) { return g_err; }

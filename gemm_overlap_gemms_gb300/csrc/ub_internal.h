@@ -55,4 +55,7 @@ struct GemmParams {
 // Launch the persistent GEMM (mode MODE_AG or MODE_RS) with `grid` CTAs on `stream`.
 cudaError_t launch_gemm(const GemmParams &p, int mode, int grid, cudaStream_t stream);
 
+// Record the message ub_last_error() returns on this host thread.
+void set_last_error(const char *msg);
+
 }  // namespace ubk

@@ -35,7 +35,9 @@ EXPORTS = [
     "ub_validate_active_shape", "ub_get_active_shape", "ub_get_capacity", "ub_get_tp",
     "ub_buffer", "ag_gemm", "gemm_rs", "ub_set_option", "ub_get_option", "ub_query_status",
     "ub_clear_status", "ub_get_counters", "ub_kernel_time", "ub_grid_ctas", "ub_last_error",
+    "ag_gemm_noalloc",
 ]
+NOALLOC_MAX_ELEMS = 16 * 1024 * 1024
 
 
 class UbError(RuntimeError):
@@ -85,6 +87,7 @@ def load():
         "ub_kernel_time": [P, I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I64)],
         "ub_grid_ctas": [P, ctypes.POINTER(I)],
         "ub_last_error": [],
+        "ag_gemm_noalloc": [PP, I, I64, I64, P, I64, P, P],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -280,6 +283,25 @@ class UserBuffer:
         _check(load().gemm_rs(self._h, _ptrs(A), _ptrs(Bt), K, _ptrs(Y_shards),
                               _stream_ptr(stream)))
         return Y_shards
+
+
+def ag_gemm_noalloc(shards, Wt: torch.Tensor, Y: torch.Tensor | None = None, stream=None):
+    """AG-GEMM through the allocation-free entry point (no handle): for callers that
+    cannot allocate device memory. Uses the library's fixed 32 MiB device scratch, so
+    T * hidden <= NOALLOC_MAX_ELEMS, and calls on one device must not overlap."""
+    tp = len(shards)
+    c, H = shards[0].shape
+    for r, s in enumerate(shards):
+        _bf16_cuda(s, "shards[%d]" % r, (c, H))
+    _bf16_cuda(Wt, "Wt")
+    N = Wt.shape[0]
+    T = c * tp
+    if Y is None:
+        Y = torch.empty((T, N), dtype=torch.bfloat16, device=Wt.device)
+    _bf16_cuda(Y, "Y")
+    _check(load().ag_gemm_noalloc(_ptrs(shards), tp, T, H, ctypes.c_void_p(Wt.data_ptr()), N,
+                                  ctypes.c_void_p(Y.data_ptr()), _stream_ptr(stream)))
+    return Y
 
 
 # ---------------------------------------------------------------- module-level manager

@@ -189,6 +189,35 @@ int ub_kernel_time(ub_handle_t h, int op, double *total_ms, int64_t *launches);
 /* Grid size a GEMM call of this handle launches (SM count minus the margin). */
 int ub_grid_ctas(ub_handle_t h, int *ctas);
 
+/*
+ * AG-GEMM without any device allocation, for callers that cannot call cudaMalloc (code
+ * running inside another framework's memory pool or a custom allocator that owns the
+ * device, plugins whose allocations are audited, processes that must not grow their
+ * device footprint after start-up). The paper has no counterpart to this entry point.
+ *
+ * Computes what ag_gemm computes for an active shape [T, hidden] split over tp
+ * virtual ranks (shards: host array of tp device pointers, each [T/tp, hidden];
+ * Wt: device [N, hidden]; Y: device [T, N]), with the ring starting at rank 0, using
+ * the same kernel. Instead of a handle's user buffer and control block it uses one
+ * file-scope device array of UB_NOALLOC_MAX_ELEMS bf16 elements (32 MiB) plus 256
+ * bytes, which every GPU that loads the library holds until the process exits. It
+ * calls no cudaMalloc or cudaFree and creates no stream or event: the chunk copies and
+ * their readiness flags are issued on `stream` itself, ahead of the kernel.
+ *  - T * hidden must not exceed UB_NOALLOC_MAX_ELEMS (UB_ERR_CAPACITY otherwise);
+ *    T % tp == 0 (UB_ERR_DIVISIBLE); hidden, N multiples of 8 and pointers 16-byte
+ *    aligned (UB_ERR_ALIGN); 1 <= tp <= UB_MAX_TP (UB_ERR_ARG).
+ *  - The first call on a device looks up the array's device address there
+ *    (cudaGetSymbolAddress); make that first call before any stream capture.
+ *  - Every call on a device shares the one array, which keeps the last call's
+ *    contents (the status word is cleared by each call; flags use growing epochs).
+ *    Calls that overlap on the GPU -- on different streams, or from several host
+ *    threads without ordering -- race on it and give undefined results.
+ *  - Device-side wait timeouts are not reported by this entry point.
+ */
+#define UB_NOALLOC_MAX_ELEMS (16ll * 1024 * 1024)
+int ag_gemm_noalloc(const void *const *shards, int tp, int64_t T, int64_t hidden, const void *Wt,
+                    int64_t N, void *Y, void *stream);
+
 /* Message of the last failed call on this host thread ("" if none). */
 const char *ub_last_error(void);
 
