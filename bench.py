@@ -39,6 +39,16 @@ from gemm_overlap_gemms_gb300 import synth  # noqa: E402
 METRIC = "AG-GEMM / GEMM-RS TFLOP/s and % of GB300 bf16 peak vs active token count T"
 WORKLOAD = "swiglu"
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SRC = os.path.join(ROOT, "gemm_overlap_gemms_gb300", "csrc", "ub_gemm.cu")
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one ncu capture per op,
+# per active token of the captured launch, and the kernel source they were taken on.
+# Traffic is reported as null once the kernel source no longer matches.
+NCU_TRAFFIC = {
+    "rs": {"sha256_16": "25d40b573b83d0ce", "bytes": 1129.3e6, "T": 8192,
+           "source": "profiles/ub_gemm_kernel_rs_swiglu_fc2_T8192.md"},
+    "ag": {"sha256_16": "25d40b573b83d0ce", "bytes": 595.4e6, "T": 8192,
+           "source": "profiles/ub_gemm_kernel_ag_swiglu_fc1_T8192.md"},
+}
 
 
 def parse():
@@ -51,6 +61,10 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--case", choices=["ag", "rs"], default=None,
+                    help="time one op of the workload at one T only (small profiling case)")
+    ap.add_argument("--case-T", type=int, default=8192)
+    ap.add_argument("--case-reps", type=int, default=3)
     return ap.parse_args()
 
 
@@ -75,6 +89,21 @@ def _peak_value(d, *keys):
                 if isinstance(v.get(kk), (int, float)):
                     return float(v[kk])
     return None
+
+
+def kernel_traffic(op: str, avg_T: float):
+    """ncu DRAM traffic of one launch of `op`, scaled from the captured launch to the
+    mean active T of the benchmark's launches (traffic grows with T: A and Y are
+    proportional, and the weight re-reads follow the number of M-tile waves)."""
+    import hashlib
+    rec = NCU_TRAFFIC.get(op)
+    if not rec or not os.path.exists(KERNEL_SRC):
+        return None
+    sha = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()[:16]
+    if sha != rec["sha256_16"]:
+        return None
+    return {"bytes_per_launch": rec["bytes"] * avg_T / rec["T"], "captured_T": rec["T"],
+            "scaled_to_mean_T": avg_T, "source": rec["source"]}
 
 
 def step_flops(Ts, w):
@@ -332,10 +361,13 @@ def run_ours(args):
     }
     dom = "rs" if rs_ms >= ag_ms else "ag"
     achieved = kernels[dom]["tflops"]
+    tr = kernel_traffic(dom, float(np.mean(wl.Ts)))
     roofline = {"bound": "tensor", "kernel": "ub_gemm_kernel<%s>" % ("MODE_RS" if dom == "rs" else "MODE_AG"),
                 "achieved": achieved, "peak": tensor_peak, "unit": "TFLOP/s",
-                "frac": achieved / tensor_peak if achieved else None, "traffic": None,
-                "peak_source": "%s bf16 sustained" % src}
+                "frac": achieved / tensor_peak if achieved else None,
+                "traffic": tr["bytes_per_launch"] if tr else None, "traffic_detail": tr,
+                "peak_source": "%s bf16 sustained (%s)" % (src, "MEASURED_PEAKS.json" if src == "measured"
+                                                             else "no MEASURED_PEAKS.json: recipe fallback")}
 
     e2e = None
     if not args.no_e2e:
@@ -485,9 +517,50 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+def run_case(args):
+    """One op of the workload at one active T: a warm-up launch, then `case_reps`
+    launches (the small case the profiler captures; holds well under 1 GB)."""
+    from gemm_overlap_gemms_gb300 import ub
+    w = synth.WORKLOADS[WORKLOAD]
+    dev = torch.device("cuda", 0)
+    T = args.case_T
+    H, N, K, tp = w.hidden, w.ag_n[0], w.rs_k[0], w.tp
+    g = synth.generator(dev)
+    buf = ub.UserBuffer([w.max_tokens, H], tp)
+    buf.set_active_shape([T, H])
+    c = T // tp
+    if args.case == "ag":
+        X = synth.normal_bf16((T, H), 1.0, g, dev)
+        W1 = synth.normal_bf16((N, H), 1.0 / math.sqrt(H), g, dev)
+        Y = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
+        shards = [X[r * c:(r + 1) * c] for r in range(tp)]
+        fn = lambda: buf.ag_gemm(shards, W1, Y)
+        flops = 2.0 * T * H * N
+    else:
+        A = [synth.normal_bf16((T, K), 1.0, g, dev) for _ in range(tp)]
+        B = [synth.normal_bf16((H, K), 1.0 / math.sqrt(K), g, dev) for _ in range(tp)]
+        Ys = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        outs = [Ys[r * c:(r + 1) * c] for r in range(tp)]
+        fn = lambda: buf.gemm_rs(A, B, outs)
+        flops = 2.0 * T * K * H * tp
+    fn()
+    torch.cuda.synchronize()
+    buf.set_option("profile", 1)
+    for _ in range(args.case_reps):
+        fn()
+    torch.cuda.synchronize()
+    ms, n = buf.kernel_time(args.case)
+    assert buf.query_status() == ub.UB_OK
+    buf.close()
+    print(json.dumps({"case": args.case, "T": T, "launches": n, "avg_us": 1e3 * ms / max(n, 1),
+                      "tflops": flops * n / (ms / 1e3) / 1e12 if ms > 0 else None}))
+
+
 def main():
     args = parse()
-    if args.impl == "reference":
+    if args.case:
+        run_case(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
