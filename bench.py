@@ -65,6 +65,8 @@ def parse():
                     help="time one op of the workload at one T only (small profiling case)")
     ap.add_argument("--case-T", type=int, default=8192)
     ap.add_argument("--case-reps", type=int, default=3)
+    ap.add_argument("--cta-pair", type=int, default=1, choices=[0, 1],
+                    help="1: 256x256 tiles on CTA pairs (default); 0: 128x256 tiles on single CTAs")
     return ap.parse_args()
 
 
@@ -220,6 +222,7 @@ class SwigluWorkload:
         self.Y1 = torch.empty((cap, N), dtype=torch.bfloat16, device=device)
         self.Yrs = torch.empty((cap, H), dtype=torch.bfloat16, device=device)
         self.buf = ub.UserBuffer([cap, H], tp)
+        self.buf.set_option("cta_pair", CTA_PAIR)
 
     def shards(self, i):
         T, tp = self.Ts[i], self.w.tp
@@ -527,6 +530,7 @@ def run_case(args):
     H, N, K, tp = w.hidden, w.ag_n[0], w.rs_k[0], w.tp
     g = synth.generator(dev)
     buf = ub.UserBuffer([w.max_tokens, H], tp)
+    buf.set_option("cta_pair", args.cta_pair)
     buf.set_active_shape([T, H])
     c = T // tp
     if args.case == "ag":
@@ -552,12 +556,17 @@ def run_case(args):
     ms, n = buf.kernel_time(args.case)
     assert buf.query_status() == ub.UB_OK
     buf.close()
-    print(json.dumps({"case": args.case, "T": T, "launches": n, "avg_us": 1e3 * ms / max(n, 1),
+    print(json.dumps({"case": args.case, "T": T, "cta_pair": args.cta_pair, "launches": n, "avg_us": 1e3 * ms / max(n, 1),
                       "tflops": flops * n / (ms / 1e3) / 1e12 if ms > 0 else None}))
 
 
+CTA_PAIR = 1
+
+
 def main():
+    global CTA_PAIR
     args = parse()
+    CTA_PAIR = args.cta_pair
     if args.case:
         run_case(args)
     elif args.impl == "reference":

@@ -138,6 +138,8 @@ struct ub_handle {
     int64_t self_rank = 0;
     int64_t drop_flag = -1;
     int64_t profile = 0;
+    int64_t cta_pair = 1;
+    int pair_clusters[2] = {-1, -1};  // resident clusters of the pair kernel, per mode
     ub_counters_t counters{};
     std::vector<CacheEntry> cache;
     uint64_t use_clock = 0;
@@ -175,6 +177,17 @@ int grid_for(ub_handle *h, int num_tiles)
     return g < num_tiles ? g : num_tiles;
 }
 
+// Clusters of the pair kernel to launch: as many as fit (resident at once, within the
+// SM margin), but no more than there are pair tiles.
+int clusters_for(ub_handle *h, int mode, int num_tiles)
+{
+    if (h->pair_clusters[mode] < 0) h->pair_clusters[mode] = ubk::max_pair_clusters(mode);
+    int g = (h->sm_count - static_cast<int>(h->sm_margin)) / 2;
+    if (h->pair_clusters[mode] > 0 && g > h->pair_clusters[mode]) g = h->pair_clusters[mode];
+    if (g < 1) g = 1;
+    return g < num_tiles ? g : num_tiles;
+}
+
 GemmParams *cache_lookup(ub_handle *h, const std::vector<const void *> &key)
 {
     for (auto &e : h->cache)
@@ -198,9 +211,9 @@ GemmParams *cache_insert(ub_handle *h, std::vector<const void *> key, const Gemm
     return &h->cache[victim].params;
 }
 
-int launch(ub_handle *h, const GemmParams &p, int mode, cudaStream_t s)
+int launch(ub_handle *h, const GemmParams &p, int mode, bool pair, cudaStream_t s)
 {
-    const int grid = grid_for(h, p.num_tiles);
+    const int grid = pair ? clusters_for(h, mode, p.num_tiles) : grid_for(h, p.num_tiles);
     ProfileRing &ring = h->prof[mode];
     const bool timed = h->profile != 0 && ring.count < kMaxProfiled;
     if (timed) {
@@ -213,7 +226,7 @@ int launch(ub_handle *h, const GemmParams &p, int mode, cudaStream_t s)
         }
         UB_CUDA(cudaEventRecord(ring.start[ring.count], s));
     }
-    cudaError_t e = ubk::launch_gemm(p, mode, grid, s);
+    cudaError_t e = pair ? ubk::launch_gemm_pair(p, mode, grid, s) : ubk::launch_gemm(p, mode, grid, s);
     if (e != cudaSuccess) return cuda_fail(e, "GEMM kernel launch");
     if (timed) {
         UB_CUDA(cudaEventRecord(ring.stop[ring.count], s));
@@ -370,7 +383,8 @@ int ub_buffer(ub_handle_t h, void **dev_ptr, size_t *bytes)
 int ub_grid_ctas(ub_handle_t h, int *ctas)
 {
     if (int rc = check_handle(h)) return rc;
-    if (ctas) *ctas = grid_for(h, 1 << 30);
+    DeviceGuard g(h->device);
+    if (ctas) *ctas = h->cta_pair ? 2 * clusters_for(h, ubk::MODE_RS, 1 << 30) : grid_for(h, 1 << 30);
     return UB_OK;
 }
 
@@ -394,9 +408,13 @@ int ag_gemm(ub_handle_t h, const void *const *shards, const void *Wt, int64_t N,
     const int self = static_cast<int>(h->self_rank);
     char *ub = static_cast<char *>(h->ub);
 
+    const bool pair = h->cta_pair != 0;
+    const int bm = pair ? ubk::PAIR_BM : ubk::BM;      // rows of a tile
+    const int bbox = pair ? ubk::BN / 2 : ubk::BN;    // rows of a B box (one CTA's half in a pair)
     std::vector<const void *> key;
-    key.reserve(tp + 6);
+    key.reserve(tp + 7);
     key.push_back(reinterpret_cast<const void *>(uintptr_t(ubk::MODE_AG)));
+    key.push_back(reinterpret_cast<const void *>(uintptr_t(pair)));
     key.push_back(reinterpret_cast<const void *>(uintptr_t(T)));
     key.push_back(reinterpret_cast<const void *>(uintptr_t(N)));
     key.push_back(reinterpret_cast<const void *>(uintptr_t(self)));
@@ -416,14 +434,14 @@ int ag_gemm(ub_handle_t h, const void *const *shards, const void *Wt, int64_t N,
                                    ubk::STORE_COLS, 32))
                 return rc;
         }
-        if (int rc = encode_2d(&p.tmB[0], Wt, H, N, H * 2, ubk::BK, ubk::BN)) return rc;
+        if (int rc = encode_2d(&p.tmB[0], Wt, H, N, H * 2, ubk::BK, bbox)) return rc;
         h->counters.tensor_map_encodes += 2 * tp + 1;
         p.tp = tp;
         p.c = static_cast<int>(c);
         p.n_out = static_cast<int>(N);
         p.k_blocks = static_cast<int>((H + ubk::BK - 1) / ubk::BK);
         p.k_blocks_per_shard = p.k_blocks;
-        p.m_tiles = static_cast<int>((c + ubk::BM - 1) / ubk::BM);
+        p.m_tiles = static_cast<int>((c + bm - 1) / bm);
         p.n_tiles = static_cast<int>((N + ubk::BN - 1) / ubk::BN);
         p.num_tiles = tp * p.m_tiles * p.n_tiles;
         p.self_rank = self;
@@ -455,7 +473,7 @@ int ag_gemm(ub_handle_t h, const void *const *shards, const void *Wt, int64_t N,
             if (cr != CUDA_SUCCESS) return fail(UB_ERR_CUDA, "cuStreamWriteValue32 failed (%d)", (int)cr);
         }
     }
-    int rc = launch(h, p, ubk::MODE_AG, s);
+    int rc = launch(h, p, ubk::MODE_AG, pair, s);
     // Join the side stream back into `s` even if the launch failed.
     UB_CUDA(cudaEventRecord(h->ev_join, h->side));
     UB_CUDA(cudaStreamWaitEvent(s, h->ev_join, 0));
@@ -484,9 +502,13 @@ int gemm_rs(ub_handle_t h, const void *const *A, const void *const *Bt, int64_t 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int64_t T = h->T, H = h->hidden, c = T / tp;
 
+    const bool pair = h->cta_pair != 0;
+    const int bm = pair ? ubk::PAIR_BM : ubk::BM;
+    const int bbox = pair ? ubk::BN / 2 : ubk::BN;
     std::vector<const void *> key;
-    key.reserve(3 * tp + 3);
+    key.reserve(3 * tp + 4);
     key.push_back(reinterpret_cast<const void *>(uintptr_t(ubk::MODE_RS)));
+    key.push_back(reinterpret_cast<const void *>(uintptr_t(pair)));
     key.push_back(reinterpret_cast<const void *>(uintptr_t(T)));
     key.push_back(reinterpret_cast<const void *>(uintptr_t(K)));
     for (int j = 0; j < tp; ++j) {
@@ -500,7 +522,7 @@ int gemm_rs(ub_handle_t h, const void *const *A, const void *const *Bt, int64_t 
         memset(&p, 0, sizeof p);
         for (int j = 0; j < tp; ++j) {
             if (int rc = encode_2d(&p.tmA[j], A[j], K, T, K * 2, ubk::BK, ubk::BM)) return rc;
-            if (int rc = encode_2d(&p.tmB[j], Bt[j], K, H, K * 2, ubk::BK, ubk::BN)) return rc;
+            if (int rc = encode_2d(&p.tmB[j], Bt[j], K, H, K * 2, ubk::BK, bbox)) return rc;
             if (int rc = encode_2d(&p.tmY[j], Y_shards[j], H, c, H * 2, ubk::STORE_COLS, 32)) return rc;
         }
         h->counters.tensor_map_encodes += 3 * tp;
@@ -509,7 +531,7 @@ int gemm_rs(ub_handle_t h, const void *const *A, const void *const *Bt, int64_t 
         p.n_out = static_cast<int>(H);
         p.k_blocks_per_shard = static_cast<int>((K + ubk::BK - 1) / ubk::BK);
         p.k_blocks = tp * p.k_blocks_per_shard;
-        p.m_tiles = static_cast<int>((c + ubk::BM - 1) / ubk::BM);
+        p.m_tiles = static_cast<int>((c + bm - 1) / bm);
         p.n_tiles = static_cast<int>((H + ubk::BN - 1) / ubk::BN);
         p.num_tiles = tp * p.m_tiles * p.n_tiles;
         p.self_rank = 0;
@@ -521,7 +543,7 @@ int gemm_rs(ub_handle_t h, const void *const *A, const void *const *Bt, int64_t 
     p.status = status_of(h);
     p.timeout_ns = static_cast<uint64_t>(h->timeout_ns);
     p.epoch = ++h->epoch;
-    if (int rc = launch(h, p, ubk::MODE_RS, s)) return rc;
+    if (int rc = launch(h, p, ubk::MODE_RS, pair, s)) return rc;
     ++h->counters.rs_calls;
     h->counters.last_T = T;
     return UB_OK;
@@ -551,6 +573,10 @@ int ub_set_option(ub_handle_t h, int key, int64_t val)
         if (val != 0 && val != 1) return fail(UB_ERR_ARG, "profile must be 0 or 1");
         h->profile = val;
         return UB_OK;
+    case UB_OPT_CTA_PAIR:
+        if (val != 0 && val != 1) return fail(UB_ERR_ARG, "cta_pair must be 0 or 1");
+        h->cta_pair = val;
+        return UB_OK;
     default:
         return fail(UB_ERR_ARG, "unknown option %d", key);
     }
@@ -566,6 +592,7 @@ int ub_get_option(ub_handle_t h, int key, int64_t *val)
     case UB_OPT_SELF_RANK: *val = h->self_rank; return UB_OK;
     case UB_OPT_DROP_FLAG: *val = h->drop_flag; return UB_OK;
     case UB_OPT_PROFILE: *val = h->profile; return UB_OK;
+    case UB_OPT_CTA_PAIR: *val = h->cta_pair; return UB_OK;
     default: return fail(UB_ERR_ARG, "unknown option %d", key);
     }
 }

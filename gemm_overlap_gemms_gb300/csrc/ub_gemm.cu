@@ -209,6 +209,96 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t *v)
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+
+// ---- CTA-pair (cta_group::2) helpers
+
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank)
+{
+    uint32_t d;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(saddr), "r"(rank));
+    return d;
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// TMA load into this CTA's shared memory that completes bytes on an mbarrier which may
+// live in either CTA of the pair.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar_cluster, int x,
+                                                 int y)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t slot, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Instruction descriptor for the pair MMA: M = 256 (128 rows in each CTA), N = 256.
+constexpr uint32_t kIdescPair = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
+                                (static_cast<uint32_t>(PAIR_BM >> 4) << 24);
+
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(kIdescPair), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on the mbarrier at `bar` in both CTAs of the pair once the MMAs issued so far
+// have completed.
+__device__ __forceinline__ void umma_commit_pair_both(uint32_t bar)
+{
+    const uint16_t mask = 0x3;
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::
+                     "r"(bar),
+                 "h"(mask)
+                 : "memory");
+}
+
+__device__ __forceinline__ void umma_commit_pair_local(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// Bounded pause used on the abort path so that copies already issued land first.
+__device__ void settle(uint64_t ns)
+{
+    const uint64_t t0 = global_timer();
+    while (global_timer() - t0 < ns) __nanosleep(1000);
+}
+
 // ------------------------------------------------------------------ bounded waits
 
 struct WaitCtx {
@@ -501,7 +591,269 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_kernel(const __grid_consta
     }
 }
 
+
+// ------------------------------------------------------------------ the CTA-pair kernel
+
+// Same roles as ub_gemm_kernel, on a cluster of two CTAs that share 256 x 256 tiles.
+// Both CTAs run a producer (own A rows, own half of B) whose loads complete on the even
+// CTA's `full` barrier; the even CTA's MMA thread issues the cta_group::2 MMAs and
+// multicasts stage releases and accumulator-ready signals to both CTAs; each CTA's
+// epilogue drains its own 128 TMEM lanes and reports back to the even CTA.
+template <int MODE>
+__global__ void __launch_bounds__(THREADS, 1) ub_gemm_pair_kernel(const __grid_constant__ GemmParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *smA = base;
+    uint8_t *smB = smA + PAIR_STAGES * PAIR_A_BYTES;
+    uint8_t *smE = smB + PAIR_STAGES * PAIR_B_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smE + EPI_WARPS * 2 * EPI_BUF_BYTES);
+    // barrier slots: full[S], empty[S], tmem_full[2], tmem_empty[2], drain
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * PAIR_STAGES + 5);
+    const uint32_t bar0 = smem_u32(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (PAIR_STAGES + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * PAIR_STAGES + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * PAIR_STAGES + 2 + a); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * PAIR_STAGES + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();  // 0 = even CTA (issues the MMAs), 1 = its peer
+    const int pair = blockIdx.x >> 1;
+    const int npairs = gridDim.x >> 1;
+    const WaitCtx w{p.abort_word, p.status, p.timeout_ns, p.epoch};
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < PAIR_STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 2 * EPI_WARPS);
+        }
+        mbar_init(drain_bar, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+    tc_fence_before();
+    cluster_sync_all();  // barriers of both CTAs initialised before any cross-CTA signal
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------------------------------------------------- producer (both CTAs)
+        const int nmaps = MODE == MODE_AG ? 1 : p.tp;
+        for (int i = 0; i < nmaps; ++i) prefetch_tmap(&p.tmB[i]);
+        uint32_t stage = 0, phase = 0, ready = 0;
+        int issued = 0;
+        bool ok = true;
+        for (int t = pair; ok && t < p.num_tiles; t += npairs) {
+            const Tile x = tile_at<MODE>(t, p);
+            if (MODE == MODE_AG && x.r != p.self_rank && !((ready >> x.r) & 1u)) {
+                if (!wait_flag(p.flags + x.r, w)) {
+                    ok = false;
+                    break;
+                }
+                ready |= 1u << x.r;
+            }
+            const int half = static_cast<int>(rank) * 128;
+            const int arow = (MODE == MODE_AG ? x.m * PAIR_BM : x.r * p.c + x.m * PAIR_BM) + half;
+            const int brow = x.n * BN + half;
+            for (int kb = 0; kb < p.k_blocks; ++kb) {
+                if (!mbar_wait(empty_bar(stage), phase ^ 1u, w)) {
+                    ok = false;
+                    break;
+                }
+                const CUtensorMap *ma;
+                const CUtensorMap *mb;
+                int kx;
+                if (MODE == MODE_AG) {
+                    ma = &p.tmA[x.r];
+                    mb = &p.tmB[0];
+                    kx = kb * BK;
+                } else {
+                    const int j = kb / p.k_blocks_per_shard;
+                    kx = (kb - j * p.k_blocks_per_shard) * BK;
+                    ma = &p.tmA[j];
+                    mb = &p.tmB[j];
+                }
+                const uint32_t fb = map_to_rank(full_bar(stage), 0);
+                if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * (PAIR_A_BYTES + PAIR_B_BYTES));
+                tma_load_2d_pair(smem_u32(smA + stage * PAIR_A_BYTES), ma, fb, kx, arow);
+                tma_load_2d_pair(smem_u32(smB + stage * PAIR_B_BYTES), mb, fb, kx, brow);
+                ++issued;
+                if (++stage == PAIR_STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (rank == 0) {
+            // The even CTA's full barriers also count the peer's bytes: once its last
+            // stages have completed, every load of both CTAs for them has landed.
+            for (int i = issued > PAIR_STAGES ? issued - PAIR_STAGES : 0; i < issued; ++i)
+                mbar_wait_drain(full_bar(i % PAIR_STAGES), static_cast<uint32_t>(i / PAIR_STAGES) & 1u, p.timeout_ns);
+        }
+        if (!ok) settle(100000);  // abort path: let copies already issued land
+    } else if (warp == 1 && lane == 0 && rank == 0) {
+        // ---------------------------------------------------------- MMA issuer (even CTA)
+        uint32_t stage = 0, phase = 0;
+        int local = 0;
+        bool ok = true;
+        for (int t = pair; ok && t < p.num_tiles; t += npairs, ++local) {
+            const uint32_t acc = local & 1;
+            const uint32_t acc_phase = (local >> 1) & 1;
+            if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, w)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + acc * BN;
+            for (int kb = 0; kb < p.k_blocks; ++kb) {
+                if (!mbar_wait(full_bar(stage), phase, w)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a0 = smem_u32(smA + stage * PAIR_A_BYTES);
+                const uint32_t b0 = smem_u32(smB + stage * PAIR_B_BYTES);
+#pragma unroll
+                for (int k = 0; k < BK / 16; ++k)
+                    umma_bf16_pair(d_tmem, smem_desc_sw128(a0 + 32u * k), smem_desc_sw128(b0 + 32u * k),
+                                   (kb | k) != 0 ? 1u : 0u);
+                umma_commit_pair_both(empty_bar(stage));
+                if (++stage == PAIR_STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            umma_commit_pair_both(tfull_bar(acc));
+        }
+        umma_commit_pair_local(drain_bar);
+        mbar_wait_drain(drain_bar, 0, p.timeout_ns);
+    } else if (warp >= 2) {
+        // ---------------------------------------------------------- epilogue (both CTAs)
+        const int quarter = warp & 3;
+        uint8_t *ebuf = smE + (warp - 2) * 2 * EPI_BUF_BYTES;
+        const uint32_t ebuf0 = smem_u32(ebuf);
+        int local = 0, nstore = 0;
+        for (int t = pair; t < p.num_tiles; t += npairs, ++local) {
+            const Tile x = tile_at<MODE>(t, p);
+            const uint32_t acc = local & 1;
+            const uint32_t acc_phase = (local >> 1) & 1;
+            int live = 0;
+            if (lane == 0) live = mbar_wait(tfull_bar(acc), acc_phase, w) ? 1 : 0;
+            if (!__shfl_sync(0xffffffffu, live, 0)) break;
+            tc_fence_after();
+            const int row0 = x.m * PAIR_BM + static_cast<int>(rank) * 128 + quarter * 32;
+            const bool rows_live = row0 < p.c;
+            const uint32_t trow = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
+#pragma unroll 1
+            for (int sub = 0; sub < BN / STORE_COLS; ++sub) {
+                uint32_t v[STORE_COLS];
+                tmem_ld32(trow + sub * STORE_COLS, v);
+                tmem_ld32(trow + sub * STORE_COLS + 32, v + 32);
+                tmem_wait_ld();
+                if (sub == BN / STORE_COLS - 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
+                }
+                const int col = x.n * BN + sub * STORE_COLS;
+                if (!rows_live || col >= p.n_out) continue;
+                const uint32_t buf = ebuf0 + (nstore & 1) * EPI_BUF_BYTES;
+                if (lane == 0) bulk_wait_read<1>();
+                __syncwarp();
+                const uint32_t rowaddr = buf + lane * 128u;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    st_shared_v4(rowaddr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4),
+                                 pack_bf16x2(v[8 * j + 0], v[8 * j + 1]), pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                                 pack_bf16x2(v[8 * j + 4], v[8 * j + 5]), pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+                }
+                fence_proxy_async_shared();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&p.tmY[x.r], buf, col, row0);
+                    bulk_commit();
+                }
+                ++nstore;
+            }
+        }
+        if (lane == 0) bulk_wait_all();
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    cluster_sync_all();  // neither CTA leaves while the pair's MMAs may touch its memory
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    }
+}
+
 }  // namespace
+
+int max_pair_clusters(int mode)
+{
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    cudaError_t e;
+    if (mode == MODE_AG) {
+        e = cudaFuncSetAttribute(ub_gemm_pair_kernel<MODE_AG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 PAIR_SMEM_BYTES);
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n, ub_gemm_pair_kernel<MODE_AG>, &cfg);
+    } else {
+        e = cudaFuncSetAttribute(ub_gemm_pair_kernel<MODE_RS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 PAIR_SMEM_BYTES);
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n, ub_gemm_pair_kernel<MODE_RS>, &cfg);
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+cudaError_t launch_gemm_pair(const GemmParams &p, int mode, int clusters, cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
+    if (mode == MODE_AG) {
+        e = cudaFuncSetAttribute(ub_gemm_pair_kernel<MODE_AG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 PAIR_SMEM_BYTES);
+        if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, ub_gemm_pair_kernel<MODE_AG>, p);
+    } else {
+        e = cudaFuncSetAttribute(ub_gemm_pair_kernel<MODE_RS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 PAIR_SMEM_BYTES);
+        if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, ub_gemm_pair_kernel<MODE_RS>, p);
+    }
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
 
 cudaError_t launch_gemm(const GemmParams &p, int mode, int grid, cudaStream_t stream)
 {

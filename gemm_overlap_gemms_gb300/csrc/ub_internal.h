@@ -28,6 +28,18 @@ constexpr int SMEM_BYTES = 1024 /* alignment slack */ + STAGES * (A_STAGE_BYTES 
                            EPI_WARPS * 2 * EPI_BUF_BYTES + 256 /* barriers */;
 constexpr int TMEM_COLS = 2 * BN;  // two accumulators
 
+// CTA-pair variant (tcgen05 cta_group::2): a cluster of two CTAs on neighbouring SMs
+// owns a 256 x 256 output tile. Each CTA loads its own 128 rows of A and its own
+// 128-row half of B per k-block (32 KiB instead of 48 KiB), the even CTA issues one
+// 256x256x16 MMA that reads both CTAs' shared memory, and each CTA's TMEM receives its
+// 128 rows. Less shared memory per stage leaves room for 6 stages.
+constexpr int PAIR_BM = 256;             // rows of a pair tile (128 per CTA)
+constexpr int PAIR_STAGES = 6;
+constexpr int PAIR_A_BYTES = 128 * BK * 2;
+constexpr int PAIR_B_BYTES = 128 * BK * 2;  // this CTA's half of the 256-row B tile
+constexpr int PAIR_SMEM_BYTES = 1024 + PAIR_STAGES * (PAIR_A_BYTES + PAIR_B_BYTES) +
+                                EPI_WARPS * 2 * EPI_BUF_BYTES + 256;
+
 enum Mode : int { MODE_AG = 0, MODE_RS = 1 };
 
 // Kernel parameters, passed by value as a __grid_constant__ (tensor maps must live
@@ -54,6 +66,13 @@ struct GemmParams {
 
 // Launch the persistent GEMM (mode MODE_AG or MODE_RS) with `grid` CTAs on `stream`.
 cudaError_t launch_gemm(const GemmParams &p, int mode, int grid, cudaStream_t stream);
+
+// Launch the CTA-pair variant with `clusters` clusters of two CTAs. The tensor maps of
+// B must have 128-row boxes and m_tiles must count 256-row pair tiles.
+cudaError_t launch_gemm_pair(const GemmParams &p, int mode, int clusters, cudaStream_t stream);
+
+// Clusters of two CTAs of the pair kernel that can be resident at once (0 on error).
+int max_pair_clusters(int mode);
 
 // Record the message ub_last_error() returns on this host thread.
 void set_last_error(const char *msg);

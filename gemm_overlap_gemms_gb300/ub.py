@@ -27,7 +27,8 @@ ERRORS = {
     -9: "UB_ERR_CUDA", -10: "UB_ERR_TIMEOUT",
 }
 CODES = {v: k for k, v in ERRORS.items()}
-OPTIONS = {"sm_margin": 1, "timeout_ns": 2, "self_rank": 3, "drop_flag": 4, "profile": 5}
+OPTIONS = {"sm_margin": 1, "timeout_ns": 2, "self_rank": 3, "drop_flag": 4, "profile": 5,
+           "cta_pair": 6}
 OPS = {"ag": 0, "rs": 1}
 MAX_TP = 8
 EXPORTS = [

@@ -74,7 +74,9 @@ enum {
     UB_OPT_SELF_RANK = 3,  /* ring start of ag_gemm: the chunk read in place; default 0 */
     UB_OPT_DROP_FLAG = 4,  /* fault injection on the host: the next ag_gemm skips the
                               readiness-flag write of this chunk (-1 = off, one-shot) */
-    UB_OPT_PROFILE = 5     /* 1 = time every GEMM kernel launch with CUDA events */
+    UB_OPT_PROFILE = 5,    /* 1 = time every GEMM kernel launch with CUDA events */
+    UB_OPT_CTA_PAIR = 6    /* 1 (default) = 256x256 tiles on CTA pairs (tcgen05 cta_group::2),
+                              0 = 128x256 tiles on single CTAs; results are identical */
 };
 
 /* Operation ids for ub_kernel_time. */

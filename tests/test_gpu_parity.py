@@ -51,13 +51,15 @@ def test_tiny_workload_ag_and_rs():
 SWEEP_C = [1, 2, 127, 128, 129, 255, 300]
 
 
+@pytest.mark.parametrize("pair", [1, 0])
 @pytest.mark.parametrize("tp", [1, 2, 4])
-def test_ag_active_T_sweep(tp):
+def test_ag_active_T_sweep(tp, pair):
     H, N = 256, 384            # two N tiles, the second one partial
     cap = tp * 320
     g = synth.generator(seed=11)
     Wt = synth.normal_bf16((N, H), H ** -0.5, g)
     with ub.UserBuffer([cap, H], tp) as buf:
+        buf.set_option("cta_pair", pair)
         for c in SWEEP_C + [cap // tp]:
             T = c * tp
             buf.buffer().view(torch.int16).fill_(-1)
@@ -74,13 +76,15 @@ def test_ag_active_T_sweep(tp):
         assert buf.counters()["device_allocations"] == 2
 
 
+@pytest.mark.parametrize("pair", [1, 0])
 @pytest.mark.parametrize("tp,K", [(1, 512), (2, 512), (4, 200)])
-def test_rs_active_T_sweep(tp, K):
+def test_rs_active_T_sweep(tp, K, pair):
     H = 256 + 64                # one full and one partial N tile
     cap = tp * 320
     g = synth.generator(seed=12)
     Bt = [synth.normal_bf16((H, K), K ** -0.5, g) for _ in range(tp)]
     with ub.UserBuffer([cap, H], tp) as buf:
+        buf.set_option("cta_pair", pair)
         for c in SWEEP_C + [cap // tp]:
             T = c * tp
             buf.set_active_shape([T, H])
@@ -92,7 +96,8 @@ def test_rs_active_T_sweep(tp, K):
         assert buf.query_status() == ub.UB_OK
 
 
-def test_integer_inputs_are_bit_exact():
+@pytest.mark.parametrize("pair", [1, 0])
+def test_integer_inputs_are_bit_exact(pair):
     tp, H, N, K = 4, 256, 264, 136
     T = tp * 133
     g = synth.generator(seed=13)
@@ -101,6 +106,7 @@ def test_integer_inputs_are_bit_exact():
     A = [synth.small_int_bf16((T, K), -3, 3, g) for _ in range(tp)]
     Bt = [synth.small_int_bf16((H, K), -3, 3, g) for _ in range(tp)]
     with ub.UserBuffer([T, H], tp) as buf:
+        buf.set_option("cta_pair", pair)
         Y = run_ag(buf, shards, Wt)
         Ys, _ = run_rs(buf, A, Bt)
     _, Yref = oracle_ag(shards, Wt)
@@ -138,9 +144,11 @@ def test_deterministic_and_independent_of_ring_start_and_margin():
     A, Bt = synth.rs_inputs(T, K, H, tp, g)
     outs = []
     with ub.UserBuffer([T, H], tp) as buf:
-        for self_rank, margin in [(0, 0), (0, 0), (2, 0), (3, 100)]:
+        for self_rank, margin, pair in [(0, 0, 1), (0, 0, 1), (2, 0, 1), (3, 100, 1), (1, 0, 0),
+                                        (0, 7, 0)]:
             buf.set_option("self_rank", self_rank)
             buf.set_option("sm_margin", margin)
+            buf.set_option("cta_pair", pair)
             Y = run_ag(buf, shards, Wt)
             R, _ = run_rs(buf, A, Bt)
             outs.append((Y.view(torch.int16).clone(), [r.view(torch.int16).clone() for r in R]))
@@ -206,7 +214,8 @@ def test_rejects_misaligned_and_wrong_shapes():
 
 # ------------------------------------------------------------------ bounded waits
 
-def test_dropped_flag_times_out_and_the_handle_recovers():
+@pytest.mark.parametrize("pair", [1, 0])
+def test_dropped_flag_times_out_and_the_handle_recovers(pair):
     """Fault injected on the host: the readiness flag of chunk 1 is never written. The
     kernel's bounded wait must expire, report UB_ERR_TIMEOUT, and leave the context and
     handle usable for the next call."""
@@ -215,6 +224,7 @@ def test_dropped_flag_times_out_and_the_handle_recovers():
     g = synth.generator(seed=17)
     shards, Wt = synth.ag_inputs(T, H, N, tp, g)
     with ub.UserBuffer([T, H], tp) as buf:
+        buf.set_option("cta_pair", pair)
         buf.set_option("timeout_ns", 20_000_000)
         buf.set_option("drop_flag", 1)
         run_ag(buf, shards, Wt)
