@@ -65,8 +65,10 @@ def parse():
                     help="time one op of the workload at one T only (small profiling case)")
     ap.add_argument("--case-T", type=int, default=8192)
     ap.add_argument("--case-reps", type=int, default=3)
-    ap.add_argument("--cta-pair", type=int, default=1, choices=[0, 1],
-                    help="1: 256x256 tiles on CTA pairs (default); 0: 128x256 tiles on single CTAs")
+    ap.add_argument("--cta-pair", type=int, default=-1, choices=[-1, 0, 1],
+                    help="-1: chosen per call (default); 1: 256x256 tiles on CTA pairs; 0: single CTAs")
+    ap.add_argument("--streamk", type=int, default=-1, choices=[-1, 0, 1],
+                    help="-1: chosen per call (default); 1: stream-K over all pairs; 0: whole tiles")
     return ap.parse_args()
 
 
@@ -223,6 +225,7 @@ class SwigluWorkload:
         self.Yrs = torch.empty((cap, H), dtype=torch.bfloat16, device=device)
         self.buf = ub.UserBuffer([cap, H], tp)
         self.buf.set_option("cta_pair", CTA_PAIR)
+        self.buf.set_option("streamk", STREAMK)
 
     def shards(self, i):
         T, tp = self.Ts[i], self.w.tp
@@ -264,24 +267,52 @@ def time_steps(fn, steps, warmup, stream, world):
 
 def e2e_measure(wl, steps, warmup, stream, world):
     """Same step, with each microbatch's activations copied in from pinned host memory
-    and its outputs copied back, inside the timed region."""
+    and its outputs copied back, inside the timed region. Copies run on their own
+    streams so that microbatch i+1's inputs and microbatch i-1's outputs move while
+    microbatch i computes (outputs alternate between two device buffers)."""
     hX = [x.cpu().pin_memory() for x in wl.X]
     hA = [[a.cpu().pin_memory() for a in As] for As in wl.A]
-    N, H = wl.w.ag_n[0], wl.w.hidden
+    N, H, cap = wl.w.ag_n[0], wl.w.hidden, wl.w.max_tokens
     hY1 = [torch.empty((T, N), dtype=torch.bfloat16).pin_memory() for T in wl.Ts]
     hY2 = [torch.empty((T, H), dtype=torch.bfloat16).pin_memory() for T in wl.Ts]
     h2d = sum(x.numel() * 2 for x in hX) + sum(a.numel() * 2 for As in hA for a in As)
     d2h = sum(y.numel() * 2 for y in hY1) + sum(y.numel() * 2 for y in hY2)
+    dev = wl.W1.device
+    Y1 = [wl.Y1, torch.empty((cap, N), dtype=torch.bfloat16, device=dev)]
+    Y2 = [wl.Yrs, torch.empty((cap, H), dtype=torch.bfloat16, device=dev)]
+    s_in = torch.cuda.Stream(dev)
+    s_out = torch.cuda.Stream(dev)
+    n = len(wl.Ts)
+    computed = [torch.cuda.Event() for _ in range(n)]
+    landed = [torch.cuda.Event() for _ in range(n)]
+    drained = [torch.cuda.Event() for _ in range(2)]
+    for e in computed + drained:
+        e.record(stream)
+    tp = wl.w.tp
 
     def step():
-        with torch.cuda.stream(stream):
-            for i, T in enumerate(wl.Ts):
+        s_in.wait_stream(stream)   # nothing of this step starts before the timer's start event
+        for i, T in enumerate(wl.Ts):
+            b = i & 1
+            c = T // tp
+            with torch.cuda.stream(s_in):
+                s_in.wait_event(computed[i])          # the previous step is done with X[i], A[i]
                 wl.X[i].copy_(hX[i], non_blocking=True)
-                for j in range(wl.w.tp):
+                for j in range(tp):
                     wl.A[i][j].copy_(hA[i][j], non_blocking=True)
-                wl.run_mb(i, stream)
-                hY1[i].copy_(wl.Y1[:T], non_blocking=True)
-                hY2[i].copy_(wl.Yrs[:T], non_blocking=True)
+                landed[i].record(s_in)
+            stream.wait_event(landed[i])
+            stream.wait_event(drained[b])              # output buffer b has been read back
+            wl.buf.set_active_shape([T, H])
+            wl.buf.ag_gemm(wl.shards(i), wl.W1, Y1[b], stream=stream)
+            wl.buf.gemm_rs(wl.A[i], wl.B, [Y2[b][r * c:(r + 1) * c] for r in range(tp)], stream=stream)
+            computed[i].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(computed[i])
+                hY1[i].copy_(Y1[b][:T], non_blocking=True)
+                hY2[i].copy_(Y2[b][:T], non_blocking=True)
+                drained[b].record(s_out)
+        stream.wait_stream(s_out)
 
     ms = time_steps(step, steps, warmup, stream, world)
     return ms, h2d, d2h
@@ -531,6 +562,7 @@ def run_case(args):
     g = synth.generator(dev)
     buf = ub.UserBuffer([w.max_tokens, H], tp)
     buf.set_option("cta_pair", args.cta_pair)
+    buf.set_option("streamk", args.streamk)
     buf.set_active_shape([T, H])
     c = T // tp
     if args.case == "ag":
@@ -556,17 +588,19 @@ def run_case(args):
     ms, n = buf.kernel_time(args.case)
     assert buf.query_status() == ub.UB_OK
     buf.close()
-    print(json.dumps({"case": args.case, "T": T, "cta_pair": args.cta_pair, "launches": n, "avg_us": 1e3 * ms / max(n, 1),
+    print(json.dumps({"case": args.case, "T": T, "cta_pair": args.cta_pair, "streamk": args.streamk, "launches": n, "avg_us": 1e3 * ms / max(n, 1),
                       "tflops": flops * n / (ms / 1e3) / 1e12 if ms > 0 else None}))
 
 
-CTA_PAIR = 1
+CTA_PAIR = -1
+STREAMK = -1
 
 
 def main():
-    global CTA_PAIR
+    global CTA_PAIR, STREAMK
     args = parse()
     CTA_PAIR = args.cta_pair
+    STREAMK = args.streamk
     if args.case:
         run_case(args)
     elif args.impl == "reference":

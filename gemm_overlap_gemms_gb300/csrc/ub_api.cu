@@ -128,7 +128,10 @@ struct ub_handle {
     int tp = 1;
     int64_t T = 0;  // active tokens
     void *ub = nullptr;      // [max_tokens, hidden] bf16
-    uint32_t *ctrl = nullptr;  // flags[UB_MAX_TP] | abort | status
+    uint32_t *ctrl = nullptr;  // flags[UB_MAX_TP] | abort | status | ... | stream-K flags (from word 64)
+    size_t ctrl_bytes = 0;
+    float *ws = nullptr;       // stream-K partial tiles of the pair kernel
+    int max_pairs = 0;         // pairs the workspace has room for
     cudaStream_t side = nullptr;
     cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
     uint32_t epoch = 0;
@@ -138,7 +141,8 @@ struct ub_handle {
     int64_t self_rank = 0;
     int64_t drop_flag = -1;
     int64_t profile = 0;
-    int64_t cta_pair = 1;
+    int64_t cta_pair = -1;  // -1 = chosen per call
+    int64_t streamk = -1;   // -1 = chosen per call
     int pair_clusters[2] = {-1, -1};  // resident clusters of the pair kernel, per mode
     ub_counters_t counters{};
     std::vector<CacheEntry> cache;
@@ -151,6 +155,7 @@ namespace {
 uint32_t *flags_of(ub_handle *h) { return h->ctrl; }
 uint32_t *abort_of(ub_handle *h) { return h->ctrl + UB_MAX_TP; }
 int32_t *status_of(ub_handle *h) { return reinterpret_cast<int32_t *>(h->ctrl + UB_MAX_TP + 1); }
+uint32_t *ws_flags_of(ub_handle *h) { return h->ctrl + 64; }
 
 // Makes the handle's device current for the duration of a call.
 struct DeviceGuard {
@@ -184,6 +189,7 @@ int clusters_for(ub_handle *h, int mode, int num_tiles)
     if (h->pair_clusters[mode] < 0) h->pair_clusters[mode] = ubk::max_pair_clusters(mode);
     int g = (h->sm_count - static_cast<int>(h->sm_margin)) / 2;
     if (h->pair_clusters[mode] > 0 && g > h->pair_clusters[mode]) g = h->pair_clusters[mode];
+    if (g > h->max_pairs) g = h->max_pairs;
     if (g < 1) g = 1;
     return g < num_tiles ? g : num_tiles;
 }
@@ -211,9 +217,67 @@ GemmParams *cache_insert(ub_handle *h, std::vector<const void *> key, const Gemm
     return &h->cache[victim].params;
 }
 
+// Stream-K partition of a pair-kernel call: as many resident pairs as allowed, but
+// never fewer than MIN_KBLOCKS_PER_PAIR k-blocks each.
+// Launch shape of a pair-kernel call. With stream-K every tile's k-blocks are spread
+// evenly over the pairs; without it each pair takes whole tiles in strided order.
+void set_pairs(ub_handle *h, GemmParams &p, int mode, bool streamk)
+{
+    const int64_t tiles = p.region_tile0[p.n_regions];
+    const int64_t units = tiles * p.k_blocks;
+    int64_t np = clusters_for(h, mode, 1 << 30);
+    int64_t dp = tiles;
+    if (streamk) {
+        dp = 0;
+        const int64_t by_work = units / ubk::MIN_KBLOCKS_PER_PAIR;
+        if (np > by_work) np = by_work;
+    } else if (np > tiles) {
+        np = tiles;
+    }
+    if (np < 1) np = 1;
+    p.num_pairs = static_cast<int>(np);
+    p.dp_tiles = static_cast<int>(dp);
+    p.ws = h->ws;
+    p.ws_flags = ws_flags_of(h);
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Which kernel runs a call, from a wave-count cost model measured on GB300 (one unit =
+// the time of one 128x256 tile on one SM, the same as one 256x256 tile on a pair):
+//   single CTAs, chunk-aligned 128-row tiles:  waves
+//   CTA pairs, whole 256-row tiles:            0.91 * waves (a third less L2 traffic)
+//   CTA pairs, stream-K:                       0.91 * 1.7 * tiles / pairs
+// Stream-K only pays when most pairs would otherwise idle: pairs that share a weight
+// panel drift apart in k and lose L2 reuse. UB_OPT_CTA_PAIR / UB_OPT_STREAMK >= 0 force
+// a choice. The choice depends only on the shapes and the SM count, so results stay
+// bitwise reproducible.
+void choose_path(ub_handle *h, int mode, int64_t single_tiles, int64_t pair_tiles, bool &pair, bool &streamk)
+{
+    const int64_t slots = h->sm_count - h->sm_margin > 0 ? h->sm_count - h->sm_margin : 1;
+    const int64_t np = clusters_for(h, mode, 1 << 30);
+    const double c_single = static_cast<double>(ceil_div(single_tiles, slots));
+    const double c_dp = 0.91 * static_cast<double>(ceil_div(pair_tiles, np));
+    const double c_sk = 0.91 * 1.7 * static_cast<double>(pair_tiles) / static_cast<double>(np);
+    if (h->cta_pair == 0) {
+        pair = false;
+    } else if (h->cta_pair == 1) {
+        pair = true;
+    } else {
+        pair = (c_dp < c_single) || (c_sk < c_single);
+    }
+    if (!pair) {
+        streamk = false;
+    } else if (h->streamk >= 0) {
+        streamk = h->streamk != 0;
+    } else {
+        streamk = c_sk < c_dp;
+    }
+}
+
 int launch(ub_handle *h, const GemmParams &p, int mode, bool pair, cudaStream_t s)
 {
-    const int grid = pair ? clusters_for(h, mode, p.num_tiles) : grid_for(h, p.num_tiles);
+    const int grid = pair ? p.num_pairs : grid_for(h, p.num_tiles);
     ProfileRing &ring = h->prof[mode];
     const bool timed = h->profile != 0 && ring.count < kMaxProfiled;
     if (timed) {
@@ -301,15 +365,21 @@ int ub_create(int64_t max_tokens, int64_t hidden, int tp, ub_dtype_t dtype, ub_h
     e = cudaMalloc(&h->ub, static_cast<size_t>(max_tokens) * hidden * 2);
     if (e != cudaSuccess) return cleanup(cuda_fail(e, "cudaMalloc(user buffer)"));
     ++h->counters.device_allocations;
-    e = cudaMalloc(reinterpret_cast<void **>(&h->ctrl), 256);
+    h->max_pairs = h->sm_count / 2 > 0 ? h->sm_count / 2 : 1;
+    h->ctrl_bytes = 256 + static_cast<size_t>(h->max_pairs) * 2 * ubk::EPI_WARPS * sizeof(uint32_t);
+    e = cudaMalloc(reinterpret_cast<void **>(&h->ctrl), h->ctrl_bytes);
     if (e != cudaSuccess) return cleanup(cuda_fail(e, "cudaMalloc(control block)"));
+    ++h->counters.device_allocations;
+    e = cudaMalloc(reinterpret_cast<void **>(&h->ws),
+                   static_cast<size_t>(h->max_pairs) * 2 * ubk::PARTIAL_FLOATS * sizeof(float));
+    if (e != cudaSuccess) return cleanup(cuda_fail(e, "cudaMalloc(stream-K workspace)"));
     ++h->counters.device_allocations;
     e = cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking);
     if (e != cudaSuccess) return cleanup(cuda_fail(e, "cudaStreamCreateWithFlags"));
     e = cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming);
     if (e != cudaSuccess) return cleanup(cuda_fail(e, "cudaEventCreateWithFlags"));
-    e = cudaMemsetAsync(h->ctrl, 0, 256, h->side);
+    e = cudaMemsetAsync(h->ctrl, 0, h->ctrl_bytes, h->side);
     if (e == cudaSuccess) e = cudaStreamSynchronize(h->side);
     if (e != cudaSuccess) return cleanup(cuda_fail(e, "clearing the control block"));
     *out = h;
@@ -329,6 +399,7 @@ int ub_destroy(ub_handle_t h)
     if (h->ev_join) cudaEventDestroy(h->ev_join);
     if (h->side) cudaStreamDestroy(h->side);
     if (h->ctrl) cudaFree(h->ctrl);
+    if (h->ws) cudaFree(h->ws);
     if (h->ub) cudaFree(h->ub);
     delete h;
     return UB_OK;
@@ -384,7 +455,7 @@ int ub_grid_ctas(ub_handle_t h, int *ctas)
 {
     if (int rc = check_handle(h)) return rc;
     DeviceGuard g(h->device);
-    if (ctas) *ctas = h->cta_pair ? 2 * clusters_for(h, ubk::MODE_RS, 1 << 30) : grid_for(h, 1 << 30);
+    if (ctas) *ctas = h->cta_pair != 0 ? 2 * clusters_for(h, ubk::MODE_RS, 1 << 30) : grid_for(h, 1 << 30);
     return UB_OK;
 }
 
@@ -408,7 +479,12 @@ int ag_gemm(ub_handle_t h, const void *const *shards, const void *Wt, int64_t N,
     const int self = static_cast<int>(h->self_rank);
     char *ub = static_cast<char *>(h->ub);
 
-    const bool pair = h->cta_pair != 0;
+    const int64_t n_tiles = (N + ubk::BN - 1) / ubk::BN;
+    int64_t pair_rows_tiles = ceil_div(c, ubk::PAIR_BM);  // regions: self chunk, after it, before it
+    if (T - (self + 1) * c > 0) pair_rows_tiles += ceil_div(T - (self + 1) * c, ubk::PAIR_BM);
+    if (self * c > 0) pair_rows_tiles += ceil_div(self * c, ubk::PAIR_BM);
+    bool pair = false, streamk = false;
+    choose_path(h, ubk::MODE_AG, tp * ceil_div(c, ubk::BM) * n_tiles, pair_rows_tiles * n_tiles, pair, streamk);
     const int bm = pair ? ubk::PAIR_BM : ubk::BM;      // rows of a tile
     const int bbox = pair ? ubk::BN / 2 : ubk::BN;    // rows of a B box (one CTA's half in a pair)
     std::vector<const void *> key;
@@ -425,17 +501,6 @@ int ag_gemm(ub_handle_t h, const void *const *shards, const void *Wt, int64_t N,
     if (!pp) {
         GemmParams p;
         memset(&p, 0, sizeof p);
-        for (int r = 0; r < tp; ++r) {
-            // Chunk r is read from the user buffer, except the self chunk, which the
-            // kernel reads in place from its shard while the copy engine stages it.
-            const void *src = r == self ? shards[r] : static_cast<const void *>(ub + r * c * H * 2);
-            if (int rc = encode_2d(&p.tmA[r], src, H, c, H * 2, ubk::BK, ubk::BM)) return rc;
-            if (int rc = encode_2d(&p.tmY[r], static_cast<char *>(Y) + r * c * N * 2, N, c, N * 2,
-                                   ubk::STORE_COLS, 32))
-                return rc;
-        }
-        if (int rc = encode_2d(&p.tmB[0], Wt, H, N, H * 2, ubk::BK, bbox)) return rc;
-        h->counters.tensor_map_encodes += 2 * tp + 1;
         p.tp = tp;
         p.c = static_cast<int>(c);
         p.n_out = static_cast<int>(N);
@@ -445,6 +510,46 @@ int ag_gemm(ub_handle_t h, const void *const *shards, const void *Wt, int64_t N,
         p.n_tiles = static_cast<int>((N + ubk::BN - 1) / ubk::BN);
         p.num_tiles = tp * p.m_tiles * p.n_tiles;
         p.self_rank = self;
+        if (!pair) {
+            for (int r = 0; r < tp; ++r) {
+                // Chunk r is read from the user buffer, except the self chunk, which the
+                // kernel reads in place from its shard while the copy engine stages it.
+                const void *src = r == self ? shards[r] : static_cast<const void *>(ub + r * c * H * 2);
+                if (int rc = encode_2d(&p.tmA[r], src, H, c, H * 2, ubk::BK, ubk::BM)) return rc;
+                if (int rc = encode_2d(&p.tmY[r], static_cast<char *>(Y) + r * c * N * 2, N, c, N * 2,
+                                       ubk::STORE_COLS, 32))
+                    return rc;
+            }
+            h->counters.tensor_map_encodes += 2 * tp;
+        } else {
+            // Row regions in ring order: the self chunk (read in place), the chunks after
+            // it, the chunks before it (both from the user buffer).
+            struct {
+                int64_t row0, rows;
+                const void *src;
+                int ub_backed;
+            } reg[3] = {{self * c, c, shards[self], 0},
+                        {(self + 1) * c, T - (self + 1) * c, ub + (self + 1) * c * H * 2, 1},
+                        {0, self * c, ub, 1}};
+            int nreg = 0;
+            for (auto &rgn : reg) {
+                if (rgn.rows <= 0) continue;
+                if (int rc = encode_2d(&p.tmA[nreg], rgn.src, H, rgn.rows, H * 2, ubk::BK, 128)) return rc;
+                if (int rc = encode_2d(&p.tmY[nreg], static_cast<char *>(Y) + rgn.row0 * N * 2, N, rgn.rows, N * 2,
+                                       ubk::STORE_COLS, 32))
+                    return rc;
+                p.region_row0[nreg] = static_cast<int>(rgn.row0);
+                p.region_rows[nreg] = static_cast<int>(rgn.rows);
+                p.region_ub[nreg] = rgn.ub_backed;
+                p.region_tile0[nreg + 1] =
+                    p.region_tile0[nreg] + static_cast<int>((rgn.rows + ubk::PAIR_BM - 1) / ubk::PAIR_BM) * p.n_tiles;
+                ++nreg;
+            }
+            p.n_regions = nreg;
+            h->counters.tensor_map_encodes += 2 * nreg;
+        }
+        if (int rc = encode_2d(&p.tmB[0], Wt, H, N, H * 2, ubk::BK, bbox)) return rc;
+        h->counters.tensor_map_encodes += 1;
         pp = cache_insert(h, std::move(key), p);
     }
     GemmParams &p = *pp;
@@ -452,6 +557,7 @@ int ag_gemm(ub_handle_t h, const void *const *shards, const void *Wt, int64_t N,
     p.abort_word = abort_of(h);
     p.status = status_of(h);
     p.timeout_ns = static_cast<uint64_t>(h->timeout_ns);
+    if (pair) set_pairs(h, p, ubk::MODE_AG, streamk);
     const uint32_t epoch = ++h->epoch;
     p.epoch = epoch;
     const int64_t drop = h->drop_flag;
@@ -502,7 +608,10 @@ int gemm_rs(ub_handle_t h, const void *const *A, const void *const *Bt, int64_t 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int64_t T = h->T, H = h->hidden, c = T / tp;
 
-    const bool pair = h->cta_pair != 0;
+    const int64_t n_tiles = (H + ubk::BN - 1) / ubk::BN;
+    bool pair = false, streamk = false;
+    choose_path(h, ubk::MODE_RS, tp * ceil_div(c, ubk::BM) * n_tiles, ceil_div(T, ubk::PAIR_BM) * n_tiles, pair,
+                streamk);
     const int bm = pair ? ubk::PAIR_BM : ubk::BM;
     const int bbox = pair ? ubk::BN / 2 : ubk::BN;
     std::vector<const void *> key;
@@ -524,8 +633,17 @@ int gemm_rs(ub_handle_t h, const void *const *A, const void *const *Bt, int64_t 
             if (int rc = encode_2d(&p.tmA[j], A[j], K, T, K * 2, ubk::BK, ubk::BM)) return rc;
             if (int rc = encode_2d(&p.tmB[j], Bt[j], K, H, K * 2, ubk::BK, bbox)) return rc;
             if (int rc = encode_2d(&p.tmY[j], Y_shards[j], H, c, H * 2, ubk::STORE_COLS, 32)) return rc;
+            p.y_ptr[j] = Y_shards[j];
         }
         h->counters.tensor_map_encodes += 3 * tp;
+        // The pair kernel tiles all T rows as one region; stores split at chunk ends.
+        p.n_regions = 1;
+        p.region_row0[0] = 0;
+        p.region_rows[0] = static_cast<int>(T);
+        p.region_ub[0] = 0;
+        p.region_tile0[1] = static_cast<int>((T + ubk::PAIR_BM - 1) / ubk::PAIR_BM) *
+                            static_cast<int>((H + ubk::BN - 1) / ubk::BN);
+        p.ldy = static_cast<int>(H);
         p.tp = tp;
         p.c = static_cast<int>(c);
         p.n_out = static_cast<int>(H);
@@ -542,6 +660,7 @@ int gemm_rs(ub_handle_t h, const void *const *A, const void *const *Bt, int64_t 
     p.abort_word = abort_of(h);
     p.status = status_of(h);
     p.timeout_ns = static_cast<uint64_t>(h->timeout_ns);
+    if (pair) set_pairs(h, p, ubk::MODE_RS, streamk);
     p.epoch = ++h->epoch;
     if (int rc = launch(h, p, ubk::MODE_RS, pair, s)) return rc;
     ++h->counters.rs_calls;
@@ -574,8 +693,12 @@ int ub_set_option(ub_handle_t h, int key, int64_t val)
         h->profile = val;
         return UB_OK;
     case UB_OPT_CTA_PAIR:
-        if (val != 0 && val != 1) return fail(UB_ERR_ARG, "cta_pair must be 0 or 1");
+        if (val < -1 || val > 1) return fail(UB_ERR_ARG, "cta_pair must be -1, 0 or 1");
         h->cta_pair = val;
+        return UB_OK;
+    case UB_OPT_STREAMK:
+        if (val < -1 || val > 1) return fail(UB_ERR_ARG, "streamk must be -1, 0 or 1");
+        h->streamk = val;
         return UB_OK;
     default:
         return fail(UB_ERR_ARG, "unknown option %d", key);
@@ -593,6 +716,7 @@ int ub_get_option(ub_handle_t h, int key, int64_t *val)
     case UB_OPT_DROP_FLAG: *val = h->drop_flag; return UB_OK;
     case UB_OPT_PROFILE: *val = h->profile; return UB_OK;
     case UB_OPT_CTA_PAIR: *val = h->cta_pair; return UB_OK;
+    case UB_OPT_STREAMK: *val = h->streamk; return UB_OK;
     default: return fail(UB_ERR_ARG, "unknown option %d", key);
     }
 }

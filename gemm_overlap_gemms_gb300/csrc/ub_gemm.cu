@@ -594,11 +594,112 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_kernel(const __grid_consta
 
 // ------------------------------------------------------------------ the CTA-pair kernel
 
+// Stream-K partition (of the tiles not handed out whole): the work is the list of
+// (pair tile, k-block) units, tiles in order; pair p owns one contiguous range of it. A tile may therefore be split between
+// neighbouring pairs: the pair holding the tile's first k-blocks (the end of its own
+// range) finishes the tile; every other pair holding part of it (always at the start of
+// its range) writes its fp32 partial tile to the workspace first thing and publishes
+// it with the call's epoch. The finisher adds the partials in pair order, so the result
+// is deterministic for a given launch shape.
+struct Range {
+    int start, end;
+};
+
+__device__ __forceinline__ Range pair_range(int pr, int num_pairs, int units)
+{
+    const int base = units / num_pairs;
+    const int extra = units - base * num_pairs;
+    Range r;
+    r.start = pr * base + (pr < extra ? pr : extra);
+    r.end = r.start + base + (pr < extra ? 1 : 0);
+    return r;
+}
+
+// The work of one pair: its data-parallel tiles (whole, strided, so that the tiles in
+// flight across all pairs stay close together and share L2), then its stream-K range of
+// the remaining tiles' k-blocks.
+struct SegIter {
+    int pair, num_pairs, kb, dp_tiles, i;
+    Range sk;  // in units of the stream-K part: (tile - dp_tiles) * kb + k-block
+    int u;
+    __device__ __forceinline__ SegIter(const GemmParams &p, int pr)
+        : pair(pr), num_pairs(p.num_pairs), kb(p.k_blocks), dp_tiles(p.dp_tiles), i(0)
+    {
+        const int sk_units = (p.region_tile0[p.n_regions] - p.dp_tiles) * p.k_blocks;
+        sk = pair_range(pr, p.num_pairs, sk_units);
+        u = sk.start;
+    }
+    // Next segment: tile t, k-blocks [k0, k1). False when the pair is done.
+    __device__ __forceinline__ bool next(int &t, int &k0, int &k1)
+    {
+        const int tdp = pair + i * num_pairs;
+        if (tdp < dp_tiles) {
+            ++i;
+            t = tdp;
+            k0 = 0;
+            k1 = kb;
+            return true;
+        }
+        if (u >= sk.end) return false;
+        const int tt = u / kb;
+        k0 = u - tt * kb;
+        k1 = min(kb, k0 + (sk.end - u));
+        u += k1 - k0;
+        t = dp_tiles + tt;
+        return true;
+    }
+};
+
+struct PTile {
+    int q;  // region
+    int m;  // 256-row pair tile inside the region
+    int n;  // 256-column tile
+};
+
+__device__ __forceinline__ PTile pair_tile_at(int t, const GemmParams &p)
+{
+    int q = 0;
+    while (q + 1 < p.n_regions && t >= p.region_tile0[q + 1]) ++q;
+    const int rem = t - p.region_tile0[q];
+    PTile x;
+    x.q = q;
+    x.m = rem / p.n_tiles;
+    x.n = rem - x.m * p.n_tiles;
+    return x;
+}
+
+__device__ __forceinline__ void st_release_u32(uint32_t *ptr, uint32_t v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
+}
+
+// Wait until a partial tile of this call is published (bounded, abort-aware).
+__device__ bool wait_partial(const uint32_t *flag, const WaitCtx &w)
+{
+    uint64_t t0 = 0;
+    for (uint32_t n = 0;; ++n) {
+        uint32_t v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+        if (v == w.epoch) return true;
+        if (n == 0) {
+            t0 = global_timer();
+        } else if ((n & 15u) == 0) {
+            if (call_aborted(w)) return false;
+            if (global_timer() - t0 > w.timeout_ns) {
+                raise_error(w, UB_ERR_TIMEOUT);
+                return false;
+            }
+        }
+        __nanosleep(64);
+    }
+}
+
 // Same roles as ub_gemm_kernel, on a cluster of two CTAs that share 256 x 256 tiles.
 // Both CTAs run a producer (own A rows, own half of B) whose loads complete on the even
 // CTA's `full` barrier; the even CTA's MMA thread issues the cta_group::2 MMAs and
 // multicasts stage releases and accumulator-ready signals to both CTAs; each CTA's
-// epilogue drains its own 128 TMEM lanes and reports back to the even CTA.
+// epilogue drains its own 128 TMEM lanes and reports back to the even CTA. Work is
+// split across pairs by stream-K (above); rows are tiled by region (see GemmParams).
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1) ub_gemm_pair_kernel(const __grid_constant__ GemmParams p)
 {
@@ -621,8 +722,8 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_pair_kernel(const __grid_c
     const int lane = threadIdx.x & 31;
     const uint32_t rank = cluster_rank();  // 0 = even CTA (issues the MMAs), 1 = its peer
     const int pair = blockIdx.x >> 1;
-    const int npairs = gridDim.x >> 1;
     const WaitCtx w{p.abort_word, p.status, p.timeout_ns, p.epoch};
+    const int KB = p.k_blocks;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < PAIR_STAGES; ++s) {
@@ -649,19 +750,24 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_pair_kernel(const __grid_c
         uint32_t stage = 0, phase = 0, ready = 0;
         int issued = 0;
         bool ok = true;
-        for (int t = pair; ok && t < p.num_tiles; t += npairs) {
-            const Tile x = tile_at<MODE>(t, p);
-            if (MODE == MODE_AG && x.r != p.self_rank && !((ready >> x.r) & 1u)) {
-                if (!wait_flag(p.flags + x.r, w)) {
-                    ok = false;
-                    break;
+        const int half = static_cast<int>(rank) * 128;
+        SegIter it(p, pair);
+        int t, k0, k1;
+        while (ok && it.next(t, k0, k1)) {
+            const PTile x = pair_tile_at(t, p);
+            const int lrow = x.m * PAIR_BM + half;  // row of this CTA's half inside the region
+            if (MODE == MODE_AG && p.region_ub[x.q]) {
+                const int g0 = p.region_row0[x.q] + lrow;
+                const int g1 = min(g0 + 128, p.region_row0[x.q] + p.region_rows[x.q]) - 1;
+                for (int ch = g0 / p.c; ok && g0 <= g1 && ch <= g1 / p.c; ++ch) {
+                    if ((ready >> ch) & 1u) continue;
+                    if (!wait_flag(p.flags + ch, w)) ok = false;
+                    ready |= 1u << ch;
                 }
-                ready |= 1u << x.r;
+                if (!ok) break;
             }
-            const int half = static_cast<int>(rank) * 128;
-            const int arow = (MODE == MODE_AG ? x.m * PAIR_BM : x.r * p.c + x.m * PAIR_BM) + half;
             const int brow = x.n * BN + half;
-            for (int kb = 0; kb < p.k_blocks; ++kb) {
+            for (int kb = k0; kb < k1; ++kb) {
                 if (!mbar_wait(empty_bar(stage), phase ^ 1u, w)) {
                     ok = false;
                     break;
@@ -670,7 +776,7 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_pair_kernel(const __grid_c
                 const CUtensorMap *mb;
                 int kx;
                 if (MODE == MODE_AG) {
-                    ma = &p.tmA[x.r];
+                    ma = &p.tmA[x.q];
                     mb = &p.tmB[0];
                     kx = kb * BK;
                 } else {
@@ -681,7 +787,7 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_pair_kernel(const __grid_c
                 }
                 const uint32_t fb = map_to_rank(full_bar(stage), 0);
                 if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * (PAIR_A_BYTES + PAIR_B_BYTES));
-                tma_load_2d_pair(smem_u32(smA + stage * PAIR_A_BYTES), ma, fb, kx, arow);
+                tma_load_2d_pair(smem_u32(smA + stage * PAIR_A_BYTES), ma, fb, kx, lrow);
                 tma_load_2d_pair(smem_u32(smB + stage * PAIR_B_BYTES), mb, fb, kx, brow);
                 ++issued;
                 if (++stage == PAIR_STAGES) {
@@ -702,7 +808,9 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_pair_kernel(const __grid_c
         uint32_t stage = 0, phase = 0;
         int local = 0;
         bool ok = true;
-        for (int t = pair; ok && t < p.num_tiles; t += npairs, ++local) {
+        SegIter it(p, pair);
+        int t, k0, k1;
+        for (; ok && it.next(t, k0, k1); ++local) {
             const uint32_t acc = local & 1;
             const uint32_t acc_phase = (local >> 1) & 1;
             if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, w)) {
@@ -711,7 +819,7 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_pair_kernel(const __grid_c
             }
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + acc * BN;
-            for (int kb = 0; kb < p.k_blocks; ++kb) {
+            for (int kb = k0; kb < k1; ++kb) {
                 if (!mbar_wait(full_bar(stage), phase, w)) {
                     ok = false;
                     break;
@@ -722,7 +830,7 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_pair_kernel(const __grid_c
 #pragma unroll
                 for (int k = 0; k < BK / 16; ++k)
                     umma_bf16_pair(d_tmem, smem_desc_sw128(a0 + 32u * k), smem_desc_sw128(b0 + 32u * k),
-                                   (kb | k) != 0 ? 1u : 0u);
+                                   (kb != k0 || k != 0) ? 1u : 0u);
                 umma_commit_pair_both(empty_bar(stage));
                 if (++stage == PAIR_STAGES) {
                     stage = 0;
@@ -739,18 +847,79 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_pair_kernel(const __grid_c
         const int quarter = warp & 3;
         uint8_t *ebuf = smE + (warp - 2) * 2 * EPI_BUF_BYTES;
         const uint32_t ebuf0 = smem_u32(ebuf);
+        const int my_slot = (pair * 2 + static_cast<int>(rank)) * EPI_WARPS + quarter;
         int local = 0, nstore = 0;
-        for (int t = pair; t < p.num_tiles; t += npairs, ++local) {
-            const Tile x = tile_at<MODE>(t, p);
+        SegIter it(p, pair);
+        int t, k0, k1;
+        for (; it.next(t, k0, k1); ++local) {
+            const PTile x = pair_tile_at(t, p);
             const uint32_t acc = local & 1;
             const uint32_t acc_phase = (local >> 1) & 1;
             int live = 0;
             if (lane == 0) live = mbar_wait(tfull_bar(acc), acc_phase, w) ? 1 : 0;
             if (!__shfl_sync(0xffffffffu, live, 0)) break;
             tc_fence_after();
-            const int row0 = x.m * PAIR_BM + static_cast<int>(rank) * 128 + quarter * 32;
-            const bool rows_live = row0 < p.c;
             const uint32_t trow = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
+            const int lrow0 = x.m * PAIR_BM + static_cast<int>(rank) * 128 + quarter * 32;  // inside the region
+            const int prow = quarter * 32 + lane;  // this thread's row inside the CTA's 128
+
+            if (k0 > 0) {
+                // Not the tile's first k-blocks: publish the fp32 partial for the finisher.
+                float4 *dst = reinterpret_cast<float4 *>(p.ws + static_cast<size_t>(pair * 2 + rank) * PARTIAL_FLOATS);
+#pragma unroll 1
+                for (int sub = 0; sub < BN / STORE_COLS; ++sub) {
+                    uint32_t v[STORE_COLS];
+                    tmem_ld32(trow + sub * STORE_COLS, v);
+                    tmem_ld32(trow + sub * STORE_COLS + 32, v + 32);
+                    tmem_wait_ld();
+                    if (sub == BN / STORE_COLS - 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
+                    }
+#pragma unroll
+                    for (int i = 0; i < STORE_COLS / 4; ++i)
+                        __stcg(dst + (sub * (STORE_COLS / 4) + i) * 128 + prow,
+                               make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                           __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])));
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    __threadfence();
+                    st_release_u32(p.ws_flags + my_slot, p.epoch);
+                }
+                continue;
+            }
+
+            // This pair finishes the tile: collect the partials of the pairs that hold the
+            // rest of its k-blocks (pair + 1, pair + 2, ... in order).
+            int n_contrib = 0;
+            if (k1 < KB) {
+                const int tile_end = (t - p.dp_tiles + 1) * KB;  // in stream-K units
+                const int sk_units = (p.region_tile0[p.n_regions] - p.dp_tiles) * KB;
+                bool okw = true;
+                for (int cp = pair + 1; cp < p.num_pairs; ++cp) {
+                    if (pair_range(cp, p.num_pairs, sk_units).start >= tile_end) break;
+                    int got = 1;
+                    if (lane == 0) {
+                        const uint32_t *f = p.ws_flags + (cp * 2 + static_cast<int>(rank)) * EPI_WARPS + quarter;
+                        got = wait_partial(f, w) ? 1 : 0;
+                    }
+                    if (!__shfl_sync(0xffffffffu, got, 0)) {
+                        okw = false;
+                        break;
+                    }
+                    ++n_contrib;
+                }
+                if (!okw) {
+                    // Abort: release the accumulator so the MMA side is not left waiting.
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
+                    break;
+                }
+            }
+
 #pragma unroll 1
             for (int sub = 0; sub < BN / STORE_COLS; ++sub) {
                 uint32_t v[STORE_COLS];
@@ -762,22 +931,65 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_pair_kernel(const __grid_c
                     __syncwarp();
                     if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
                 }
+                for (int ci = 1; ci <= n_contrib; ++ci) {
+                    const float4 *src = reinterpret_cast<const float4 *>(
+                        p.ws + static_cast<size_t>((pair + ci) * 2 + rank) * PARTIAL_FLOATS);
+#pragma unroll
+                    for (int i = 0; i < STORE_COLS / 4; ++i) {
+                        const float4 q = __ldcg(src + (sub * (STORE_COLS / 4) + i) * 128 + prow);
+                        v[4 * i + 0] = __float_as_uint(__uint_as_float(v[4 * i + 0]) + q.x);
+                        v[4 * i + 1] = __float_as_uint(__uint_as_float(v[4 * i + 1]) + q.y);
+                        v[4 * i + 2] = __float_as_uint(__uint_as_float(v[4 * i + 2]) + q.z);
+                        v[4 * i + 3] = __float_as_uint(__uint_as_float(v[4 * i + 3]) + q.w);
+                    }
+                }
                 const int col = x.n * BN + sub * STORE_COLS;
-                if (!rows_live || col >= p.n_out) continue;
+                if (col >= p.n_out || lrow0 >= p.region_rows[x.q]) continue;
+                // Pack to bf16 (row-major, 8 x 16 bytes per thread).
+                uint32_t pk[STORE_COLS / 2];
+#pragma unroll
+                for (int j = 0; j < STORE_COLS / 2; ++j) pk[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+
+                int chunk = 0;  // output block of a TMA store (RS), or -1 = direct stores
+                int brow = lrow0;
+                if (MODE == MODE_RS) {
+                    const int last = min(lrow0 + 31, p.region_rows[0] - 1);
+                    chunk = lrow0 / p.c;
+                    if (last / p.c != chunk) {
+                        chunk = -1;
+                    } else {
+                        brow = lrow0 - chunk * p.c;
+                    }
+                } else {
+                    chunk = x.q;
+                }
+                if (chunk < 0) {
+                    // The 32 rows cross a chunk end: each thread writes its own row to the
+                    // output block that owns it.
+                    const int row = lrow0 + lane;
+                    if (row < p.region_rows[0]) {
+                        const int r = row / p.c;
+                        const int i = row - r * p.c;
+                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.y_ptr[r]) +
+                                                               static_cast<size_t>(i) * p.ldy + col);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            if (col + 8 * j < p.n_out) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                    }
+                    continue;
+                }
                 const uint32_t buf = ebuf0 + (nstore & 1) * EPI_BUF_BYTES;
                 if (lane == 0) bulk_wait_read<1>();
                 __syncwarp();
                 const uint32_t rowaddr = buf + lane * 128u;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    st_shared_v4(rowaddr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4),
-                                 pack_bf16x2(v[8 * j + 0], v[8 * j + 1]), pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
-                                 pack_bf16x2(v[8 * j + 4], v[8 * j + 5]), pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
-                }
+                for (int j = 0; j < 8; ++j)
+                    st_shared_v4(rowaddr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4), pk[4 * j],
+                                 pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
                 fence_proxy_async_shared();
                 __syncwarp();
                 if (lane == 0) {
-                    tma_store_2d(&p.tmY[x.r], buf, col, row0);
+                    tma_store_2d(&p.tmY[chunk], buf, col, brow);
                     bulk_commit();
                 }
                 ++nstore;

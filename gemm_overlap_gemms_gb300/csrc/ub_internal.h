@@ -39,6 +39,11 @@ constexpr int PAIR_A_BYTES = 128 * BK * 2;
 constexpr int PAIR_B_BYTES = 128 * BK * 2;  // this CTA's half of the 256-row B tile
 constexpr int PAIR_SMEM_BYTES = 1024 + PAIR_STAGES * (PAIR_A_BYTES + PAIR_B_BYTES) +
                                 EPI_WARPS * 2 * EPI_BUF_BYTES + 256;
+// One CTA's share of a partial pair tile: 128 rows x 256 fp32 columns.
+constexpr int PARTIAL_FLOATS = 128 * BN;
+// Stream-K: a pair's share of the k-blocks is never cut below this many k-blocks
+// (fewer clusters are launched instead), so every partial tile carries real work.
+constexpr int MIN_KBLOCKS_PER_PAIR = 16;
 
 enum Mode : int { MODE_AG = 0, MODE_RS = 1 };
 
@@ -62,6 +67,27 @@ struct GemmParams {
     int n_tiles;                 // ceil(n_out / BN)
     int num_tiles;               // tp * m_tiles * n_tiles
     int self_rank;               // AG: chunk read in place, no flag wait
+
+    // ---- CTA-pair kernel only: row regions and the stream-K split.
+    // The pair kernel tiles rows by region instead of by chunk. RS has one region,
+    // [0, T): its tiles may span chunks, and the epilogue splits stores at chunk ends.
+    // AG has one region per source of A rows, in ring order: the self chunk (read in
+    // place from its shard), then the chunks after it, then the chunks before it (both
+    // read from the user buffer, each row only once its chunk's flag is set). Region q
+    // uses tmA[q] and tmY[q], whose row extents end exactly at the region's end.
+    int n_regions;
+    int region_row0[3];          // first row of region q (global row of the active prefix)
+    int region_rows[3];
+    int region_ub[3];            // 1: rows come from the user buffer (flag waits)
+    int region_tile0[4];         // first pair tile of region q; [n_regions] = total
+    int num_pairs;               // clusters launched
+    int dp_tiles;                // tiles [0, dp_tiles) go whole to pairs in strided order
+                                 // (pair p: p, p + num_pairs, ...); the rest are split by
+                                 // stream-K over the k-blocks
+    int ldy;                     // RS: leading dimension of Y_shards (= hidden)
+    void *y_ptr[UB_MAX_TP];      // RS: Y_shards[r], for stores that cross a chunk end
+    float *ws;                   // stream-K partial tiles: [num_pairs][2][256/4][128][4] fp32
+    uint32_t *ws_flags;          // [num_pairs][2][EPI_WARPS]: epoch of the partial written
 };
 
 // Launch the persistent GEMM (mode MODE_AG or MODE_RS) with `grid` CTAs on `stream`.

@@ -75,8 +75,12 @@ enum {
     UB_OPT_DROP_FLAG = 4,  /* fault injection on the host: the next ag_gemm skips the
                               readiness-flag write of this chunk (-1 = off, one-shot) */
     UB_OPT_PROFILE = 5,    /* 1 = time every GEMM kernel launch with CUDA events */
-    UB_OPT_CTA_PAIR = 6    /* 1 (default) = 256x256 tiles on CTA pairs (tcgen05 cta_group::2),
-                              0 = 128x256 tiles on single CTAs; results are identical */
+    UB_OPT_CTA_PAIR = 6,   /* -1 (default) = chosen per call from the tile counts; 1 = 256x256
+                              tiles on CTA pairs (tcgen05 cta_group::2); 0 = chunk-aligned
+                              128x256 tiles on single CTAs */
+    UB_OPT_STREAMK = 7     /* pair tiles only. -1 (default) = chosen per call; 1 = every tile's
+                              k-blocks spread evenly over all pairs (stream-K, fixed-order
+                              fp32 fix-up: deterministic); 0 = whole tiles only */
 };
 
 /* Operation ids for ub_kernel_time. */
