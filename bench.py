@@ -44,10 +44,10 @@ KERNEL_SRC = os.path.join(ROOT, "gemm_overlap_gemms_gb300", "csrc", "ub_gemm.cu"
 # per active token of the captured launch, and the kernel source they were taken on.
 # Traffic is reported as null once the kernel source no longer matches.
 NCU_TRAFFIC = {
-    "rs": {"sha256_16": "25d40b573b83d0ce", "bytes": 1129.3e6, "T": 8192,
-           "source": "profiles/ub_gemm_kernel_rs_swiglu_fc2_T8192.md"},
-    "ag": {"sha256_16": "25d40b573b83d0ce", "bytes": 595.4e6, "T": 8192,
-           "source": "profiles/ub_gemm_kernel_ag_swiglu_fc1_T8192.md"},
+    "rs": {"sha256_16": "d611b2b1ac61bb3d", "bytes": 1156.0e6, "T": 8192,
+           "source": "profiles/ub_gemm_pair_kernel_rs_swiglu_fc2_T8192.md"},
+    "ag": {"sha256_16": "d611b2b1ac61bb3d", "bytes": 561.1e6, "T": 8192,
+           "source": "profiles/ub_gemm_pair_kernel_ag_swiglu_fc1_T8192.md"},
 }
 
 
@@ -67,6 +67,7 @@ def parse():
     ap.add_argument("--case-reps", type=int, default=3)
     ap.add_argument("--cta-pair", type=int, default=-1, choices=[-1, 0, 1],
                     help="-1: chosen per call (default); 1: 256x256 tiles on CTA pairs; 0: single CTAs")
+    ap.add_argument("--copy-streams", type=int, default=4)
     ap.add_argument("--streamk", type=int, default=-1, choices=[-1, 0, 1],
                     help="-1: chosen per call (default); 1: stream-K over all pairs; 0: whole tiles")
     return ap.parse_args()
@@ -396,7 +397,7 @@ def run_ours(args):
     dom = "rs" if rs_ms >= ag_ms else "ag"
     achieved = kernels[dom]["tflops"]
     tr = kernel_traffic(dom, float(np.mean(wl.Ts)))
-    roofline = {"bound": "tensor", "kernel": "ub_gemm_kernel<%s>" % ("MODE_RS" if dom == "rs" else "MODE_AG"),
+    roofline = {"bound": "tensor", "kernel": "ub_gemm_pair_kernel<%s>" % ("MODE_RS" if dom == "rs" else "MODE_AG"),
                 "achieved": achieved, "peak": tensor_peak, "unit": "TFLOP/s",
                 "frac": achieved / tensor_peak if achieved else None,
                 "traffic": tr["bytes_per_launch"] if tr else None, "traffic_detail": tr,
@@ -563,6 +564,7 @@ def run_case(args):
     buf = ub.UserBuffer([w.max_tokens, H], tp)
     buf.set_option("cta_pair", args.cta_pair)
     buf.set_option("streamk", args.streamk)
+    buf.set_option("copy_streams", args.copy_streams)
     buf.set_active_shape([T, H])
     c = T // tp
     if args.case == "ag":
@@ -588,7 +590,8 @@ def run_case(args):
     ms, n = buf.kernel_time(args.case)
     assert buf.query_status() == ub.UB_OK
     buf.close()
-    print(json.dumps({"case": args.case, "T": T, "cta_pair": args.cta_pair, "streamk": args.streamk, "launches": n, "avg_us": 1e3 * ms / max(n, 1),
+    print(json.dumps({"case": args.case, "T": T, "cta_pair": args.cta_pair, "streamk": args.streamk,
+                      "copy_streams": args.copy_streams, "launches": n, "avg_us": 1e3 * ms / max(n, 1),
                       "tflops": flops * n / (ms / 1e3) / 1e12 if ms > 0 else None}))
 
 

@@ -132,7 +132,10 @@ struct ub_handle {
     size_t ctrl_bytes = 0;
     float *ws = nullptr;       // stream-K partial tiles of the pair kernel
     int max_pairs = 0;         // pairs the workspace has room for
-    cudaStream_t side = nullptr;
+    cudaStream_t side = nullptr;                  // copy stream 0; also status reads
+    cudaStream_t extra_side[UB_MAX_TP] = {};      // copy streams 1.. (created on demand)
+    cudaEvent_t ev_join_extra[UB_MAX_TP] = {};
+    int64_t copy_streams = 1;  // raised to min(tp, 4) at creation
     cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
     uint32_t epoch = 0;
     // options
@@ -376,6 +379,7 @@ int ub_create(int64_t max_tokens, int64_t hidden, int tp, ub_dtype_t dtype, ub_h
     ++h->counters.device_allocations;
     e = cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking);
     if (e != cudaSuccess) return cleanup(cuda_fail(e, "cudaStreamCreateWithFlags"));
+    if (int rc = ub_set_option(h, UB_OPT_COPY_STREAMS, tp < 4 ? tp : 4)) return cleanup(rc);
     e = cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming);
     if (e != cudaSuccess) return cleanup(cuda_fail(e, "cudaEventCreateWithFlags"));
@@ -398,6 +402,13 @@ int ub_destroy(ub_handle_t h)
     if (h->ev_fork) cudaEventDestroy(h->ev_fork);
     if (h->ev_join) cudaEventDestroy(h->ev_join);
     if (h->side) cudaStreamDestroy(h->side);
+    for (int i = 0; i < UB_MAX_TP; ++i) {
+        if (h->extra_side[i]) {
+            cudaStreamSynchronize(h->extra_side[i]);
+            cudaStreamDestroy(h->extra_side[i]);
+        }
+        if (h->ev_join_extra[i]) cudaEventDestroy(h->ev_join_extra[i]);
+    }
     if (h->ctrl) cudaFree(h->ctrl);
     if (h->ws) cudaFree(h->ws);
     if (h->ub) cudaFree(h->ub);
@@ -563,26 +574,34 @@ int ag_gemm(ub_handle_t h, const void *const *shards, const void *Wt, int64_t N,
     const int64_t drop = h->drop_flag;
     h->drop_flag = -1;
 
-    // Fork the copy-engine stream off `s`: it starts once the work already queued on
+    // Fork the copy-engine streams off `s`: they start once the work already queued on
     // `s` (which may still read the buffer) is done.
+    const int ncs = static_cast<int>(h->copy_streams < tp ? h->copy_streams : tp);
+    auto copy_stream = [&](int i) { return i == 0 ? h->side : h->extra_side[i]; };
     UB_CUDA(cudaEventRecord(h->ev_fork, s));
-    UB_CUDA(cudaStreamWaitEvent(h->side, h->ev_fork, 0));
+    for (int i = 0; i < ncs; ++i) UB_CUDA(cudaStreamWaitEvent(copy_stream(i), h->ev_fork, 0));
     // Ring order after the self rank; the self chunk (read in place by the GEMM) last.
+    // With several copy streams the chunks are dealt round-robin over them.
     for (int q = 1; q <= tp; ++q) {
         const int r = (self + q) % tp;
+        cudaStream_t cs = copy_stream((q - 1) % ncs);
         UB_CUDA(cudaMemcpyAsync(ub + r * c * H * 2, shards[r], static_cast<size_t>(c * H * 2),
-                                cudaMemcpyDeviceToDevice, h->side));
+                                cudaMemcpyDeviceToDevice, cs));
         if (r != drop) {
-            CUresult cr = driver().write_value32(reinterpret_cast<CUstream>(h->side),
+            CUresult cr = driver().write_value32(reinterpret_cast<CUstream>(cs),
                                                  reinterpret_cast<CUdeviceptr>(flags_of(h) + r), epoch,
                                                  CU_STREAM_WRITE_VALUE_DEFAULT);
             if (cr != CUDA_SUCCESS) return fail(UB_ERR_CUDA, "cuStreamWriteValue32 failed (%d)", (int)cr);
         }
     }
     int rc = launch(h, p, ubk::MODE_AG, pair, s);
-    // Join the side stream back into `s` even if the launch failed.
+    // Join the copy streams back into `s` even if the launch failed.
     UB_CUDA(cudaEventRecord(h->ev_join, h->side));
     UB_CUDA(cudaStreamWaitEvent(s, h->ev_join, 0));
+    for (int i = 1; i < ncs; ++i) {
+        UB_CUDA(cudaEventRecord(h->ev_join_extra[i], h->extra_side[i]));
+        UB_CUDA(cudaStreamWaitEvent(s, h->ev_join_extra[i], 0));
+    }
     if (rc != UB_OK) return rc;
     ++h->counters.ag_calls;
     h->counters.last_T = T;
@@ -700,6 +719,16 @@ int ub_set_option(ub_handle_t h, int key, int64_t val)
         if (val < -1 || val > 1) return fail(UB_ERR_ARG, "streamk must be -1, 0 or 1");
         h->streamk = val;
         return UB_OK;
+    case UB_OPT_COPY_STREAMS: {
+        if (val < 1 || val > UB_MAX_TP) return fail(UB_ERR_ARG, "copy_streams must be in [1, %d]", UB_MAX_TP);
+        DeviceGuard g(h->device);
+        for (int i = 1; i < val; ++i) {
+            if (!h->extra_side[i]) UB_CUDA(cudaStreamCreateWithFlags(&h->extra_side[i], cudaStreamNonBlocking));
+            if (!h->ev_join_extra[i]) UB_CUDA(cudaEventCreateWithFlags(&h->ev_join_extra[i], cudaEventDisableTiming));
+        }
+        h->copy_streams = val;
+        return UB_OK;
+    }
     default:
         return fail(UB_ERR_ARG, "unknown option %d", key);
     }
@@ -717,6 +746,7 @@ int ub_get_option(ub_handle_t h, int key, int64_t *val)
     case UB_OPT_PROFILE: *val = h->profile; return UB_OK;
     case UB_OPT_CTA_PAIR: *val = h->cta_pair; return UB_OK;
     case UB_OPT_STREAMK: *val = h->streamk; return UB_OK;
+    case UB_OPT_COPY_STREAMS: *val = h->copy_streams; return UB_OK;
     default: return fail(UB_ERR_ARG, "unknown option %d", key);
     }
 }

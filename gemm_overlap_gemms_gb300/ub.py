@@ -28,7 +28,7 @@ ERRORS = {
 }
 CODES = {v: k for k, v in ERRORS.items()}
 OPTIONS = {"sm_margin": 1, "timeout_ns": 2, "self_rank": 3, "drop_flag": 4, "profile": 5,
-           "cta_pair": 6, "streamk": 7}
+           "cta_pair": 6, "streamk": 7, "copy_streams": 8}
 OPS = {"ag": 0, "rs": 1}
 MAX_TP = 8
 EXPORTS = [

@@ -146,15 +146,17 @@ def test_deterministic_and_consistent_across_launch_shapes():
     g = synth.generator(seed=15)
     shards, Wt = synth.ag_inputs(T, H, N, tp, g)
     A, Bt = synth.rs_inputs(T, K, H, tp, g)
-    configs = [(0, 0, 1, 1), (0, 0, 1, 1), (2, 0, 1, 1), (3, 100, 1, 1), (1, 0, 0, 1), (0, 7, 0, 1),
-               (1, 0, 0, 1), (0, 0, 1, 0), (2, 90, 1, 0)]
+    configs = [(0, 0, 1, 1, 1), (0, 0, 1, 1, 3), (2, 0, 1, 1, 1), (3, 100, 1, 1, 2),
+               (1, 0, 0, 1, 1), (0, 7, 0, 1, 4), (1, 0, 0, 1, 2), (0, 0, 1, 0, 1), (2, 90, 1, 0, 4),
+               (0, 0, -1, -1, 1)]
     outs = []
     with ub.UserBuffer([T, H], tp) as buf:
-        for self_rank, margin, pair, streamk in configs:
+        for self_rank, margin, pair, streamk, copy_streams in configs:
             buf.set_option("self_rank", self_rank)
             buf.set_option("sm_margin", margin)
             buf.set_option("cta_pair", pair)
             buf.set_option("streamk", streamk)
+            buf.set_option("copy_streams", copy_streams)
             Y = run_ag(buf, shards, Wt)
             R, _ = run_rs(buf, A, Bt)
             outs.append((Y.view(torch.int16).clone(), [r.view(torch.int16).clone() for r in R]))
