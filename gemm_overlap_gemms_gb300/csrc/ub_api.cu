@@ -220,61 +220,67 @@ GemmParams *cache_insert(ub_handle *h, std::vector<const void *> key, const Gemm
     return &h->cache[victim].params;
 }
 
-// Stream-K partition of a pair-kernel call: as many resident pairs as allowed, but
-// never fewer than MIN_KBLOCKS_PER_PAIR k-blocks each.
-// Launch shape of a pair-kernel call. With stream-K every tile's k-blocks are spread
-// evenly over the pairs; without it each pair takes whole tiles in strided order.
-void set_pairs(ub_handle *h, GemmParams &p, int mode, bool streamk)
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// How many k-pieces the last wave's tiles are cut into: enough to give every pair one
+// piece, at most MAX_TAIL_SPLIT, each at least MIN_KBLOCKS_PER_PIECE k-blocks long.
+int64_t tail_split_for(int64_t tiles, int64_t np, int64_t kb)
+{
+    const int64_t rem = tiles % np;
+    if (rem == 0) return 1;
+    int64_t s = np / rem;
+    if (s > ubk::MAX_TAIL_SPLIT) s = ubk::MAX_TAIL_SPLIT;
+    if (s > kb / ubk::MIN_KBLOCKS_PER_PIECE) s = kb / ubk::MIN_KBLOCKS_PER_PIECE;
+    return s < 1 ? 1 : s;
+}
+
+// Launch shape of a pair-kernel call: whole tiles in strided waves, and (with the
+// split on) the last, partial wave's tiles cut into k-pieces over the idle pairs.
+void set_pairs(ub_handle *h, GemmParams &p, int mode, bool split)
 {
     const int64_t tiles = p.region_tile0[p.n_regions];
-    const int64_t units = tiles * p.k_blocks;
     int64_t np = clusters_for(h, mode, 1 << 30);
-    int64_t dp = tiles;
-    if (streamk) {
-        dp = 0;
-        const int64_t by_work = units / ubk::MIN_KBLOCKS_PER_PAIR;
-        if (np > by_work) np = by_work;
-    } else if (np > tiles) {
-        np = tiles;
-    }
+    int64_t sp = split ? tail_split_for(tiles, np, p.k_blocks) : 1;
+    if (sp == 1 && np > tiles) np = tiles;
     if (np < 1) np = 1;
     p.num_pairs = static_cast<int>(np);
-    p.dp_tiles = static_cast<int>(dp);
+    p.dp_tiles = static_cast<int>((tiles / np) * np);
+    p.tail_split = static_cast<int>(sp);
+    if (p.dp_tiles == tiles) p.tail_split = 1;
     p.ws = h->ws;
     p.ws_flags = ws_flags_of(h);
 }
 
-int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
-
 // Which kernel runs a call, from a wave-count cost model measured on GB300 (one unit =
 // the time of one 128x256 tile on one SM, the same as one 256x256 tile on a pair):
-//   single CTAs, chunk-aligned 128-row tiles:  waves
-//   CTA pairs, whole 256-row tiles:            0.91 * waves (a third less L2 traffic)
-//   CTA pairs, stream-K:                       0.91 * 1.7 * tiles / pairs
-// Stream-K only pays when most pairs would otherwise idle: pairs that share a weight
-// panel drift apart in k and lose L2 reuse. UB_OPT_CTA_PAIR / UB_OPT_STREAMK >= 0 force
-// a choice. The choice depends only on the shapes and the SM count, so results stay
-// bitwise reproducible.
-void choose_path(ub_handle *h, int mode, int64_t single_tiles, int64_t pair_tiles, bool &pair, bool &streamk)
+//   single CTAs, chunk-aligned 128-row tiles:    waves
+//   CTA pairs, whole tiles:                      0.91 * waves (a third less L2 traffic)
+//   CTA pairs, last wave split into s k-pieces:  0.91 * (full waves + 1.1 / s)
+// UB_OPT_CTA_PAIR / UB_OPT_STREAMK >= 0 force a choice. The choice depends only on the
+// shapes and the SM count, so results stay bitwise reproducible.
+void choose_path(ub_handle *h, int mode, int64_t single_tiles, int64_t pair_tiles, int64_t kb, bool &pair,
+                 bool &split)
 {
     const int64_t slots = h->sm_count - h->sm_margin > 0 ? h->sm_count - h->sm_margin : 1;
     const int64_t np = clusters_for(h, mode, 1 << 30);
     const double c_single = static_cast<double>(ceil_div(single_tiles, slots));
     const double c_dp = 0.91 * static_cast<double>(ceil_div(pair_tiles, np));
-    const double c_sk = 0.91 * 1.7 * static_cast<double>(pair_tiles) / static_cast<double>(np);
+    const int64_t s = tail_split_for(pair_tiles, np, kb);
+    const double c_split =
+        s > 1 ? 0.91 * (static_cast<double>(pair_tiles / np) + 1.1 / static_cast<double>(s)) : c_dp;
     if (h->cta_pair == 0) {
         pair = false;
     } else if (h->cta_pair == 1) {
         pair = true;
     } else {
-        pair = (c_dp < c_single) || (c_sk < c_single);
+        pair = (c_dp < c_single) || (c_split < c_single);
     }
     if (!pair) {
-        streamk = false;
+        split = false;
     } else if (h->streamk >= 0) {
-        streamk = h->streamk != 0;
+        split = h->streamk != 0;
     } else {
-        streamk = c_sk < c_dp;
+        split = c_split < c_dp;
     }
 }
 
@@ -495,7 +501,8 @@ int ag_gemm(ub_handle_t h, const void *const *shards, const void *Wt, int64_t N,
     if (T - (self + 1) * c > 0) pair_rows_tiles += ceil_div(T - (self + 1) * c, ubk::PAIR_BM);
     if (self * c > 0) pair_rows_tiles += ceil_div(self * c, ubk::PAIR_BM);
     bool pair = false, streamk = false;
-    choose_path(h, ubk::MODE_AG, tp * ceil_div(c, ubk::BM) * n_tiles, pair_rows_tiles * n_tiles, pair, streamk);
+    choose_path(h, ubk::MODE_AG, tp * ceil_div(c, ubk::BM) * n_tiles, pair_rows_tiles * n_tiles,
+                (H + ubk::BK - 1) / ubk::BK, pair, streamk);
     const int bm = pair ? ubk::PAIR_BM : ubk::BM;      // rows of a tile
     const int bbox = pair ? ubk::BN / 2 : ubk::BN;    // rows of a B box (one CTA's half in a pair)
     std::vector<const void *> key;
@@ -629,8 +636,8 @@ int gemm_rs(ub_handle_t h, const void *const *A, const void *const *Bt, int64_t 
 
     const int64_t n_tiles = (H + ubk::BN - 1) / ubk::BN;
     bool pair = false, streamk = false;
-    choose_path(h, ubk::MODE_RS, tp * ceil_div(c, ubk::BM) * n_tiles, ceil_div(T, ubk::PAIR_BM) * n_tiles, pair,
-                streamk);
+    choose_path(h, ubk::MODE_RS, tp * ceil_div(c, ubk::BM) * n_tiles, ceil_div(T, ubk::PAIR_BM) * n_tiles,
+                tp * ((K + ubk::BK - 1) / ubk::BK), pair, streamk);
     const int bm = pair ? ubk::PAIR_BM : ubk::BM;
     const int bbox = pair ? ubk::BN / 2 : ubk::BN;
     std::vector<const void *> key;

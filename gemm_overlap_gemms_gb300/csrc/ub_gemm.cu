@@ -594,40 +594,22 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_kernel(const __grid_consta
 
 // ------------------------------------------------------------------ the CTA-pair kernel
 
-// Stream-K partition (of the tiles not handed out whole): the work is the list of
-// (pair tile, k-block) units, tiles in order; pair p owns one contiguous range of it. A tile may therefore be split between
-// neighbouring pairs: the pair holding the tile's first k-blocks (the end of its own
-// range) finishes the tile; every other pair holding part of it (always at the start of
-// its range) writes its fp32 partial tile to the workspace first thing and publishes
-// it with the call's epoch. The finisher adds the partials in pair order, so the result
-// is deterministic for a given launch shape.
-struct Range {
-    int start, end;
-};
-
-__device__ __forceinline__ Range pair_range(int pr, int num_pairs, int units)
-{
-    const int base = units / num_pairs;
-    const int extra = units - base * num_pairs;
-    Range r;
-    r.start = pr * base + (pr < extra ? pr : extra);
-    r.end = r.start + base + (pr < extra ? 1 : 0);
-    return r;
-}
-
-// The work of one pair: its data-parallel tiles (whole, strided, so that the tiles in
-// flight across all pairs stay close together and share L2), then its stream-K range of
-// the remaining tiles' k-blocks.
+// Work split of the pair kernel. Tiles [0, dp_tiles) go whole to the pairs in strided
+// order (pair p: p, p + P, p + 2P, ...), so the tiles in flight across all pairs stay
+// close together and share L2. The remaining R tiles (fewer than P) form the last wave;
+// with tail_split = s > 1 each of them is cut into s equal k-ranges ("pieces") held by
+// s consecutive pairs, so that up to R * s pairs work on the last wave instead of R.
+// All pieces start together and have the same length, so pairs that share a weight
+// panel stay in step. The pair holding piece 0 finishes the tile: it adds the other
+// pieces' fp32 partials, which their pairs publish in the workspace with the call's
+// epoch, in piece order — a deterministic result for a given launch shape.
 struct SegIter {
-    int pair, num_pairs, kb, dp_tiles, i;
-    Range sk;  // in units of the stream-K part: (tile - dp_tiles) * kb + k-block
-    int u;
+    int pair, num_pairs, kb, dp_tiles, tiles, split, i;
+    bool tail_done;
     __device__ __forceinline__ SegIter(const GemmParams &p, int pr)
-        : pair(pr), num_pairs(p.num_pairs), kb(p.k_blocks), dp_tiles(p.dp_tiles), i(0)
+        : pair(pr), num_pairs(p.num_pairs), kb(p.k_blocks), dp_tiles(p.dp_tiles),
+          tiles(p.region_tile0[p.n_regions]), split(p.tail_split), i(0), tail_done(false)
     {
-        const int sk_units = (p.region_tile0[p.n_regions] - p.dp_tiles) * p.k_blocks;
-        sk = pair_range(pr, p.num_pairs, sk_units);
-        u = sk.start;
     }
     // Next segment: tile t, k-blocks [k0, k1). False when the pair is done.
     __device__ __forceinline__ bool next(int &t, int &k0, int &k1)
@@ -640,12 +622,13 @@ struct SegIter {
             k1 = kb;
             return true;
         }
-        if (u >= sk.end) return false;
-        const int tt = u / kb;
-        k0 = u - tt * kb;
-        k1 = min(kb, k0 + (sk.end - u));
-        u += k1 - k0;
-        t = dp_tiles + tt;
+        if (tail_done) return false;
+        tail_done = true;
+        if (pair >= (tiles - dp_tiles) * split) return false;
+        t = dp_tiles + pair / split;
+        const int q = pair - (pair / split) * split;
+        k0 = q * kb / split;
+        k1 = (q + 1) * kb / split;
         return true;
     }
 };
@@ -864,7 +847,7 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_pair_kernel(const __grid_c
             const int prow = quarter * 32 + lane;  // this thread's row inside the CTA's 128
 
             if (k0 > 0) {
-                // Not the tile's first k-blocks: publish the fp32 partial for the finisher.
+                // Not the tile's first piece: publish the fp32 partial for the finisher.
                 float4 *dst = reinterpret_cast<float4 *>(p.ws + static_cast<size_t>(pair * 2 + rank) * PARTIAL_FLOATS);
 #pragma unroll 1
                 for (int sub = 0; sub < BN / STORE_COLS; ++sub) {
@@ -891,15 +874,12 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_pair_kernel(const __grid_c
                 continue;
             }
 
-            // This pair finishes the tile: collect the partials of the pairs that hold the
-            // rest of its k-blocks (pair + 1, pair + 2, ... in order).
+            // This pair holds piece 0 of the tile: collect the partials of the pairs that
+            // hold its other pieces (pair + 1 ... pair + split - 1, in order).
             int n_contrib = 0;
             if (k1 < KB) {
-                const int tile_end = (t - p.dp_tiles + 1) * KB;  // in stream-K units
-                const int sk_units = (p.region_tile0[p.n_regions] - p.dp_tiles) * KB;
                 bool okw = true;
-                for (int cp = pair + 1; cp < p.num_pairs; ++cp) {
-                    if (pair_range(cp, p.num_pairs, sk_units).start >= tile_end) break;
+                for (int cp = pair + 1; cp < pair + p.tail_split && cp < p.num_pairs; ++cp) {
                     int got = 1;
                     if (lane == 0) {
                         const uint32_t *f = p.ws_flags + (cp * 2 + static_cast<int>(rank)) * EPI_WARPS + quarter;

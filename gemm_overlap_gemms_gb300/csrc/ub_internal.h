@@ -41,9 +41,10 @@ constexpr int PAIR_SMEM_BYTES = 1024 + PAIR_STAGES * (PAIR_A_BYTES + PAIR_B_BYTE
                                 EPI_WARPS * 2 * EPI_BUF_BYTES + 256;
 // One CTA's share of a partial pair tile: 128 rows x 256 fp32 columns.
 constexpr int PARTIAL_FLOATS = 128 * BN;
-// Stream-K: a pair's share of the k-blocks is never cut below this many k-blocks
-// (fewer clusters are launched instead), so every partial tile carries real work.
-constexpr int MIN_KBLOCKS_PER_PAIR = 16;
+// A split tail tile is never cut into pieces of fewer than this many k-blocks.
+constexpr int MIN_KBLOCKS_PER_PIECE = 16;
+// Nor into more than this many pieces.
+constexpr int MAX_TAIL_SPLIT = 8;
 
 enum Mode : int { MODE_AG = 0, MODE_RS = 1 };
 
@@ -82,11 +83,11 @@ struct GemmParams {
     int region_tile0[4];         // first pair tile of region q; [n_regions] = total
     int num_pairs;               // clusters launched
     int dp_tiles;                // tiles [0, dp_tiles) go whole to pairs in strided order
-                                 // (pair p: p, p + num_pairs, ...); the rest are split by
-                                 // stream-K over the k-blocks
+                                 // (pair p: p, p + num_pairs, ...)
+    int tail_split;              // the remaining tiles are cut into this many k-pieces
     int ldy;                     // RS: leading dimension of Y_shards (= hidden)
     void *y_ptr[UB_MAX_TP];      // RS: Y_shards[r], for stores that cross a chunk end
-    float *ws;                   // stream-K partial tiles: [num_pairs][2][256/4][128][4] fp32
+    float *ws;                   // partial tiles of split tail tiles: [num_pairs][2][256/4][128][4] fp32
     uint32_t *ws_flags;          // [num_pairs][2][EPI_WARPS]: epoch of the partial written
 };
 

@@ -78,9 +78,10 @@ enum {
     UB_OPT_CTA_PAIR = 6,   /* -1 (default) = chosen per call from the tile counts; 1 = 256x256
                               tiles on CTA pairs (tcgen05 cta_group::2); 0 = chunk-aligned
                               128x256 tiles on single CTAs */
-    UB_OPT_STREAMK = 7,    /* pair tiles only. -1 (default) = chosen per call; 1 = every tile's
-                              k-blocks spread evenly over all pairs (stream-K, fixed-order
-                              fp32 fix-up: deterministic); 0 = whole tiles only */
+    UB_OPT_STREAMK = 7,    /* pair tiles only. -1 (default) = chosen per call; 1 = the last,
+                              partial wave's tiles are cut into equal k-pieces spread over the
+                              idle pairs (fixed-order fp32 fix-up: deterministic); 0 = whole
+                              tiles only */
     UB_OPT_COPY_STREAMS = 8 /* copy-engine streams the ag_gemm chunk copies are dealt over
                               (round-robin in ring order), 1..UB_MAX_TP; default min(tp, 4) */
 };
