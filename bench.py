@@ -60,6 +60,8 @@ def parse():
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-padded", action="store_true",
+                    help="skip the padded-to-capacity comparator")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--case", choices=["ag", "rs"], default=None,
                     help="time one op of the workload at one T only (small profiling case)")
@@ -319,6 +321,38 @@ def e2e_measure(wl, steps, warmup, stream, world):
     return ms, h2d, d2h
 
 
+def padded_measure(wl, steps, warmup, stream, world):
+    """The same microbatches padded to capacity, the fallback the pages describe when
+    buffers are sized for the maximum token count: every microbatch runs at
+    T = max_tokens, its real tokens first and zeros after them. Returns ms per step."""
+    w = wl.w
+    cap, H, K, tp = w.max_tokens, w.hidden, w.rs_k[0], w.tp
+    dev = wl.W1.device
+    Xp, Ap = [], []
+    for i, T in enumerate(wl.Ts):
+        x = torch.zeros((cap, H), dtype=torch.bfloat16, device=dev)
+        x[:T].copy_(wl.X[i])
+        Xp.append(x)
+        As = []
+        for j in range(tp):
+            a = torch.zeros((cap, K), dtype=torch.bfloat16, device=dev)
+            a[:T].copy_(wl.A[i][j])
+            As.append(a)
+        Ap.append(As)
+    c = cap // tp
+    outs = [wl.Yrs[r * c:(r + 1) * c] for r in range(tp)]
+
+    def step():
+        wl.buf.set_active_shape([cap, H])
+        for i in range(len(wl.Ts)):
+            wl.buf.ag_gemm([Xp[i][r * c:(r + 1) * c] for r in range(tp)], wl.W1, wl.Y1, stream=stream)
+            wl.buf.gemm_rs(Ap[i], wl.B, outs, stream=stream)
+
+    ms = time_steps(step, steps, warmup, stream, world)
+    del Xp, Ap
+    return ms
+
+
 def cpu_baseline(wl, seconds):
     """The oracle as it stands, on a row sample of one microbatch of the workload."""
     import oracle
@@ -413,6 +447,14 @@ def run_ours(args):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e_ms / e_steps}
 
+    padded = None
+    if not args.no_padded:
+        p_steps = max(2, min(args.steps, 5))
+        p_ms = max_over_ranks(padded_measure(wl, p_steps, 1, stream, world), world) / p_steps
+        padded = {"ms_per_step": p_ms, "useful_tflops": flops * world / (p_ms / 1e3) / 1e12,
+                  "active_speedup": p_ms / (ms / args.steps),
+                  "what": "same microbatches padded to max_tokens=%d (real tokens first, zeros "
+                          "after); useful FLOPs only" % w.max_tokens}
     sweep = sweep_points(wl, stream) if args.sweep and rank == 0 else None
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -437,6 +479,7 @@ def run_ours(args):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "padded_comparator": padded,
         "clocks": clk,
         "flops_per_step": {"ag": ag_flops, "rs": rs_flops},
     }

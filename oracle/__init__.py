@@ -19,6 +19,8 @@ What it computes (fp64 accumulation of exactly widened bf16 inputs):
   over ranks, output split by rows).
 * ``check_active_shape`` -- the five constraints of issue #3564, "Constrain the initial
   behavior".
+* ``swiglu`` -- the activation between fc1 and fc2 (the GELU/SwiGLU box of the MLP
+  diagram in discussion #1240): fc1's row is [gate | up] and ``Z = silu(gate) * up``.
 
 Weights are stored out x in (PyTorch ``nn.Linear`` layout): ``Wt`` is ``[N, H]``,
 ``Bt_j`` is ``[H, K]``. bf16 tensors cross the boundary as uint16 bit patterns.
@@ -66,6 +68,9 @@ def _load():
         lib.oracle_gemm_rs.argtypes = [ctypes.c_int, I64, I64, I64, P, P, P, P]
         lib.oracle_gemm_rs_rows.argtypes = [ctypes.c_int, I64, I64, I64, P, P, P, I64,
                                             P, P, P]
+        lib.oracle_silu.restype = ctypes.c_double
+        lib.oracle_silu.argtypes = [ctypes.c_double]
+        lib.oracle_swiglu.argtypes = [P, I64, I64, P]
         lib.oracle_check_active_shape.restype = ctypes.c_int
         lib.oracle_check_active_shape.argtypes = [ctypes.c_int, I64, I64, I64, I64,
                                                   ctypes.c_int]
@@ -200,3 +205,19 @@ def gemm_rs_rows(A_rows, Bt, rows, T: int):
     _load().oracle_gemm_rs_rows(tp, T, K, H, _ptr_array(A_rows), _ptr_array(Bt), _ptr(rows),
                                 rows.size, _ptr(out), _ptr(owner), _ptr(local))
     return out, owner, local
+
+
+def silu(x: float) -> float:
+    """x / (1 + exp(-x)) in double."""
+    return float(_load().oracle_silu(float(x)))
+
+
+def swiglu(Y: np.ndarray) -> np.ndarray:
+    """Z = silu(Y[:, :F]) * Y[:, F:] for fp64 rows Y = [gate | up] of width 2F."""
+    Y = np.ascontiguousarray(Y, dtype=np.float64)
+    rows, two_f = Y.shape
+    assert two_f % 2 == 0
+    F = two_f // 2
+    Z = np.empty((rows, F), dtype=np.float64)
+    _load().oracle_swiglu(_ptr(Y), rows, F, _ptr(Z))
+    return Z

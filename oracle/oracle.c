@@ -198,6 +198,22 @@ void oracle_gemm_rs_rows(int tp, int64_t T, int64_t K, int64_t H,
     }
 }
 
+/* SwiGLU between the column-parallel fc1 and the row-parallel fc2 (the GELU/SwiGLU box
+ * of the MLP diagram in "Do tp overlap support thd..."): fc1's output row holds the
+ * gate half first and the up half second, Y[t] = [g_0..g_{F-1}, u_0..u_{F-1}], and
+ * Z[t][f] = silu(g_f) * u_f with silu(x) = x / (1 + e^{-x}), all in double. */
+double oracle_silu(double x)
+{
+    return x / (1.0 + exp(-x));
+}
+
+void oracle_swiglu(const double *Y, int64_t rows, int64_t F, double *Z)
+{
+    for (int64_t t = 0; t < rows; ++t)
+        for (int64_t f = 0; f < F; ++f)
+            Z[t * F + f] = oracle_silu(Y[t * 2 * F + f]) * Y[t * 2 * F + F + f];
+}
+
 /* Active-shape constraints, in the order the page lists them: two-dimensional,
  * nonzero, within capacity, hidden unchanged, first dimension divisible by tp.
  * Returns 0 when accepted, else the 1-based index of the first violated rule. */

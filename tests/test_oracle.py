@@ -322,3 +322,34 @@ def test_rows_helpers_agree_with_full_products():
 ])
 def test_active_shape_constraints(shape, expect):
     assert oracle.check_active_shape(shape, cap_tokens=32, cap_hidden=16, tp=4) == expect
+
+
+# ---------------------------------------------------------------- SwiGLU
+
+def test_silu_textbook_values_and_identity():
+    # silu(x) = x * sigmoid(x); sigmoid(1) = 0.7310585786300049 (textbook value)
+    assert oracle.silu(0.0) == 0.0
+    assert abs(oracle.silu(1.0) - 0.7310585786300049) < 1e-15
+    assert abs(oracle.silu(-1.0) + 0.2689414213699951) < 1e-15
+    for x in (-30.0, -2.5, -0.1, 0.3, 4.0, 25.0):
+        # silu(x) - silu(-x) = x * (sigmoid(x) + sigmoid(-x)) = x
+        assert abs(oracle.silu(x) - oracle.silu(-x) - x) < 1e-12 * max(1.0, abs(x))
+    assert oracle.silu(-800.0) == 0.0 or abs(oracle.silu(-800.0)) < 1e-300
+    assert oracle.silu(800.0) == 800.0
+
+
+def test_silu_matches_library_routine():
+    x = torch.linspace(-20, 20, 2001, dtype=torch.float64)
+    want = torch.nn.functional.silu(x).numpy()
+    got = np.array([oracle.silu(v) for v in x.tolist()])
+    np.testing.assert_allclose(got, want, rtol=1e-14, atol=1e-300)
+
+
+def test_swiglu_takes_gate_first_then_up():
+    F = 3
+    Y = np.array([[1.0, 0.0, -1.0, 2.0, 5.0, 7.0]])     # gate = (1, 0, -1), up = (2, 5, 7)
+    Z = oracle.swiglu(Y)
+    np.testing.assert_allclose(Z[0], [2 * 0.7310585786300049, 0.0, 7 * -0.2689414213699951], rtol=1e-15)
+    # planted mistake: halves swapped
+    Zs = oracle.swiglu(np.concatenate([Y[:, F:], Y[:, :F]], axis=1))
+    assert not np.allclose(Zs, Z)
