@@ -146,11 +146,11 @@ struct ub_handle {
     int64_t profile = 0;
     int64_t cta_pair = -1;  // -1 = chosen per call
     int64_t streamk = -1;   // -1 = chosen per call
-    int pair_clusters[2] = {-1, -1};  // resident clusters of the pair kernel, per mode
+    int pair_clusters[3] = {-1, -1, -1};  // resident clusters of the pair kernel, per mode
     ub_counters_t counters{};
     std::vector<CacheEntry> cache;
     uint64_t use_clock = 0;
-    ProfileRing prof[2];
+    ProfileRing prof[3];
 };
 
 namespace {
@@ -476,7 +476,10 @@ int ub_grid_ctas(ub_handle_t h, int *ctas)
     return UB_OK;
 }
 
-int ag_gemm(ub_handle_t h, const void *const *shards, const void *Wt, int64_t N, void *Y, void *stream)
+// AG-GEMM, optionally with the SwiGLU epilogue (glu_f > 0: Wt is [2 * glu_f, hidden],
+// gate rows first, and Y receives [T, glu_f]).
+static int ag_gemm_impl(ub_handle_t h, const void *const *shards, const void *Wt, int64_t N, void *Y, void *stream,
+                        int64_t glu_f)
 {
     if (int rc = check_handle(h)) return rc;
     if (!shards || !Wt || !Y) return fail(UB_ERR_ARG, "ag_gemm: null pointer argument");
@@ -496,18 +499,22 @@ int ag_gemm(ub_handle_t h, const void *const *shards, const void *Wt, int64_t N,
     const int self = static_cast<int>(h->self_rank);
     char *ub = static_cast<char *>(h->ub);
 
-    const int64_t n_tiles = (N + ubk::BN - 1) / ubk::BN;
+    const bool glu = glu_f > 0;
+    const int mode = glu ? ubk::MODE_AG_GLU : ubk::MODE_AG;
+    const int64_t n_out = glu ? glu_f : N;                    // columns of Y
+    const int64_t n_tiles = glu ? (glu_f + 127) / 128 : (N + ubk::BN - 1) / ubk::BN;
     int64_t pair_rows_tiles = ceil_div(c, ubk::PAIR_BM);  // regions: self chunk, after it, before it
     if (T - (self + 1) * c > 0) pair_rows_tiles += ceil_div(T - (self + 1) * c, ubk::PAIR_BM);
     if (self * c > 0) pair_rows_tiles += ceil_div(self * c, ubk::PAIR_BM);
     bool pair = false, streamk = false;
-    choose_path(h, ubk::MODE_AG, tp * ceil_div(c, ubk::BM) * n_tiles, pair_rows_tiles * n_tiles,
+    choose_path(h, mode, tp * ceil_div(c, ubk::BM) * n_tiles, pair_rows_tiles * n_tiles,
                 (H + ubk::BK - 1) / ubk::BK, pair, streamk);
+    if (glu) pair = true;  // the fused epilogue needs the pair layout (gate half, up half)
     const int bm = pair ? ubk::PAIR_BM : ubk::BM;      // rows of a tile
     const int bbox = pair ? ubk::BN / 2 : ubk::BN;    // rows of a B box (one CTA's half in a pair)
     std::vector<const void *> key;
     key.reserve(tp + 7);
-    key.push_back(reinterpret_cast<const void *>(uintptr_t(ubk::MODE_AG)));
+    key.push_back(reinterpret_cast<const void *>(uintptr_t(mode)));
     key.push_back(reinterpret_cast<const void *>(uintptr_t(pair)));
     key.push_back(reinterpret_cast<const void *>(uintptr_t(T)));
     key.push_back(reinterpret_cast<const void *>(uintptr_t(N)));
@@ -521,11 +528,12 @@ int ag_gemm(ub_handle_t h, const void *const *shards, const void *Wt, int64_t N,
         memset(&p, 0, sizeof p);
         p.tp = tp;
         p.c = static_cast<int>(c);
-        p.n_out = static_cast<int>(N);
+        p.n_out = static_cast<int>(n_out);
+        p.glu_f = static_cast<int>(glu_f);
         p.k_blocks = static_cast<int>((H + ubk::BK - 1) / ubk::BK);
         p.k_blocks_per_shard = p.k_blocks;
         p.m_tiles = static_cast<int>((c + bm - 1) / bm);
-        p.n_tiles = static_cast<int>((N + ubk::BN - 1) / ubk::BN);
+        p.n_tiles = static_cast<int>(n_tiles);
         p.num_tiles = tp * p.m_tiles * p.n_tiles;
         p.self_rank = self;
         if (!pair) {
@@ -553,8 +561,8 @@ int ag_gemm(ub_handle_t h, const void *const *shards, const void *Wt, int64_t N,
             for (auto &rgn : reg) {
                 if (rgn.rows <= 0) continue;
                 if (int rc = encode_2d(&p.tmA[nreg], rgn.src, H, rgn.rows, H * 2, ubk::BK, 128)) return rc;
-                if (int rc = encode_2d(&p.tmY[nreg], static_cast<char *>(Y) + rgn.row0 * N * 2, N, rgn.rows, N * 2,
-                                       ubk::STORE_COLS, 32))
+                if (int rc = encode_2d(&p.tmY[nreg], static_cast<char *>(Y) + rgn.row0 * n_out * 2, n_out,
+                                       rgn.rows, n_out * 2, ubk::STORE_COLS, 32))
                     return rc;
                 p.region_row0[nreg] = static_cast<int>(rgn.row0);
                 p.region_rows[nreg] = static_cast<int>(rgn.rows);
@@ -575,7 +583,7 @@ int ag_gemm(ub_handle_t h, const void *const *shards, const void *Wt, int64_t N,
     p.abort_word = abort_of(h);
     p.status = status_of(h);
     p.timeout_ns = static_cast<uint64_t>(h->timeout_ns);
-    if (pair) set_pairs(h, p, ubk::MODE_AG, streamk);
+    if (pair) set_pairs(h, p, mode, streamk);
     const uint32_t epoch = ++h->epoch;
     p.epoch = epoch;
     const int64_t drop = h->drop_flag;
@@ -601,7 +609,7 @@ int ag_gemm(ub_handle_t h, const void *const *shards, const void *Wt, int64_t N,
             if (cr != CUDA_SUCCESS) return fail(UB_ERR_CUDA, "cuStreamWriteValue32 failed (%d)", (int)cr);
         }
     }
-    int rc = launch(h, p, ubk::MODE_AG, pair, s);
+    int rc = launch(h, p, mode, pair, s);
     // Join the copy streams back into `s` even if the launch failed.
     UB_CUDA(cudaEventRecord(h->ev_join, h->side));
     UB_CUDA(cudaStreamWaitEvent(s, h->ev_join, 0));
@@ -613,6 +621,18 @@ int ag_gemm(ub_handle_t h, const void *const *shards, const void *Wt, int64_t N,
     ++h->counters.ag_calls;
     h->counters.last_T = T;
     return UB_OK;
+}
+
+int ag_gemm(ub_handle_t h, const void *const *shards, const void *Wt, int64_t N, void *Y, void *stream)
+{
+    return ag_gemm_impl(h, shards, Wt, N, Y, stream, 0);
+}
+
+int ag_gemm_swiglu(ub_handle_t h, const void *const *shards, const void *Wt, int64_t F, void *Z, void *stream)
+{
+    if (F <= 0) return fail(UB_ERR_ZERO, "ag_gemm_swiglu: F = %lld", (long long)F);
+    if (F % 8 != 0) return fail(UB_ERR_ALIGN, "ag_gemm_swiglu: F = %lld is not a multiple of 8", (long long)F);
+    return ag_gemm_impl(h, shards, Wt, 2 * F, Z, stream, F);
 }
 
 int gemm_rs(ub_handle_t h, const void *const *A, const void *const *Bt, int64_t K, void *const *Y_shards,
@@ -788,7 +808,7 @@ int ub_get_counters(ub_handle_t h, ub_counters_t *out)
 int ub_kernel_time(ub_handle_t h, int op, double *total_ms, int64_t *launches)
 {
     if (int rc = check_handle(h)) return rc;
-    if (op != UB_OP_AG && op != UB_OP_RS) return fail(UB_ERR_ARG, "unknown op %d", op);
+    if (op != UB_OP_AG && op != UB_OP_RS && op != UB_OP_AG_SWIGLU) return fail(UB_ERR_ARG, "unknown op %d", op);
     DeviceGuard g(h->device);
     ProfileRing &ring = h->prof[op];
     double sum = 0.0;

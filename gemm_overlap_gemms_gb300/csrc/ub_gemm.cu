@@ -686,6 +686,8 @@ __device__ bool wait_partial(const uint32_t *flag, const WaitCtx &w)
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1) ub_gemm_pair_kernel(const __grid_constant__ GemmParams p)
 {
+    constexpr bool IS_AG = MODE != MODE_RS;     // A rows come from regions of the gathered input
+    constexpr bool GLU = MODE == MODE_AG_GLU;   // B tile = 128 gate rows (even CTA) + 128 up rows (odd CTA)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *smA = base;
@@ -728,7 +730,7 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_pair_kernel(const __grid_c
 
     if (warp == 0 && lane == 0) {
         // ---------------------------------------------------------- producer (both CTAs)
-        const int nmaps = MODE == MODE_AG ? 1 : p.tp;
+        const int nmaps = IS_AG ? 1 : p.tp;
         for (int i = 0; i < nmaps; ++i) prefetch_tmap(&p.tmB[i]);
         uint32_t stage = 0, phase = 0, ready = 0;
         int issued = 0;
@@ -739,7 +741,7 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_pair_kernel(const __grid_c
         while (ok && it.next(t, k0, k1)) {
             const PTile x = pair_tile_at(t, p);
             const int lrow = x.m * PAIR_BM + half;  // row of this CTA's half inside the region
-            if (MODE == MODE_AG && p.region_ub[x.q]) {
+            if (IS_AG && p.region_ub[x.q]) {
                 const int g0 = p.region_row0[x.q] + lrow;
                 const int g1 = min(g0 + 128, p.region_row0[x.q] + p.region_rows[x.q]) - 1;
                 for (int ch = g0 / p.c; ok && g0 <= g1 && ch <= g1 / p.c; ++ch) {
@@ -749,7 +751,10 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_pair_kernel(const __grid_c
                 }
                 if (!ok) break;
             }
-            const int brow = x.n * BN + half;
+            // GLU: the even CTA loads gate rows [128n, 128n + 128) and the odd CTA the
+            // matching up rows, F further down, so TMEM columns 0..127 hold the gate and
+            // 128..255 the up projections of the same 128 outputs.
+            const int brow = GLU ? x.n * 128 + (rank ? p.glu_f : 0) : x.n * BN + half;
             for (int kb = k0; kb < k1; ++kb) {
                 if (!mbar_wait(empty_bar(stage), phase ^ 1u, w)) {
                     ok = false;
@@ -758,7 +763,7 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_pair_kernel(const __grid_c
                 const CUtensorMap *ma;
                 const CUtensorMap *mb;
                 int kx;
-                if (MODE == MODE_AG) {
+                if (IS_AG) {
                     ma = &p.tmA[x.q];
                     mb = &p.tmB[0];
                     kx = kb * BK;
@@ -900,6 +905,69 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_pair_kernel(const __grid_c
                 }
             }
 
+            if (GLU) {
+                // Two output groups of 64 columns: gate columns [64h, 64h + 64) and up
+                // columns 128 + [64h, 64h + 64) of the accumulator give
+                // Z[:, 128n + 64h + j] = silu(gate) * up, computed in fp32.
+#pragma unroll 1
+                for (int hs = 0; hs < 2; ++hs) {
+                    uint32_t g[STORE_COLS], u[STORE_COLS];
+                    tmem_ld32(trow + hs * STORE_COLS, g);
+                    tmem_ld32(trow + hs * STORE_COLS + 32, g + 32);
+                    tmem_ld32(trow + 128 + hs * STORE_COLS, u);
+                    tmem_ld32(trow + 128 + hs * STORE_COLS + 32, u + 32);
+                    tmem_wait_ld();
+                    if (hs == 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
+                    }
+                    for (int ci = 1; ci <= n_contrib; ++ci) {
+                        const float4 *src = reinterpret_cast<const float4 *>(
+                            p.ws + static_cast<size_t>((pair + ci) * 2 + rank) * PARTIAL_FLOATS);
+#pragma unroll
+                        for (int i = 0; i < STORE_COLS / 4; ++i) {
+                            const float4 a = __ldcg(src + (hs * (STORE_COLS / 4) + i) * 128 + prow);
+                            const float4 b = __ldcg(src + ((2 + hs) * (STORE_COLS / 4) + i) * 128 + prow);
+                            g[4 * i + 0] = __float_as_uint(__uint_as_float(g[4 * i + 0]) + a.x);
+                            g[4 * i + 1] = __float_as_uint(__uint_as_float(g[4 * i + 1]) + a.y);
+                            g[4 * i + 2] = __float_as_uint(__uint_as_float(g[4 * i + 2]) + a.z);
+                            g[4 * i + 3] = __float_as_uint(__uint_as_float(g[4 * i + 3]) + a.w);
+                            u[4 * i + 0] = __float_as_uint(__uint_as_float(u[4 * i + 0]) + b.x);
+                            u[4 * i + 1] = __float_as_uint(__uint_as_float(u[4 * i + 1]) + b.y);
+                            u[4 * i + 2] = __float_as_uint(__uint_as_float(u[4 * i + 2]) + b.z);
+                            u[4 * i + 3] = __float_as_uint(__uint_as_float(u[4 * i + 3]) + b.w);
+                        }
+                    }
+                    const int col = x.n * 128 + hs * STORE_COLS;
+                    if (col >= p.n_out || lrow0 >= p.region_rows[x.q]) continue;
+                    uint32_t pk[STORE_COLS / 2];
+#pragma unroll
+                    for (int j = 0; j < STORE_COLS / 2; ++j) {
+                        const float g0 = __uint_as_float(g[2 * j]), g1 = __uint_as_float(g[2 * j + 1]);
+                        const float z0 = g0 / (1.0f + __expf(-g0)) * __uint_as_float(u[2 * j]);
+                        const float z1 = g1 / (1.0f + __expf(-g1)) * __uint_as_float(u[2 * j + 1]);
+                        pk[j] = pack_bf16x2(__float_as_uint(z0), __float_as_uint(z1));
+                    }
+                    const uint32_t buf = ebuf0 + (nstore & 1) * EPI_BUF_BYTES;
+                    if (lane == 0) bulk_wait_read<1>();
+                    __syncwarp();
+                    const uint32_t rowaddr = buf + lane * 128u;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        st_shared_v4(rowaddr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4), pk[4 * j],
+                                     pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                    fence_proxy_async_shared();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&p.tmY[x.q], buf, col, lrow0);
+                        bulk_commit();
+                    }
+                    ++nstore;
+                }
+                continue;
+            }
+
 #pragma unroll 1
             for (int sub = 0; sub < BN / STORE_COLS; ++sub) {
                 uint32_t v[STORE_COLS];
@@ -1008,6 +1076,10 @@ int max_pair_clusters(int mode)
         e = cudaFuncSetAttribute(ub_gemm_pair_kernel<MODE_AG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  PAIR_SMEM_BYTES);
         if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n, ub_gemm_pair_kernel<MODE_AG>, &cfg);
+    } else if (mode == MODE_AG_GLU) {
+        e = cudaFuncSetAttribute(ub_gemm_pair_kernel<MODE_AG_GLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 PAIR_SMEM_BYTES);
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n, ub_gemm_pair_kernel<MODE_AG_GLU>, &cfg);
     } else {
         e = cudaFuncSetAttribute(ub_gemm_pair_kernel<MODE_RS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  PAIR_SMEM_BYTES);
@@ -1039,6 +1111,10 @@ cudaError_t launch_gemm_pair(const GemmParams &p, int mode, int clusters, cudaSt
         e = cudaFuncSetAttribute(ub_gemm_pair_kernel<MODE_AG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  PAIR_SMEM_BYTES);
         if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, ub_gemm_pair_kernel<MODE_AG>, p);
+    } else if (mode == MODE_AG_GLU) {
+        e = cudaFuncSetAttribute(ub_gemm_pair_kernel<MODE_AG_GLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 PAIR_SMEM_BYTES);
+        if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, ub_gemm_pair_kernel<MODE_AG_GLU>, p);
     } else {
         e = cudaFuncSetAttribute(ub_gemm_pair_kernel<MODE_RS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  PAIR_SMEM_BYTES);

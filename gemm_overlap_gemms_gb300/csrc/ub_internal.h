@@ -46,7 +46,7 @@ constexpr int MIN_KBLOCKS_PER_PIECE = 16;
 // Nor into more than this many pieces.
 constexpr int MAX_TAIL_SPLIT = 8;
 
-enum Mode : int { MODE_AG = 0, MODE_RS = 1 };
+enum Mode : int { MODE_AG = 0, MODE_RS = 1, MODE_AG_GLU = 2 /* AG-GEMM + SwiGLU epilogue, pair kernel only */ };
 
 // Kernel parameters, passed by value as a __grid_constant__ (tensor maps must live
 // in parameter, constant or global memory).
@@ -87,6 +87,7 @@ struct GemmParams {
     int tail_split;              // the remaining tiles are cut into this many k-pieces
     int ldy;                     // RS: leading dimension of Y_shards (= hidden)
     void *y_ptr[UB_MAX_TP];      // RS: Y_shards[r], for stores that cross a chunk end
+    int glu_f;                   // MODE_AG_GLU: F, the width of each half (gate, up) of Wt
     float *ws;                   // partial tiles of split tail tiles: [num_pairs][2][256/4][128][4] fp32
     uint32_t *ws_flags;          // [num_pairs][2][EPI_WARPS]: epoch of the partial written
 };

@@ -29,14 +29,14 @@ ERRORS = {
 CODES = {v: k for k, v in ERRORS.items()}
 OPTIONS = {"sm_margin": 1, "timeout_ns": 2, "self_rank": 3, "drop_flag": 4, "profile": 5,
            "cta_pair": 6, "streamk": 7, "copy_streams": 8}
-OPS = {"ag": 0, "rs": 1}
+OPS = {"ag": 0, "rs": 1, "ag_swiglu": 2}
 MAX_TP = 8
 EXPORTS = [
     "ub_create", "ub_destroy", "ub_set_active_shape", "ub_set_active_shape_nd",
     "ub_validate_active_shape", "ub_get_active_shape", "ub_get_capacity", "ub_get_tp",
     "ub_buffer", "ag_gemm", "gemm_rs", "ub_set_option", "ub_get_option", "ub_query_status",
     "ub_clear_status", "ub_get_counters", "ub_kernel_time", "ub_grid_ctas", "ub_last_error",
-    "ag_gemm_noalloc",
+    "ag_gemm_noalloc", "ag_gemm_swiglu",
 ]
 NOALLOC_MAX_ELEMS = 16 * 1024 * 1024
 
@@ -79,6 +79,7 @@ def load():
         "ub_get_tp": [P, ctypes.POINTER(I)],
         "ub_buffer": [P, PP, ctypes.POINTER(ctypes.c_size_t)],
         "ag_gemm": [P, PP, P, I64, P, P],
+        "ag_gemm_swiglu": [P, PP, P, I64, P, P],
         "gemm_rs": [P, PP, PP, I64, PP, P],
         "ub_set_option": [P, I, I64],
         "ub_get_option": [P, I, ctypes.POINTER(I64)],
@@ -261,6 +262,28 @@ class UserBuffer:
         _check(load().ag_gemm(self._h, _ptrs(shards), ctypes.c_void_p(Wt.data_ptr()), N,
                               ctypes.c_void_p(Y.data_ptr()), _stream_ptr(stream)))
         return Y
+
+    def ag_gemm_swiglu(self, shards, Wt: torch.Tensor, Z: torch.Tensor | None = None, stream=None):
+        """Z[T, F] = silu(G @ Wt[:F].T) * (G @ Wt[F:].T), G = concat_r(shards[r]); Wt is
+        [2F, hidden] with the gate rows first. The gathered input stays in the buffer."""
+        T, H = self.active_shape
+        if len(shards) != self.tp:
+            raise ValueError("expected %d shards, got %d" % (self.tp, len(shards)))
+        c = T // self.tp
+        for r, s in enumerate(shards):
+            _bf16_cuda(s, "shards[%d]" % r, (c, H))
+        _bf16_cuda(Wt, "Wt")
+        if Wt.dim() != 2 or Wt.shape[1] != H or Wt.shape[0] % 2:
+            raise ValueError("Wt must be [2F, %d], got %s" % (H, tuple(Wt.shape)))
+        F = Wt.shape[0] // 2
+        if Z is None:
+            Z = torch.empty((T, F), dtype=torch.bfloat16, device=Wt.device)
+        _bf16_cuda(Z, "Z")
+        if Z.dim() != 2 or Z.shape[0] < T or Z.shape[1] != F:
+            raise ValueError("Z must be [>=%d, %d], got %s" % (T, F, tuple(Z.shape)))
+        _check(load().ag_gemm_swiglu(self._h, _ptrs(shards), ctypes.c_void_p(Wt.data_ptr()), F,
+                                     ctypes.c_void_p(Z.data_ptr()), _stream_ptr(stream)))
+        return Z
 
     def gemm_rs(self, A, Bt, Y_shards=None, stream=None):
         """Y_shards[r] = rows [r*c, (r+1)*c) of sum_j A[j] @ Bt[j].T (c = T / tp)."""

@@ -87,7 +87,7 @@ enum {
 };
 
 /* Operation ids for ub_kernel_time. */
-enum { UB_OP_AG = 0, UB_OP_RS = 1 };
+enum { UB_OP_AG = 0, UB_OP_RS = 1, UB_OP_AG_SWIGLU = 2 };
 
 /*
  * Register a user buffer at capacity [max_tokens, hidden] for tp virtual ranks
@@ -149,6 +149,20 @@ int ag_gemm(ub_handle_t h, const void *const *shards, const void *Wt, int64_t N,
             void *stream);
 
 /*
+ * AG-GEMM with the SwiGLU activation fused into the epilogue: the column-parallel fc1
+ * followed by the GELU/SwiGLU box of [P1]'s MLP diagram, whose output feeds fc2.
+ * Wt is [2F, hidden] with the gate rows first and the up rows second (fc1's output row
+ * is [gate | up]); the all-gather is the one of ag_gemm, and
+ *     Z[t][f] = silu(g) * u,  g = sum_h UB[t][h] * Wt[f][h],  u = sum_h UB[t][h] * Wt[F + f][h],
+ * with silu(x) = x / (1 + e^-x), evaluated in fp32 on the fp32 accumulators and rounded
+ * once to BF16. Z: device [T, F]. Always runs on CTA pairs (the even CTA of a pair
+ * loads 128 gate rows and the odd CTA the matching up rows of each 256-row B tile).
+ * Errors: as ag_gemm; UB_ERR_ZERO (F <= 0), UB_ERR_ALIGN (F % 8 != 0).
+ */
+int ag_gemm_swiglu(ub_handle_t h, const void *const *shards, const void *Wt, int64_t F, void *Z,
+                   void *stream);
+
+/*
  * GEMM + reduce-scatter for the row-parallel linear ([P1] MLP diagram, fc2; [P2]
  * "Implementation approach": row blocks from the active first dimension):
  *     S[t][n]        = sum_{j<tp} sum_{k<K} A_j[t][k] * Bt_j[n][k]   (fp32, in TMEM)
@@ -188,8 +202,8 @@ typedef struct {
 int ub_get_counters(ub_handle_t h, ub_counters_t *out);
 
 /*
- * With UB_OPT_PROFILE = 1, every GEMM kernel launch of operation `op` (UB_OP_AG or
- * UB_OP_RS) is bracketed by CUDA events on its launch stream (up to 4096 launches are
+ * With UB_OPT_PROFILE = 1, every GEMM kernel launch of operation `op` (UB_OP_AG,
+ * UB_OP_RS or UB_OP_AG_SWIGLU) is bracketed by CUDA events on its launch stream (up to 4096 launches are
  * kept). This call waits for the last recorded launch, returns the summed kernel time
  * in milliseconds and the launch count, and clears the record.
  */
