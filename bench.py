@@ -60,13 +60,19 @@ def parse():
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mlp", choices=["fused", "unfused"], default="fused",
+                    help="fused: fc1 runs with the SwiGLU epilogue and feeds virtual rank 0's fc2 "
+                         "input (default); unfused: plain fc1 output [T, 7168]")
     ap.add_argument("--no-padded", action="store_true",
                     help="skip the padded-to-capacity comparator")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--case", choices=["ag", "rs"], default=None,
+    ap.add_argument("--case", choices=["ag", "rs", "ag_swiglu"], default=None,
                     help="time one op of the workload at one T only (small profiling case)")
     ap.add_argument("--case-T", type=int, default=8192)
     ap.add_argument("--case-reps", type=int, default=3)
+    ap.add_argument("--sm-margin", type=int, default=0)
+    ap.add_argument("--timeout-ms", type=float, default=None,
+                    help="bound of the device-side waits (default: the library's 1 s)")
     ap.add_argument("--cta-pair", type=int, default=-1, choices=[-1, 0, 1],
                     help="-1: chosen per call (default); 1: 256x256 tiles on CTA pairs; 0: single CTAs")
     ap.add_argument("--copy-streams", type=int, default=4)
@@ -243,7 +249,11 @@ class SwigluWorkload:
     def run_mb(self, i, stream):
         T = self.Ts[i]
         self.buf.set_active_shape([T, self.w.hidden])
-        self.buf.ag_gemm(self.shards(i), self.W1, self.Y1, stream=stream)
+        if MLP == "fused":
+            # fc1 with the SwiGLU epilogue writes virtual rank 0's fc2 input directly
+            self.buf.ag_gemm_swiglu(self.shards(i), self.W1, self.A[i][0], stream=stream)
+        else:
+            self.buf.ag_gemm(self.shards(i), self.W1, self.Y1, stream=stream)
         self.buf.gemm_rs(self.A[i], self.B, self.out_shards(i), stream=stream)
 
     def step(self, stream):
@@ -273,10 +283,12 @@ def e2e_measure(wl, steps, warmup, stream, world):
     and its outputs copied back, inside the timed region. Copies run on their own
     streams so that microbatch i+1's inputs and microbatch i-1's outputs move while
     microbatch i computes (outputs alternate between two device buffers)."""
+    fused = MLP == "fused"
+    a0 = 1 if fused else 0      # fused: A[i][0] is produced on the device by fc1
     hX = [x.cpu().pin_memory() for x in wl.X]
-    hA = [[a.cpu().pin_memory() for a in As] for As in wl.A]
+    hA = [[a.cpu().pin_memory() for a in As[a0:]] for As in wl.A]
     N, H, cap = wl.w.ag_n[0], wl.w.hidden, wl.w.max_tokens
-    hY1 = [torch.empty((T, N), dtype=torch.bfloat16).pin_memory() for T in wl.Ts]
+    hY1 = [] if fused else [torch.empty((T, N), dtype=torch.bfloat16).pin_memory() for T in wl.Ts]
     hY2 = [torch.empty((T, H), dtype=torch.bfloat16).pin_memory() for T in wl.Ts]
     h2d = sum(x.numel() * 2 for x in hX) + sum(a.numel() * 2 for As in hA for a in As)
     d2h = sum(y.numel() * 2 for y in hY1) + sum(y.numel() * 2 for y in hY2)
@@ -301,18 +313,22 @@ def e2e_measure(wl, steps, warmup, stream, world):
             with torch.cuda.stream(s_in):
                 s_in.wait_event(computed[i])          # the previous step is done with X[i], A[i]
                 wl.X[i].copy_(hX[i], non_blocking=True)
-                for j in range(tp):
-                    wl.A[i][j].copy_(hA[i][j], non_blocking=True)
+                for j in range(a0, tp):
+                    wl.A[i][j].copy_(hA[i][j - a0], non_blocking=True)
                 landed[i].record(s_in)
             stream.wait_event(landed[i])
             stream.wait_event(drained[b])              # output buffer b has been read back
             wl.buf.set_active_shape([T, H])
-            wl.buf.ag_gemm(wl.shards(i), wl.W1, Y1[b], stream=stream)
+            if fused:
+                wl.buf.ag_gemm_swiglu(wl.shards(i), wl.W1, wl.A[i][0], stream=stream)
+            else:
+                wl.buf.ag_gemm(wl.shards(i), wl.W1, Y1[b], stream=stream)
             wl.buf.gemm_rs(wl.A[i], wl.B, [Y2[b][r * c:(r + 1) * c] for r in range(tp)], stream=stream)
             computed[i].record(stream)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(computed[i])
-                hY1[i].copy_(Y1[b][:T], non_blocking=True)
+                if not fused:
+                    hY1[i].copy_(Y1[b][:T], non_blocking=True)
                 hY2[i].copy_(Y2[b][:T], non_blocking=True)
                 drained[b].record(s_out)
         stream.wait_stream(s_out)
@@ -345,7 +361,11 @@ def padded_measure(wl, steps, warmup, stream, world):
     def step():
         wl.buf.set_active_shape([cap, H])
         for i in range(len(wl.Ts)):
-            wl.buf.ag_gemm([Xp[i][r * c:(r + 1) * c] for r in range(tp)], wl.W1, wl.Y1, stream=stream)
+            sh = [Xp[i][r * c:(r + 1) * c] for r in range(tp)]
+            if MLP == "fused":
+                wl.buf.ag_gemm_swiglu(sh, wl.W1, Ap[i][0], stream=stream)
+            else:
+                wl.buf.ag_gemm(sh, wl.W1, wl.Y1, stream=stream)
             wl.buf.gemm_rs(Ap[i], wl.B, outs, stream=stream)
 
     ms = time_steps(step, steps, warmup, stream, world)
@@ -371,7 +391,9 @@ def cpu_baseline(wl, seconds):
     def run(nrows):
         rows = np.sort(rng.choice(T, size=nrows, replace=False))
         t0 = time.perf_counter()
-        oracle.gemm_rows(G, W1, rows)
+        y1 = oracle.gemm_rows(G, W1, rows)
+        if MLP == "fused":
+            oracle.swiglu(y1)
         oracle.gemm_rs_rows([a[rows] for a in A], B, rows, T)
         return time.perf_counter() - t0, nrows * (2.0 * H * N + 2.0 * K * H * tp)
 
@@ -404,15 +426,16 @@ def run_ours(args):
     def step():
         wl.step(stream)
 
+    ag_op = "ag_swiglu" if MLP == "fused" else "ag"
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    wl.buf.kernel_time("ag")
+    wl.buf.kernel_time(ag_op)
     wl.buf.kernel_time("rs")
     clocks.start()
     ms = time_steps(step, args.steps, 0, stream, world)
     clk = clocks.stop()
-    ag_ms, ag_n = wl.buf.kernel_time("ag")
+    ag_ms, ag_n = wl.buf.kernel_time(ag_op)
     rs_ms, rs_n = wl.buf.kernel_time("rs")
     wl.buf.set_option("profile", 0)
     assert wl.buf.query_status() == ub.UB_OK, "device status %d" % wl.buf.query_status()
@@ -431,7 +454,9 @@ def run_ours(args):
     dom = "rs" if rs_ms >= ag_ms else "ag"
     achieved = kernels[dom]["tflops"]
     tr = kernel_traffic(dom, float(np.mean(wl.Ts)))
-    roofline = {"bound": "tensor", "kernel": "ub_gemm_pair_kernel<%s>" % ("MODE_RS" if dom == "rs" else "MODE_AG"),
+    roofline = {"bound": "tensor",
+                "kernel": "ub_gemm_pair_kernel<%s>" % ("MODE_RS" if dom == "rs" else
+                                                       ("MODE_AG_GLU" if MLP == "fused" else "MODE_AG")),
                 "achieved": achieved, "peak": tensor_peak, "unit": "TFLOP/s",
                 "frac": achieved / tensor_peak if achieved else None,
                 "traffic": tr["bytes_per_launch"] if tr else None, "traffic_detail": tr,
@@ -469,6 +494,8 @@ def run_ours(args):
         "config": {"workload": "SwiGLU MLP: tp=4 virtual shards, hidden=4096, ffn=14336, "
                                "max_tokens=8192, 16 microbatches T~U{1024..8192 step 4}; "
                                "fc1 AG-GEMM N=7168 + fc2 GEMM-RS K=3584",
+                   "mlp": ("fc1 with fused SwiGLU epilogue writes virtual rank 0's fc2 input"
+                           if MLP == "fused" else "fc1 output [T, 7168] unfused"),
                    "tp": w.tp, "hidden": w.hidden, "max_tokens": w.max_tokens,
                    "microbatches": len(wl.Ts), "tokens_per_step": int(sum(wl.Ts)),
                    "parallelism": "replicas" if world > 1 else "single GPU",
@@ -549,7 +576,9 @@ def run_reference(args):
         a = [synth.to_u16(synth.normal_bf16((nrows, K), 1.0, g)) for _ in range(tp)]
         rows = np.sort(rng.choice(T, size=nrows, replace=False))
         t0 = time.perf_counter()
-        oracle.gemm_rows(x, W1, np.arange(nrows))
+        y1 = oracle.gemm_rows(x, W1, np.arange(nrows))
+        if MLP == "fused":
+            oracle.swiglu(y1)
         oracle.gemm_rs_rows(a, B, rows, T)
         return time.perf_counter() - t0, nrows * (2.0 * H * N + 2.0 * K * H * tp)
 
@@ -608,14 +637,21 @@ def run_case(args):
     buf.set_option("cta_pair", args.cta_pair)
     buf.set_option("streamk", args.streamk)
     buf.set_option("copy_streams", args.copy_streams)
+    if args.timeout_ms:
+        buf.set_option("timeout_ns", int(args.timeout_ms * 1e6))
+    buf.set_option("sm_margin", args.sm_margin)
     buf.set_active_shape([T, H])
     c = T // tp
-    if args.case == "ag":
+    if args.case in ("ag", "ag_swiglu"):
         X = synth.normal_bf16((T, H), 1.0, g, dev)
         W1 = synth.normal_bf16((N, H), 1.0 / math.sqrt(H), g, dev)
-        Y = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
         shards = [X[r * c:(r + 1) * c] for r in range(tp)]
-        fn = lambda: buf.ag_gemm(shards, W1, Y)
+        if args.case == "ag":
+            Y = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
+            fn = lambda: buf.ag_gemm(shards, W1, Y)
+        else:
+            Z = torch.empty((T, N // 2), dtype=torch.bfloat16, device=dev)
+            fn = lambda: buf.ag_gemm_swiglu(shards, W1, Z)
         flops = 2.0 * T * H * N
     else:
         A = [synth.normal_bf16((T, K), 1.0, g, dev) for _ in range(tp)]
@@ -624,29 +660,36 @@ def run_case(args):
         outs = [Ys[r * c:(r + 1) * c] for r in range(tp)]
         fn = lambda: buf.gemm_rs(A, B, outs)
         flops = 2.0 * T * K * H * tp
+    buf.set_option("profile", 1)
     fn()
     torch.cuda.synchronize()
-    buf.set_option("profile", 1)
+    first_ms, _ = buf.kernel_time(args.case)
+    first_status = buf.query_status()
     for _ in range(args.case_reps):
         fn()
     torch.cuda.synchronize()
     ms, n = buf.kernel_time(args.case)
-    assert buf.query_status() == ub.UB_OK
+    status = buf.query_status()
     buf.close()
     print(json.dumps({"case": args.case, "T": T, "cta_pair": args.cta_pair, "streamk": args.streamk,
-                      "copy_streams": args.copy_streams, "launches": n, "avg_us": 1e3 * ms / max(n, 1),
-                      "tflops": flops * n / (ms / 1e3) / 1e12 if ms > 0 else None}))
+                      "copy_streams": args.copy_streams, "sm_margin": args.sm_margin, "launches": n, "avg_us": 1e3 * ms / max(n, 1),
+                      "tflops": flops * n / (ms / 1e3) / 1e12 if ms > 0 else None,
+                      "first_us": 1e3 * first_ms, "first_status": first_status, "status": status}))
+    if status != ub.UB_OK:
+        sys.exit("device status %d (%s)" % (status, ub.ERRORS.get(status, "?")))
 
 
 CTA_PAIR = -1
 STREAMK = -1
+MLP = "fused"
 
 
 def main():
-    global CTA_PAIR, STREAMK
+    global CTA_PAIR, STREAMK, MLP
     args = parse()
     CTA_PAIR = args.cta_pair
     STREAMK = args.streamk
+    MLP = args.mlp
     if args.case:
         run_case(args)
     elif args.impl == "reference":

@@ -684,7 +684,10 @@ __device__ bool wait_partial(const uint32_t *flag, const WaitCtx &w)
 // epilogue drains its own 128 TMEM lanes and reports back to the even CTA. Work is
 // split across pairs by stream-K (above); rows are tiled by region (see GemmParams).
 template <int MODE>
-__global__ void __launch_bounds__(THREADS, 1) ub_gemm_pair_kernel(const __grid_constant__ GemmParams p)
+// The register cap leaves room on every SM for another kernel's CTA next to this one:
+// same-device cudaMemcpyAsync (the all-gather's chunk copies) runs as a kernel on SMs on
+// this platform, and the GEMM waits for those copies, so they must be able to start.
+__global__ void __maxnreg__(PAIR_MAX_REGS) ub_gemm_pair_kernel(const __grid_constant__ GemmParams p)
 {
     constexpr bool IS_AG = MODE != MODE_RS;     // A rows come from regions of the gathered input
     constexpr bool GLU = MODE == MODE_AG_GLU;   // B tile = 128 gate rows (even CTA) + 128 up rows (odd CTA)
@@ -911,44 +914,48 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_pair_kernel(const __grid_c
                 // Z[:, 128n + 64h + j] = silu(gate) * up, computed in fp32.
 #pragma unroll 1
                 for (int hs = 0; hs < 2; ++hs) {
-                    uint32_t g[STORE_COLS], u[STORE_COLS];
-                    tmem_ld32(trow + hs * STORE_COLS, g);
-                    tmem_ld32(trow + hs * STORE_COLS + 32, g + 32);
-                    tmem_ld32(trow + 128 + hs * STORE_COLS, u);
-                    tmem_ld32(trow + 128 + hs * STORE_COLS + 32, u + 32);
-                    tmem_wait_ld();
-                    if (hs == 1) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
-                    }
-                    for (int ci = 1; ci <= n_contrib; ++ci) {
-                        const float4 *src = reinterpret_cast<const float4 *>(
-                            p.ws + static_cast<size_t>((pair + ci) * 2 + rank) * PARTIAL_FLOATS);
+                    // 32 columns at a time keeps the live registers low enough for the
+                    // kernel's register cap.
+                    uint32_t pk[STORE_COLS / 2];
 #pragma unroll
-                        for (int i = 0; i < STORE_COLS / 4; ++i) {
-                            const float4 a = __ldcg(src + (hs * (STORE_COLS / 4) + i) * 128 + prow);
-                            const float4 b = __ldcg(src + ((2 + hs) * (STORE_COLS / 4) + i) * 128 + prow);
-                            g[4 * i + 0] = __float_as_uint(__uint_as_float(g[4 * i + 0]) + a.x);
-                            g[4 * i + 1] = __float_as_uint(__uint_as_float(g[4 * i + 1]) + a.y);
-                            g[4 * i + 2] = __float_as_uint(__uint_as_float(g[4 * i + 2]) + a.z);
-                            g[4 * i + 3] = __float_as_uint(__uint_as_float(g[4 * i + 3]) + a.w);
-                            u[4 * i + 0] = __float_as_uint(__uint_as_float(u[4 * i + 0]) + b.x);
-                            u[4 * i + 1] = __float_as_uint(__uint_as_float(u[4 * i + 1]) + b.y);
-                            u[4 * i + 2] = __float_as_uint(__uint_as_float(u[4 * i + 2]) + b.z);
-                            u[4 * i + 3] = __float_as_uint(__uint_as_float(u[4 * i + 3]) + b.w);
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const int c0 = hs * STORE_COLS + hf * 32;  // gate column; up is c0 + 128
+                        uint32_t g[32], u[32];
+                        tmem_ld32(trow + c0, g);
+                        tmem_ld32(trow + 128 + c0, u);
+                        tmem_wait_ld();
+                        if (hs == 1 && hf == 1) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
+                        }
+                        for (int ci = 1; ci <= n_contrib; ++ci) {
+                            const float4 *src = reinterpret_cast<const float4 *>(
+                                p.ws + static_cast<size_t>((pair + ci) * 2 + rank) * PARTIAL_FLOATS);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const float4 a = __ldcg(src + (c0 / 4 + i) * 128 + prow);
+                                const float4 b = __ldcg(src + ((128 + c0) / 4 + i) * 128 + prow);
+                                g[4 * i + 0] = __float_as_uint(__uint_as_float(g[4 * i + 0]) + a.x);
+                                g[4 * i + 1] = __float_as_uint(__uint_as_float(g[4 * i + 1]) + a.y);
+                                g[4 * i + 2] = __float_as_uint(__uint_as_float(g[4 * i + 2]) + a.z);
+                                g[4 * i + 3] = __float_as_uint(__uint_as_float(g[4 * i + 3]) + a.w);
+                                u[4 * i + 0] = __float_as_uint(__uint_as_float(u[4 * i + 0]) + b.x);
+                                u[4 * i + 1] = __float_as_uint(__uint_as_float(u[4 * i + 1]) + b.y);
+                                u[4 * i + 2] = __float_as_uint(__uint_as_float(u[4 * i + 2]) + b.z);
+                                u[4 * i + 3] = __float_as_uint(__uint_as_float(u[4 * i + 3]) + b.w);
+                            }
+                        }
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const float g0 = __uint_as_float(g[2 * j]), g1 = __uint_as_float(g[2 * j + 1]);
+                            const float z0 = g0 / (1.0f + __expf(-g0)) * __uint_as_float(u[2 * j]);
+                            const float z1 = g1 / (1.0f + __expf(-g1)) * __uint_as_float(u[2 * j + 1]);
+                            pk[hf * 16 + j] = pack_bf16x2(__float_as_uint(z0), __float_as_uint(z1));
                         }
                     }
                     const int col = x.n * 128 + hs * STORE_COLS;
                     if (col >= p.n_out || lrow0 >= p.region_rows[x.q]) continue;
-                    uint32_t pk[STORE_COLS / 2];
-#pragma unroll
-                    for (int j = 0; j < STORE_COLS / 2; ++j) {
-                        const float g0 = __uint_as_float(g[2 * j]), g1 = __uint_as_float(g[2 * j + 1]);
-                        const float z0 = g0 / (1.0f + __expf(-g0)) * __uint_as_float(u[2 * j]);
-                        const float z1 = g1 / (1.0f + __expf(-g1)) * __uint_as_float(u[2 * j + 1]);
-                        pk[j] = pack_bf16x2(__float_as_uint(z0), __float_as_uint(z1));
-                    }
                     const uint32_t buf = ebuf0 + (nstore & 1) * EPI_BUF_BYTES;
                     if (lane == 0) bulk_wait_read<1>();
                     __syncwarp();

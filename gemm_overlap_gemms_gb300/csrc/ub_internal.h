@@ -34,6 +34,7 @@ constexpr int TMEM_COLS = 2 * BN;  // two accumulators
 // 256x256x16 MMA that reads both CTAs' shared memory, and each CTA's TMEM receives its
 // 128 rows. Less shared memory per stage leaves room for 6 stages.
 constexpr int PAIR_BM = 256;             // rows of a pair tile (128 per CTA)
+constexpr int PAIR_MAX_REGS = 168;       // per thread: 192 x 168 leaves half of an SM's registers free
 constexpr int PAIR_STAGES = 6;
 constexpr int PAIR_A_BYTES = 128 * BK * 2;
 constexpr int PAIR_B_BYTES = 128 * BK * 2;  // this CTA's half of the 256-row B tile

@@ -250,3 +250,30 @@ def test_dropped_flag_times_out_and_the_handle_recovers(pair):
         assert buf.query_status() == ub.UB_OK
     _, Yref = oracle_ag(shards, Wt)
     assert_close(Y, Yref, "AG after recovery")
+
+
+@pytest.mark.parametrize("op", ["ag", "rs", "ag_swiglu"])
+def test_back_to_back_calls_at_full_hidden(op):
+    """Ten calls in a row on one handle at hidden 4096 without synchronising in
+    between: every call's chunk copies must be able to run next to the GEMM kernels."""
+    tp, H, N, K, T = 4, 4096, 1024, 1024, 2048
+    g = synth.generator(dev(), seed=51)
+    X = synth.normal_bf16((T, H), 1.0, g, dev())
+    Wt = synth.normal_bf16((2 * N if op == "ag_swiglu" else N, H), H ** -0.5, g, dev())
+    A = [synth.normal_bf16((T, K), 1.0, g, dev()) for _ in range(tp)]
+    Bt = [synth.normal_bf16((H, K), K ** -0.5, g, dev()) for _ in range(tp)]
+    c = T // tp
+    shards = [X[r * c:(r + 1) * c] for r in range(tp)]
+    with ub.UserBuffer([T, H], tp) as buf:
+        outs = []
+        for _ in range(10):
+            if op == "ag":
+                outs.append(buf.ag_gemm(shards, Wt))
+            elif op == "ag_swiglu":
+                outs.append(buf.ag_gemm_swiglu(shards, Wt))
+            else:
+                outs.append(torch.cat(buf.gemm_rs(A, Bt)))
+        torch.cuda.synchronize()
+        assert buf.query_status() == ub.UB_OK
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
