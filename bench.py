@@ -550,7 +550,7 @@ def sweep_points(wl, stream):
             fl = 2.0 * T * H * N if op == "ag" else 2.0 * T * K * H * tp
             tf = fl / (ms / 1e3) / 1e12
             out.append({"sweep": op, "T": T, "us": ms * 1e3, "tflops": tf,
-                        "frac_of_peak": tf / tensor_peak, "note": "includes the copy-engine gather" if op == "ag" else ""})
+                        "frac_of_peak": tf / tensor_peak, "note": "includes the gather copies" if op == "ag" else ""})
     return out
 
 

@@ -4,11 +4,14 @@
 // communication/GEMM overlap" (TransformerEngine issue #3564): one allocation at
 // capacity [max_tokens, hidden], an active shape that is only a logical view (nothing
 // allocated, freed or re-registered per microbatch), and chunk offsets computed from
-// the active first dimension. The all-gather is the copy-engine ("use_ce") variant of
-// the "ring_exchange" method of "How to setup TP Overlap configs" (TransformerEngine
-// issue #1344), collapsed onto one GPU: each virtual rank's chunk is a device-to-device
-// cudaMemcpyAsync on a side stream, followed by a stream memory write of the call's
-// epoch into the chunk's readiness flag, which the persistent GEMM polls.
+// the active first dimension. The all-gather stands in for the "ring_exchange" method
+// with copy-engine send/recv ("use_ce") of "How to setup TP Overlap configs"
+// (TransformerEngine issue #1344), collapsed onto one GPU: each virtual rank's chunk is
+// a device-to-device cudaMemcpyAsync on a side stream, followed by a stream memory
+// write of the call's epoch into the chunk's readiness flag, which the persistent GEMM
+// polls. On GB300 the driver runs such a same-device copy as a kernel on SMs, not on a
+// copy engine; the GEMM kernels therefore leave each SM room for a copy CTA (see the
+// register cap of the pair kernel), and every flag wait is bounded.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdarg.h>
@@ -539,7 +542,7 @@ static int ag_gemm_impl(ub_handle_t h, const void *const *shards, const void *Wt
         if (!pair) {
             for (int r = 0; r < tp; ++r) {
                 // Chunk r is read from the user buffer, except the self chunk, which the
-                // kernel reads in place from its shard while the copy engine stages it.
+                // kernel reads in place from its shard while its copy stages it.
                 const void *src = r == self ? shards[r] : static_cast<const void *>(ub + r * c * H * 2);
                 if (int rc = encode_2d(&p.tmA[r], src, H, c, H * 2, ubk::BK, ubk::BM)) return rc;
                 if (int rc = encode_2d(&p.tmY[r], static_cast<char *>(Y) + r * c * N * 2, N, c, N * 2,
@@ -589,7 +592,7 @@ static int ag_gemm_impl(ub_handle_t h, const void *const *shards, const void *Wt
     const int64_t drop = h->drop_flag;
     h->drop_flag = -1;
 
-    // Fork the copy-engine streams off `s`: they start once the work already queued on
+    // Fork the copy streams off `s`: they start once the work already queued on
     // `s` (which may still read the buffer) is done.
     const int ncs = static_cast<int>(h->copy_streams < tp ? h->copy_streams : tp);
     auto copy_stream = [&](int i) { return i == 0 ? h->side : h->extra_side[i]; };

@@ -6,7 +6,7 @@
 //    are walked chunk by chunk in ring order from the self rank ("ring_exchange" of
 //    "How to setup TP Overlap configs", with the chunk loop on the device as in its
 //    "atomic_gemm"); the producer waits for a chunk's readiness flag, written by the
-//    copy engine's stream after it lands the chunk, before loading any of its rows.
+//    copy's stream after it lands the chunk, before loading any of its rows.
 //  * MODE_RS -- the row-parallel linear followed by the reduce-scatter (MLP diagram):
 //    the K loop runs over (shard j, k-block), so sum_j A_j * Bt_j^T accumulates in
 //    TMEM, and the epilogue writes the rows of block r straight into Y_shards[r].

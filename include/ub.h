@@ -82,7 +82,7 @@ enum {
                               partial wave's tiles are cut into equal k-pieces spread over the
                               idle pairs (fixed-order fp32 fix-up: deterministic); 0 = whole
                               tiles only */
-    UB_OPT_COPY_STREAMS = 8 /* copy-engine streams the ag_gemm chunk copies are dealt over
+    UB_OPT_COPY_STREAMS = 8 /* side streams the ag_gemm chunk copies are dealt over
                               (round-robin in ring order), 1..UB_MAX_TP; default min(tp, 4) */
 };
 
@@ -136,8 +136,10 @@ int ub_buffer(ub_handle_t h, void **dev_ptr, size_t *bytes);
  *     UB[r*c + i][:] = shards[r][i][:]            for r < tp, i < c
  *     Y[t][n]       = sum_h UB[t][h] * Wt[n][h]   for t < T, n < N.
  * shards: host array of tp device pointers, each [c, hidden]. Wt: device [N, hidden].
- * Y: device [T, N] (leading dimension N). The chunk copies run on the copy engine on
- * the handle's side stream, each followed by a readiness-flag write; one persistent
+ * Y: device [T, N] (leading dimension N). The chunk copies are cudaMemcpyAsync calls on
+ * the handle's side streams (the stand-in for copy-engine send/recv; on GB300 the
+ * driver runs a same-device copy as a kernel on SMs, next to the GEMM, whose CTAs leave
+ * room for it), each followed by a readiness-flag write; one persistent
  * GEMM kernel on `stream` walks the chunks in ring order starting at
  * UB_OPT_SELF_RANK (whose chunk it reads in place, without waiting), waits for each
  * other chunk's flag, and never reads or writes rows >= T. The side stream is joined
