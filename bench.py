@@ -4,10 +4,12 @@
 One step = one pass of the whole hot path over the 16 packed-sequence microbatches
 of the SwiGLU MLP workload (tp=4 virtual ranks, hidden=4096, ffn=14336, capacity
 8192 tokens, T ~ U{1024..8192 step 4}): per microbatch, set the active shape, then
-  fc1  AG-GEMM  Y1 = concat_r X_r @ W1^T       (X_r [T/4, 4096], W1 [7168, 4096])
-  fc2  GEMM-RS  Y_r = rows_r sum_j A_j @ B_j^T (A_j [T, 3584],   B_j [4096, 3584])
-with every activation distinct per microbatch (2.7 GB per step, far larger than L2)
-and the weights shared. FLOPs are algorithmic: 2*T*H*N for AG, 2*T*K*H*tp for RS.
+  fc1  AG-GEMM + SwiGLU  A_0 = swiglu(concat_r X_r @ W1^T)  (X_r [T/4, 4096], W1 [7168, 4096])
+  fc2  GEMM-RS           Y_r = rows_r sum_j A_j @ B_j^T      (A_j [T, 3584],   B_j [4096, 3584])
+fc1 is virtual rank 0's column shard; its activated output is rank 0's fc2 input and
+the other ranks' A_j are inputs (``--mlp unfused`` writes fc1's [T, 7168] output
+instead). Every activation is distinct per microbatch (far larger than L2) and the
+weights are shared. FLOPs are algorithmic: 2*T*H*N for AG, 2*T*K*H*tp for RS.
 
   python bench.py [--steps K] [--warmup W] [--gpus N] [--impl ours|reference] [--sweep]
 
@@ -44,10 +46,10 @@ KERNEL_SRC = os.path.join(ROOT, "gemm_overlap_gemms_gb300", "csrc", "ub_gemm.cu"
 # per active token of the captured launch, and the kernel source they were taken on.
 # Traffic is reported as null once the kernel source no longer matches.
 NCU_TRAFFIC = {
-    "rs": {"sha256_16": "d611b2b1ac61bb3d", "bytes": 1156.0e6, "T": 8192,
+    "rs": {"sha256_16": "22b435fe73f2cd1a", "bytes": 1202.2e6, "T": 8192,
            "source": "profiles/ub_gemm_pair_kernel_rs_swiglu_fc2_T8192.md"},
-    "ag": {"sha256_16": "d611b2b1ac61bb3d", "bytes": 561.1e6, "T": 8192,
-           "source": "profiles/ub_gemm_pair_kernel_ag_swiglu_fc1_T8192.md"},
+    "ag_swiglu": {"sha256_16": "22b435fe73f2cd1a", "bytes": 377.0e6, "T": 8192,
+                  "source": "profiles/ub_gemm_pair_kernel_ag_glu_swiglu_fc1_T8192.md"},
 }
 
 
@@ -231,6 +233,7 @@ class SwigluWorkload:
             self.A.append([synth.normal_bf16((T, K), 1.0, g, device) for _ in range(tp)])
         cap = w.max_tokens
         self.Y1 = torch.empty((cap, N), dtype=torch.bfloat16, device=device)
+        self.Yz = torch.empty((cap, N // 2), dtype=torch.bfloat16, device=device)
         self.Yrs = torch.empty((cap, H), dtype=torch.bfloat16, device=device)
         self.buf = ub.UserBuffer([cap, H], tp)
         self.buf.set_option("cta_pair", CTA_PAIR)
@@ -453,7 +456,7 @@ def run_ours(args):
     }
     dom = "rs" if rs_ms >= ag_ms else "ag"
     achieved = kernels[dom]["tflops"]
-    tr = kernel_traffic(dom, float(np.mean(wl.Ts)))
+    tr = kernel_traffic("ag_swiglu" if (dom == "ag" and MLP == "fused") else dom, float(np.mean(wl.Ts)))
     roofline = {"bound": "tensor",
                 "kernel": "ub_gemm_pair_kernel<%s>" % ("MODE_RS" if dom == "rs" else
                                                        ("MODE_AG_GLU" if MLP == "fused" else "MODE_AG")),
@@ -542,15 +545,20 @@ def sweep_points(wl, stream):
         shards = [X[r * c:(r + 1) * c] for r in range(tp)]
         outs = [wl.Yrs[r * c:(r + 1) * c] for r in range(tp)]
         wl.buf.set_active_shape([T, H])
-        for op in ("ag", "rs"):
-            fn = (lambda: wl.buf.ag_gemm(shards, wl.W1, wl.Y1, stream=stream)) if op == "ag" else \
-                 (lambda: wl.buf.gemm_rs(A, wl.B, outs, stream=stream))
+        for op in ("ag", "ag_swiglu", "rs"):
+            if op == "ag":
+                fn = lambda: wl.buf.ag_gemm(shards, wl.W1, wl.Y1, stream=stream)
+            elif op == "ag_swiglu":
+                fn = lambda: wl.buf.ag_gemm_swiglu(shards, wl.W1, wl.Yz, stream=stream)
+            else:
+                fn = lambda: wl.buf.gemm_rs(A, wl.B, outs, stream=stream)
             reps = 20
             ms = time_steps(fn, reps, 3, stream, 1) / reps
-            fl = 2.0 * T * H * N if op == "ag" else 2.0 * T * K * H * tp
+            fl = 2.0 * T * H * N if op != "rs" else 2.0 * T * K * H * tp
             tf = fl / (ms / 1e3) / 1e12
             out.append({"sweep": op, "T": T, "us": ms * 1e3, "tflops": tf,
-                        "frac_of_peak": tf / tensor_peak, "note": "includes the gather copies" if op == "ag" else ""})
+                        "frac_of_peak": tf / tensor_peak,
+                        "note": "includes the gather copies" if op != "rs" else ""})
     return out
 
 
