@@ -19,6 +19,9 @@ What it computes (fp64 accumulation of exactly widened bf16 inputs):
   over ranks, output split by rows).
 * ``check_active_shape`` -- the five constraints of issue #3564, "Constrain the initial
   behavior".
+* ``gemm_xw_rows`` / ``gemm_tn`` -- the weight in its K x N layout, and the
+  contraction over the T active tokens: the products of the backward pass (input and
+  weight gradients of both layers).
 * ``swiglu`` -- the activation between fc1 and fc2 (the GELU/SwiGLU box of the MLP
   diagram in discussion #1240): fc1's row is [gate | up] and ``Z = silu(gate) * up``.
 
@@ -68,6 +71,8 @@ def _load():
         lib.oracle_gemm_rs.argtypes = [ctypes.c_int, I64, I64, I64, P, P, P, P]
         lib.oracle_gemm_rs_rows.argtypes = [ctypes.c_int, I64, I64, I64, P, P, P, I64,
                                             P, P, P]
+        lib.oracle_gemm_xw_rows.argtypes = [P, I64, P, I64, I64, P, I64, P]
+        lib.oracle_gemm_tn.argtypes = [P, I64, P, I64, I64, P]
         lib.oracle_silu.restype = ctypes.c_double
         lib.oracle_silu.argtypes = [ctypes.c_double]
         lib.oracle_swiglu.argtypes = [P, I64, I64, P]
@@ -221,3 +226,28 @@ def swiglu(Y: np.ndarray) -> np.ndarray:
     Z = np.empty((rows, F), dtype=np.float64)
     _load().oracle_swiglu(_ptr(Y), rows, F, _ptr(Z))
     return Z
+
+
+def gemm_xw_rows(X, W, rows):
+    """Y[q] = X[rows[q]] @ W in fp64, W stored K x N row-major."""
+    X = _u16(X)
+    W = _u16(W)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    K, N = W.shape
+    assert X.shape[1] == K
+    assert rows.size == 0 or (rows.min() >= 0 and rows.max() < X.shape[0])
+    Y = np.empty((rows.size, N), dtype=np.float64)
+    _load().oracle_gemm_xw_rows(_ptr(X), X.shape[1], _ptr(W), N, K, _ptr(rows), rows.size, _ptr(Y))
+    return Y
+
+
+def gemm_tn(D, G):
+    """out = D.T @ G in fp64 for D [T, M], G [T, N] (the sum runs over the T rows)."""
+    D = _u16(D)
+    G = _u16(G)
+    T, M = D.shape
+    assert G.shape[0] == T
+    N = G.shape[1]
+    out = np.empty((M, N), dtype=np.float64)
+    _load().oracle_gemm_tn(_ptr(D), M, _ptr(G), N, T, _ptr(out))
+    return out

@@ -198,6 +198,45 @@ void oracle_gemm_rs_rows(int tp, int64_t T, int64_t K, int64_t H,
     }
 }
 
+/* The weight operand in its mathematical layout, K x N row-major (the layout the
+ * workloads write W[hidden, N] and B_j[K, hidden] in): Y[q][n] = sum_k X[rows[q]][k] *
+ * W[k][n]. With W stored this way the same products serve the backward pass: the
+ * column-parallel layer's input gradient is sum_j dY_j * Wt_j (Wt_j stored [N_j, H],
+ * i.e. K x N with K = N_j), the row-parallel layer's is dS * Bt_j. */
+void oracle_gemm_xw_rows(const uint16_t *X, int64_t ldx, const uint16_t *W, int64_t N, int64_t K,
+                         const int64_t *rows, int64_t nrows, double *Y)
+{
+    int64_t q;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (q = 0; q < nrows; ++q) {
+        const uint16_t *x = X + rows[q] * ldx;
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                acc += bf16_to_double(x[k]) * bf16_to_double(W[k * N + n]);
+            Y[q * N + n] = acc;
+        }
+    }
+}
+
+/* Weight gradient: the contraction over the T active tokens of two [T, .] activations,
+ * out[m][n] = sum_{t<T} D[t][m] * G[t][n] (D [T, M], G [T, N], out [M, N], double).
+ * For the column-parallel layer D = dY and G = the gathered input (dWt = dY^T G); for
+ * the row-parallel layer D = the gathered dS and G = A_j (dBt_j = dS^T A_j). */
+void oracle_gemm_tn(const uint16_t *D, int64_t M, const uint16_t *G, int64_t N, int64_t T, double *out)
+{
+    int64_t m;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (m = 0; m < M; ++m) {
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int64_t t = 0; t < T; ++t)
+                acc += bf16_to_double(D[t * M + m]) * bf16_to_double(G[t * N + n]);
+            out[m * N + n] = acc;
+        }
+    }
+}
+
 /* SwiGLU between the column-parallel fc1 and the row-parallel fc2 (the GELU/SwiGLU box
  * of the MLP diagram in "Do tp overlap support thd..."): fc1's output row holds the
  * gate half first and the up half second, Y[t] = [g_0..g_{F-1}, u_0..u_{F-1}], and

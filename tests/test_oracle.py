@@ -353,3 +353,57 @@ def test_swiglu_takes_gate_first_then_up():
     # planted mistake: halves swapped
     Zs = oracle.swiglu(np.concatenate([Y[:, F:], Y[:, :F]], axis=1))
     assert not np.allclose(Zs, Z)
+
+
+# ---------------------------------------------------------------- backward-pass products
+
+def test_gemm_xw_brute_force_and_transpose_identity():
+    g = synth.generator(seed=61)
+    for T, K, N in [(5, 3, 4), (16, 16, 8), (9, 7, 13)]:
+        X = synth.to_u16(synth.small_int_bf16((T, K), -8, 8, g))
+        W = synth.to_u16(synth.small_int_bf16((K, N), -8, 8, g))
+        rows = np.arange(T)
+        Y = oracle.gemm_xw_rows(X, W, rows)
+        want = bits_to_f64(X).astype(np.int64) @ bits_to_f64(W).astype(np.int64)
+        np.testing.assert_array_equal(Y, want.astype(np.float64))
+        # the same product through the pinned out-x-in path with the weight transposed
+        np.testing.assert_array_equal(Y, oracle.gemm_rows(X, np.ascontiguousarray(W.T), rows))
+        if K != N:  # planted mistake: W read as if it were stored N x K
+            with pytest.raises(AssertionError):
+                oracle.gemm_xw_rows(X, np.ascontiguousarray(W.T), rows)
+
+
+def test_gemm_tn_brute_force_and_library():
+    g = synth.generator(seed=62)
+    for T, M, N in [(6, 4, 5), (33, 16, 24)]:
+        D = synth.to_u16(synth.small_int_bf16((T, M), -8, 8, g))
+        G = synth.to_u16(synth.small_int_bf16((T, N), -8, 8, g))
+        out = oracle.gemm_tn(D, G)
+        want = bits_to_f64(D).astype(np.int64).T @ bits_to_f64(G).astype(np.int64)
+        np.testing.assert_array_equal(out, want.astype(np.float64))
+        # gemm_tn(D, G) == gemm_tn(G, D).T (the sum over t is symmetric in its operands)
+        np.testing.assert_array_equal(out, oracle.gemm_tn(G, D).T)
+    D, G = [synth.to_u16(synth.normal_bf16((40, 12), 1.0, g)) for _ in range(2)]
+    ref = bits_to_f64(D).T @ bits_to_f64(G)
+    bound = 40 * 2.0 ** -52 * (np.abs(bits_to_f64(D)).T @ np.abs(bits_to_f64(G)))
+    assert np.all(np.abs(oracle.gemm_tn(D, G) - ref) <= bound)
+
+
+def test_backward_products_match_forward_identities():
+    """Chain rule on a tiny layer, by finite algebra: for Y = X Wt^T the input gradient
+    dY Wt and the weight gradient dY^T X are the unique linear maps with
+    <dY, X' Wt^T> = <dY Wt, X'> and <dY, X Wt'^T> = <dY^T X, Wt'> for every X', Wt'."""
+    g = synth.generator(seed=63)
+    T, H, N = 7, 5, 6
+    X = synth.to_u16(synth.small_int_bf16((T, H), -4, 4, g))
+    Wt = synth.to_u16(synth.small_int_bf16((N, H), -4, 4, g))
+    dY = synth.to_u16(synth.small_int_bf16((T, N), -4, 4, g))
+    dX = oracle.gemm_xw_rows(dY, Wt, np.arange(T))      # dY @ Wt  ([T, N] x [N, H])
+    dWt = oracle.gemm_tn(dY, X)                          # dY^T @ X ([N, H])
+    for trial in range(3):
+        Xp = synth.to_u16(synth.small_int_bf16((T, H), -3, 3, g))
+        Wp = synth.to_u16(synth.small_int_bf16((N, H), -3, 3, g))
+        lhs_x = np.sum(bits_to_f64(dY) * oracle.gemm_rows(Xp, Wt, np.arange(T)))
+        assert lhs_x == np.sum(dX * bits_to_f64(Xp))
+        lhs_w = np.sum(bits_to_f64(dY) * oracle.gemm_rows(X, Wp, np.arange(T)))
+        assert lhs_w == np.sum(dWt * bits_to_f64(Wp))
