@@ -153,7 +153,7 @@ struct ub_handle {
     ub_counters_t counters{};
     std::vector<CacheEntry> cache;
     uint64_t use_clock = 0;
-    ProfileRing prof[3];
+    ProfileRing prof[UB_NUM_OPS];
 };
 
 namespace {
@@ -287,10 +287,10 @@ void choose_path(ub_handle *h, int mode, int64_t single_tiles, int64_t pair_tile
     }
 }
 
-int launch(ub_handle *h, const GemmParams &p, int mode, bool pair, cudaStream_t s)
+int launch(ub_handle *h, const GemmParams &p, int mode, bool pair, cudaStream_t s, int prof_op)
 {
     const int grid = pair ? p.num_pairs : grid_for(h, p.num_tiles);
-    ProfileRing &ring = h->prof[mode];
+    ProfileRing &ring = h->prof[prof_op];
     const bool timed = h->profile != 0 && ring.count < kMaxProfiled;
     if (timed) {
         if (static_cast<int>(ring.start.size()) <= ring.count) {
@@ -480,9 +480,10 @@ int ub_grid_ctas(ub_handle_t h, int *ctas)
 }
 
 // AG-GEMM, optionally with the SwiGLU epilogue (glu_f > 0: Wt is [2 * glu_f, hidden],
-// gate rows first, and Y receives [T, glu_f]).
+// gate rows first, and Y receives [T, glu_f]), or with the weight stored hidden x N
+// (b_kn: the tensor core reads it MN-major).
 static int ag_gemm_impl(ub_handle_t h, const void *const *shards, const void *Wt, int64_t N, void *Y, void *stream,
-                        int64_t glu_f)
+                        int64_t glu_f, bool b_kn)
 {
     if (int rc = check_handle(h)) return rc;
     if (!shards || !Wt || !Y) return fail(UB_ERR_ARG, "ag_gemm: null pointer argument");
@@ -504,6 +505,7 @@ static int ag_gemm_impl(ub_handle_t h, const void *const *shards, const void *Wt
 
     const bool glu = glu_f > 0;
     const int mode = glu ? ubk::MODE_AG_GLU : ubk::MODE_AG;
+    const int prof_op = glu ? UB_OP_AG_SWIGLU : (b_kn ? UB_OP_AG_KN : UB_OP_AG);
     const int64_t n_out = glu ? glu_f : N;                    // columns of Y
     const int64_t n_tiles = glu ? (glu_f + 127) / 128 : (N + ubk::BN - 1) / ubk::BN;
     int64_t pair_rows_tiles = ceil_div(c, ubk::PAIR_BM);  // regions: self chunk, after it, before it
@@ -512,13 +514,13 @@ static int ag_gemm_impl(ub_handle_t h, const void *const *shards, const void *Wt
     bool pair = false, streamk = false;
     choose_path(h, mode, tp * ceil_div(c, ubk::BM) * n_tiles, pair_rows_tiles * n_tiles,
                 (H + ubk::BK - 1) / ubk::BK, pair, streamk);
-    if (glu) pair = true;  // the fused epilogue needs the pair layout (gate half, up half)
+    if (glu || b_kn) pair = true;  // the fused epilogue and MN-major operands exist on CTA pairs only
     const int bm = pair ? ubk::PAIR_BM : ubk::BM;      // rows of a tile
     const int bbox = pair ? ubk::BN / 2 : ubk::BN;    // rows of a B box (one CTA's half in a pair)
     std::vector<const void *> key;
     key.reserve(tp + 7);
     key.push_back(reinterpret_cast<const void *>(uintptr_t(mode)));
-    key.push_back(reinterpret_cast<const void *>(uintptr_t(pair)));
+    key.push_back(reinterpret_cast<const void *>(uintptr_t(pair + 2 * b_kn)));
     key.push_back(reinterpret_cast<const void *>(uintptr_t(T)));
     key.push_back(reinterpret_cast<const void *>(uintptr_t(N)));
     key.push_back(reinterpret_cast<const void *>(uintptr_t(self)));
@@ -577,7 +579,13 @@ static int ag_gemm_impl(ub_handle_t h, const void *const *shards, const void *Wt
             p.n_regions = nreg;
             h->counters.tensor_map_encodes += 2 * nreg;
         }
-        if (int rc = encode_2d(&p.tmB[0], Wt, H, N, H * 2, ubk::BK, bbox)) return rc;
+        if (b_kn) {
+            // W is [hidden, N]: inner dimension N, boxes of 64 N x 64 K rows
+            if (int rc = encode_2d(&p.tmB[0], Wt, N, H, N * 2, 64, ubk::BK)) return rc;
+            p.b_mn = 1;
+        } else if (int rc = encode_2d(&p.tmB[0], Wt, H, N, H * 2, ubk::BK, bbox)) {
+            return rc;
+        }
         h->counters.tensor_map_encodes += 1;
         pp = cache_insert(h, std::move(key), p);
     }
@@ -612,7 +620,7 @@ static int ag_gemm_impl(ub_handle_t h, const void *const *shards, const void *Wt
             if (cr != CUDA_SUCCESS) return fail(UB_ERR_CUDA, "cuStreamWriteValue32 failed (%d)", (int)cr);
         }
     }
-    int rc = launch(h, p, mode, pair, s);
+    int rc = launch(h, p, mode, pair, s, prof_op);
     // Join the copy streams back into `s` even if the launch failed.
     UB_CUDA(cudaEventRecord(h->ev_join, h->side));
     UB_CUDA(cudaStreamWaitEvent(s, h->ev_join, 0));
@@ -628,18 +636,24 @@ static int ag_gemm_impl(ub_handle_t h, const void *const *shards, const void *Wt
 
 int ag_gemm(ub_handle_t h, const void *const *shards, const void *Wt, int64_t N, void *Y, void *stream)
 {
-    return ag_gemm_impl(h, shards, Wt, N, Y, stream, 0);
+    return ag_gemm_impl(h, shards, Wt, N, Y, stream, 0, false);
+}
+
+int ag_gemm_kn(ub_handle_t h, const void *const *shards, const void *W, int64_t N, void *Y, void *stream)
+{
+    return ag_gemm_impl(h, shards, W, N, Y, stream, 0, true);
 }
 
 int ag_gemm_swiglu(ub_handle_t h, const void *const *shards, const void *Wt, int64_t F, void *Z, void *stream)
 {
     if (F <= 0) return fail(UB_ERR_ZERO, "ag_gemm_swiglu: F = %lld", (long long)F);
     if (F % 8 != 0) return fail(UB_ERR_ALIGN, "ag_gemm_swiglu: F = %lld is not a multiple of 8", (long long)F);
-    return ag_gemm_impl(h, shards, Wt, 2 * F, Z, stream, F);
+    return ag_gemm_impl(h, shards, Wt, 2 * F, Z, stream, F, false);
 }
 
-int gemm_rs(ub_handle_t h, const void *const *A, const void *const *Bt, int64_t K, void *const *Y_shards,
-            void *stream)
+// GEMM-RS; with b_kn the shard weights are stored K x hidden (read MN-major).
+static int gemm_rs_impl(ub_handle_t h, const void *const *A, const void *const *Bt, int64_t K, void *const *Y_shards,
+                        void *stream, bool b_kn)
 {
     if (int rc = check_handle(h)) return rc;
     if (!A || !Bt || !Y_shards) return fail(UB_ERR_ARG, "gemm_rs: null pointer argument");
@@ -661,12 +675,13 @@ int gemm_rs(ub_handle_t h, const void *const *A, const void *const *Bt, int64_t 
     bool pair = false, streamk = false;
     choose_path(h, ubk::MODE_RS, tp * ceil_div(c, ubk::BM) * n_tiles, ceil_div(T, ubk::PAIR_BM) * n_tiles,
                 tp * ((K + ubk::BK - 1) / ubk::BK), pair, streamk);
+    if (b_kn) pair = true;  // MN-major operands exist on CTA pairs only
     const int bm = pair ? ubk::PAIR_BM : ubk::BM;
     const int bbox = pair ? ubk::BN / 2 : ubk::BN;
     std::vector<const void *> key;
     key.reserve(3 * tp + 4);
     key.push_back(reinterpret_cast<const void *>(uintptr_t(ubk::MODE_RS)));
-    key.push_back(reinterpret_cast<const void *>(uintptr_t(pair)));
+    key.push_back(reinterpret_cast<const void *>(uintptr_t(pair + 2 * b_kn)));
     key.push_back(reinterpret_cast<const void *>(uintptr_t(T)));
     key.push_back(reinterpret_cast<const void *>(uintptr_t(K)));
     for (int j = 0; j < tp; ++j) {
@@ -680,7 +695,12 @@ int gemm_rs(ub_handle_t h, const void *const *A, const void *const *Bt, int64_t 
         memset(&p, 0, sizeof p);
         for (int j = 0; j < tp; ++j) {
             if (int rc = encode_2d(&p.tmA[j], A[j], K, T, K * 2, ubk::BK, ubk::BM)) return rc;
-            if (int rc = encode_2d(&p.tmB[j], Bt[j], K, H, K * 2, ubk::BK, bbox)) return rc;
+            if (b_kn) {
+                // B_j is [K, hidden]: inner dimension hidden, boxes of 64 x 64 K rows
+                if (int rc = encode_2d(&p.tmB[j], Bt[j], H, K, H * 2, 64, ubk::BK)) return rc;
+            } else if (int rc = encode_2d(&p.tmB[j], Bt[j], K, H, K * 2, ubk::BK, bbox)) {
+                return rc;
+            }
             if (int rc = encode_2d(&p.tmY[j], Y_shards[j], H, c, H * 2, ubk::STORE_COLS, 32)) return rc;
             p.y_ptr[j] = Y_shards[j];
         }
@@ -693,6 +713,7 @@ int gemm_rs(ub_handle_t h, const void *const *A, const void *const *Bt, int64_t 
         p.region_tile0[1] = static_cast<int>((T + ubk::PAIR_BM - 1) / ubk::PAIR_BM) *
                             static_cast<int>((H + ubk::BN - 1) / ubk::BN);
         p.ldy = static_cast<int>(H);
+        p.b_mn = b_kn ? 1 : 0;
         p.tp = tp;
         p.c = static_cast<int>(c);
         p.n_out = static_cast<int>(H);
@@ -711,8 +732,78 @@ int gemm_rs(ub_handle_t h, const void *const *A, const void *const *Bt, int64_t 
     p.timeout_ns = static_cast<uint64_t>(h->timeout_ns);
     if (pair) set_pairs(h, p, ubk::MODE_RS, streamk);
     p.epoch = ++h->epoch;
-    if (int rc = launch(h, p, ubk::MODE_RS, pair, s)) return rc;
+    if (int rc = launch(h, p, ubk::MODE_RS, pair, s, b_kn ? UB_OP_RS_KN : UB_OP_RS)) return rc;
     ++h->counters.rs_calls;
+    h->counters.last_T = T;
+    return UB_OK;
+}
+
+int gemm_rs(ub_handle_t h, const void *const *A, const void *const *Bt, int64_t K, void *const *Y_shards,
+            void *stream)
+{
+    return gemm_rs_impl(h, A, Bt, K, Y_shards, stream, false);
+}
+
+int gemm_rs_kn(ub_handle_t h, const void *const *A, const void *const *B, int64_t K, void *const *Y_shards,
+               void *stream)
+{
+    return gemm_rs_impl(h, A, B, K, Y_shards, stream, true);
+}
+
+int ub_wgrad(ub_handle_t h, const void *D, int64_t M, int ub_is_a, void *out, void *stream)
+{
+    if (int rc = check_handle(h)) return rc;
+    if (!D || !out) return fail(UB_ERR_ARG, "ub_wgrad: null pointer argument");
+    if (M <= 0) return fail(UB_ERR_ZERO, "ub_wgrad: M = %lld", (long long)M);
+    if (M % 8 != 0) return fail(UB_ERR_ALIGN, "ub_wgrad: M = %lld is not a multiple of 8", (long long)M);
+    if (M > (int64_t(1) << 24)) return fail(UB_ERR_ARG, "ub_wgrad: M = %lld too large", (long long)M);
+    if (!aligned16(D) || !aligned16(out)) return fail(UB_ERR_ALIGN, "ub_wgrad: D / out not 16-byte aligned");
+    if (ub_is_a != 0 && ub_is_a != 1) return fail(UB_ERR_ARG, "ub_wgrad: ub_is_a must be 0 or 1");
+    DeviceGuard g(h->device);
+    if (!g.ok) return fail(UB_ERR_CUDA, "ub_wgrad: cannot select the handle's device");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t T = h->T, H = h->hidden;
+    // out = A^T B over the T active rows; A and B are [T, .] row-major (MN-major operands)
+    const void *Aop = ub_is_a ? h->ub : D;
+    const void *Bop = ub_is_a ? D : h->ub;
+    const int64_t rows = ub_is_a ? H : M, cols = ub_is_a ? M : H;
+
+    std::vector<const void *> key = {reinterpret_cast<const void *>(uintptr_t(100 + ub_is_a)),
+                                     reinterpret_cast<const void *>(uintptr_t(T)),
+                                     reinterpret_cast<const void *>(uintptr_t(M)), D, out};
+    GemmParams *pp = cache_lookup(h, key);
+    if (!pp) {
+        GemmParams p;
+        memset(&p, 0, sizeof p);
+        if (int rc = encode_2d(&p.tmA[0], Aop, rows, T, rows * 2, 64, ubk::BK)) return rc;
+        if (int rc = encode_2d(&p.tmB[0], Bop, cols, T, cols * 2, 64, ubk::BK)) return rc;
+        if (int rc = encode_2d(&p.tmY[0], out, cols, rows, cols * 2, ubk::STORE_COLS, 32)) return rc;
+        h->counters.tensor_map_encodes += 3;
+        p.tp = h->tp;
+        p.c = static_cast<int>(T / h->tp);
+        p.n_out = static_cast<int>(cols);
+        p.k_blocks = static_cast<int>((T + ubk::BK - 1) / ubk::BK);
+        p.k_blocks_per_shard = p.k_blocks;
+        p.n_tiles = static_cast<int>((cols + ubk::BN - 1) / ubk::BN);
+        p.n_regions = 1;
+        p.region_row0[0] = 0;
+        p.region_rows[0] = static_cast<int>(rows);
+        p.region_ub[0] = 0;  // the buffer already holds the gathered rows: no flags to wait for
+        p.region_tile0[1] = static_cast<int>((rows + ubk::PAIR_BM - 1) / ubk::PAIR_BM) * p.n_tiles;
+        p.a_mn = 1;
+        p.b_mn = 1;
+        pp = cache_insert(h, std::move(key), p);
+    }
+    GemmParams &p = *pp;
+    p.flags = flags_of(h);
+    p.abort_word = abort_of(h);
+    p.status = status_of(h);
+    p.timeout_ns = static_cast<uint64_t>(h->timeout_ns);
+    bool pair = true, split = false;
+    choose_path(h, ubk::MODE_AG, 1 << 30, p.region_tile0[1], p.k_blocks, pair, split);
+    set_pairs(h, p, ubk::MODE_AG, split);
+    p.epoch = ++h->epoch;
+    if (int rc = launch(h, p, ubk::MODE_AG, true, s, UB_OP_WGRAD)) return rc;
     h->counters.last_T = T;
     return UB_OK;
 }
@@ -811,7 +902,7 @@ int ub_get_counters(ub_handle_t h, ub_counters_t *out)
 int ub_kernel_time(ub_handle_t h, int op, double *total_ms, int64_t *launches)
 {
     if (int rc = check_handle(h)) return rc;
-    if (op != UB_OP_AG && op != UB_OP_RS && op != UB_OP_AG_SWIGLU) return fail(UB_ERR_ARG, "unknown op %d", op);
+    if (op < 0 || op >= UB_NUM_OPS) return fail(UB_ERR_ARG, "unknown op %d", op);
     DeviceGuard g(h->device);
     ProfileRing &ring = h->prof[op];
     double sum = 0.0;

@@ -167,6 +167,23 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr)
     return d;
 }
 
+// Shared-memory matrix descriptor of an MN-major operand tile (MN contiguous in global
+// memory, e.g. a weight stored K x N) written by TMA with the 128-byte swizzle in boxes
+// of 64 MN elements x 64 K rows: each 8 K-rows x 64 MN group is one 1024-byte swizzle
+// atom; atoms follow each other along K every 1024 bytes (stride offset) and the second
+// box of 64 MN elements starts 8 KiB later (leading offset).
+__device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address      [0,14)
+    d |= static_cast<uint64_t>(8192u >> 4) << 16;         // leading offset: next 64 MN
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;         // stride offset: next 8 K rows
+    d |= static_cast<uint64_t>(1u) << 46;                 // descriptor version
+    d |= static_cast<uint64_t>(2u) << 61;                 // swizzle: 128 B
+    return d;
+}
+constexpr uint32_t MN_BOX_BYTES = 64 * BK * 2;           // one 64 (MN) x 64 (K) box
+
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both K-major,
 // N = BN, M = BM.
 constexpr uint32_t kIdesc = (1u << 4)                           // D format: f32
@@ -265,13 +282,15 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
 constexpr uint32_t kIdescPair = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
                                 (static_cast<uint32_t>(PAIR_BM >> 4) << 24);
 
-__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate)
+// idesc: kIdescPair, plus bit 15 (A MN-major) / bit 16 (B MN-major) when set.
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate)
 {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(kIdescPair), "r"(accumulate)
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -778,8 +797,22 @@ __global__ void __maxnreg__(PAIR_MAX_REGS) ub_gemm_pair_kernel(const __grid_cons
                 }
                 const uint32_t fb = map_to_rank(full_bar(stage), 0);
                 if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * (PAIR_A_BYTES + PAIR_B_BYTES));
-                tma_load_2d_pair(smem_u32(smA + stage * PAIR_A_BYTES), ma, fb, kx, lrow);
-                tma_load_2d_pair(smem_u32(smB + stage * PAIR_B_BYTES), mb, fb, kx, brow);
+                const uint32_t sa = smem_u32(smA + stage * PAIR_A_BYTES);
+                const uint32_t sb = smem_u32(smB + stage * PAIR_B_BYTES);
+                // K-major operands: one 128-row x 64-K box. MN-major operands: two boxes of
+                // 64 MN x 64 K rows (the tensor map's inner dimension is MN).
+                if (p.a_mn) {
+                    tma_load_2d_pair(sa, ma, fb, lrow, kx);
+                    tma_load_2d_pair(sa + MN_BOX_BYTES, ma, fb, lrow + 64, kx);
+                } else {
+                    tma_load_2d_pair(sa, ma, fb, kx, lrow);
+                }
+                if (p.b_mn) {
+                    tma_load_2d_pair(sb, mb, fb, brow, kx);
+                    tma_load_2d_pair(sb + MN_BOX_BYTES, mb, fb, brow + 64, kx);
+                } else {
+                    tma_load_2d_pair(sb, mb, fb, kx, brow);
+                }
                 ++issued;
                 if (++stage == PAIR_STAGES) {
                     stage = 0;
@@ -796,6 +829,7 @@ __global__ void __maxnreg__(PAIR_MAX_REGS) ub_gemm_pair_kernel(const __grid_cons
         if (!ok) settle(100000);  // abort path: let copies already issued land
     } else if (warp == 1 && lane == 0 && rank == 0) {
         // ---------------------------------------------------------- MMA issuer (even CTA)
+        const uint32_t idesc = kIdescPair | (p.a_mn ? (1u << 15) : 0u) | (p.b_mn ? (1u << 16) : 0u);
         uint32_t stage = 0, phase = 0;
         int local = 0;
         bool ok = true;
@@ -820,7 +854,9 @@ __global__ void __maxnreg__(PAIR_MAX_REGS) ub_gemm_pair_kernel(const __grid_cons
                 const uint32_t b0 = smem_u32(smB + stage * PAIR_B_BYTES);
 #pragma unroll
                 for (int k = 0; k < BK / 16; ++k)
-                    umma_bf16_pair(d_tmem, smem_desc_sw128(a0 + 32u * k), smem_desc_sw128(b0 + 32u * k),
+                    umma_bf16_pair(d_tmem,
+                                   p.a_mn ? smem_desc_mn_sw128(a0 + 2048u * k) : smem_desc_sw128(a0 + 32u * k),
+                                   p.b_mn ? smem_desc_mn_sw128(b0 + 2048u * k) : smem_desc_sw128(b0 + 32u * k), idesc,
                                    (kb != k0 || k != 0) ? 1u : 0u);
                 umma_commit_pair_both(empty_bar(stage));
                 if (++stage == PAIR_STAGES) {

@@ -89,6 +89,8 @@ struct GemmParams {
     int ldy;                     // RS: leading dimension of Y_shards (= hidden)
     void *y_ptr[UB_MAX_TP];      // RS: Y_shards[r], for stores that cross a chunk end
     int glu_f;                   // MODE_AG_GLU: F, the width of each half (gate, up) of Wt
+    int a_mn;                    // 1: A is MN-major (stored K x M; tensor map inner dim = M)
+    int b_mn;                    // 1: B is MN-major (stored K x N; tensor map inner dim = N)
     float *ws;                   // partial tiles of split tail tiles: [num_pairs][2][256/4][128][4] fp32
     uint32_t *ws_flags;          // [num_pairs][2][EPI_WARPS]: epoch of the partial written
 };

@@ -29,14 +29,14 @@ ERRORS = {
 CODES = {v: k for k, v in ERRORS.items()}
 OPTIONS = {"sm_margin": 1, "timeout_ns": 2, "self_rank": 3, "drop_flag": 4, "profile": 5,
            "cta_pair": 6, "streamk": 7, "copy_streams": 8}
-OPS = {"ag": 0, "rs": 1, "ag_swiglu": 2}
+OPS = {"ag": 0, "rs": 1, "ag_swiglu": 2, "ag_kn": 3, "rs_kn": 4, "wgrad": 5}
 MAX_TP = 8
 EXPORTS = [
     "ub_create", "ub_destroy", "ub_set_active_shape", "ub_set_active_shape_nd",
     "ub_validate_active_shape", "ub_get_active_shape", "ub_get_capacity", "ub_get_tp",
     "ub_buffer", "ag_gemm", "gemm_rs", "ub_set_option", "ub_get_option", "ub_query_status",
     "ub_clear_status", "ub_get_counters", "ub_kernel_time", "ub_grid_ctas", "ub_last_error",
-    "ag_gemm_noalloc", "ag_gemm_swiglu",
+    "ag_gemm_noalloc", "ag_gemm_swiglu", "ag_gemm_kn", "gemm_rs_kn", "ub_wgrad",
 ]
 NOALLOC_MAX_ELEMS = 16 * 1024 * 1024
 
@@ -80,6 +80,9 @@ def load():
         "ub_buffer": [P, PP, ctypes.POINTER(ctypes.c_size_t)],
         "ag_gemm": [P, PP, P, I64, P, P],
         "ag_gemm_swiglu": [P, PP, P, I64, P, P],
+        "ag_gemm_kn": [P, PP, P, I64, P, P],
+        "gemm_rs_kn": [P, PP, PP, I64, PP, P],
+        "ub_wgrad": [P, P, I64, I, P, P],
         "gemm_rs": [P, PP, PP, I64, PP, P],
         "ub_set_option": [P, I, I64],
         "ub_get_option": [P, I, ctypes.POINTER(I64)],
@@ -284,6 +287,67 @@ class UserBuffer:
         _check(load().ag_gemm_swiglu(self._h, _ptrs(shards), ctypes.c_void_p(Wt.data_ptr()), F,
                                      ctypes.c_void_p(Z.data_ptr()), _stream_ptr(stream)))
         return Z
+
+    def ag_gemm_kn(self, shards, W: torch.Tensor, Y: torch.Tensor | None = None, stream=None):
+        """Y[T, N] = concat_r(shards[r]) @ W with W stored [hidden, N] (e.g. the
+        row-parallel input gradient dS @ Bt_j). The gathered input stays in the buffer."""
+        T, H = self.active_shape
+        if len(shards) != self.tp:
+            raise ValueError("expected %d shards, got %d" % (self.tp, len(shards)))
+        c = T // self.tp
+        for r, s in enumerate(shards):
+            _bf16_cuda(s, "shards[%d]" % r, (c, H))
+        _bf16_cuda(W, "W")
+        if W.dim() != 2 or W.shape[0] != H:
+            raise ValueError("W must be [%d, N], got %s" % (H, tuple(W.shape)))
+        N = W.shape[1]
+        if Y is None:
+            Y = torch.empty((T, N), dtype=torch.bfloat16, device=W.device)
+        _bf16_cuda(Y, "Y")
+        if Y.dim() != 2 or Y.shape[0] < T or Y.shape[1] != N:
+            raise ValueError("Y must be [>=%d, %d], got %s" % (T, N, tuple(Y.shape)))
+        _check(load().ag_gemm_kn(self._h, _ptrs(shards), ctypes.c_void_p(W.data_ptr()), N,
+                                 ctypes.c_void_p(Y.data_ptr()), _stream_ptr(stream)))
+        return Y
+
+    def gemm_rs_kn(self, A, B, Y_shards=None, stream=None):
+        """Y_shards[r] = rows [r*c, (r+1)*c) of sum_j A[j] @ B[j], B[j] stored [K, hidden]
+        (e.g. the column-parallel input gradient sum_j dY_j @ Wt_j)."""
+        T, H = self.active_shape
+        if len(A) != self.tp or len(B) != self.tp:
+            raise ValueError("expected %d A and B operands" % self.tp)
+        K = A[0].shape[1] if A[0].dim() == 2 else -1
+        for j in range(self.tp):
+            _bf16_cuda(A[j], "A[%d]" % j, (T, K))
+            _bf16_cuda(B[j], "B[%d]" % j, (K, H))
+        c = T // self.tp
+        if Y_shards is None:
+            Y_shards = [torch.empty((c, H), dtype=torch.bfloat16, device=A[0].device)
+                        for _ in range(self.tp)]
+        for r, y in enumerate(Y_shards):
+            _bf16_cuda(y, "Y_shards[%d]" % r)
+            if y.dim() != 2 or y.shape[0] < c or y.shape[1] != H:
+                raise ValueError("Y_shards[%d] must be [>=%d, %d]" % (r, c, H))
+        _check(load().gemm_rs_kn(self._h, _ptrs(A), _ptrs(B), K, _ptrs(Y_shards),
+                                 _stream_ptr(stream)))
+        return Y_shards
+
+    def wgrad(self, D: torch.Tensor, ub_is_a: bool = False, out: torch.Tensor | None = None,
+              stream=None):
+        """Weight gradient over the T active rows of the gathered buffer G:
+        ub_is_a=False -> out [M, hidden] = D.T @ G; ub_is_a=True -> out [hidden, M] = G.T @ D."""
+        T, H = self.active_shape
+        _bf16_cuda(D, "D")
+        if D.dim() != 2 or D.shape[0] != T:
+            raise ValueError("D must be [%d, M], got %s" % (T, tuple(D.shape)))
+        M = D.shape[1]
+        shape = (H, M) if ub_is_a else (M, H)
+        if out is None:
+            out = torch.empty(shape, dtype=torch.bfloat16, device=D.device)
+        _bf16_cuda(out, "out", shape)
+        _check(load().ub_wgrad(self._h, ctypes.c_void_p(D.data_ptr()), M, int(bool(ub_is_a)),
+                               ctypes.c_void_p(out.data_ptr()), _stream_ptr(stream)))
+        return out
 
     def gemm_rs(self, A, Bt, Y_shards=None, stream=None):
         """Y_shards[r] = rows [r*c, (r+1)*c) of sum_j A[j] @ Bt[j].T (c = T / tp)."""

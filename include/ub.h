@@ -87,7 +87,15 @@ enum {
 };
 
 /* Operation ids for ub_kernel_time. */
-enum { UB_OP_AG = 0, UB_OP_RS = 1, UB_OP_AG_SWIGLU = 2 };
+enum {
+    UB_OP_AG = 0,
+    UB_OP_RS = 1,
+    UB_OP_AG_SWIGLU = 2,
+    UB_OP_AG_KN = 3,
+    UB_OP_RS_KN = 4,
+    UB_OP_WGRAD = 5,
+    UB_NUM_OPS = 6
+};
 
 /*
  * Register a user buffer at capacity [max_tokens, hidden] for tp virtual ranks
@@ -165,6 +173,19 @@ int ag_gemm_swiglu(ub_handle_t h, const void *const *shards, const void *Wt, int
                    void *stream);
 
 /*
+ * The same all-gather + GEMM with the weight stored in its mathematical layout,
+ * W[hidden][N] row-major (the tensor core reads it MN-major):
+ *     Y[t][n] = sum_h UB[t][h] * W[h][n].
+ * This is also the input gradient of the row-parallel layer ([P1] MLP diagram, fc2, in
+ * the backward pass): the shards are the output-gradient chunks dY_r [c, hidden] and W
+ * is that layer's shard weight Bt_j [hidden, K] (N = K), giving dA_j = dS * Bt_j with dS
+ * the gathered dY (left in the buffer for ub_wgrad). Always on CTA pairs.
+ * Errors: as ag_gemm.
+ */
+int ag_gemm_kn(ub_handle_t h, const void *const *shards, const void *W, int64_t N, void *Y,
+               void *stream);
+
+/*
  * GEMM + reduce-scatter for the row-parallel linear ([P1] MLP diagram, fc2; [P2]
  * "Implementation approach": row blocks from the active first dimension):
  *     S[t][n]        = sum_{j<tp} sum_{k<K} A_j[t][k] * Bt_j[n][k]   (fp32, in TMEM)
@@ -177,6 +198,30 @@ int ag_gemm_swiglu(ub_handle_t h, const void *const *shards, const void *Wt, int
  */
 int gemm_rs(ub_handle_t h, const void *const *A, const void *const *Bt, int64_t K,
             void *const *Y_shards, void *stream);
+
+/*
+ * The same GEMM + reduce-scatter with the shard weights stored K x hidden row-major
+ * (B_j[k][n], read MN-major):  Y_shards[r][i][n] = sum_j sum_k A_j[r*c + i][k] * B_j[k][n].
+ * This is also the input gradient of the column-parallel layer ([P1] QKV / fc1, in the
+ * backward pass): A_j = dY_j [T, N_j] and B_j = that layer's weight shard Wt_j [N_j,
+ * hidden] (K = N_j), so dX_r = rows_r of sum_j dY_j * Wt_j. Always on CTA pairs.
+ * Errors: as gemm_rs.
+ */
+int gemm_rs_kn(ub_handle_t h, const void *const *A, const void *const *B, int64_t K,
+               void *const *Y_shards, void *stream);
+
+/*
+ * Weight gradient over the active tokens, reading the gathered rows G = UB[0:T] that
+ * the last ag_gemm / ag_gemm_kn / ag_gemm_swiglu of this handle left in the buffer:
+ *   ub_is_a = 0:  out[m][h] = sum_{t<T} D[t][m] * G[t][h]   (out [M, hidden]: dWt of the
+ *                 column-parallel layer, D = dY [T, M])
+ *   ub_is_a = 1:  out[h][m] = sum_{t<T} G[t][h] * D[t][m]   (out [hidden, M]: dBt_j of
+ *                 the row-parallel layer, G = the gathered dS, D = A_j [T, M])
+ * fp32 accumulation over t, one BF16 rounding. Both operands are read MN-major; CTA
+ * pairs. Call it on the stream of that gather (it reads the buffer without waiting).
+ * Errors: UB_ERR_ARG, UB_ERR_ZERO (M <= 0), UB_ERR_ALIGN (M % 8, pointers), UB_ERR_CUDA.
+ */
+int ub_wgrad(ub_handle_t h, const void *D, int64_t M, int ub_is_a, void *out, void *stream);
 
 /* Options (UB_OPT_*). UB_ERR_ARG for an unknown key or an out-of-range value. */
 int ub_set_option(ub_handle_t h, int key, int64_t val);
@@ -204,8 +249,7 @@ typedef struct {
 int ub_get_counters(ub_handle_t h, ub_counters_t *out);
 
 /*
- * With UB_OPT_PROFILE = 1, every GEMM kernel launch of operation `op` (UB_OP_AG,
- * UB_OP_RS or UB_OP_AG_SWIGLU) is bracketed by CUDA events on its launch stream (up to 4096 launches are
+ * With UB_OPT_PROFILE = 1, every GEMM kernel launch of operation `op` (a UB_OP_* id) is bracketed by CUDA events on its launch stream (up to 4096 launches are
  * kept). This call waits for the last recorded launch, returns the summed kernel time
  * in milliseconds and the launch count, and clears the record.
  */
