@@ -68,7 +68,8 @@ def parse():
     ap.add_argument("--no-padded", action="store_true",
                     help="skip the padded-to-capacity comparator")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--case", choices=["ag", "rs", "ag_swiglu"], default=None,
+    ap.add_argument("--case", choices=["ag", "rs", "ag_swiglu", "ag_kn", "rs_kn", "wgrad_g", "wgrad_s"],
+                    default=None,
                     help="time one op of the workload at one T only (small profiling case)")
     ap.add_argument("--case-T", type=int, default=8192)
     ap.add_argument("--case-reps", type=int, default=3)
@@ -650,7 +651,33 @@ def run_case(args):
     buf.set_option("sm_margin", args.sm_margin)
     buf.set_active_shape([T, H])
     c = T // tp
-    if args.case in ("ag", "ag_swiglu"):
+    if args.case in ("ag_kn", "rs_kn", "wgrad_g", "wgrad_s"):
+        # backward of the workload's MLP: fc2 dgrad (AG of dY times Bt [H, K]), fc1 dgrad
+        # (RS over dZ_j Wt_j, Wt_j [N, H] with K = N/2 per rank as in the fused fc1),
+        # fc1 wgrad dWt = dZ^T G, fc2 wgrad dBt = dS^T A
+        F = K
+        if args.case == "ag_kn":
+            dY = synth.normal_bf16((T, H), 1.0, g, dev)
+            Bt = synth.normal_bf16((H, F), 1.0 / math.sqrt(F), g, dev)
+            out = torch.empty((T, F), dtype=torch.bfloat16, device=dev)
+            shards = [dY[r * c:(r + 1) * c] for r in range(tp)]
+            fn = lambda: buf.ag_gemm_kn(shards, Bt, out)
+            flops = 2.0 * T * H * F
+        elif args.case == "rs_kn":
+            dZ = [synth.normal_bf16((T, F), 1.0, g, dev) for _ in range(tp)]
+            Wt = [synth.normal_bf16((F, H), 1.0 / math.sqrt(H), g, dev) for _ in range(tp)]
+            Ys = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+            outs = [Ys[r * c:(r + 1) * c] for r in range(tp)]
+            fn = lambda: buf.gemm_rs_kn(dZ, Wt, outs)
+            flops = 2.0 * T * F * H * tp
+        else:
+            X = synth.normal_bf16((T, H), 1.0, g, dev)
+            W1 = synth.normal_bf16((N, H), 1.0 / math.sqrt(H), g, dev)
+            buf.ag_gemm([X[r * c:(r + 1) * c] for r in range(tp)], W1)   # gathers G
+            Dm = synth.normal_bf16((T, N if args.case == "wgrad_g" else F), 1.0, g, dev)
+            fn = (lambda: buf.wgrad(Dm)) if args.case == "wgrad_g" else (lambda: buf.wgrad(Dm, ub_is_a=True))
+            flops = 2.0 * T * H * Dm.shape[1]
+    elif args.case in ("ag", "ag_swiglu"):
         X = synth.normal_bf16((T, H), 1.0, g, dev)
         W1 = synth.normal_bf16((N, H), 1.0 / math.sqrt(H), g, dev)
         shards = [X[r * c:(r + 1) * c] for r in range(tp)]
@@ -671,12 +698,13 @@ def run_case(args):
     buf.set_option("profile", 1)
     fn()
     torch.cuda.synchronize()
-    first_ms, _ = buf.kernel_time(args.case)
+    op_name = {"wgrad_g": "wgrad", "wgrad_s": "wgrad"}.get(args.case, args.case)
+    first_ms, _ = buf.kernel_time(op_name)
     first_status = buf.query_status()
     for _ in range(args.case_reps):
         fn()
     torch.cuda.synchronize()
-    ms, n = buf.kernel_time(args.case)
+    ms, n = buf.kernel_time(op_name)
     status = buf.query_status()
     buf.close()
     print(json.dumps({"case": args.case, "T": T, "cta_pair": args.cta_pair, "streamk": args.streamk,
