@@ -22,6 +22,8 @@ What it computes (fp64 accumulation of exactly widened bf16 inputs):
 * ``gemm_xw_rows`` / ``gemm_tn`` -- the weight in its K x N layout, and the
   contraction over the T active tokens: the products of the backward pass (input and
   weight gradients of both layers).
+* ``reduce_scatter`` -- the "bulk" method's independent reduce-scatter of tp partial
+  results ("How to setup TP Overlap configs", option "method": "bulk").
 * ``swiglu`` -- the activation between fc1 and fc2 (the GELU/SwiGLU box of the MLP
   diagram in discussion #1240): fc1's row is [gate | up] and ``Z = silu(gate) * up``.
 
@@ -73,6 +75,7 @@ def _load():
                                             P, P, P]
         lib.oracle_gemm_xw_rows.argtypes = [P, I64, P, I64, I64, P, I64, P]
         lib.oracle_gemm_tn.argtypes = [P, I64, P, I64, I64, P]
+        lib.oracle_reduce_scatter.argtypes = [ctypes.c_int, I64, I64, P, P]
         lib.oracle_silu.restype = ctypes.c_double
         lib.oracle_silu.argtypes = [ctypes.c_double]
         lib.oracle_swiglu.argtypes = [P, I64, I64, P]
@@ -251,3 +254,18 @@ def gemm_tn(D, G):
     out = np.empty((M, N), dtype=np.float64)
     _load().oracle_gemm_tn(_ptr(D), M, _ptr(G), N, T, _ptr(out))
     return out
+
+
+def reduce_scatter(P):
+    """[Y_r]: rank r's row block of sum_j P[j] (fp64), P[j] [T, H] bf16 bit patterns."""
+    P = [_u16(a) for a in P]
+    tp = len(P)
+    T, H = P[0].shape
+    for a in P:
+        assert a.shape == (T, H)
+    assert T % tp == 0
+    c = T // tp
+    Y = [np.empty((c, H), dtype=np.float64) for _ in range(tp)]
+    yptrs = (ctypes.c_void_p * tp)(*[_ptr(y) for y in Y])
+    _load().oracle_reduce_scatter(tp, T, H, _ptr_array(P), yptrs)
+    return Y

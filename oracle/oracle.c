@@ -237,6 +237,26 @@ void oracle_gemm_tn(const uint16_t *D, int64_t M, const uint16_t *G, int64_t N, 
     }
 }
 
+/* Reduce-scatter of tp partial results (the "bulk" method's independent reduce-scatter
+ * in "How to setup TP Overlap configs"): every rank holds a full partial P_j [T, H];
+ * rank r keeps rows [r*c, (r+1)*c) of their sum, Y_r[i][n] = sum_{j<tp} P_j[r*c + i][n],
+ * summed in the order j = 0..tp-1 in double. */
+void oracle_reduce_scatter(int tp, int64_t T, int64_t H, const uint16_t *const *P, double *const *Yr)
+{
+    int64_t c = oracle_chunk_rows(T, tp);
+    int64_t t;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (t = 0; t < T; ++t) {
+        int r = (int)(t / c);
+        int64_t i = t - oracle_chunk_offset(T, tp, r);
+        for (int64_t n = 0; n < H; ++n) {
+            double s = 0.0;
+            for (int j = 0; j < tp; ++j) s += bf16_to_double(P[j][t * H + n]);
+            Yr[r][i * H + n] = s;
+        }
+    }
+}
+
 /* SwiGLU between the column-parallel fc1 and the row-parallel fc2 (the GELU/SwiGLU box
  * of the MLP diagram in "Do tp overlap support thd..."): fc1's output row holds the
  * gate half first and the up half second, Y[t] = [g_0..g_{F-1}, u_0..u_{F-1}], and

@@ -407,3 +407,33 @@ def test_backward_products_match_forward_identities():
         assert lhs_x == np.sum(dX * bits_to_f64(Xp))
         lhs_w = np.sum(bits_to_f64(dY) * oracle.gemm_rows(X, Wp, np.arange(T)))
         assert lhs_w == np.sum(dWt * bits_to_f64(Wp))
+
+
+# ---------------------------------------------------------------- bulk reduce-scatter
+
+def test_reduce_scatter_integer_and_ownership():
+    g = synth.generator(seed=81)
+    for tp, T, H in [(1, 5, 3), (2, 8, 4), (4, 12, 7), (3, 9, 16)]:
+        P = [synth.to_u16(synth.small_int_bf16((T, H), -8, 8, g)) for _ in range(tp)]
+        Y = oracle.reduce_scatter(P)
+        S = sum(bits_to_f64(p).astype(np.int64) for p in P)
+        c = T // tp
+        for r in range(tp):
+            np.testing.assert_array_equal(Y[r], S[r * c:(r + 1) * c].astype(np.float64))
+        # planted mistake: a shard left out of the sum
+        if tp > 1:
+            Yd = oracle.reduce_scatter(P[:-1] + [np.zeros_like(P[0])])
+            assert not all(np.array_equal(a, b) for a, b in zip(Yd, Y)) or not np.any(bits_to_f64(P[-1]))
+
+
+def test_reduce_scatter_of_shard_products_is_gemm_rs():
+    """RS of the per-shard products equals the pinned GEMM-RS (exact on integers)."""
+    g = synth.generator(seed=82)
+    tp, T, K, H = 4, 8, 5, 6
+    A = [synth.to_u16(synth.small_int_bf16((T, K), -3, 3, g)) for _ in range(tp)]
+    Bt = [synth.to_u16(synth.small_int_bf16((H, K), -3, 3, g)) for _ in range(tp)]
+    # each product is small enough to be exact in bf16, so P_j can be stored as bf16
+    P = [bf16_bits(oracle.gemm_rows(a, b, np.arange(T))) for a, b in zip(A, Bt)]
+    _, Yrs = oracle.gemm_rs(A, Bt)
+    for a, b in zip(oracle.reduce_scatter(P), Yrs):
+        np.testing.assert_array_equal(a, b)
