@@ -65,6 +65,8 @@ def parse():
     ap.add_argument("--mlp", choices=["fused", "unfused"], default="fused",
                     help="fused: fc1 runs with the SwiGLU epilogue and feeds virtual rank 0's fc2 "
                          "input (default); unfused: plain fc1 output [T, 7168]")
+    ap.add_argument("--no-bulk", action="store_true",
+                    help="skip the bulk-overlap measurement")
     ap.add_argument("--no-padded", action="store_true",
                     help="skip the padded-to-capacity comparator")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -377,6 +379,63 @@ def padded_measure(wl, steps, warmup, stream, world):
     return ms
 
 
+def bulk_measure(wl, stream, T=4096, reps=10):
+    """The "bulk" method at one microbatch of the workload: an independent collective on
+    a second stream beside an unrelated GEMM. fc1 backward: its input-gradient GEMM
+    (gemm_rs_kn over dZ_j Wt_j) beside the bulk all-gather of its input X (needed by its
+    weight gradient); then its weight-gradient GEMM beside a bulk reduce-scatter of tp
+    bf16 partials [T, hidden]. Times are ms per pair of operations."""
+    w = wl.w
+    H, F, tp = w.hidden, w.rs_k[0], w.tp
+    dev = wl.W1.device
+    g = synth.generator(dev, 17)
+    c = T // tp
+    X = synth.normal_bf16((T, H), 1.0, g, dev)
+    dZ = [synth.normal_bf16((T, F), 1.0, g, dev) for _ in range(tp)]
+    Wt = [synth.normal_bf16((F, H), 1.0 / math.sqrt(H), g, dev) for _ in range(tp)]
+    P = [synth.normal_bf16((T, H), 1.0, g, dev) for _ in range(tp)]
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    outs = [out[r * c:(r + 1) * c] for r in range(tp)]
+    Ys = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    ys = [Ys[r * c:(r + 1) * c] for r in range(tp)]
+    dW = torch.empty((F, H), dtype=torch.bfloat16, device=dev)
+    shards = [X[r * c:(r + 1) * c] for r in range(tp)]
+    side = torch.cuda.Stream(dev)
+    buf = wl.buf
+    buf.set_active_shape([T, H])
+    buf.allgather(shards, stream=stream)      # the buffer holds X for the wgrad runs
+
+    def timed(fn):
+        return time_steps(fn, reps, 2, stream, 1) / reps
+
+    def both(gemm, coll):
+        def fn():
+            side.wait_stream(stream)
+            gemm()
+            coll()
+            stream.wait_stream(side)
+        return fn
+
+    dgrad = lambda: buf.gemm_rs_kn(dZ, Wt, outs, stream=stream)
+    ag_side = lambda: buf.allgather(shards, stream=side)
+    ag_alone = lambda: buf.allgather(shards, stream=stream)
+    wgrad = lambda: buf.wgrad(dZ[0], out=dW, stream=stream)
+    rs_side = lambda: buf.reduce_scatter(P, ys, stream=side)
+    rs_alone = lambda: buf.reduce_scatter(P, ys, stream=stream)
+    res = {"T": T}
+    for name, gemm, coll_side, coll_alone, coll_bytes in (
+            ("allgather_beside_dgrad", dgrad, ag_side, ag_alone, 2 * T * H * 2),
+            ("reduce_scatter_beside_wgrad", wgrad, rs_side, rs_alone, (tp + 1) * T * H * 2)):
+        t_g = timed(gemm)
+        t_c = timed(coll_alone)
+        t_b = timed(both(gemm, coll_side))
+        res[name] = {"gemm_ms": t_g, "collective_ms": t_c, "sequential_ms": t_g + t_c,
+                     "overlapped_ms": t_b, "hidden_fraction": (t_g + t_c - t_b) / t_c if t_c > 0 else None,
+                     "collective_gbs": coll_bytes / (t_c / 1e3) / 1e9}
+    assert buf.query_status() == 0
+    return res
+
+
 def cpu_baseline(wl, seconds):
     """The oracle as it stands, on a row sample of one microbatch of the workload."""
     import oracle
@@ -484,6 +543,7 @@ def run_ours(args):
                   "active_speedup": p_ms / (ms / args.steps),
                   "what": "same microbatches padded to max_tokens=%d (real tokens first, zeros "
                           "after); useful FLOPs only" % w.max_tokens}
+    bulk = bulk_measure(wl, stream) if not args.no_bulk and rank == 0 else None
     sweep = sweep_points(wl, stream) if args.sweep and rank == 0 else None
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -511,6 +571,7 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "padded_comparator": padded,
+        "bulk_overlap": bulk,
         "clocks": clk,
         "flops_per_step": {"ag": ag_flops, "rs": rs_flops},
     }

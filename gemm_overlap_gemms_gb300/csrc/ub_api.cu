@@ -311,6 +311,50 @@ int launch(ub_handle *h, const GemmParams &p, int mode, bool pair, cudaStream_t 
     return UB_OK;
 }
 
+
+// The all-gather of the chunks into the user buffer: device-to-device copies dealt over
+// the copy streams in ring order after the self rank (the self chunk last), each
+// followed by a stream memory write of `epoch` into the chunk's readiness flag (skipped
+// for chunk `drop`, a host-side fault injection). The copy streams first wait for the
+// work already queued on `s`.
+int issue_gather(ub_handle *h, const void *const *shards, cudaStream_t s, uint32_t epoch, int64_t drop)
+{
+    const int tp = h->tp;
+    const int64_t T = h->T, H = h->hidden, c = T / tp;
+    const int self = static_cast<int>(h->self_rank);
+    char *ub = static_cast<char *>(h->ub);
+    const int ncs = static_cast<int>(h->copy_streams < tp ? h->copy_streams : tp);
+    auto copy_stream = [&](int i) { return i == 0 ? h->side : h->extra_side[i]; };
+    UB_CUDA(cudaEventRecord(h->ev_fork, s));
+    for (int i = 0; i < ncs; ++i) UB_CUDA(cudaStreamWaitEvent(copy_stream(i), h->ev_fork, 0));
+    for (int q = 1; q <= tp; ++q) {
+        const int r = (self + q) % tp;
+        cudaStream_t cs = copy_stream((q - 1) % ncs);
+        UB_CUDA(cudaMemcpyAsync(ub + r * c * H * 2, shards[r], static_cast<size_t>(c * H * 2),
+                                cudaMemcpyDeviceToDevice, cs));
+        if (r != drop) {
+            CUresult cr = driver().write_value32(reinterpret_cast<CUstream>(cs),
+                                                 reinterpret_cast<CUdeviceptr>(flags_of(h) + r), epoch,
+                                                 CU_STREAM_WRITE_VALUE_DEFAULT);
+            if (cr != CUDA_SUCCESS) return fail(UB_ERR_CUDA, "cuStreamWriteValue32 failed (%d)", (int)cr);
+        }
+    }
+    return UB_OK;
+}
+
+// Make `s` wait for every copy stream the last gather used.
+int join_gather(ub_handle *h, cudaStream_t s)
+{
+    const int ncs = static_cast<int>(h->copy_streams < h->tp ? h->copy_streams : h->tp);
+    UB_CUDA(cudaEventRecord(h->ev_join, h->side));
+    UB_CUDA(cudaStreamWaitEvent(s, h->ev_join, 0));
+    for (int i = 1; i < ncs; ++i) {
+        UB_CUDA(cudaEventRecord(h->ev_join_extra[i], h->extra_side[i]));
+        UB_CUDA(cudaStreamWaitEvent(s, h->ev_join_extra[i], 0));
+    }
+    return UB_OK;
+}
+
 int check_handle(ub_handle *h)
 {
     if (!h) return fail(UB_ERR_ARG, "null handle");
@@ -600,34 +644,10 @@ static int ag_gemm_impl(ub_handle_t h, const void *const *shards, const void *Wt
     const int64_t drop = h->drop_flag;
     h->drop_flag = -1;
 
-    // Fork the copy streams off `s`: they start once the work already queued on
-    // `s` (which may still read the buffer) is done.
-    const int ncs = static_cast<int>(h->copy_streams < tp ? h->copy_streams : tp);
-    auto copy_stream = [&](int i) { return i == 0 ? h->side : h->extra_side[i]; };
-    UB_CUDA(cudaEventRecord(h->ev_fork, s));
-    for (int i = 0; i < ncs; ++i) UB_CUDA(cudaStreamWaitEvent(copy_stream(i), h->ev_fork, 0));
-    // Ring order after the self rank; the self chunk (read in place by the GEMM) last.
-    // With several copy streams the chunks are dealt round-robin over them.
-    for (int q = 1; q <= tp; ++q) {
-        const int r = (self + q) % tp;
-        cudaStream_t cs = copy_stream((q - 1) % ncs);
-        UB_CUDA(cudaMemcpyAsync(ub + r * c * H * 2, shards[r], static_cast<size_t>(c * H * 2),
-                                cudaMemcpyDeviceToDevice, cs));
-        if (r != drop) {
-            CUresult cr = driver().write_value32(reinterpret_cast<CUstream>(cs),
-                                                 reinterpret_cast<CUdeviceptr>(flags_of(h) + r), epoch,
-                                                 CU_STREAM_WRITE_VALUE_DEFAULT);
-            if (cr != CUDA_SUCCESS) return fail(UB_ERR_CUDA, "cuStreamWriteValue32 failed (%d)", (int)cr);
-        }
-    }
+    if (int rc = issue_gather(h, shards, s, epoch, drop)) return rc;
     int rc = launch(h, p, mode, pair, s, prof_op);
     // Join the copy streams back into `s` even if the launch failed.
-    UB_CUDA(cudaEventRecord(h->ev_join, h->side));
-    UB_CUDA(cudaStreamWaitEvent(s, h->ev_join, 0));
-    for (int i = 1; i < ncs; ++i) {
-        UB_CUDA(cudaEventRecord(h->ev_join_extra[i], h->extra_side[i]));
-        UB_CUDA(cudaStreamWaitEvent(s, h->ev_join_extra[i], 0));
-    }
+    if (int jrc = join_gather(h, s)) return jrc;
     if (rc != UB_OK) return rc;
     ++h->counters.ag_calls;
     h->counters.last_T = T;
@@ -748,6 +768,71 @@ int gemm_rs_kn(ub_handle_t h, const void *const *A, const void *const *B, int64_
                void *stream)
 {
     return gemm_rs_impl(h, A, B, K, Y_shards, stream, true);
+}
+
+int ub_allgather(ub_handle_t h, const void *const *shards, void *stream)
+{
+    if (int rc = check_handle(h)) return rc;
+    if (!shards) return fail(UB_ERR_ARG, "ub_allgather: null pointer argument");
+    for (int r = 0; r < h->tp; ++r) {
+        if (!shards[r]) return fail(UB_ERR_ARG, "ub_allgather: shard %d is null", r);
+        if (!aligned16(shards[r])) return fail(UB_ERR_ALIGN, "ub_allgather: shard %d not 16-byte aligned", r);
+    }
+    DeviceGuard g(h->device);
+    if (!g.ok) return fail(UB_ERR_CUDA, "ub_allgather: cannot select the handle's device");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const uint32_t epoch = ++h->epoch;
+    if (int rc = issue_gather(h, shards, s, epoch, -1)) return rc;
+    if (int rc = join_gather(h, s)) return rc;
+    h->counters.last_T = h->T;
+    return UB_OK;
+}
+
+int ub_reduce_scatter(ub_handle_t h, const void *const *P, void *const *Y_shards, void *stream)
+{
+    if (int rc = check_handle(h)) return rc;
+    if (!P || !Y_shards) return fail(UB_ERR_ARG, "ub_reduce_scatter: null pointer argument");
+    const int tp = h->tp;
+    ubk::BulkRsParams p;
+    memset(&p, 0, sizeof p);
+    for (int j = 0; j < tp; ++j) {
+        if (!P[j] || !Y_shards[j]) return fail(UB_ERR_ARG, "ub_reduce_scatter: pointer %d is null", j);
+        if (!aligned16(P[j]) || !aligned16(Y_shards[j]))
+            return fail(UB_ERR_ALIGN, "ub_reduce_scatter: pointer %d not 16-byte aligned", j);
+        p.P[j] = P[j];
+        p.Y[j] = Y_shards[j];
+    }
+    DeviceGuard g(h->device);
+    if (!g.ok) return fail(UB_ERR_CUDA, "ub_reduce_scatter: cannot select the handle's device");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    p.tp = tp;
+    p.T = h->T;
+    p.H = h->hidden;
+    p.c = h->T / tp;
+    // Two small CTAs per SM: they fit beside a persistent GEMM CTA on the same SM.
+    const int64_t vecs = p.T * (p.H / 8);
+    int64_t grid = 2 * static_cast<int64_t>(h->sm_count);
+    if (grid > (vecs + 255) / 256) grid = (vecs + 255) / 256;
+    ProfileRing &ring = h->prof[UB_OP_REDUCE_SCATTER];
+    const bool timed = h->profile != 0 && ring.count < kMaxProfiled;
+    if (timed) {
+        if (static_cast<int>(ring.start.size()) <= ring.count) {
+            cudaEvent_t e0, e1;
+            UB_CUDA(cudaEventCreate(&e0));
+            UB_CUDA(cudaEventCreate(&e1));
+            ring.start.push_back(e0);
+            ring.stop.push_back(e1);
+        }
+        UB_CUDA(cudaEventRecord(ring.start[ring.count], s));
+    }
+    cudaError_t e = ubk::launch_bulk_rs(p, static_cast<int>(grid), s);
+    if (e != cudaSuccess) return cuda_fail(e, "reduce-scatter kernel launch");
+    if (timed) {
+        UB_CUDA(cudaEventRecord(ring.stop[ring.count], s));
+        ++ring.count;
+    }
+    h->counters.last_T = h->T;
+    return UB_OK;
 }
 
 int ub_wgrad(ub_handle_t h, const void *D, int64_t M, int ub_is_a, void *out, void *stream)

@@ -1,0 +1,73 @@
+// Standalone reduce-scatter of tp partial results: the independent reduce-scatter of
+// the "bulk" overlap method in "How to setup TP Overlap configs" (TransformerEngine
+// issue #1344), run beside an unrelated GEMM (for example the input-gradient partials
+// of a column-parallel layer reduced while its weight-gradient GEMM runs).
+//
+//   Y_shards[r][i][n] = bf16( sum_{j<tp} P_j[r*c + i][n] ),  c = T / tp, fp32 sum in j order
+//
+// The work is HBM-bound: (tp + 1) * T * hidden * 2 bytes for tp * T * hidden adds. Each
+// thread owns 8 consecutive columns of one row (16-byte loads and stores, coalesced
+// across the warp); a grid-stride loop covers the active rows only. The CTAs are small
+// (256 threads, no shared memory) so that they fit on SMs beside a persistent GEMM CTA.
+#include <cuda_bf16.h>
+
+#include "ub_internal.h"
+
+namespace ubk {
+namespace {
+
+__device__ __forceinline__ uint4 ld_stream(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// bf16 -> fp32 is exact: the bf16 pattern is the top half of the fp32 pattern.
+__device__ __forceinline__ void add_bf16x2(uint32_t w, float &lo, float &hi)
+{
+    lo += __uint_as_float(w << 16);
+    hi += __uint_as_float(w & 0xFFFF0000u);
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi)
+{
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+__global__ void __launch_bounds__(256) bulk_rs_kernel(const __grid_constant__ BulkRsParams p)
+{
+    const int64_t vecs_per_row = p.H / 8;
+    const int64_t total = p.T * vecs_per_row;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < total; v += stride) {
+        const int64_t t = v / vecs_per_row;
+        const int64_t col = (v - t * vecs_per_row) * 8;
+        float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int j = 0; j < p.tp; ++j) {
+            const uint4 q = ld_stream(static_cast<const __nv_bfloat16 *>(p.P[j]) + t * p.H + col);
+            add_bf16x2(q.x, a[0], a[1]);
+            add_bf16x2(q.y, a[2], a[3]);
+            add_bf16x2(q.z, a[4], a[5]);
+            add_bf16x2(q.w, a[6], a[7]);
+        }
+        const int64_t r = t / p.c;
+        const int64_t i = t - r * p.c;
+        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.Y[r]) + i * p.H + col);
+        *dst = make_uint4(pack2(a[0], a[1]), pack2(a[2], a[3]), pack2(a[4], a[5]), pack2(a[6], a[7]));
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_bulk_rs(const BulkRsParams &p, int grid, cudaStream_t stream)
+{
+    bulk_rs_kernel<<<grid, 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace ubk

@@ -105,6 +105,17 @@ cudaError_t launch_gemm_pair(const GemmParams &p, int mode, int clusters, cudaSt
 // Clusters of two CTAs of the pair kernel that can be resident at once (0 on error).
 int max_pair_clusters(int mode);
 
+// Standalone reduce-scatter (ub_bulk.cu): Y[r][i][:] = sum_j P[j][r*c + i][:].
+struct BulkRsParams {
+    const void *P[UB_MAX_TP];  // tp partials [T, H] bf16
+    void *Y[UB_MAX_TP];        // tp row blocks [c, H] bf16
+    int tp;
+    int64_t T;
+    int64_t H;                 // multiple of 8
+    int64_t c;
+};
+cudaError_t launch_bulk_rs(const BulkRsParams &p, int grid, cudaStream_t stream);
+
 // Record the message ub_last_error() returns on this host thread.
 void set_last_error(const char *msg);
 

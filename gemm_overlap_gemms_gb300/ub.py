@@ -29,7 +29,7 @@ ERRORS = {
 CODES = {v: k for k, v in ERRORS.items()}
 OPTIONS = {"sm_margin": 1, "timeout_ns": 2, "self_rank": 3, "drop_flag": 4, "profile": 5,
            "cta_pair": 6, "streamk": 7, "copy_streams": 8}
-OPS = {"ag": 0, "rs": 1, "ag_swiglu": 2, "ag_kn": 3, "rs_kn": 4, "wgrad": 5}
+OPS = {"ag": 0, "rs": 1, "ag_swiglu": 2, "ag_kn": 3, "rs_kn": 4, "wgrad": 5, "reduce_scatter": 6}
 MAX_TP = 8
 EXPORTS = [
     "ub_create", "ub_destroy", "ub_set_active_shape", "ub_set_active_shape_nd",
@@ -37,6 +37,7 @@ EXPORTS = [
     "ub_buffer", "ag_gemm", "gemm_rs", "ub_set_option", "ub_get_option", "ub_query_status",
     "ub_clear_status", "ub_get_counters", "ub_kernel_time", "ub_grid_ctas", "ub_last_error",
     "ag_gemm_noalloc", "ag_gemm_swiglu", "ag_gemm_kn", "gemm_rs_kn", "ub_wgrad",
+    "ub_allgather", "ub_reduce_scatter",
 ]
 NOALLOC_MAX_ELEMS = 16 * 1024 * 1024
 
@@ -83,6 +84,8 @@ def load():
         "ag_gemm_kn": [P, PP, P, I64, P, P],
         "gemm_rs_kn": [P, PP, PP, I64, PP, P],
         "ub_wgrad": [P, P, I64, I, P, P],
+        "ub_allgather": [P, PP, P],
+        "ub_reduce_scatter": [P, PP, PP, P],
         "gemm_rs": [P, PP, PP, I64, PP, P],
         "ub_set_option": [P, I, I64],
         "ub_get_option": [P, I, ctypes.POINTER(I64)],
@@ -348,6 +351,34 @@ class UserBuffer:
         _check(load().ub_wgrad(self._h, ctypes.c_void_p(D.data_ptr()), M, int(bool(ub_is_a)),
                                ctypes.c_void_p(out.data_ptr()), _stream_ptr(stream)))
         return out
+
+    def allgather(self, shards, stream=None):
+        """Bulk all-gather: UB[r*c + i] = shards[r][i] for the active shape, no GEMM."""
+        T, H = self.active_shape
+        if len(shards) != self.tp:
+            raise ValueError("expected %d shards, got %d" % (self.tp, len(shards)))
+        c = T // self.tp
+        for r, s in enumerate(shards):
+            _bf16_cuda(s, "shards[%d]" % r, (c, H))
+        _check(load().ub_allgather(self._h, _ptrs(shards), _stream_ptr(stream)))
+
+    def reduce_scatter(self, P, Y_shards=None, stream=None):
+        """Bulk reduce-scatter: Y_shards[r] = rows [r*c, (r+1)*c) of sum_j P[j]."""
+        T, H = self.active_shape
+        if len(P) != self.tp:
+            raise ValueError("expected %d partials" % self.tp)
+        for j, x in enumerate(P):
+            _bf16_cuda(x, "P[%d]" % j, (T, H))
+        c = T // self.tp
+        if Y_shards is None:
+            Y_shards = [torch.empty((c, H), dtype=torch.bfloat16, device=P[0].device)
+                        for _ in range(self.tp)]
+        for r, y in enumerate(Y_shards):
+            _bf16_cuda(y, "Y_shards[%d]" % r)
+            if y.dim() != 2 or y.shape[0] < c or y.shape[1] != H:
+                raise ValueError("Y_shards[%d] must be [>=%d, %d]" % (r, c, H))
+        _check(load().ub_reduce_scatter(self._h, _ptrs(P), _ptrs(Y_shards), _stream_ptr(stream)))
+        return Y_shards
 
     def gemm_rs(self, A, Bt, Y_shards=None, stream=None):
         """Y_shards[r] = rows [r*c, (r+1)*c) of sum_j A[j] @ Bt[j].T (c = T / tp)."""

@@ -94,7 +94,8 @@ enum {
     UB_OP_AG_KN = 3,
     UB_OP_RS_KN = 4,
     UB_OP_WGRAD = 5,
-    UB_NUM_OPS = 6
+    UB_OP_REDUCE_SCATTER = 6,
+    UB_NUM_OPS = 7
 };
 
 /*
@@ -222,6 +223,26 @@ int gemm_rs_kn(ub_handle_t h, const void *const *A, const void *const *B, int64_
  * Errors: UB_ERR_ARG, UB_ERR_ZERO (M <= 0), UB_ERR_ALIGN (M % 8, pointers), UB_ERR_CUDA.
  */
 int ub_wgrad(ub_handle_t h, const void *D, int64_t M, int ub_is_a, void *out, void *stream);
+
+/*
+ * The "bulk" method of [P3] ("Overlap GEMM with an independent bulk all-gather or
+ * reduce-scatter"): the collective alone, to run on one stream while an unrelated GEMM
+ * runs on another (for example, gather a layer's input for its weight gradient while
+ * its input-gradient GEMM runs, or reduce the input-gradient partials while the
+ * weight-gradient GEMM runs).
+ *
+ * ub_allgather: the all-gather of ag_gemm without the GEMM -- UB[r*c + i] = shards[r][i]
+ * for the active shape, copies and readiness flags on the handle's side streams, joined
+ * back into `stream`. A following ub_wgrad on `stream` reads the gathered rows.
+ *
+ * ub_reduce_scatter: Y_shards[r][i][n] = bf16(sum_{j<tp} P[j][r*c + i][n]) for the
+ * active shape (P: tp device pointers [T, hidden]; Y_shards: tp pointers [c, hidden]);
+ * fp32 sum in j order, one small HBM-bound kernel on `stream` whose CTAs fit beside a
+ * persistent GEMM CTA. Rows >= T of P and rows >= c of each Y_shards[r] are untouched.
+ * Errors: UB_ERR_ARG, UB_ERR_ALIGN (pointers not 16-byte aligned), UB_ERR_CUDA.
+ */
+int ub_allgather(ub_handle_t h, const void *const *shards, void *stream);
+int ub_reduce_scatter(ub_handle_t h, const void *const *P, void *const *Y_shards, void *stream);
 
 /* Options (UB_OPT_*). UB_ERR_ARG for an unknown key or an out-of-range value. */
 int ub_set_option(ub_handle_t h, int key, int64_t val);
