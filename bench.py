@@ -70,7 +70,8 @@ def parse():
     ap.add_argument("--no-padded", action="store_true",
                     help="skip the padded-to-capacity comparator")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--case", choices=["ag", "rs", "ag_swiglu", "ag_kn", "rs_kn", "wgrad_g", "wgrad_s"],
+    ap.add_argument("--case", choices=["ag", "rs", "ag_swiglu", "ag_kn", "rs_kn", "wgrad_g", "wgrad_s",
+                                       "bulk_rs", "bulk_ag"],
                     default=None,
                     help="time one op of the workload at one T only (small profiling case)")
     ap.add_argument("--case-T", type=int, default=8192)
@@ -712,7 +713,22 @@ def run_case(args):
     buf.set_option("sm_margin", args.sm_margin)
     buf.set_active_shape([T, H])
     c = T // tp
-    if args.case in ("ag_kn", "rs_kn", "wgrad_g", "wgrad_s"):
+    nbytes = None
+    if args.case in ("bulk_rs", "bulk_ag"):
+        # the bulk method's collectives alone: bytes moved per call
+        if args.case == "bulk_rs":
+            P = [synth.normal_bf16((T, H), 1.0, g, dev) for _ in range(tp)]
+            Ys = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+            ys = [Ys[r * c:(r + 1) * c] for r in range(tp)]
+            fn = lambda: buf.reduce_scatter(P, ys)
+            nbytes = (tp + 1) * T * H * 2
+        else:
+            X = synth.normal_bf16((T, H), 1.0, g, dev)
+            shards = [X[r * c:(r + 1) * c] for r in range(tp)]
+            fn = lambda: buf.allgather(shards)
+            nbytes = 2 * T * H * 2
+        flops = 0.0
+    elif args.case in ("ag_kn", "rs_kn", "wgrad_g", "wgrad_s"):
         # backward of the workload's MLP: fc2 dgrad (AG of dY times Bt [H, K]), fc1 dgrad
         # (RS over dZ_j Wt_j, Wt_j [N, H] with K = N/2 per rank as in the fused fc1),
         # fc1 wgrad dWt = dZ^T G, fc2 wgrad dBt = dS^T A
@@ -759,7 +775,14 @@ def run_case(args):
     buf.set_option("profile", 1)
     fn()
     torch.cuda.synchronize()
-    op_name = {"wgrad_g": "wgrad", "wgrad_s": "wgrad"}.get(args.case, args.case)
+    op_name = {"wgrad_g": "wgrad", "wgrad_s": "wgrad", "bulk_rs": "reduce_scatter"}.get(args.case, args.case)
+    if args.case == "bulk_ag":
+        # no kernel of ours to time: CUDA events around the whole call on the stream
+        torch.cuda.synchronize()
+        t_ms = time_steps(fn, args.case_reps, 2, torch.cuda.current_stream(), 1) / args.case_reps
+        print(json.dumps({"case": args.case, "T": T, "us": 1e3 * t_ms, "gbs": nbytes / (t_ms / 1e3) / 1e9}))
+        buf.close()
+        return
     first_ms, _ = buf.kernel_time(op_name)
     first_status = buf.query_status()
     for _ in range(args.case_reps):
@@ -770,7 +793,8 @@ def run_case(args):
     buf.close()
     print(json.dumps({"case": args.case, "T": T, "cta_pair": args.cta_pair, "streamk": args.streamk,
                       "copy_streams": args.copy_streams, "sm_margin": args.sm_margin, "launches": n, "avg_us": 1e3 * ms / max(n, 1),
-                      "tflops": flops * n / (ms / 1e3) / 1e12 if ms > 0 else None,
+                      "tflops": flops * n / (ms / 1e3) / 1e12 if ms > 0 and flops else None,
+                      "gbs": nbytes * n / (ms / 1e3) / 1e9 if ms > 0 and nbytes else None,
                       "first_us": 1e3 * first_ms, "first_status": first_status, "status": status}))
     if status != ub.UB_OK:
         sys.exit("device status %d (%s)" % (status, ub.ERRORS.get(status, "?")))

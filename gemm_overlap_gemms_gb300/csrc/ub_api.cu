@@ -809,9 +809,10 @@ int ub_reduce_scatter(ub_handle_t h, const void *const *P, void *const *Y_shards
     p.T = h->T;
     p.H = h->hidden;
     p.c = h->T / tp;
-    // Two small CTAs per SM: they fit beside a persistent GEMM CTA on the same SM.
+    // Small CTAs, four per SM: two fit beside a persistent GEMM CTA on the same SM (the
+    // rest start as GEMM CTAs leave); alone, all four keep enough loads in flight.
     const int64_t vecs = p.T * (p.H / 8);
-    int64_t grid = 2 * static_cast<int64_t>(h->sm_count);
+    int64_t grid = 4 * static_cast<int64_t>(h->sm_count);
     if (grid > (vecs + 255) / 256) grid = (vecs + 255) / 256;
     ProfileRing &ring = h->prof[UB_OP_REDUCE_SCATTER];
     const bool timed = h->profile != 0 && ring.count < kMaxProfiled;

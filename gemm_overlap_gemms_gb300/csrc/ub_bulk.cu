@@ -39,26 +39,47 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi)
     return d;
 }
 
+// TP partials, U vectors of 8 columns per thread per iteration: all TP * U 16-byte loads
+// are issued before the first add, so enough bytes are in flight to cover HBM latency.
+template <int TP, int U>
 __global__ void __launch_bounds__(256) bulk_rs_kernel(const __grid_constant__ BulkRsParams p)
 {
     const int64_t vecs_per_row = p.H / 8;
     const int64_t total = p.T * vecs_per_row;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < total; v += stride) {
-        const int64_t t = v / vecs_per_row;
-        const int64_t col = (v - t * vecs_per_row) * 8;
-        float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int j = 0; j < p.tp; ++j) {
-            const uint4 q = ld_stream(static_cast<const __nv_bfloat16 *>(p.P[j]) + t * p.H + col);
-            add_bf16x2(q.x, a[0], a[1]);
-            add_bf16x2(q.y, a[2], a[3]);
-            add_bf16x2(q.z, a[4], a[5]);
-            add_bf16x2(q.w, a[6], a[7]);
+    for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; base < total;
+         base += stride * U) {
+        uint4 q[U][TP];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t v = base + u * stride;
+            if (v < total) {
+                const int64_t t = v / vecs_per_row;
+                const int64_t col = (v - t * vecs_per_row) * 8;
+#pragma unroll
+                for (int j = 0; j < TP; ++j)
+                    q[u][j] = ld_stream(static_cast<const __nv_bfloat16 *>(p.P[j]) + t * p.H + col);
+            }
         }
-        const int64_t r = t / p.c;
-        const int64_t i = t - r * p.c;
-        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.Y[r]) + i * p.H + col);
-        *dst = make_uint4(pack2(a[0], a[1]), pack2(a[2], a[3]), pack2(a[4], a[5]), pack2(a[6], a[7]));
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t v = base + u * stride;
+            if (v >= total) break;
+            const int64_t t = v / vecs_per_row;
+            const int64_t col = (v - t * vecs_per_row) * 8;
+            float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int j = 0; j < TP; ++j) {
+                add_bf16x2(q[u][j].x, a[0], a[1]);
+                add_bf16x2(q[u][j].y, a[2], a[3]);
+                add_bf16x2(q[u][j].z, a[4], a[5]);
+                add_bf16x2(q[u][j].w, a[6], a[7]);
+            }
+            const int64_t r = t / p.c;
+            const int64_t i = t - r * p.c;
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.Y[r]) + i * p.H + col);
+            *dst = make_uint4(pack2(a[0], a[1]), pack2(a[2], a[3]), pack2(a[4], a[5]), pack2(a[6], a[7]));
+        }
     }
 }
 
@@ -66,7 +87,16 @@ __global__ void __launch_bounds__(256) bulk_rs_kernel(const __grid_constant__ Bu
 
 cudaError_t launch_bulk_rs(const BulkRsParams &p, int grid, cudaStream_t stream)
 {
-    bulk_rs_kernel<<<grid, 256, 0, stream>>>(p);
+    switch (p.tp) {
+    case 1: bulk_rs_kernel<1, 4><<<grid, 256, 0, stream>>>(p); break;
+    case 2: bulk_rs_kernel<2, 4><<<grid, 256, 0, stream>>>(p); break;
+    case 3: bulk_rs_kernel<3, 2><<<grid, 256, 0, stream>>>(p); break;
+    case 4: bulk_rs_kernel<4, 2><<<grid, 256, 0, stream>>>(p); break;
+    case 5: bulk_rs_kernel<5, 2><<<grid, 256, 0, stream>>>(p); break;
+    case 6: bulk_rs_kernel<6, 2><<<grid, 256, 0, stream>>>(p); break;
+    case 7: bulk_rs_kernel<7, 1><<<grid, 256, 0, stream>>>(p); break;
+    default: bulk_rs_kernel<8, 1><<<grid, 256, 0, stream>>>(p); break;
+    }
     return cudaGetLastError();
 }
 
