@@ -77,6 +77,8 @@ def parse():
     ap.add_argument("--case-T", type=int, default=8192)
     ap.add_argument("--case-reps", type=int, default=3)
     ap.add_argument("--sm-margin", type=int, default=0)
+    ap.add_argument("--gather-kernel", type=int, default=0, choices=[0, 1],
+                    help="1: the all-gather is one kernel launch instead of driver copies")
     ap.add_argument("--timeout-ms", type=float, default=None,
                     help="bound of the device-side waits (default: the library's 1 s)")
     ap.add_argument("--cta-pair", type=int, default=-1, choices=[-1, 0, 1],
@@ -711,6 +713,7 @@ def run_case(args):
     if args.timeout_ms:
         buf.set_option("timeout_ns", int(args.timeout_ms * 1e6))
     buf.set_option("sm_margin", args.sm_margin)
+    buf.set_option("gather_kernel", args.gather_kernel)
     buf.set_active_shape([T, H])
     c = T // tp
     nbytes = None
@@ -780,7 +783,8 @@ def run_case(args):
         # no kernel of ours to time: CUDA events around the whole call on the stream
         torch.cuda.synchronize()
         t_ms = time_steps(fn, args.case_reps, 2, torch.cuda.current_stream(), 1) / args.case_reps
-        print(json.dumps({"case": args.case, "T": T, "us": 1e3 * t_ms, "gbs": nbytes / (t_ms / 1e3) / 1e9}))
+        print(json.dumps({"case": args.case, "T": T, "gather_kernel": args.gather_kernel, "us": 1e3 * t_ms,
+                          "gbs": nbytes / (t_ms / 1e3) / 1e9}))
         buf.close()
         return
     first_ms, _ = buf.kernel_time(op_name)
@@ -792,7 +796,8 @@ def run_case(args):
     status = buf.query_status()
     buf.close()
     print(json.dumps({"case": args.case, "T": T, "cta_pair": args.cta_pair, "streamk": args.streamk,
-                      "copy_streams": args.copy_streams, "sm_margin": args.sm_margin, "launches": n, "avg_us": 1e3 * ms / max(n, 1),
+                      "copy_streams": args.copy_streams, "sm_margin": args.sm_margin,
+                      "gather_kernel": args.gather_kernel, "launches": n, "avg_us": 1e3 * ms / max(n, 1),
                       "tflops": flops * n / (ms / 1e3) / 1e12 if ms > 0 and flops else None,
                       "gbs": nbytes * n / (ms / 1e3) / 1e9 if ms > 0 and nbytes else None,
                       "first_us": 1e3 * first_ms, "first_status": first_status, "status": status}))

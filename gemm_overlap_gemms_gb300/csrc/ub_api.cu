@@ -139,6 +139,7 @@ struct ub_handle {
     cudaStream_t extra_side[UB_MAX_TP] = {};      // copy streams 1.. (created on demand)
     cudaEvent_t ev_join_extra[UB_MAX_TP] = {};
     int64_t copy_streams = 1;  // raised to min(tp, 4) at creation
+    int64_t gather_kernel = 0; // 1: the gather is one kernel launch instead of driver copies
     cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
     uint32_t epoch = 0;
     // options
@@ -162,6 +163,7 @@ uint32_t *flags_of(ub_handle *h) { return h->ctrl; }
 uint32_t *abort_of(ub_handle *h) { return h->ctrl + UB_MAX_TP; }
 int32_t *status_of(ub_handle *h) { return reinterpret_cast<int32_t *>(h->ctrl + UB_MAX_TP + 1); }
 uint32_t *ws_flags_of(ub_handle *h) { return h->ctrl + 64; }
+uint32_t *gather_counters_of(ub_handle *h) { return h->ctrl + 16; }  // UB_MAX_TP words, zero between calls
 
 // Makes the handle's device current for the duration of a call.
 struct DeviceGuard {
@@ -323,6 +325,30 @@ int issue_gather(ub_handle *h, const void *const *shards, cudaStream_t s, uint32
     const int64_t T = h->T, H = h->hidden, c = T / tp;
     const int self = static_cast<int>(h->self_rank);
     char *ub = static_cast<char *>(h->ub);
+    if (h->gather_kernel) {
+        // One launch on the side stream: small CTAs (they fit beside the GEMM's), about
+        // one per SM per chunk, each chunk's flag published by its last CTA.
+        ubk::GatherParams g;
+        memset(&g, 0, sizeof g);
+        for (int r = 0; r < tp; ++r) g.src[r] = shards[r];
+        g.ub = h->ub;
+        g.flags = flags_of(h);
+        g.counters = gather_counters_of(h);
+        g.epoch = epoch;
+        g.tp = tp;
+        g.self_rank = self;
+        g.drop = static_cast<int>(drop);
+        g.chunk_vecs = c * H / 8;
+        int64_t per = (h->sm_count + tp - 1) / tp;
+        const int64_t need = (g.chunk_vecs + 511) / 512;  // at least two vectors per thread
+        if (per > need) per = need;
+        g.ctas_per_chunk = static_cast<int>(per < 1 ? 1 : per);
+        UB_CUDA(cudaEventRecord(h->ev_fork, s));
+        UB_CUDA(cudaStreamWaitEvent(h->side, h->ev_fork, 0));
+        cudaError_t e = ubk::launch_gather(g, h->side);
+        if (e != cudaSuccess) return cuda_fail(e, "gather kernel launch");
+        return UB_OK;
+    }
     const int ncs = static_cast<int>(h->copy_streams < tp ? h->copy_streams : tp);
     auto copy_stream = [&](int i) { return i == 0 ? h->side : h->extra_side[i]; };
     UB_CUDA(cudaEventRecord(h->ev_fork, s));
@@ -345,7 +371,7 @@ int issue_gather(ub_handle *h, const void *const *shards, cudaStream_t s, uint32
 // Make `s` wait for every copy stream the last gather used.
 int join_gather(ub_handle *h, cudaStream_t s)
 {
-    const int ncs = static_cast<int>(h->copy_streams < h->tp ? h->copy_streams : h->tp);
+    const int ncs = h->gather_kernel ? 1 : static_cast<int>(h->copy_streams < h->tp ? h->copy_streams : h->tp);
     UB_CUDA(cudaEventRecord(h->ev_join, h->side));
     UB_CUDA(cudaStreamWaitEvent(s, h->ev_join, 0));
     for (int i = 1; i < ncs; ++i) {
@@ -926,6 +952,10 @@ int ub_set_option(ub_handle_t h, int key, int64_t val)
         if (val < -1 || val > 1) return fail(UB_ERR_ARG, "streamk must be -1, 0 or 1");
         h->streamk = val;
         return UB_OK;
+    case UB_OPT_GATHER_KERNEL:
+        if (val != 0 && val != 1) return fail(UB_ERR_ARG, "gather_kernel must be 0 or 1");
+        h->gather_kernel = val;
+        return UB_OK;
     case UB_OPT_COPY_STREAMS: {
         if (val < 1 || val > UB_MAX_TP) return fail(UB_ERR_ARG, "copy_streams must be in [1, %d]", UB_MAX_TP);
         DeviceGuard g(h->device);
@@ -954,6 +984,7 @@ int ub_get_option(ub_handle_t h, int key, int64_t *val)
     case UB_OPT_CTA_PAIR: *val = h->cta_pair; return UB_OK;
     case UB_OPT_STREAMK: *val = h->streamk; return UB_OK;
     case UB_OPT_COPY_STREAMS: *val = h->copy_streams; return UB_OK;
+    case UB_OPT_GATHER_KERNEL: *val = h->gather_kernel; return UB_OK;
     default: return fail(UB_ERR_ARG, "unknown option %d", key);
     }
 }

@@ -83,7 +83,46 @@ __global__ void __launch_bounds__(256) bulk_rs_kernel(const __grid_constant__ Bu
     }
 }
 
+// One CTA group per chunk, ring order: block b copies part (b % ctas_per_chunk) of the
+// q-th chunk after the self rank (b / ctas_per_chunk), the self chunk last.
+__global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ GatherParams p)
+{
+    const int q = blockIdx.x / p.ctas_per_chunk + 1;  // 1..tp
+    const int part = blockIdx.x - (q - 1) * p.ctas_per_chunk;
+    const int r = (p.self_rank + q) % p.tp;
+    const uint4 *src = static_cast<const uint4 *>(p.src[r]);
+    uint4 *dst = static_cast<uint4 *>(p.ub) + static_cast<int64_t>(r) * p.chunk_vecs;
+    const int64_t stride = static_cast<int64_t>(p.ctas_per_chunk) * blockDim.x;
+    for (int64_t v = static_cast<int64_t>(part) * blockDim.x + threadIdx.x; v < p.chunk_vecs; v += 2 * stride) {
+        const uint4 a = ld_stream(src + v);
+        const bool two = v + stride < p.chunk_vecs;
+        uint4 b2;
+        if (two) b2 = ld_stream(src + v + stride);
+        dst[v] = a;
+        if (two) dst[v + stride] = b2;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const uint32_t done = atomicAdd(p.counters + r, 1u) + 1u;
+        if (done == static_cast<uint32_t>(p.ctas_per_chunk)) {
+            // last CTA of this chunk: every part is written (each CTA fenced before
+            // counting); reset the counter for the next call, then publish the flag
+            p.counters[r] = 0u;
+            __threadfence();
+            if (r != p.drop)
+                asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p.flags + r), "r"(p.epoch) : "memory");
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_gather(const GatherParams &p, cudaStream_t stream)
+{
+    gather_kernel<<<p.tp * p.ctas_per_chunk, 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_bulk_rs(const BulkRsParams &p, int grid, cudaStream_t stream)
 {

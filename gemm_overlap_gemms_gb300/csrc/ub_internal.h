@@ -116,6 +116,23 @@ struct BulkRsParams {
 };
 cudaError_t launch_bulk_rs(const BulkRsParams &p, int grid, cudaStream_t stream);
 
+// One-launch gather (ub_bulk.cu): chunk r of the active shape into the user buffer, in
+// ring order after the self rank, each chunk's readiness flag published (release) by
+// the CTA that finishes it. Counters are reset by that CTA for the next call.
+struct GatherParams {
+    const void *src[UB_MAX_TP];  // shards [c, H]
+    void *ub;                    // user buffer [T, H]
+    uint32_t *flags;             // readiness flag per chunk
+    uint32_t *counters;          // CTAs done per chunk (zero between calls)
+    uint32_t epoch;
+    int tp;
+    int self_rank;
+    int drop;                    // chunk whose flag is not published (-1: none)
+    int ctas_per_chunk;
+    int64_t chunk_vecs;          // 16-byte vectors per chunk = c * H / 8
+};
+cudaError_t launch_gather(const GatherParams &p, cudaStream_t stream);
+
 // Record the message ub_last_error() returns on this host thread.
 void set_last_error(const char *msg);
 

@@ -82,8 +82,12 @@ enum {
                               partial wave's tiles are cut into equal k-pieces spread over the
                               idle pairs (fixed-order fp32 fix-up: deterministic); 0 = whole
                               tiles only */
-    UB_OPT_COPY_STREAMS = 8 /* side streams the ag_gemm chunk copies are dealt over
+    UB_OPT_COPY_STREAMS = 8, /* side streams the ag_gemm chunk copies are dealt over
                               (round-robin in ring order), 1..UB_MAX_TP; default min(tp, 4) */
+    UB_OPT_GATHER_KERNEL = 9 /* 0 (default): the gather is one cudaMemcpyAsync plus one stream
+                              flag write per chunk; 1: one kernel launch on the side stream
+                              lands every chunk in ring order and publishes each chunk's flag
+                              as its last CTA finishes (fewer driver operations per call) */
 };
 
 /* Operation ids for ub_kernel_time. */

@@ -51,15 +51,17 @@ def test_tiny_workload_ag_and_rs():
 SWEEP_C = [1, 2, 127, 128, 129, 255, 300]
 
 
+@pytest.mark.parametrize("gather", [0, 1])
 @pytest.mark.parametrize("pair", [1, 0])
 @pytest.mark.parametrize("tp", [1, 2, 4])
-def test_ag_active_T_sweep(tp, pair):
+def test_ag_active_T_sweep(tp, pair, gather):
     H, N = 256, 384            # two N tiles, the second one partial
     cap = tp * 320
     g = synth.generator(seed=11)
     Wt = synth.normal_bf16((N, H), H ** -0.5, g)
     with ub.UserBuffer([cap, H], tp) as buf:
         buf.set_option("cta_pair", pair)
+        buf.set_option("gather_kernel", gather)
         for c in SWEEP_C + [cap // tp]:
             T = c * tp
             buf.buffer().view(torch.int16).fill_(-1)
@@ -228,8 +230,9 @@ def test_rejects_misaligned_and_wrong_shapes():
 
 # ------------------------------------------------------------------ bounded waits
 
+@pytest.mark.parametrize("gather", [0, 1])
 @pytest.mark.parametrize("pair", [1, 0])
-def test_dropped_flag_times_out_and_the_handle_recovers(pair):
+def test_dropped_flag_times_out_and_the_handle_recovers(pair, gather):
     """Fault injected on the host: the readiness flag of chunk 1 is never written. The
     kernel's bounded wait must expire, report UB_ERR_TIMEOUT, and leave the context and
     handle usable for the next call."""
@@ -239,6 +242,7 @@ def test_dropped_flag_times_out_and_the_handle_recovers(pair):
     shards, Wt = synth.ag_inputs(T, H, N, tp, g)
     with ub.UserBuffer([T, H], tp) as buf:
         buf.set_option("cta_pair", pair)
+        buf.set_option("gather_kernel", gather)
         buf.set_option("timeout_ns", 20_000_000)
         buf.set_option("drop_flag", 1)
         run_ag(buf, shards, Wt)
@@ -252,8 +256,9 @@ def test_dropped_flag_times_out_and_the_handle_recovers(pair):
     assert_close(Y, Yref, "AG after recovery")
 
 
+@pytest.mark.parametrize("gather", [0, 1])
 @pytest.mark.parametrize("op", ["ag", "rs", "ag_swiglu"])
-def test_back_to_back_calls_at_full_hidden(op):
+def test_back_to_back_calls_at_full_hidden(op, gather):
     """Ten calls in a row on one handle at hidden 4096 without synchronising in
     between: every call's chunk copies must be able to run next to the GEMM kernels."""
     tp, H, N, K, T = 4, 4096, 1024, 1024, 2048
@@ -265,6 +270,7 @@ def test_back_to_back_calls_at_full_hidden(op):
     c = T // tp
     shards = [X[r * c:(r + 1) * c] for r in range(tp)]
     with ub.UserBuffer([T, H], tp) as buf:
+        buf.set_option("gather_kernel", gather)
         outs = []
         for _ in range(10):
             if op == "ag":
