@@ -610,20 +610,25 @@ def sweep_points(wl, stream):
         shards = [X[r * c:(r + 1) * c] for r in range(tp)]
         outs = [wl.Yrs[r * c:(r + 1) * c] for r in range(tp)]
         wl.buf.set_active_shape([T, H])
-        for op in ("ag", "ag_swiglu", "rs"):
+        for op in ("ag", "ag_swiglu", "ag_swiglu_no_overlap", "rs"):
             if op == "ag":
                 fn = lambda: wl.buf.ag_gemm(shards, wl.W1, wl.Y1, stream=stream)
-            elif op == "ag_swiglu":
+            elif op.startswith("ag_swiglu"):
                 fn = lambda: wl.buf.ag_gemm_swiglu(shards, wl.W1, wl.Yz, stream=stream)
             else:
                 fn = lambda: wl.buf.gemm_rs(A, wl.B, outs, stream=stream)
             reps = 20
+            # the no-overlap comparator puts the gather copies on the GEMM's stream, ahead of it
+            wl.buf.set_option("copy_streams", 0 if op == "ag_swiglu_no_overlap" else 4)
             ms = time_steps(fn, reps, 3, stream, 1) / reps
+            wl.buf.set_option("copy_streams", 4)
             fl = 2.0 * T * H * N if op != "rs" else 2.0 * T * K * H * tp
             tf = fl / (ms / 1e3) / 1e12
             out.append({"sweep": op, "T": T, "us": ms * 1e3, "tflops": tf,
                         "frac_of_peak": tf / tensor_peak,
-                        "note": "includes the gather copies" if op != "rs" else ""})
+                        "note": ("gather copies on the GEMM's stream, before it (no overlap)"
+                                 if op == "ag_swiglu_no_overlap" else
+                                 "includes the gather copies, overlapped" if op != "rs" else "")})
     return out
 
 
@@ -793,6 +798,9 @@ def run_case(args):
         fn()
     torch.cuda.synchronize()
     ms, n = buf.kernel_time(op_name)
+    buf.set_option("profile", 0)
+    # whole calls (gather copies, flag writes, joins included), CUDA events on the stream
+    call_ms = time_steps(fn, args.case_reps, 1, torch.cuda.current_stream(), 1) / args.case_reps
     status = buf.query_status()
     buf.close()
     print(json.dumps({"case": args.case, "T": T, "cta_pair": args.cta_pair, "streamk": args.streamk,
@@ -800,6 +808,7 @@ def run_case(args):
                       "gather_kernel": args.gather_kernel, "launches": n, "avg_us": 1e3 * ms / max(n, 1),
                       "tflops": flops * n / (ms / 1e3) / 1e12 if ms > 0 and flops else None,
                       "gbs": nbytes * n / (ms / 1e3) / 1e9 if ms > 0 and nbytes else None,
+                      "call_us": 1e3 * call_ms,
                       "first_us": 1e3 * first_ms, "first_status": first_status, "status": status}))
     if status != ub.UB_OK:
         sys.exit("device status %d (%s)" % (status, ub.ERRORS.get(status, "?")))

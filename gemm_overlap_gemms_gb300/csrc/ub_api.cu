@@ -325,6 +325,22 @@ int issue_gather(ub_handle *h, const void *const *shards, cudaStream_t s, uint32
     const int64_t T = h->T, H = h->hidden, c = T / tp;
     const int self = static_cast<int>(h->self_rank);
     char *ub = static_cast<char *>(h->ub);
+    if (h->copy_streams == 0 && !h->gather_kernel) {
+        // In-stream: the copies and flag writes go on `s` itself, ahead of the GEMM,
+        // which then finds every flag set (no overlap, no cross-stream hops).
+        for (int q = 1; q <= tp; ++q) {
+            const int r = (self + q) % tp;
+            UB_CUDA(cudaMemcpyAsync(ub + r * c * H * 2, shards[r], static_cast<size_t>(c * H * 2),
+                                    cudaMemcpyDeviceToDevice, s));
+            if (r != drop) {
+                CUresult cr = driver().write_value32(reinterpret_cast<CUstream>(s),
+                                                     reinterpret_cast<CUdeviceptr>(flags_of(h) + r), epoch,
+                                                     CU_STREAM_WRITE_VALUE_DEFAULT);
+                if (cr != CUDA_SUCCESS) return fail(UB_ERR_CUDA, "cuStreamWriteValue32 failed (%d)", (int)cr);
+            }
+        }
+        return UB_OK;
+    }
     if (h->gather_kernel) {
         // One launch on the side stream: small CTAs (they fit beside the GEMM's), about
         // one per SM per chunk, each chunk's flag published by its last CTA.
@@ -371,6 +387,7 @@ int issue_gather(ub_handle *h, const void *const *shards, cudaStream_t s, uint32
 // Make `s` wait for every copy stream the last gather used.
 int join_gather(ub_handle *h, cudaStream_t s)
 {
+    if (h->copy_streams == 0 && !h->gather_kernel) return UB_OK;  // in-stream: nothing to join
     const int ncs = h->gather_kernel ? 1 : static_cast<int>(h->copy_streams < h->tp ? h->copy_streams : h->tp);
     UB_CUDA(cudaEventRecord(h->ev_join, h->side));
     UB_CUDA(cudaStreamWaitEvent(s, h->ev_join, 0));
@@ -957,7 +974,7 @@ int ub_set_option(ub_handle_t h, int key, int64_t val)
         h->gather_kernel = val;
         return UB_OK;
     case UB_OPT_COPY_STREAMS: {
-        if (val < 1 || val > UB_MAX_TP) return fail(UB_ERR_ARG, "copy_streams must be in [1, %d]", UB_MAX_TP);
+        if (val < 0 || val > UB_MAX_TP) return fail(UB_ERR_ARG, "copy_streams must be in [0, %d]", UB_MAX_TP);
         DeviceGuard g(h->device);
         for (int i = 1; i < val; ++i) {
             if (!h->extra_side[i]) UB_CUDA(cudaStreamCreateWithFlags(&h->extra_side[i], cudaStreamNonBlocking));

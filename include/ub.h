@@ -83,7 +83,9 @@ enum {
                               idle pairs (fixed-order fp32 fix-up: deterministic); 0 = whole
                               tiles only */
     UB_OPT_COPY_STREAMS = 8, /* side streams the ag_gemm chunk copies are dealt over
-                              (round-robin in ring order), 1..UB_MAX_TP; default min(tp, 4) */
+                              (round-robin in ring order), 1..UB_MAX_TP; default min(tp, 4).
+                              0 = no overlap: the copies and flag writes go on the call's own
+                              stream ahead of the GEMM (a comparator; slower on GB300) */
     UB_OPT_GATHER_KERNEL = 9 /* 0 (default): the gather is one cudaMemcpyAsync plus one stream
                               flag write per chunk; 1: one kernel launch on the side stream
                               lands every chunk in ring order and publishes each chunk's flag
