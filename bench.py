@@ -84,6 +84,8 @@ def parse():
     ap.add_argument("--cta-pair", type=int, default=-1, choices=[-1, 0, 1],
                     help="-1: chosen per call (default); 1: 256x256 tiles on CTA pairs; 0: single CTAs")
     ap.add_argument("--copy-streams", type=int, default=4)
+    ap.add_argument("--skinny", type=int, default=-1, choices=[-1, 0, 1],
+                    help="few-token kernel: -1 whenever usable (default), 0 never, 1 whenever usable")
     ap.add_argument("--streamk", type=int, default=-1, choices=[-1, 0, 1],
                     help="-1: chosen per call (default); 1: stream-K over all pairs; 0: whole tiles")
     return ap.parse_args()
@@ -183,13 +185,13 @@ class ClockSampler:
             return
         self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
         self.proc = subprocess.Popen([smi, "-i", str(self.index), "--query-gpu=" + self.FIELDS,
-                                      "--format=csv,noheader,nounits", "-lms", "200"],
+                                      "--format=csv,noheader,nounits", "-lms", "50"],
                                      stdout=self.out, stderr=subprocess.DEVNULL)
 
     def stop(self):
         if self.proc is None:
             return None
-        time.sleep(0.25)
+        time.sleep(0.06)  # one more sample, without a run of idle ones after the timed region
         self.proc.send_signal(signal.SIGTERM)
         try:
             self.proc.wait(timeout=5)
@@ -719,6 +721,7 @@ def run_case(args):
         buf.set_option("timeout_ns", int(args.timeout_ms * 1e6))
     buf.set_option("sm_margin", args.sm_margin)
     buf.set_option("gather_kernel", args.gather_kernel)
+    buf.set_option("skinny", args.skinny)
     buf.set_active_shape([T, H])
     c = T // tp
     nbytes = None

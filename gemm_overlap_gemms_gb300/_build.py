@@ -12,7 +12,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libubgemm.so")
-SOURCES = ["ub_gemm.cu", "ub_api.cu", "ub_noalloc.cu", "ub_bulk.cu"]
+SOURCES = ["ub_gemm.cu", "ub_skinny.cu", "ub_api.cu", "ub_noalloc.cu", "ub_bulk.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-I", INCLUDE, "-I", CSRC]
 

@@ -133,7 +133,8 @@ struct ub_handle {
     void *ub = nullptr;      // [max_tokens, hidden] bf16
     uint32_t *ctrl = nullptr;  // flags[UB_MAX_TP] | abort | status | ... | stream-K flags (from word 64)
     size_t ctrl_bytes = 0;
-    float *ws = nullptr;       // stream-K partial tiles of the pair kernel
+    float *ws = nullptr;       // partial tiles of split work: ws_slots x PARTIAL_FLOATS fp32
+    int ws_slots = 0;          // 2 per SM: pair kernel (pair, rank) slots, skinny-kernel pieces
     int max_pairs = 0;         // pairs the workspace has room for
     cudaStream_t side = nullptr;                  // copy stream 0; also status reads
     cudaStream_t extra_side[UB_MAX_TP] = {};      // copy streams 1.. (created on demand)
@@ -150,6 +151,7 @@ struct ub_handle {
     int64_t profile = 0;
     int64_t cta_pair = -1;  // -1 = chosen per call
     int64_t streamk = -1;   // -1 = chosen per call
+    int64_t skinny = -1;    // -1 = whenever the few-token kernel is usable
     int pair_clusters[3] = {-1, -1, -1};  // resident clusters of the pair kernel, per mode
     ub_counters_t counters{};
     std::vector<CacheEntry> cache;
@@ -256,6 +258,45 @@ void set_pairs(ub_handle *h, GemmParams &p, int mode, bool split)
     p.ws_flags = ws_flags_of(h);
 }
 
+// The few-token kernel runs a call when its token tile (`cols` TMEM columns) fits one
+// accumulator and neither it nor the CTA-pair choice is forced the other way. Chosen
+// automatically up to SK_AUTO_MAX_COLS columns: measured on GB300 (fc1 / fc2 of the
+// SwiGLU MLP, hidden 4096, tp 4) it beats the tile kernels up to T = 128 and loses at
+// T = 256, where the work is no longer bound by the weight read.
+bool use_skinny(ub_handle *h, int64_t cols)
+{
+    if (cols > ubk::SK_MAX_COLS || h->skinny == 0) return false;
+    if (h->skinny == 1) return true;
+    return h->cta_pair < 0 && cols <= ubk::SK_AUTO_MAX_COLS;
+}
+
+// Launch shape of a skinny-kernel call: k-pieces per weight tile so that about one unit
+// runs per SM (each piece at least SK_MIN_KBLOCKS long, the partials within the
+// workspace), and the deepest pipeline that fits in shared memory.
+void set_skinny(ub_handle *h, GemmParams &p, int slot_mult, int w_bytes)
+{
+    const int64_t slots = h->sm_count - h->sm_margin > 0 ? h->sm_count - h->sm_margin : 1;
+    int64_t s = slots / p.n_tiles;
+    if (s > ubk::SK_MAX_SPLIT) s = ubk::SK_MAX_SPLIT;
+    if (s > p.k_blocks / ubk::SK_MIN_KBLOCKS) s = p.k_blocks / ubk::SK_MIN_KBLOCKS;
+    const int64_t ws_cap = 1 + h->ws_slots / (static_cast<int64_t>(p.n_tiles) * slot_mult);
+    if (s > ws_cap) s = ws_cap;
+    if (s < 1) s = 1;
+    p.sk_split = static_cast<int>(s);
+    p.sk_units = p.n_tiles * p.sk_split;
+    // split pieces run one unit per CTA (the finisher reuses its stage buffers): all
+    // units fit in one wave of the grid the launch uses (grid_for: slots CTAs at most)
+    const int x_bytes = p.sk_n_sub * p.sk_sub_n * 128;
+    int st = (ubk::SK_SMEM_LIMIT - ubk::skinny_smem_bytes(0, w_bytes, x_bytes)) / (w_bytes + x_bytes);
+    if (st > ubk::SK_MAX_STAGES) st = ubk::SK_MAX_STAGES;
+    p.sk_stages = st < 1 ? 1 : st;
+    int stride = 16;
+    while (stride < p.sk_n_sub * p.sk_sub_n) stride *= 2;
+    p.sk_stride = stride;
+    p.ws = h->ws;
+    p.ws_flags = ws_flags_of(h);
+}
+
 // Which kernel runs a call, from a wave-count cost model measured on GB300 (one unit =
 // the time of one 128x256 tile on one SM, the same as one 256x256 tile on a pair):
 //   single CTAs, chunk-aligned 128-row tiles:    waves
@@ -289,9 +330,13 @@ void choose_path(ub_handle *h, int mode, int64_t single_tiles, int64_t pair_tile
     }
 }
 
-int launch(ub_handle *h, const GemmParams &p, int mode, bool pair, cudaStream_t s, int prof_op)
+enum Path : int { PATH_SINGLE = 0, PATH_PAIR = 1, PATH_SKINNY = 2 };
+
+int launch(ub_handle *h, const GemmParams &p, int mode, int path, cudaStream_t s, int prof_op)
 {
-    const int grid = pair ? p.num_pairs : grid_for(h, p.num_tiles);
+    const int grid = path == PATH_PAIR ? p.num_pairs : grid_for(h, path == PATH_SKINNY ? p.sk_units : p.num_tiles);
+    if (path == PATH_SKINNY && p.sk_split > 1 && grid < p.sk_units)
+        return fail(UB_ERR_ARG, "skinny launch: %d split units on %d CTAs", p.sk_units, grid);
     ProfileRing &ring = h->prof[prof_op];
     const bool timed = h->profile != 0 && ring.count < kMaxProfiled;
     if (timed) {
@@ -304,7 +349,9 @@ int launch(ub_handle *h, const GemmParams &p, int mode, bool pair, cudaStream_t 
         }
         UB_CUDA(cudaEventRecord(ring.start[ring.count], s));
     }
-    cudaError_t e = pair ? ubk::launch_gemm_pair(p, mode, grid, s) : ubk::launch_gemm(p, mode, grid, s);
+    cudaError_t e = path == PATH_PAIR     ? ubk::launch_gemm_pair(p, mode, grid, s)
+                    : path == PATH_SKINNY ? ubk::launch_gemm_skinny(p, mode, grid, s)
+                                          : ubk::launch_gemm(p, mode, grid, s);
     if (e != cudaSuccess) return cuda_fail(e, "GEMM kernel launch");
     if (timed) {
         UB_CUDA(cudaEventRecord(ring.stop[ring.count], s));
@@ -465,13 +512,14 @@ int ub_create(int64_t max_tokens, int64_t hidden, int tp, ub_dtype_t dtype, ub_h
     if (e != cudaSuccess) return cleanup(cuda_fail(e, "cudaMalloc(user buffer)"));
     ++h->counters.device_allocations;
     h->max_pairs = h->sm_count / 2 > 0 ? h->sm_count / 2 : 1;
-    h->ctrl_bytes = 256 + static_cast<size_t>(h->max_pairs) * 2 * ubk::EPI_WARPS * sizeof(uint32_t);
+    h->ws_slots = 2 * (h->sm_count > 0 ? h->sm_count : 1);
+    h->ctrl_bytes = 256 + static_cast<size_t>(h->ws_slots) * ubk::EPI_WARPS * sizeof(uint32_t);
     e = cudaMalloc(reinterpret_cast<void **>(&h->ctrl), h->ctrl_bytes);
     if (e != cudaSuccess) return cleanup(cuda_fail(e, "cudaMalloc(control block)"));
     ++h->counters.device_allocations;
     e = cudaMalloc(reinterpret_cast<void **>(&h->ws),
-                   static_cast<size_t>(h->max_pairs) * 2 * ubk::PARTIAL_FLOATS * sizeof(float));
-    if (e != cudaSuccess) return cleanup(cuda_fail(e, "cudaMalloc(stream-K workspace)"));
+                   static_cast<size_t>(h->ws_slots) * ubk::PARTIAL_FLOATS * sizeof(float));
+    if (e != cudaSuccess) return cleanup(cuda_fail(e, "cudaMalloc(split workspace)"));
     ++h->counters.device_allocations;
     e = cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking);
     if (e != cudaSuccess) return cleanup(cuda_fail(e, "cudaStreamCreateWithFlags"));
@@ -601,13 +649,16 @@ static int ag_gemm_impl(ub_handle_t h, const void *const *shards, const void *Wt
     bool pair = false, streamk = false;
     choose_path(h, mode, tp * ceil_div(c, ubk::BM) * n_tiles, pair_rows_tiles * n_tiles,
                 (H + ubk::BK - 1) / ubk::BK, pair, streamk);
-    if (glu || b_kn) pair = true;  // the fused epilogue and MN-major operands exist on CTA pairs only
+    const int64_t c16 = ceil_div(c, 16) * 16;  // token columns of one chunk in the skinny kernel
+    const bool skinny = use_skinny(h, tp * c16);
+    if (skinny) pair = false;
+    else if (glu || b_kn) pair = true;  // otherwise the fused epilogue and MN-major operands need CTA pairs
     const int bm = pair ? ubk::PAIR_BM : ubk::BM;      // rows of a tile
     const int bbox = pair ? ubk::BN / 2 : ubk::BN;    // rows of a B box (one CTA's half in a pair)
     std::vector<const void *> key;
     key.reserve(tp + 7);
     key.push_back(reinterpret_cast<const void *>(uintptr_t(mode)));
-    key.push_back(reinterpret_cast<const void *>(uintptr_t(pair + 2 * b_kn)));
+    key.push_back(reinterpret_cast<const void *>(uintptr_t(pair + 2 * b_kn + 4 * skinny)));
     key.push_back(reinterpret_cast<const void *>(uintptr_t(T)));
     key.push_back(reinterpret_cast<const void *>(uintptr_t(N)));
     key.push_back(reinterpret_cast<const void *>(uintptr_t(self)));
@@ -628,7 +679,32 @@ static int ag_gemm_impl(ub_handle_t h, const void *const *shards, const void *Wt
         p.n_tiles = static_cast<int>(n_tiles);
         p.num_tiles = tp * p.m_tiles * p.n_tiles;
         p.self_rank = self;
-        if (!pair) {
+        if (skinny) {
+            // Token sub-tile r = chunk r (c rows, zero-filled to c16), the self chunk in place.
+            for (int r = 0; r < tp; ++r) {
+                const void *src = r == self ? shards[r] : static_cast<const void *>(ub + r * c * H * 2);
+                if (int rc = encode_2d(&p.tmA[r], src, H, c, H * 2, ubk::BK, static_cast<uint32_t>(c16))) return rc;
+            }
+            if (b_kn) {
+                if (int rc = encode_2d(&p.tmB[0], Wt, N, H, N * 2, 64, ubk::BK)) return rc;
+                p.b_mn = 1;
+            } else if (glu) {
+                // gate rows [0, F) and up rows [F, 2F) of Wt as two maps of F rows each
+                if (int rc = encode_2d(&p.tmB[0], Wt, H, glu_f, H * 2, ubk::BK, ubk::SK_BM)) return rc;
+                if (int rc = encode_2d(&p.tmB[1], static_cast<const char *>(Wt) + glu_f * H * 2, H, glu_f, H * 2,
+                                       ubk::BK, ubk::SK_BM))
+                    return rc;
+            } else if (int rc = encode_2d(&p.tmB[0], Wt, H, N, H * 2, ubk::BK, ubk::SK_BM)) {
+                return rc;
+            }
+            h->counters.tensor_map_encodes += tp + (glu ? 2 : 1);
+            p.y_ptr[0] = Y;
+            p.ldy = static_cast<int>(n_out);
+            p.n_tiles = static_cast<int>((n_out + ubk::SK_BM - 1) / ubk::SK_BM);
+            p.sk_sub_n = static_cast<int>(c16);
+            p.sk_n_sub = tp;
+            pp = cache_insert(h, std::move(key), p);
+        } else if (!pair) {
             for (int r = 0; r < tp; ++r) {
                 // Chunk r is read from the user buffer, except the self chunk, which the
                 // kernel reads in place from its shard while its copy stages it.
@@ -666,29 +742,32 @@ static int ag_gemm_impl(ub_handle_t h, const void *const *shards, const void *Wt
             p.n_regions = nreg;
             h->counters.tensor_map_encodes += 2 * nreg;
         }
-        if (b_kn) {
-            // W is [hidden, N]: inner dimension N, boxes of 64 N x 64 K rows
-            if (int rc = encode_2d(&p.tmB[0], Wt, N, H, N * 2, 64, ubk::BK)) return rc;
-            p.b_mn = 1;
-        } else if (int rc = encode_2d(&p.tmB[0], Wt, H, N, H * 2, ubk::BK, bbox)) {
-            return rc;
+        if (!skinny) {
+            if (b_kn) {
+                // W is [hidden, N]: inner dimension N, boxes of 64 N x 64 K rows
+                if (int rc = encode_2d(&p.tmB[0], Wt, N, H, N * 2, 64, ubk::BK)) return rc;
+                p.b_mn = 1;
+            } else if (int rc = encode_2d(&p.tmB[0], Wt, H, N, H * 2, ubk::BK, bbox)) {
+                return rc;
+            }
+            h->counters.tensor_map_encodes += 1;
+            pp = cache_insert(h, std::move(key), p);
         }
-        h->counters.tensor_map_encodes += 1;
-        pp = cache_insert(h, std::move(key), p);
     }
     GemmParams &p = *pp;
     p.flags = flags_of(h);
     p.abort_word = abort_of(h);
     p.status = status_of(h);
     p.timeout_ns = static_cast<uint64_t>(h->timeout_ns);
-    if (pair) set_pairs(h, p, mode, streamk);
+    if (skinny) set_skinny(h, p, glu ? 2 : 1, glu ? 2 * ubk::SK_W_BYTES : ubk::SK_W_BYTES);
+    else if (pair) set_pairs(h, p, mode, streamk);
     const uint32_t epoch = ++h->epoch;
     p.epoch = epoch;
     const int64_t drop = h->drop_flag;
     h->drop_flag = -1;
 
     if (int rc = issue_gather(h, shards, s, epoch, drop)) return rc;
-    int rc = launch(h, p, mode, pair, s, prof_op);
+    int rc = launch(h, p, mode, skinny ? PATH_SKINNY : pair ? PATH_PAIR : PATH_SINGLE, s, prof_op);
     // Join the copy streams back into `s` even if the launch failed.
     if (int jrc = join_gather(h, s)) return jrc;
     if (rc != UB_OK) return rc;
@@ -738,13 +817,16 @@ static int gemm_rs_impl(ub_handle_t h, const void *const *A, const void *const *
     bool pair = false, streamk = false;
     choose_path(h, ubk::MODE_RS, tp * ceil_div(c, ubk::BM) * n_tiles, ceil_div(T, ubk::PAIR_BM) * n_tiles,
                 tp * ((K + ubk::BK - 1) / ubk::BK), pair, streamk);
-    if (b_kn) pair = true;  // MN-major operands exist on CTA pairs only
+    const int64_t T16 = ceil_div(T, 16) * 16;  // token columns in the skinny kernel
+    const bool skinny = use_skinny(h, T16);
+    if (skinny) pair = false;
+    else if (b_kn) pair = true;  // otherwise MN-major operands need CTA pairs
     const int bm = pair ? ubk::PAIR_BM : ubk::BM;
     const int bbox = pair ? ubk::BN / 2 : ubk::BN;
     std::vector<const void *> key;
     key.reserve(3 * tp + 4);
     key.push_back(reinterpret_cast<const void *>(uintptr_t(ubk::MODE_RS)));
-    key.push_back(reinterpret_cast<const void *>(uintptr_t(pair + 2 * b_kn)));
+    key.push_back(reinterpret_cast<const void *>(uintptr_t(pair + 2 * b_kn + 4 * skinny)));
     key.push_back(reinterpret_cast<const void *>(uintptr_t(T)));
     key.push_back(reinterpret_cast<const void *>(uintptr_t(K)));
     for (int j = 0; j < tp; ++j) {
@@ -753,6 +835,32 @@ static int gemm_rs_impl(ub_handle_t h, const void *const *A, const void *const *
         key.push_back(Y_shards[j]);
     }
     GemmParams *pp = cache_lookup(h, key);
+    if (!pp && skinny) {
+        GemmParams p;
+        memset(&p, 0, sizeof p);
+        for (int j = 0; j < tp; ++j) {
+            // all T tokens of A_j in one box (zero-filled to T16 rows)
+            if (int rc = encode_2d(&p.tmA[j], A[j], K, T, K * 2, ubk::BK, static_cast<uint32_t>(T16))) return rc;
+            if (b_kn) {
+                if (int rc = encode_2d(&p.tmB[j], Bt[j], H, K, H * 2, 64, ubk::BK)) return rc;
+            } else if (int rc = encode_2d(&p.tmB[j], Bt[j], K, H, K * 2, ubk::BK, ubk::SK_BM)) {
+                return rc;
+            }
+            p.y_ptr[j] = Y_shards[j];
+        }
+        h->counters.tensor_map_encodes += 2 * tp;
+        p.b_mn = b_kn ? 1 : 0;
+        p.tp = tp;
+        p.c = static_cast<int>(c);
+        p.n_out = static_cast<int>(H);
+        p.ldy = static_cast<int>(H);
+        p.k_blocks_per_shard = static_cast<int>((K + ubk::BK - 1) / ubk::BK);
+        p.k_blocks = tp * p.k_blocks_per_shard;
+        p.n_tiles = static_cast<int>((H + ubk::SK_BM - 1) / ubk::SK_BM);
+        p.sk_sub_n = static_cast<int>(T16);
+        p.sk_n_sub = 1;
+        pp = cache_insert(h, std::move(key), p);
+    }
     if (!pp) {
         GemmParams p;
         memset(&p, 0, sizeof p);
@@ -793,9 +901,12 @@ static int gemm_rs_impl(ub_handle_t h, const void *const *A, const void *const *
     p.abort_word = abort_of(h);
     p.status = status_of(h);
     p.timeout_ns = static_cast<uint64_t>(h->timeout_ns);
-    if (pair) set_pairs(h, p, ubk::MODE_RS, streamk);
+    if (skinny) set_skinny(h, p, 1, ubk::SK_W_BYTES);
+    else if (pair) set_pairs(h, p, ubk::MODE_RS, streamk);
     p.epoch = ++h->epoch;
-    if (int rc = launch(h, p, ubk::MODE_RS, pair, s, b_kn ? UB_OP_RS_KN : UB_OP_RS)) return rc;
+    if (int rc = launch(h, p, ubk::MODE_RS, skinny ? PATH_SKINNY : pair ? PATH_PAIR : PATH_SINGLE, s,
+                        b_kn ? UB_OP_RS_KN : UB_OP_RS))
+        return rc;
     ++h->counters.rs_calls;
     h->counters.last_T = T;
     return UB_OK;
@@ -932,7 +1043,7 @@ int ub_wgrad(ub_handle_t h, const void *D, int64_t M, int ub_is_a, void *out, vo
     choose_path(h, ubk::MODE_AG, 1 << 30, p.region_tile0[1], p.k_blocks, pair, split);
     set_pairs(h, p, ubk::MODE_AG, split);
     p.epoch = ++h->epoch;
-    if (int rc = launch(h, p, ubk::MODE_AG, true, s, UB_OP_WGRAD)) return rc;
+    if (int rc = launch(h, p, ubk::MODE_AG, PATH_PAIR, s, UB_OP_WGRAD)) return rc;
     h->counters.last_T = T;
     return UB_OK;
 }
@@ -969,6 +1080,10 @@ int ub_set_option(ub_handle_t h, int key, int64_t val)
         if (val < -1 || val > 1) return fail(UB_ERR_ARG, "streamk must be -1, 0 or 1");
         h->streamk = val;
         return UB_OK;
+    case UB_OPT_SKINNY:
+        if (val < -1 || val > 1) return fail(UB_ERR_ARG, "UB_OPT_SKINNY must be -1, 0 or 1");
+        h->skinny = val;
+        return UB_OK;
     case UB_OPT_GATHER_KERNEL:
         if (val != 0 && val != 1) return fail(UB_ERR_ARG, "gather_kernel must be 0 or 1");
         h->gather_kernel = val;
@@ -1002,6 +1117,7 @@ int ub_get_option(ub_handle_t h, int key, int64_t *val)
     case UB_OPT_STREAMK: *val = h->streamk; return UB_OK;
     case UB_OPT_COPY_STREAMS: *val = h->copy_streams; return UB_OK;
     case UB_OPT_GATHER_KERNEL: *val = h->gather_kernel; return UB_OK;
+    case UB_OPT_SKINNY: *val = h->skinny; return UB_OK;
     default: return fail(UB_ERR_ARG, "unknown option %d", key);
     }
 }

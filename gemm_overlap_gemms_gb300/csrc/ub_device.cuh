@@ -1,0 +1,299 @@
+// Device-side building blocks shared by the GEMM kernels: inline-PTX wrappers for
+// mbarriers, the tensor memory accelerator (TMA), tcgen05 MMAs and tensor memory, and
+// the bounded waits. Every wait gives up after the call's timeout, records
+// UB_ERR_TIMEOUT and publishes the call's epoch in the abort word; nothing traps.
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+#include "ub_internal.h"
+
+namespace ubk {
+namespace {
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int x, int y)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int x, int y)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(x), "r"(y)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void bulk_wait_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+__device__ __forceinline__ void fence_proxy_async_shared()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+// fp32 pair -> packed bf16x2 (round to nearest even); `lo` lands at the lower address.
+__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo, uint32_t hi)
+{
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(__uint_as_float(hi)), "f"(__uint_as_float(lo)));
+    return d;
+}
+
+// ---- tcgen05
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand tile written by TMA with the
+// 128-byte swizzle: rows of 128 bytes (64 bf16 of K), 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address      [0,14)
+    d |= static_cast<uint64_t>(16u >> 4) << 16;           // leading offset     [16,30) (unused: K fits one row)
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;         // stride offset      [32,46)
+    d |= static_cast<uint64_t>(1u) << 46;                 // descriptor version [46,48)
+    d |= static_cast<uint64_t>(2u) << 61;                 // swizzle: 128 B     [61,64)
+    return d;
+}
+
+// Shared-memory matrix descriptor of an MN-major operand tile (MN contiguous in global
+// memory, e.g. a weight stored K x N) written by TMA with the 128-byte swizzle in boxes
+// of 64 MN elements x 64 K rows: each 8 K-rows x 64 MN group is one 1024-byte swizzle
+// atom; atoms follow each other along K every 1024 bytes (stride offset) and the second
+// box of 64 MN elements starts 8 KiB later (leading offset).
+__device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address      [0,14)
+    d |= static_cast<uint64_t>(8192u >> 4) << 16;         // leading offset: next 64 MN
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;         // stride offset: next 8 K rows
+    d |= static_cast<uint64_t>(1u) << 46;                 // descriptor version
+    d |= static_cast<uint64_t>(2u) << 61;                 // swizzle: 128 B
+    return d;
+}
+constexpr uint32_t MN_BOX_BYTES = 64 * BK * 2;           // one 64 (MN) x 64 (K) box
+
+// Arrive on `bar` once every tcgen05 operation this thread issued so far has completed.
+__device__ __forceinline__ void umma_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t *v)
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
+          "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),
+          "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]),
+          "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+
+// Bounded pause used on the abort path so that copies already issued land first.
+__device__ void settle(uint64_t ns)
+{
+    const uint64_t t0 = global_timer();
+    while (global_timer() - t0 < ns) __nanosleep(1000);
+}
+
+// ------------------------------------------------------------------ bounded waits
+
+struct WaitCtx {
+    uint32_t *abort_word;
+    int32_t *status;
+    uint64_t timeout_ns;
+    uint32_t epoch;
+};
+
+__device__ __forceinline__ bool call_aborted(const WaitCtx &w)
+{
+    return *reinterpret_cast<volatile uint32_t *>(w.abort_word) == w.epoch;
+}
+
+__device__ void raise_error(const WaitCtx &w, int code)
+{
+    atomicCAS(reinterpret_cast<int *>(w.status), 0, code);
+    __threadfence();
+    atomicExch(w.abort_word, w.epoch);
+}
+
+// A waiting thread reads the abort word at most once per this many ns. Every waiting
+// thread of every CTA polls the same word, so frequent reads would queue on the one L2
+// slice that holds it, in front of the operand loads that the waits are waiting for.
+constexpr uint64_t kAbortPollNs = 16000;
+
+// Timeout and abort checks of a spinning wait, made every few spins: false when the
+// wait must give up (the call was aborted, or the timeout ran out: UB_ERR_TIMEOUT).
+struct WaitClock {
+    uint64_t t0, next_poll;
+    __device__ __forceinline__ WaitClock() : t0(global_timer()), next_poll(t0 + kAbortPollNs) {}
+    __device__ __forceinline__ bool ok(const WaitCtx &w)
+    {
+        const uint64_t now = global_timer();
+        if (now - t0 > w.timeout_ns) {
+            raise_error(w, UB_ERR_TIMEOUT);
+            return false;
+        }
+        if (now >= next_poll) {
+            if (call_aborted(w)) return false;
+            next_poll = now + kAbortPollNs;
+        }
+        return true;
+    }
+};
+
+// Wait for phase `parity` of an mbarrier. False when this call was aborted or the
+// wait ran past the timeout (which then raises UB_ERR_TIMEOUT).
+__device__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtx &w)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    WaitClock clk;
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 15u) == 0 && !clk.ok(w)) return false;
+    }
+}
+
+// Wait used while draining at exit: ignores the abort word, still bounded in time.
+__device__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns)
+{
+    const uint64_t t0 = global_timer();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer() - t0 > timeout_ns) return false;
+    }
+    return true;
+}
+
+// Wait until the readiness flag of a chunk has reached this call's epoch (wrap-safe),
+// then order the tensor-memory-accelerator reads that follow after it.
+__device__ bool wait_flag(const uint32_t *flag, const WaitCtx &w)
+{
+    WaitClock clk;
+    for (uint32_t n = 0;; ++n) {
+        uint32_t v;
+        asm volatile("ld.acquire.sys.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+        if (static_cast<int32_t>(v - w.epoch) >= 0) {
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            return true;
+        }
+        if ((n & 7u) == 7u && !clk.ok(w)) return false;
+        __nanosleep(512);
+    }
+}
+
+
+__device__ __forceinline__ void st_release_u32(uint32_t *ptr, uint32_t v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
+}
+
+// Wait until a partial tile of this call is published (bounded, abort-aware).
+__device__ bool wait_partial(const uint32_t *flag, const WaitCtx &w)
+{
+    WaitClock clk;
+    for (uint32_t n = 0;; ++n) {
+        uint32_t v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+        if (v == w.epoch) return true;
+        if ((n & 15u) == 15u && !clk.ok(w)) return false;
+        __nanosleep(64);
+    }
+}
+
+}  // namespace
+}  // namespace ubk

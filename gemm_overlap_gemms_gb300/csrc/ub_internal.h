@@ -47,6 +47,17 @@ constexpr int MIN_KBLOCKS_PER_PIECE = 16;
 // Nor into more than this many pieces.
 constexpr int MAX_TAIL_SPLIT = 8;
 
+// Skinny kernel (few active tokens): 128 weight rows per tile, pipeline depth chosen per
+// call from the token tile's size, partial tiles of split pieces in the workspace.
+constexpr int SK_BM = 128;
+constexpr int SK_MAX_COLS = 256;         // token columns of one accumulator
+constexpr int SK_AUTO_MAX_COLS = 128;    // chosen by default up to here (beyond, the tile kernels win)
+constexpr int SK_MAX_STAGES = 12;
+constexpr int SK_MIN_KBLOCKS = 8;        // a k-piece is never shorter than this
+constexpr int SK_MAX_SPLIT = 6;          // nor is a tile cut into more pieces
+constexpr int SK_SMEM_LIMIT = 232448;    // dynamic shared memory a CTA may opt into
+constexpr int SK_W_BYTES = SK_BM * BK * 2;
+
 enum Mode : int { MODE_AG = 0, MODE_RS = 1, MODE_AG_GLU = 2 /* AG-GEMM + SwiGLU epilogue, pair kernel only */ };
 
 // Kernel parameters, passed by value as a __grid_constant__ (tensor maps must live
@@ -93,6 +104,16 @@ struct GemmParams {
     int b_mn;                    // 1: B is MN-major (stored K x N; tensor map inner dim = N)
     float *ws;                   // partial tiles of split tail tiles: [num_pairs][2][256/4][128][4] fp32
     uint32_t *ws_flags;          // [num_pairs][2][EPI_WARPS]: epoch of the partial written
+
+    // ---- skinny kernel only (few tokens): weight rows on the MMA's M dimension, tokens
+    // on its N dimension. Tiles are SK_BM weight rows (SwiGLU: SK_BM gate + SK_BM up rows)
+    // by all T tokens; work units are (tile, k-piece), unit u = piece * n_tiles + tile.
+    int sk_sub_n;                // token columns per sub-tile (multiple of 16, <= 256)
+    int sk_n_sub;                // sub-tiles: AG one per chunk (rows of chunk r), RS one
+    int sk_stride;               // TMEM columns between the two accumulators (power of two)
+    int sk_split;                // k-pieces per tile; the last piece finishes the tile
+    int sk_stages;               // shared-memory pipeline depth (<= SK_MAX_STAGES)
+    int sk_units;                // n_tiles * sk_split
 };
 
 // Launch the persistent GEMM (mode MODE_AG or MODE_RS) with `grid` CTAs on `stream`.
@@ -104,6 +125,14 @@ cudaError_t launch_gemm_pair(const GemmParams &p, int mode, int clusters, cudaSt
 
 // Clusters of two CTAs of the pair kernel that can be resident at once (0 on error).
 int max_pair_clusters(int mode);
+
+// Launch the skinny kernel (ub_skinny.cu) with `grid` CTAs; the tensor maps of the weight
+// have 128-row boxes (K-major) or 64 x 64 boxes (MN-major), those of the tokens
+// sk_sub_n-row boxes.
+cudaError_t launch_gemm_skinny(const GemmParams &p, int mode, int grid, cudaStream_t stream);
+
+// Dynamic shared memory of the skinny kernel for a pipeline of `stages`.
+int skinny_smem_bytes(int stages, int w_bytes, int x_bytes);
 
 // Standalone reduce-scatter (ub_bulk.cu): Y[r][i][:] = sum_j P[j][r*c + i][:].
 struct BulkRsParams {
@@ -135,5 +164,9 @@ cudaError_t launch_gather(const GatherParams &p, cudaStream_t stream);
 
 // Record the message ub_last_error() returns on this host thread.
 void set_last_error(const char *msg);
+
+// Raise a kernel's dynamic shared memory limit to `bytes`, once per kernel and device
+// (the runtime call costs microseconds of host time, paid once instead of per launch).
+cudaError_t raise_smem_limit(const void *kernel, int bytes);
 
 }  // namespace ubk
