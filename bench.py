@@ -77,8 +77,9 @@ def parse():
     ap.add_argument("--case-T", type=int, default=8192)
     ap.add_argument("--case-reps", type=int, default=3)
     ap.add_argument("--sm-margin", type=int, default=0)
-    ap.add_argument("--gather-kernel", type=int, default=0, choices=[0, 1],
-                    help="1: the all-gather is one kernel launch instead of driver copies")
+    ap.add_argument("--gather-kernel", type=int, default=-1, choices=[-1, 0, 1],
+                    help="-1: the library's choice by T (default); 1: the all-gather is one kernel "
+                         "launch; 0: driver copies")
     ap.add_argument("--timeout-ms", type=float, default=None,
                     help="bound of the device-side waits (default: the library's 1 s)")
     ap.add_argument("--cta-pair", type=int, default=-1, choices=[-1, 0, 1],
@@ -804,6 +805,21 @@ def run_case(args):
     buf.set_option("profile", 0)
     # whole calls (gather copies, flag writes, joins included), CUDA events on the stream
     call_ms = time_steps(fn, args.case_reps, 1, torch.cuda.current_stream(), 1) / args.case_reps
+    # host time to enqueue one call (no synchronisation inside the loop)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.case_reps):
+        fn()
+    host_us = 1e6 * (time.perf_counter() - t0) / args.case_reps
+    torch.cuda.synchronize()
+    # the same call captured once into a CUDA graph and replayed: no host work per call
+    cs = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cs):
+        with torch.cuda.graph(graph, stream=cs):
+            fn()
+    graph_ms = time_steps(graph.replay, args.case_reps, 2, torch.cuda.current_stream(), 1) / args.case_reps
+    del graph
     status = buf.query_status()
     buf.close()
     print(json.dumps({"case": args.case, "T": T, "cta_pair": args.cta_pair, "streamk": args.streamk,
@@ -811,7 +827,7 @@ def run_case(args):
                       "gather_kernel": args.gather_kernel, "launches": n, "avg_us": 1e3 * ms / max(n, 1),
                       "tflops": flops * n / (ms / 1e3) / 1e12 if ms > 0 and flops else None,
                       "gbs": nbytes * n / (ms / 1e3) / 1e9 if ms > 0 and nbytes else None,
-                      "call_us": 1e3 * call_ms,
+                      "call_us": 1e3 * call_ms, "host_us": host_us, "graph_us": 1e3 * graph_ms,
                       "first_us": 1e3 * first_ms, "first_status": first_status, "status": status}))
     if status != ub.UB_OK:
         sys.exit("device status %d (%s)" % (status, ub.ERRORS.get(status, "?")))

@@ -140,7 +140,8 @@ struct ub_handle {
     cudaStream_t extra_side[UB_MAX_TP] = {};      // copy streams 1.. (created on demand)
     cudaEvent_t ev_join_extra[UB_MAX_TP] = {};
     int64_t copy_streams = 1;  // raised to min(tp, 4) at creation
-    int64_t gather_kernel = 0; // 1: the gather is one kernel launch instead of driver copies
+    int64_t gather_kernel = -1; // 1: the gather is one kernel launch; 0: driver copies; -1: by T
+    bool gather_by_kernel = false;  // what the last issue_gather chose (join_gather follows it)
     cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
     uint32_t epoch = 0;
     // options
@@ -228,6 +229,8 @@ GemmParams *cache_insert(ub_handle *h, std::vector<const void *> key, const Gemm
 }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+constexpr int64_t kGatherKernelMaxT = 512;  // UB_OPT_GATHER_KERNEL = -1: kernel up to this T
 
 // How many k-pieces the last wave's tiles are cut into: enough to give every pair one
 // piece, at most MAX_TAIL_SPLIT, each at least MIN_KBLOCKS_PER_PIECE k-blocks long.
@@ -372,7 +375,12 @@ int issue_gather(ub_handle *h, const void *const *shards, cudaStream_t s, uint32
     const int64_t T = h->T, H = h->hidden, c = T / tp;
     const int self = static_cast<int>(h->self_rank);
     char *ub = static_cast<char *>(h->ub);
-    if (h->copy_streams == 0 && !h->gather_kernel) {
+    // The one-launch gather kernel replaces tp copies and tp flag writes, each a driver
+    // operation with its own host cost and launch latency; for few tokens those dominate
+    // the call (GB300, tp 4: AG at T <= 512 takes 26-33 us with the kernel, 39-44 us with
+    // the copies), while for many tokens the copies are as fast or faster.
+    h->gather_by_kernel = h->gather_kernel == 1 || (h->gather_kernel < 0 && T <= kGatherKernelMaxT);
+    if (h->copy_streams == 0 && !h->gather_by_kernel) {
         // In-stream: the copies and flag writes go on `s` itself, ahead of the GEMM,
         // which then finds every flag set (no overlap, no cross-stream hops).
         for (int q = 1; q <= tp; ++q) {
@@ -388,7 +396,7 @@ int issue_gather(ub_handle *h, const void *const *shards, cudaStream_t s, uint32
         }
         return UB_OK;
     }
-    if (h->gather_kernel) {
+    if (h->gather_by_kernel) {
         // One launch on the side stream: small CTAs (they fit beside the GEMM's), about
         // one per SM per chunk, each chunk's flag published by its last CTA.
         ubk::GatherParams g;
@@ -434,13 +442,31 @@ int issue_gather(ub_handle *h, const void *const *shards, cudaStream_t s, uint32
 // Make `s` wait for every copy stream the last gather used.
 int join_gather(ub_handle *h, cudaStream_t s)
 {
-    if (h->copy_streams == 0 && !h->gather_kernel) return UB_OK;  // in-stream: nothing to join
-    const int ncs = h->gather_kernel ? 1 : static_cast<int>(h->copy_streams < h->tp ? h->copy_streams : h->tp);
+    if (h->copy_streams == 0 && !h->gather_by_kernel) return UB_OK;  // in-stream: nothing to join
+    const int ncs = h->gather_by_kernel ? 1 : static_cast<int>(h->copy_streams < h->tp ? h->copy_streams : h->tp);
     UB_CUDA(cudaEventRecord(h->ev_join, h->side));
     UB_CUDA(cudaStreamWaitEvent(s, h->ev_join, 0));
     for (int i = 1; i < ncs; ++i) {
         UB_CUDA(cudaEventRecord(h->ev_join_extra[i], h->extra_side[i]));
         UB_CUDA(cudaStreamWaitEvent(s, h->ev_join_extra[i], 0));
+    }
+    return UB_OK;
+}
+
+// A new call's epoch. When `s` is being captured into a CUDA graph, the epoch becomes a
+// constant of the graph, so every replay would find the readiness flags, the partial-tile
+// flags and the abort word still holding it from the replay before. The captured call
+// therefore starts, in stream order, by clearing them (never the sticky status word).
+// An uncaptured call pays nothing: epochs only grow there.
+int begin_call(ub_handle *h, cudaStream_t s, uint32_t &epoch)
+{
+    epoch = ++h->epoch;
+    if (epoch == 0) epoch = ++h->epoch;  // 0 is what a cleared word holds
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    UB_CUDA(cudaStreamIsCapturing(s, &cs));
+    if (cs == cudaStreamCaptureStatusActive) {
+        UB_CUDA(cudaMemsetAsync(h->ctrl, 0, (UB_MAX_TP + 1) * sizeof(uint32_t), s));  // flags, abort word
+        UB_CUDA(cudaMemsetAsync(ws_flags_of(h), 0, h->ctrl_bytes - 64 * sizeof(uint32_t), s));
     }
     return UB_OK;
 }
@@ -761,7 +787,8 @@ static int ag_gemm_impl(ub_handle_t h, const void *const *shards, const void *Wt
     p.timeout_ns = static_cast<uint64_t>(h->timeout_ns);
     if (skinny) set_skinny(h, p, glu ? 2 : 1, glu ? 2 * ubk::SK_W_BYTES : ubk::SK_W_BYTES);
     else if (pair) set_pairs(h, p, mode, streamk);
-    const uint32_t epoch = ++h->epoch;
+    uint32_t epoch = 0;
+    if (int rc = begin_call(h, s, epoch)) return rc;
     p.epoch = epoch;
     const int64_t drop = h->drop_flag;
     h->drop_flag = -1;
@@ -903,7 +930,9 @@ static int gemm_rs_impl(ub_handle_t h, const void *const *A, const void *const *
     p.timeout_ns = static_cast<uint64_t>(h->timeout_ns);
     if (skinny) set_skinny(h, p, 1, ubk::SK_W_BYTES);
     else if (pair) set_pairs(h, p, ubk::MODE_RS, streamk);
-    p.epoch = ++h->epoch;
+    uint32_t epoch = 0;
+    if (int rc = begin_call(h, s, epoch)) return rc;
+    p.epoch = epoch;
     if (int rc = launch(h, p, ubk::MODE_RS, skinny ? PATH_SKINNY : pair ? PATH_PAIR : PATH_SINGLE, s,
                         b_kn ? UB_OP_RS_KN : UB_OP_RS))
         return rc;
@@ -935,7 +964,8 @@ int ub_allgather(ub_handle_t h, const void *const *shards, void *stream)
     DeviceGuard g(h->device);
     if (!g.ok) return fail(UB_ERR_CUDA, "ub_allgather: cannot select the handle's device");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const uint32_t epoch = ++h->epoch;
+    uint32_t epoch = 0;
+    if (int rc = begin_call(h, s, epoch)) return rc;
     if (int rc = issue_gather(h, shards, s, epoch, -1)) return rc;
     if (int rc = join_gather(h, s)) return rc;
     h->counters.last_T = h->T;
@@ -1042,7 +1072,9 @@ int ub_wgrad(ub_handle_t h, const void *D, int64_t M, int ub_is_a, void *out, vo
     bool pair = true, split = false;
     choose_path(h, ubk::MODE_AG, 1 << 30, p.region_tile0[1], p.k_blocks, pair, split);
     set_pairs(h, p, ubk::MODE_AG, split);
-    p.epoch = ++h->epoch;
+    uint32_t epoch = 0;
+    if (int rc = begin_call(h, s, epoch)) return rc;
+    p.epoch = epoch;
     if (int rc = launch(h, p, ubk::MODE_AG, PATH_PAIR, s, UB_OP_WGRAD)) return rc;
     h->counters.last_T = T;
     return UB_OK;
@@ -1085,7 +1117,7 @@ int ub_set_option(ub_handle_t h, int key, int64_t val)
         h->skinny = val;
         return UB_OK;
     case UB_OPT_GATHER_KERNEL:
-        if (val != 0 && val != 1) return fail(UB_ERR_ARG, "gather_kernel must be 0 or 1");
+        if (val < -1 || val > 1) return fail(UB_ERR_ARG, "gather_kernel must be -1, 0 or 1");
         h->gather_kernel = val;
         return UB_OK;
     case UB_OPT_COPY_STREAMS: {

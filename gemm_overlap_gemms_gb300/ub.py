@@ -164,6 +164,7 @@ class UserBuffer:
         _check(L.ub_create(int(shape[0]), int(shape[1]), int(tp_size), 0, ctypes.byref(h)))
         self._h = h
         self.max_tokens, self.hidden, self.tp = int(shape[0]), int(shape[1]), int(tp_size)
+        self._active = None
         self.device = torch.device("cuda", torch.cuda.current_device())
 
     # -- lifetime
@@ -188,12 +189,16 @@ class UserBuffer:
     def set_active_shape(self, shape):
         dims = (ctypes.c_int64 * max(1, len(shape)))(*[int(d) for d in shape])
         _check(load().ub_set_active_shape_nd(self._h, len(shape), dims))
+        self._active = (int(shape[0]), int(shape[1]))
 
     @property
     def active_shape(self):
-        T, H = ctypes.c_int64(), ctypes.c_int64()
-        _check(load().ub_get_active_shape(self._h, ctypes.byref(T), ctypes.byref(H)))
-        return (T.value, H.value)
+        """[T, hidden] as last set (kept on this side: every call reads it)."""
+        if self._active is None:
+            T, H = ctypes.c_int64(), ctypes.c_int64()
+            _check(load().ub_get_active_shape(self._h, ctypes.byref(T), ctypes.byref(H)))
+            self._active = (T.value, H.value)
+        return self._active
 
     @property
     def capacity_shape(self):

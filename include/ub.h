@@ -86,10 +86,11 @@ enum {
                               (round-robin in ring order), 1..UB_MAX_TP; default min(tp, 4).
                               0 = no overlap: the copies and flag writes go on the call's own
                               stream ahead of the GEMM (a comparator; slower on GB300) */
-    UB_OPT_GATHER_KERNEL = 9, /* 0 (default): the gather is one cudaMemcpyAsync plus one stream
-                              flag write per chunk; 1: one kernel launch on the side stream
-                              lands every chunk in ring order and publishes each chunk's flag
-                              as its last CTA finishes (fewer driver operations per call) */
+    UB_OPT_GATHER_KERNEL = 9, /* 0: the gather is one cudaMemcpyAsync plus one stream flag write
+                              per chunk; 1: one kernel launch on the side stream lands every
+                              chunk in ring order and publishes each chunk's flag as its last
+                              CTA finishes (fewer driver operations per call); -1 (default):
+                              the kernel for T <= 512, the copies above */
     UB_OPT_SKINNY = 10     /* few-token kernel: weight rows on the MMA's M, tokens on its N, so
                               the work follows T and the weight is read once. Usable while the
                               token columns (ag_gemm*: tp * roundup(T/tp, 16); gemm_rs*:
