@@ -46,9 +46,9 @@ KERNEL_SRC = os.path.join(ROOT, "gemm_overlap_gemms_gb300", "csrc", "ub_gemm.cu"
 # per active token of the captured launch, and the kernel source they were taken on.
 # Traffic is reported as null once the kernel source no longer matches.
 NCU_TRAFFIC = {
-    "rs": {"sha256_16": "22b435fe73f2cd1a", "bytes": 1202.2e6, "T": 8192,
+    "rs": {"sha256_16": "a04e5b8d4d55e22d", "bytes": 1153.98e6, "T": 8192,
            "source": "profiles/ub_gemm_pair_kernel_rs_swiglu_fc2_T8192.md"},
-    "ag_swiglu": {"sha256_16": "22b435fe73f2cd1a", "bytes": 377.0e6, "T": 8192,
+    "ag_swiglu": {"sha256_16": "a04e5b8d4d55e22d", "bytes": 485.38e6, "T": 8192,
                   "source": "profiles/ub_gemm_pair_kernel_ag_glu_swiglu_fc1_T8192.md"},
 }
 
@@ -602,7 +602,8 @@ def sweep_points(wl, stream):
     Tmax = max(wl.Ts)
     pk, src = peaks()
     tensor_peak = _peak_value(pk, "bf16_tflops_sustained", "bf16_tflops") or FALLBACK["bf16_tflops_sustained"]
-    for T in (4, 64, 256, 512, 1024, 2048, 4096, 6144, 8192):
+    hbm_peak = _peak_value(pk, "hbm_gbs") or FALLBACK["hbm_gbs"]
+    for T in (4, 64, 128, 256, 512, 1024, 2048, 4096, 6144, 8192):
         if T > Tmax:
             X = synth.normal_bf16((T, H), 1.0, synth.generator(Xmax.device, 5), Xmax.device)
             A = [synth.normal_bf16((T, K), 1.0, synth.generator(Xmax.device, 6 + j), Xmax.device)
@@ -622,13 +623,24 @@ def sweep_points(wl, stream):
                 fn = lambda: wl.buf.gemm_rs(A, wl.B, outs, stream=stream)
             reps = 20
             # the no-overlap comparator puts the gather copies on the GEMM's stream, ahead of it
-            wl.buf.set_option("copy_streams", 0 if op == "ag_swiglu_no_overlap" else 4)
+            no_overlap = op == "ag_swiglu_no_overlap"
+            wl.buf.set_option("copy_streams", 0 if no_overlap else 4)
+            wl.buf.set_option("gather_kernel", 0 if no_overlap else -1)
             ms = time_steps(fn, reps, 3, stream, 1) / reps
             wl.buf.set_option("copy_streams", 4)
+            wl.buf.set_option("gather_kernel", -1)
             fl = 2.0 * T * H * N if op != "rs" else 2.0 * T * K * H * tp
             tf = fl / (ms / 1e3) / 1e12
+            # algorithmic HBM bytes: weights once, activations in, results out (AG: the
+            # shards read and the gathered buffer written as well)
+            if op == "rs":
+                nbytes = 2.0 * (tp * K * H + tp * T * K + T * H)
+            else:
+                n_out = N // 2 if op.startswith("ag_swiglu") else N
+                nbytes = 2.0 * (N * H + 2 * T * H + T * n_out)
             out.append({"sweep": op, "T": T, "us": ms * 1e3, "tflops": tf,
                         "frac_of_peak": tf / tensor_peak,
+                        "hbm_gbs": nbytes / (ms / 1e3) / 1e9, "hbm_frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak,
                         "note": ("gather copies on the GEMM's stream, before it (no overlap)"
                                  if op == "ag_swiglu_no_overlap" else
                                  "includes the gather copies, overlapped" if op != "rs" else "")})
