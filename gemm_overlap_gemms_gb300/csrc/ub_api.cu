@@ -678,9 +678,10 @@ static int ag_gemm_impl(ub_handle_t h, const void *const *shards, const void *Wt
     const int64_t c16 = ceil_div(c, 16) * 16;  // token columns of one chunk in the skinny kernel
     const bool skinny = use_skinny(h, tp * c16);
     if (skinny) pair = false;
-    else if (glu || b_kn) pair = true;  // otherwise the fused epilogue and MN-major operands need CTA pairs
+    else if (b_kn) pair = true;  // otherwise MN-major operands need CTA pairs
     const int bm = pair ? ubk::PAIR_BM : ubk::BM;      // rows of a tile
-    const int bbox = pair ? ubk::BN / 2 : ubk::BN;    // rows of a B box (one CTA's half in a pair)
+    // rows of a B box: one CTA's half in a pair; SwiGLU: the gate or the up half of a tile
+    const int bbox = pair || glu ? ubk::BN / 2 : ubk::BN;
     std::vector<const void *> key;
     key.reserve(tp + 7);
     key.push_back(reinterpret_cast<const void *>(uintptr_t(mode)));
@@ -736,7 +737,7 @@ static int ag_gemm_impl(ub_handle_t h, const void *const *shards, const void *Wt
                 // kernel reads in place from its shard while its copy stages it.
                 const void *src = r == self ? shards[r] : static_cast<const void *>(ub + r * c * H * 2);
                 if (int rc = encode_2d(&p.tmA[r], src, H, c, H * 2, ubk::BK, ubk::BM)) return rc;
-                if (int rc = encode_2d(&p.tmY[r], static_cast<char *>(Y) + r * c * N * 2, N, c, N * 2,
+                if (int rc = encode_2d(&p.tmY[r], static_cast<char *>(Y) + r * c * n_out * 2, n_out, c, n_out * 2,
                                        ubk::STORE_COLS, 32))
                     return rc;
             }

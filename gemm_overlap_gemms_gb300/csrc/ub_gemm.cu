@@ -157,7 +157,7 @@ __device__ __forceinline__ Tile tile_at(int t, const GemmParams &p)
     const int q = t / per_chunk;  // position in the ring
     const int rem = t - q * per_chunk;
     Tile x;
-    if (MODE == MODE_AG) {
+    if (MODE != MODE_RS) {
         int r = p.self_rank + q;
         x.r = r >= p.tp ? r - p.tp : r;
     } else {
@@ -173,6 +173,11 @@ __device__ __forceinline__ Tile tile_at(int t, const GemmParams &p)
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1) ub_gemm_kernel(const __grid_constant__ GemmParams p)
 {
+    constexpr bool IS_AG = MODE != MODE_RS;
+    // SwiGLU: the 256-row B tile is 128 gate rows and the matching 128 up rows (F further
+    // down), so accumulator columns 0..127 hold the gate and 128..255 the up projections
+    // of the same 128 outputs.
+    constexpr bool GLU = MODE == MODE_AG_GLU;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *smA = base;
@@ -212,22 +217,22 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_kernel(const __grid_consta
 
     if (warp == 0 && lane == 0) {
         // ---------------------------------------------------------- producer
-        const int nmaps = MODE == MODE_AG ? 1 : p.tp;
+        const int nmaps = IS_AG ? 1 : p.tp;
         for (int i = 0; i < nmaps; ++i) prefetch_tmap(&p.tmB[i]);
         uint32_t stage = 0, phase = 0, ready = 0;
         int issued = 0;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
             const Tile x = tile_at<MODE>(t, p);
-            if (MODE == MODE_AG && x.r != p.self_rank && !((ready >> x.r) & 1u)) {
+            if (IS_AG && x.r != p.self_rank && !((ready >> x.r) & 1u)) {
                 if (!wait_flag(p.flags + x.r, w)) {
                     ok = false;
                     break;
                 }
                 ready |= 1u << x.r;
             }
-            const int arow = MODE == MODE_AG ? x.m * BM : x.r * p.c + x.m * BM;
-            const int brow = x.n * BN;
+            const int arow = IS_AG ? x.m * BM : x.r * p.c + x.m * BM;
+            const int brow = GLU ? x.n * 128 : x.n * BN;
             for (int kb = 0; kb < p.k_blocks; ++kb) {
                 if (!mbar_wait(empty_bar(stage), phase ^ 1u, w)) {
                     ok = false;
@@ -236,7 +241,7 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_kernel(const __grid_consta
                 const CUtensorMap *ma;
                 const CUtensorMap *mb;
                 int kx;
-                if (MODE == MODE_AG) {
+                if (IS_AG) {
                     ma = &p.tmA[x.r];
                     mb = &p.tmB[0];
                     kx = kb * BK;
@@ -249,6 +254,9 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_kernel(const __grid_consta
                 mbar_arrive_expect_tx(full_bar(stage), A_STAGE_BYTES + B_STAGE_BYTES);
                 tma_load_2d(smem_u32(smA + stage * A_STAGE_BYTES), ma, full_bar(stage), kx, arow);
                 tma_load_2d(smem_u32(smB + stage * B_STAGE_BYTES), mb, full_bar(stage), kx, brow);
+                if (GLU)  // B map boxes are 128 rows: the up rows go to the second half
+                    tma_load_2d(smem_u32(smB + stage * B_STAGE_BYTES) + B_STAGE_BYTES / 2, mb, full_bar(stage), kx,
+                                brow + p.glu_f);
                 ++issued;
                 if (++stage == STAGES) {
                     stage = 0;
@@ -316,36 +324,82 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_kernel(const __grid_consta
             const int row0 = x.m * BM + quarter * 32;  // first row of this warp's slab, inside block r
             const bool rows_live = row0 < p.c;
             const uint32_t trow = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
+            if constexpr (GLU) {
+                // Two output groups of 64 features: Z[:, 128n + 64h + j] = silu(gate) * up
+                // from gate column 64h + j and up column 128 + 64h + j, in fp32.
 #pragma unroll 1
-            for (int sub = 0; sub < BN / STORE_COLS; ++sub) {
-                uint32_t v[STORE_COLS];
-                tmem_ld32(trow + sub * STORE_COLS, v);
-                tmem_ld32(trow + sub * STORE_COLS + 32, v + 32);
-                tmem_wait_ld();
-                if (sub == BN / STORE_COLS - 1) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(tempty_bar(acc));
-                }
-                const int col = x.n * BN + sub * STORE_COLS;
-                if (!rows_live || col >= p.n_out) continue;
-                const uint32_t buf = ebuf0 + (nstore & 1) * EPI_BUF_BYTES;
-                if (lane == 0) bulk_wait_read<1>();  // the store that last used `buf` has read it
-                __syncwarp();
-                const uint32_t rowaddr = buf + lane * 128u;
+                for (int hs = 0; hs < 2; ++hs) {
+                    uint32_t pk[STORE_COLS / 2];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    st_shared_v4(rowaddr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4),
-                                 pack_bf16x2(v[8 * j + 0], v[8 * j + 1]), pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
-                                 pack_bf16x2(v[8 * j + 4], v[8 * j + 5]), pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const int c0 = hs * STORE_COLS + hf * 32;
+                        uint32_t g[32], u[32];
+                        tmem_ld32(trow + c0, g);
+                        tmem_ld32(trow + 128 + c0, u);
+                        tmem_wait_ld();
+                        if (hs == 1 && hf == 1) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(tempty_bar(acc));
+                        }
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const float g0 = __uint_as_float(g[2 * j]), g1 = __uint_as_float(g[2 * j + 1]);
+                            const float z0 = g0 / (1.0f + __expf(-g0)) * __uint_as_float(u[2 * j]);
+                            const float z1 = g1 / (1.0f + __expf(-g1)) * __uint_as_float(u[2 * j + 1]);
+                            pk[hf * 16 + j] = pack_bf16x2(__float_as_uint(z0), __float_as_uint(z1));
+                        }
+                    }
+                    const int col = x.n * 128 + hs * STORE_COLS;
+                    if (!rows_live || col >= p.n_out) continue;
+                    const uint32_t buf = ebuf0 + (nstore & 1) * EPI_BUF_BYTES;
+                    if (lane == 0) bulk_wait_read<1>();
+                    __syncwarp();
+                    const uint32_t rowaddr = buf + lane * 128u;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        st_shared_v4(rowaddr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4), pk[4 * j],
+                                     pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                    fence_proxy_async_shared();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&p.tmY[x.r], buf, col, row0);
+                        bulk_commit();
+                    }
+                    ++nstore;
                 }
-                fence_proxy_async_shared();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_2d(&p.tmY[x.r], buf, col, row0);
-                    bulk_commit();
+            } else {
+#pragma unroll 1
+                for (int sub = 0; sub < BN / STORE_COLS; ++sub) {
+                    uint32_t v[STORE_COLS];
+                    tmem_ld32(trow + sub * STORE_COLS, v);
+                    tmem_ld32(trow + sub * STORE_COLS + 32, v + 32);
+                    tmem_wait_ld();
+                    if (sub == BN / STORE_COLS - 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(tempty_bar(acc));
+                    }
+                    const int col = x.n * BN + sub * STORE_COLS;
+                    if (!rows_live || col >= p.n_out) continue;
+                    const uint32_t buf = ebuf0 + (nstore & 1) * EPI_BUF_BYTES;
+                    if (lane == 0) bulk_wait_read<1>();  // the store that last used `buf` has read it
+                    __syncwarp();
+                    const uint32_t rowaddr = buf + lane * 128u;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        st_shared_v4(rowaddr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4),
+                                     pack_bf16x2(v[8 * j + 0], v[8 * j + 1]), pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                                     pack_bf16x2(v[8 * j + 4], v[8 * j + 5]), pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+                    }
+                    fence_proxy_async_shared();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&p.tmY[x.r], buf, col, row0);
+                        bulk_commit();
+                    }
+                    ++nstore;
                 }
-                ++nstore;
             }
         }
         if (lane == 0) bulk_wait_all();
@@ -672,7 +726,7 @@ __global__ void __maxnreg__(PAIR_MAX_REGS) ub_gemm_pair_kernel(const __grid_cons
                 }
             }
 
-            if (GLU) {
+            if constexpr (GLU) {
                 // Two output groups of 64 columns: gate columns [64h, 64h + 64) and up
                 // columns 128 + [64h, 64h + 64) of the accumulator give
                 // Z[:, 128n + 64h + j] = silu(gate) * up, computed in fp32.
@@ -736,82 +790,81 @@ __global__ void __maxnreg__(PAIR_MAX_REGS) ub_gemm_pair_kernel(const __grid_cons
                     }
                     ++nstore;
                 }
-                continue;
-            }
-
+            } else {
 #pragma unroll 1
-            for (int sub = 0; sub < BN / STORE_COLS; ++sub) {
-                uint32_t v[STORE_COLS];
-                tmem_ld32(trow + sub * STORE_COLS, v);
-                tmem_ld32(trow + sub * STORE_COLS + 32, v + 32);
-                tmem_wait_ld();
-                if (sub == BN / STORE_COLS - 1) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
-                }
-                for (int ci = 1; ci <= n_contrib; ++ci) {
-                    const float4 *src = reinterpret_cast<const float4 *>(
-                        p.ws + static_cast<size_t>((pair + ci) * 2 + rank) * PARTIAL_FLOATS);
-#pragma unroll
-                    for (int i = 0; i < STORE_COLS / 4; ++i) {
-                        const float4 q = __ldcg(src + (sub * (STORE_COLS / 4) + i) * 128 + prow);
-                        v[4 * i + 0] = __float_as_uint(__uint_as_float(v[4 * i + 0]) + q.x);
-                        v[4 * i + 1] = __float_as_uint(__uint_as_float(v[4 * i + 1]) + q.y);
-                        v[4 * i + 2] = __float_as_uint(__uint_as_float(v[4 * i + 2]) + q.z);
-                        v[4 * i + 3] = __float_as_uint(__uint_as_float(v[4 * i + 3]) + q.w);
+                for (int sub = 0; sub < BN / STORE_COLS; ++sub) {
+                    uint32_t v[STORE_COLS];
+                    tmem_ld32(trow + sub * STORE_COLS, v);
+                    tmem_ld32(trow + sub * STORE_COLS + 32, v + 32);
+                    tmem_wait_ld();
+                    if (sub == BN / STORE_COLS - 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
                     }
-                }
-                const int col = x.n * BN + sub * STORE_COLS;
-                if (col >= p.n_out || lrow0 >= p.region_rows[x.q]) continue;
-                // Pack to bf16 (row-major, 8 x 16 bytes per thread).
-                uint32_t pk[STORE_COLS / 2];
+                    for (int ci = 1; ci <= n_contrib; ++ci) {
+                        const float4 *src = reinterpret_cast<const float4 *>(
+                            p.ws + static_cast<size_t>((pair + ci) * 2 + rank) * PARTIAL_FLOATS);
 #pragma unroll
-                for (int j = 0; j < STORE_COLS / 2; ++j) pk[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+                        for (int i = 0; i < STORE_COLS / 4; ++i) {
+                            const float4 q = __ldcg(src + (sub * (STORE_COLS / 4) + i) * 128 + prow);
+                            v[4 * i + 0] = __float_as_uint(__uint_as_float(v[4 * i + 0]) + q.x);
+                            v[4 * i + 1] = __float_as_uint(__uint_as_float(v[4 * i + 1]) + q.y);
+                            v[4 * i + 2] = __float_as_uint(__uint_as_float(v[4 * i + 2]) + q.z);
+                            v[4 * i + 3] = __float_as_uint(__uint_as_float(v[4 * i + 3]) + q.w);
+                        }
+                    }
+                    const int col = x.n * BN + sub * STORE_COLS;
+                    if (col >= p.n_out || lrow0 >= p.region_rows[x.q]) continue;
+                    // Pack to bf16 (row-major, 8 x 16 bytes per thread).
+                    uint32_t pk[STORE_COLS / 2];
+#pragma unroll
+                    for (int j = 0; j < STORE_COLS / 2; ++j) pk[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
 
-                int chunk = 0;  // output block of a TMA store (RS), or -1 = direct stores
-                int brow = lrow0;
-                if (MODE == MODE_RS) {
-                    const int last = min(lrow0 + 31, p.region_rows[0] - 1);
-                    chunk = lrow0 / p.c;
-                    if (last / p.c != chunk) {
-                        chunk = -1;
+                    int chunk = 0;  // output block of a TMA store (RS), or -1 = direct stores
+                    int brow = lrow0;
+                    if (MODE == MODE_RS) {
+                        const int last = min(lrow0 + 31, p.region_rows[0] - 1);
+                        chunk = lrow0 / p.c;
+                        if (last / p.c != chunk) {
+                            chunk = -1;
+                        } else {
+                            brow = lrow0 - chunk * p.c;
+                        }
                     } else {
-                        brow = lrow0 - chunk * p.c;
+                        chunk = x.q;
                     }
-                } else {
-                    chunk = x.q;
-                }
-                if (chunk < 0) {
-                    // The 32 rows cross a chunk end: each thread writes its own row to the
-                    // output block that owns it.
-                    const int row = lrow0 + lane;
-                    if (row < p.region_rows[0]) {
-                        const int r = row / p.c;
-                        const int i = row - r * p.c;
-                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.y_ptr[r]) +
-                                                               static_cast<size_t>(i) * p.ldy + col);
+                    if (chunk < 0) {
+                        // The 32 rows cross a chunk end: each thread writes its own row to the
+                        // output block that owns it.
+                        const int row = lrow0 + lane;
+                        if (row < p.region_rows[0]) {
+                            const int r = row / p.c;
+                            const int i = row - r * p.c;
+                            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.y_ptr[r]) +
+                                                                   static_cast<size_t>(i) * p.ldy + col);
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            if (col + 8 * j < p.n_out) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                            for (int j = 0; j < 8; ++j)
+                                if (col + 8 * j < p.n_out) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                        }
+                        continue;
                     }
-                    continue;
-                }
-                const uint32_t buf = ebuf0 + (nstore & 1) * EPI_BUF_BYTES;
-                if (lane == 0) bulk_wait_read<1>();
-                __syncwarp();
-                const uint32_t rowaddr = buf + lane * 128u;
+                    const uint32_t buf = ebuf0 + (nstore & 1) * EPI_BUF_BYTES;
+                    if (lane == 0) bulk_wait_read<1>();
+                    __syncwarp();
+                    const uint32_t rowaddr = buf + lane * 128u;
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    st_shared_v4(rowaddr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4), pk[4 * j],
-                                 pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-                fence_proxy_async_shared();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_2d(&p.tmY[chunk], buf, col, brow);
-                    bulk_commit();
+                    for (int j = 0; j < 8; ++j)
+                        st_shared_v4(rowaddr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4), pk[4 * j],
+                                     pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                    fence_proxy_async_shared();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&p.tmY[chunk], buf, col, brow);
+                        bulk_commit();
+                    }
+                    ++nstore;
                 }
-                ++nstore;
             }
         }
         if (lane == 0) bulk_wait_all();
@@ -908,7 +961,11 @@ cudaError_t launch_gemm_pair(const GemmParams &p, int mode, int clusters, cudaSt
 cudaError_t launch_gemm(const GemmParams &p, int mode, int grid, cudaStream_t stream)
 {
     cudaError_t e;
-    if (mode == MODE_AG) {
+    if (mode == MODE_AG_GLU) {
+        e = raise_smem_limit(reinterpret_cast<const void *>(ub_gemm_kernel<MODE_AG_GLU>), SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        ub_gemm_kernel<MODE_AG_GLU><<<grid, THREADS, SMEM_BYTES, stream>>>(p);
+    } else if (mode == MODE_AG) {
         e = raise_smem_limit(reinterpret_cast<const void *>(ub_gemm_kernel<MODE_AG>), SMEM_BYTES);
         if (e != cudaSuccess) return e;
         ub_gemm_kernel<MODE_AG><<<grid, THREADS, SMEM_BYTES, stream>>>(p);

@@ -58,7 +58,7 @@ constexpr int SK_MAX_SPLIT = 6;          // nor is a tile cut into more pieces
 constexpr int SK_SMEM_LIMIT = 232448;    // dynamic shared memory a CTA may opt into
 constexpr int SK_W_BYTES = SK_BM * BK * 2;
 
-enum Mode : int { MODE_AG = 0, MODE_RS = 1, MODE_AG_GLU = 2 /* AG-GEMM + SwiGLU epilogue, pair kernel only */ };
+enum Mode : int { MODE_AG = 0, MODE_RS = 1, MODE_AG_GLU = 2 /* AG-GEMM + SwiGLU epilogue */ };
 
 // Kernel parameters, passed by value as a __grid_constant__ (tensor maps must live
 // in parameter, constant or global memory).
@@ -116,7 +116,9 @@ struct GemmParams {
     int sk_units;                // n_tiles * sk_split
 };
 
-// Launch the persistent GEMM (mode MODE_AG or MODE_RS) with `grid` CTAs on `stream`.
+// Launch the persistent GEMM (mode MODE_AG, MODE_AG_GLU or MODE_RS) with `grid` CTAs on
+// `stream`. SwiGLU: the tensor map of Wt has 128-row boxes (gate at row 128n, up at
+// glu_f + 128n) and n_tiles counts 128-feature tiles.
 cudaError_t launch_gemm(const GemmParams &p, int mode, int grid, cudaStream_t stream);
 
 // Launch the CTA-pair variant with `clusters` clusters of two CTAs. The tensor maps of

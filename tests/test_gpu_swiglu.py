@@ -43,6 +43,30 @@ def test_swiglu_epilogue_matches_oracle(tp, c, F, H, split):
     assert is_sentinel(Z[T:]), "Z rows >= T touched"
 
 
+@pytest.mark.parametrize("tp,c,F,H", [(4, 1, 128, 256), (4, 129, 328, 256), (2, 200, 200, 512),
+                                      (1, 77, 136, 256), (4, 128, 3584, 1024)])
+def test_swiglu_on_single_ctas_matches_oracle(tp, c, F, H):
+    """The single-CTA kernel's SwiGLU epilogue (128 gate + 128 up rows per 256-column
+    tile, chunk-aligned 128-row tiles), forced on."""
+    T = c * tp
+    g = synth.generator(seed=42)
+    shards = [synth.normal_bf16((c, H), 1.0, g) for _ in range(tp)]
+    Wt = synth.normal_bf16((2 * F, H), 1.0 / math.sqrt(H), g)
+    with ub.UserBuffer([T + 4 * tp, H], tp) as buf:
+        buf.set_option("cta_pair", 0)
+        buf.set_option("skinny", 0)
+        buf.set_active_shape([T, H])
+        Z = sentinel((T + 8, F))
+        buf.ag_gemm_swiglu([s.to(dev()) for s in shards], Wt.to(dev()), Z)
+        torch.cuda.synchronize()
+        assert buf.query_status() == ub.UB_OK
+    rows = np.arange(T) if T * F <= 600000 else np.unique(
+        np.concatenate([[0, c - 1, c, T - 1], np.random.default_rng(2).integers(0, T, 16)]))
+    assert_close(Z[torch.as_tensor(rows, device=dev())], oracle_swiglu_rows(shards, Wt, rows),
+                 "single-CTA SwiGLU tp=%d c=%d F=%d" % (tp, c, F))
+    assert is_sentinel(Z[T:]), "Z rows >= T touched"
+
+
 def test_swiglu_full_size_repeated_calls():
     """SwiGLU fc1 of the MLP workload (hidden 4096, F = 3584 per rank), three calls in a
     row on one handle with fresh inputs each time: later calls overlap their chunk copies
