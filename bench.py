@@ -77,9 +77,9 @@ def parse():
     ap.add_argument("--case-T", type=int, default=8192)
     ap.add_argument("--case-reps", type=int, default=3)
     ap.add_argument("--sm-margin", type=int, default=0)
-    ap.add_argument("--gather-kernel", type=int, default=-1, choices=[-1, 0, 1],
-                    help="-1: the library's choice by T (default); 1: the all-gather is one kernel "
-                         "launch; 0: driver copies")
+    ap.add_argument("--gather-kernel", type=int, default=-1, choices=[-1, 0, 1, 2],
+                    help="-1: the library's choice by T (default); 0: driver copies; 1: the all-gather "
+                         "is one kernel launch; 2: inside the GEMM kernel")
     ap.add_argument("--timeout-ms", type=float, default=None,
                     help="bound of the device-side waits (default: the library's 1 s)")
     ap.add_argument("--cta-pair", type=int, default=-1, choices=[-1, 0, 1],

@@ -140,7 +140,7 @@ struct ub_handle {
     cudaStream_t extra_side[UB_MAX_TP] = {};      // copy streams 1.. (created on demand)
     cudaEvent_t ev_join_extra[UB_MAX_TP] = {};
     int64_t copy_streams = 1;  // raised to min(tp, 4) at creation
-    int64_t gather_kernel = -1; // 1: the gather is one kernel launch; 0: driver copies; -1: by T
+    int64_t gather_kernel = -1; // 0: driver copies; 1: one kernel launch; 2: inside the GEMM; -1: by T
     bool gather_by_kernel = false;  // what the last issue_gather chose (join_gather follows it)
     cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
     uint32_t epoch = 0;
@@ -231,6 +231,10 @@ GemmParams *cache_insert(ub_handle *h, std::vector<const void *> key, const Gemm
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 constexpr int64_t kGatherKernelMaxT = 512;  // UB_OPT_GATHER_KERNEL = -1: kernel up to this T
+// The gather inside the GEMM is not chosen automatically: on GB300 (tp 4, hidden 4096)
+// it measured even with the driver copies at T = 2048-4096 and 1-6 us slower at
+// T = 1024 and 8192 -- above T = 512 the copies already overlap the self chunk's tiles.
+constexpr bool kFusedGatherAuto = false;
 
 // How many k-pieces the last wave's tiles are cut into: enough to give every pair one
 // piece, at most MAX_TAIL_SPLIT, each at least MIN_KBLOCKS_PER_PIECE k-blocks long.
@@ -369,6 +373,15 @@ int launch(ub_handle *h, const GemmParams &p, int mode, int path, cudaStream_t s
 // followed by a stream memory write of `epoch` into the chunk's readiness flag (skipped
 // for chunk `drop`, a host-side fault injection). The copy streams first wait for the
 // work already queued on `s`.
+// Whether this AG call's gather runs inside the GEMM kernel (its epilogue warps copy the
+// chunks before their first tile; the tile kernels only): UB_OPT_GATHER_KERNEL = 2, or
+// the automatic choice above kGatherKernelMaxT tokens.
+bool gather_in_gemm(ub_handle *h, bool tile_kernel)
+{
+    if (!tile_kernel) return false;
+    return h->gather_kernel == 2 || (h->gather_kernel < 0 && kFusedGatherAuto && h->T > kGatherKernelMaxT);
+}
+
 int issue_gather(ub_handle *h, const void *const *shards, cudaStream_t s, uint32_t epoch, int64_t drop)
 {
     const int tp = h->tp;
@@ -379,7 +392,8 @@ int issue_gather(ub_handle *h, const void *const *shards, cudaStream_t s, uint32
     // operation with its own host cost and launch latency; for few tokens those dominate
     // the call (GB300, tp 4: AG at T <= 512 takes 26-33 us with the kernel, 39-44 us with
     // the copies), while for many tokens the copies are as fast or faster.
-    h->gather_by_kernel = h->gather_kernel == 1 || (h->gather_kernel < 0 && T <= kGatherKernelMaxT);
+    h->gather_by_kernel = h->gather_kernel == 1 || h->gather_kernel == 2 ||
+                          (h->gather_kernel < 0 && T <= kGatherKernelMaxT);
     if (h->copy_streams == 0 && !h->gather_by_kernel) {
         // In-stream: the copies and flag writes go on `s` itself, ahead of the GEMM,
         // which then finds every flag set (no overlap, no cross-stream hops).
@@ -794,11 +808,23 @@ static int ag_gemm_impl(ub_handle_t h, const void *const *shards, const void *Wt
     const int64_t drop = h->drop_flag;
     h->drop_flag = -1;
 
-    if (int rc = issue_gather(h, shards, s, epoch, drop)) return rc;
-    int rc = launch(h, p, mode, skinny ? PATH_SKINNY : pair ? PATH_PAIR : PATH_SINGLE, s, prof_op);
-    // Join the copy streams back into `s` even if the launch failed.
-    if (int jrc = join_gather(h, s)) return jrc;
-    if (rc != UB_OK) return rc;
+    const bool in_gemm = gather_in_gemm(h, !skinny);
+    p.fused_gather = in_gemm ? 1 : 0;
+    if (in_gemm) {
+        for (int r = 0; r < tp; ++r) p.g_src[r] = shards[r];
+        p.g_ub = h->ub;
+        p.g_counters = gather_counters_of(h);
+        p.g_chunk_vecs = c * H / 8;
+        p.g_drop = static_cast<int>(drop);
+        int rc = launch(h, p, mode, pair ? PATH_PAIR : PATH_SINGLE, s, prof_op);
+        if (rc != UB_OK) return rc;
+    } else {
+        if (int rc = issue_gather(h, shards, s, epoch, drop)) return rc;
+        int rc = launch(h, p, mode, skinny ? PATH_SKINNY : pair ? PATH_PAIR : PATH_SINGLE, s, prof_op);
+        // Join the copy streams back into `s` even if the launch failed.
+        if (int jrc = join_gather(h, s)) return jrc;
+        if (rc != UB_OK) return rc;
+    }
     ++h->counters.ag_calls;
     h->counters.last_T = T;
     return UB_OK;
@@ -1118,7 +1144,7 @@ int ub_set_option(ub_handle_t h, int key, int64_t val)
         h->skinny = val;
         return UB_OK;
     case UB_OPT_GATHER_KERNEL:
-        if (val < -1 || val > 1) return fail(UB_ERR_ARG, "gather_kernel must be -1, 0 or 1");
+        if (val < -1 || val > 2) return fail(UB_ERR_ARG, "gather_kernel must be -1, 0, 1 or 2");
         h->gather_kernel = val;
         return UB_OK;
     case UB_OPT_COPY_STREAMS: {

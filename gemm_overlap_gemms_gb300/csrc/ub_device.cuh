@@ -303,6 +303,48 @@ __device__ __forceinline__ void st_release_u32(uint32_t *ptr, uint32_t v)
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
 }
 
+// All-gather done by the GEMM's own epilogue warps (128 threads, named barrier 1) before
+// their first tile, while the producer already loads the self chunk's tiles: every CTA
+// copies its 1/gridDim.x share of each chunk in ring order after the self rank (the
+// self chunk last), with 16-byte loads that bypass L1, four in flight per thread; the
+// CTA that completes a chunk's count resets the counter and publishes the chunk's
+// readiness flag with the call's epoch (no flag for chunk p.g_drop).
+__device__ void fused_gather(const GemmParams &p, int et)
+{
+    const int G = static_cast<int>(gridDim.x);
+    const int64_t per = (p.g_chunk_vecs + G - 1) / G;
+    const int64_t v0 = static_cast<int64_t>(blockIdx.x) * per;
+    const int64_t v1 = v0 + per < p.g_chunk_vecs ? v0 + per : p.g_chunk_vecs;
+    for (int q = 1; q <= p.tp; ++q) {
+        int r = p.self_rank + q;
+        if (r >= p.tp) r -= p.tp;
+        const uint4 *src = static_cast<const uint4 *>(p.g_src[r]);
+        uint4 *dst = static_cast<uint4 *>(p.g_ub) + static_cast<int64_t>(r) * p.g_chunk_vecs;
+        for (int64_t v = v0 + et; v < v1; v += 4 * 128) {
+            uint4 x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (v + u * 128 < v1)
+                    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(x[u].x), "=r"(x[u].y), "=r"(x[u].z), "=r"(x[u].w)
+                                 : "l"(src + v + u * 128));
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (v + u * 128 < v1) dst[v + u * 128] = x[u];
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // this CTA's share of chunk r is written
+        if (et == 0) {
+            __threadfence();
+            const uint32_t done = atomicAdd(p.g_counters + r, 1u) + 1u;
+            if (done == static_cast<uint32_t>(G)) {
+                p.g_counters[r] = 0u;  // zero again for the next call
+                __threadfence();
+                if (r != p.g_drop) st_release_u32(const_cast<uint32_t *>(p.flags) + r, p.epoch);
+            }
+        }
+    }
+}
+
 // Wait until a partial tile of this call is published (bounded, abort-aware).
 __device__ bool wait_partial(const uint32_t *flag, const WaitCtx &w)
 {

@@ -307,6 +307,7 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_kernel(const __grid_consta
         mbar_wait_drain(drain_bar, 0, p.timeout_ns);
     } else if (warp >= 2) {
         // ---------------------------------------------------------- epilogue
+        if (IS_AG && p.fused_gather) fused_gather(p, static_cast<int>(threadIdx.x) - 64);
         const int quarter = warp & 3;  // TMEM lanes this warp may read: 32*quarter ...
         uint8_t *ebuf = smE + (warp - 2) * 2 * EPI_BUF_BYTES;
         const uint32_t ebuf0 = smem_u32(ebuf);
@@ -653,6 +654,7 @@ __global__ void __maxnreg__(PAIR_MAX_REGS) ub_gemm_pair_kernel(const __grid_cons
         mbar_wait_drain(drain_bar, 0, p.timeout_ns);
     } else if (warp >= 2) {
         // ---------------------------------------------------------- epilogue (both CTAs)
+        if (IS_AG && p.fused_gather) fused_gather(p, static_cast<int>(threadIdx.x) - 64);
         const int quarter = warp & 3;
         uint8_t *ebuf = smE + (warp - 2) * 2 * EPI_BUF_BYTES;
         const uint32_t ebuf0 = smem_u32(ebuf);

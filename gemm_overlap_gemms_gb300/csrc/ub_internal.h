@@ -105,6 +105,15 @@ struct GemmParams {
     float *ws;                   // partial tiles of split tail tiles: [num_pairs][2][256/4][128][4] fp32
     uint32_t *ws_flags;          // [num_pairs][2][EPI_WARPS]: epoch of the partial written
 
+    // ---- fused gather (tile kernels, AG modes): the epilogue warps copy the chunks into
+    // the user buffer before their first tile and publish each chunk's readiness flag
+    int fused_gather;            // 1: on; the host then issues no copies for the call
+    int g_drop;                  // chunk whose flag is not published (-1: none)
+    const void *g_src[UB_MAX_TP];  // shard r ([c, hidden])
+    void *g_ub;                  // user buffer base
+    uint32_t *g_counters;        // CTAs done per chunk (zero between calls)
+    int64_t g_chunk_vecs;        // 16-byte vectors per chunk = c * hidden / 8
+
     // ---- skinny kernel only (few tokens): weight rows on the MMA's M dimension, tokens
     // on its N dimension. Tiles are SK_BM weight rows (SwiGLU: SK_BM gate + SK_BM up rows)
     // by all T tokens; work units are (tile, k-piece), unit u = piece * n_tiles + tile.

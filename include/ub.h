@@ -89,8 +89,10 @@ enum {
     UB_OPT_GATHER_KERNEL = 9, /* 0: the gather is one cudaMemcpyAsync plus one stream flag write
                               per chunk; 1: one kernel launch on the side stream lands every
                               chunk in ring order and publishes each chunk's flag as its last
-                              CTA finishes (fewer driver operations per call); -1 (default):
-                              the kernel for T <= 512, the copies above */
+                              CTA finishes (fewer driver operations per call); 2: the GEMM's
+                              own epilogue warps copy the chunks before their first tile and
+                              publish the flags (tile kernels; the few-token kernel uses 1);
+                              -1 (default): 1 for T <= 512, 0 above */
     UB_OPT_SKINNY = 10     /* few-token kernel: weight rows on the MMA's M, tokens on its N, so
                               the work follows T and the weight is read once. Usable while the
                               token columns (ag_gemm*: tp * roundup(T/tp, 16); gemm_rs*:

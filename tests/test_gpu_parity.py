@@ -51,7 +51,7 @@ def test_tiny_workload_ag_and_rs():
 SWEEP_C = [1, 2, 127, 128, 129, 255, 300]
 
 
-@pytest.mark.parametrize("gather", [0, 1])
+@pytest.mark.parametrize("gather", [0, 1, 2])
 @pytest.mark.parametrize("pair", [1, 0])
 @pytest.mark.parametrize("tp", [1, 2, 4])
 def test_ag_active_T_sweep(tp, pair, gather):
@@ -230,7 +230,7 @@ def test_rejects_misaligned_and_wrong_shapes():
 
 # ------------------------------------------------------------------ bounded waits
 
-@pytest.mark.parametrize("gather", [0, 1])
+@pytest.mark.parametrize("gather", [0, 1, 2])
 @pytest.mark.parametrize("pair", [1, 0])
 def test_dropped_flag_times_out_and_the_handle_recovers(pair, gather):
     """Fault injected on the host: the readiness flag of chunk 1 is never written. The
@@ -256,7 +256,7 @@ def test_dropped_flag_times_out_and_the_handle_recovers(pair, gather):
     assert_close(Y, Yref, "AG after recovery")
 
 
-@pytest.mark.parametrize("gather", [0, 1])
+@pytest.mark.parametrize("gather", [0, 1, 2])
 @pytest.mark.parametrize("op", ["ag", "rs", "ag_swiglu"])
 def test_back_to_back_calls_at_full_hidden(op, gather):
     """Ten calls in a row on one handle at hidden 4096 without synchronising in
