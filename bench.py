@@ -85,6 +85,8 @@ def parse():
     ap.add_argument("--cta-pair", type=int, default=-1, choices=[-1, 0, 1],
                     help="-1: chosen per call (default); 1: 256x256 tiles on CTA pairs; 0: single CTAs")
     ap.add_argument("--copy-streams", type=int, default=4)
+    ap.add_argument("--pdl", type=int, default=1, choices=[0, 1],
+                    help="1: kernels launched with programmatic dependent launch (default); 0: plain")
     ap.add_argument("--skinny", type=int, default=-1, choices=[-1, 0, 1],
                     help="few-token kernel: -1 whenever usable (default), 0 never, 1 whenever usable")
     ap.add_argument("--streamk", type=int, default=-1, choices=[-1, 0, 1],
@@ -247,6 +249,7 @@ class SwigluWorkload:
         self.buf = ub.UserBuffer([cap, H], tp)
         self.buf.set_option("cta_pair", CTA_PAIR)
         self.buf.set_option("streamk", STREAMK)
+        self.buf.set_option("pdl", PDL)
 
     def shards(self, i):
         T, tp = self.Ts[i], self.w.tp
@@ -735,6 +738,7 @@ def run_case(args):
     buf.set_option("sm_margin", args.sm_margin)
     buf.set_option("gather_kernel", args.gather_kernel)
     buf.set_option("skinny", args.skinny)
+    buf.set_option("pdl", args.pdl)
     buf.set_active_shape([T, H])
     c = T // tp
     nbytes = None
@@ -847,14 +851,16 @@ def run_case(args):
 
 CTA_PAIR = -1
 STREAMK = -1
+PDL = 1
 MLP = "fused"
 
 
 def main():
-    global CTA_PAIR, STREAMK, MLP
+    global CTA_PAIR, STREAMK, PDL, MLP
     args = parse()
     CTA_PAIR = args.cta_pair
     STREAMK = args.streamk
+    PDL = args.pdl
     MLP = args.mlp
     if args.case:
         run_case(args)

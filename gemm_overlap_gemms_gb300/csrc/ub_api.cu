@@ -153,6 +153,7 @@ struct ub_handle {
     int64_t cta_pair = -1;  // -1 = chosen per call
     int64_t streamk = -1;   // -1 = chosen per call
     int64_t skinny = -1;    // -1 = whenever the few-token kernel is usable
+    int64_t pdl = 1;        // programmatic dependent launch of every kernel
     int pair_clusters[3] = {-1, -1, -1};  // resident clusters of the pair kernel, per mode
     ub_counters_t counters{};
     std::vector<CacheEntry> cache;
@@ -339,8 +340,9 @@ void choose_path(ub_handle *h, int mode, int64_t single_tiles, int64_t pair_tile
 
 enum Path : int { PATH_SINGLE = 0, PATH_PAIR = 1, PATH_SKINNY = 2 };
 
-int launch(ub_handle *h, const GemmParams &p, int mode, int path, cudaStream_t s, int prof_op)
+int launch(ub_handle *h, GemmParams &p, int mode, int path, cudaStream_t s, int prof_op)
 {
+    p.pdl = static_cast<int>(h->pdl);
     const int grid = path == PATH_PAIR ? p.num_pairs : grid_for(h, path == PATH_SKINNY ? p.sk_units : p.num_tiles);
     if (path == PATH_SKINNY && p.sk_split > 1 && grid < p.sk_units)
         return fail(UB_ERR_ARG, "skinny launch: %d split units on %d CTAs", p.sk_units, grid);
@@ -428,6 +430,7 @@ int issue_gather(ub_handle *h, const void *const *shards, cudaStream_t s, uint32
         const int64_t need = (g.chunk_vecs + 511) / 512;  // at least two vectors per thread
         if (per > need) per = need;
         g.ctas_per_chunk = static_cast<int>(per < 1 ? 1 : per);
+        g.pdl = static_cast<int>(h->pdl);
         UB_CUDA(cudaEventRecord(h->ev_fork, s));
         UB_CUDA(cudaStreamWaitEvent(h->side, h->ev_fork, 0));
         cudaError_t e = ubk::launch_gather(g, h->side);
@@ -1020,6 +1023,7 @@ int ub_reduce_scatter(ub_handle_t h, const void *const *P, void *const *Y_shards
     p.T = h->T;
     p.H = h->hidden;
     p.c = h->T / tp;
+    p.pdl = static_cast<int>(h->pdl);
     // Small CTAs, four per SM: two fit beside a persistent GEMM CTA on the same SM (the
     // rest start as GEMM CTAs leave); alone, all four keep enough loads in flight.
     const int64_t vecs = p.T * (p.H / 8);
@@ -1143,6 +1147,10 @@ int ub_set_option(ub_handle_t h, int key, int64_t val)
         if (val < -1 || val > 1) return fail(UB_ERR_ARG, "UB_OPT_SKINNY must be -1, 0 or 1");
         h->skinny = val;
         return UB_OK;
+    case UB_OPT_PDL:
+        if (val != 0 && val != 1) return fail(UB_ERR_ARG, "UB_OPT_PDL must be 0 or 1");
+        h->pdl = val;
+        return UB_OK;
     case UB_OPT_GATHER_KERNEL:
         if (val < -1 || val > 2) return fail(UB_ERR_ARG, "gather_kernel must be -1, 0, 1 or 2");
         h->gather_kernel = val;
@@ -1177,6 +1185,7 @@ int ub_get_option(ub_handle_t h, int key, int64_t *val)
     case UB_OPT_COPY_STREAMS: *val = h->copy_streams; return UB_OK;
     case UB_OPT_GATHER_KERNEL: *val = h->gather_kernel; return UB_OK;
     case UB_OPT_SKINNY: *val = h->skinny; return UB_OK;
+    case UB_OPT_PDL: *val = h->pdl; return UB_OK;
     default: return fail(UB_ERR_ARG, "unknown option %d", key);
     }
 }

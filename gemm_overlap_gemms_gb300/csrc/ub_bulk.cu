@@ -16,6 +16,14 @@
 namespace ubk {
 namespace {
 
+// Programmatic dependent launch (see ub_device.cuh): let the next kernel launch, then
+// wait for the previous one before touching memory.
+__device__ __forceinline__ void pdl_enter()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ uint4 ld_stream(const void *p)
 {
     uint4 v;
@@ -44,6 +52,7 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi)
 template <int TP, int U>
 __global__ void __launch_bounds__(256) bulk_rs_kernel(const __grid_constant__ BulkRsParams p)
 {
+    pdl_enter();
     const int64_t vecs_per_row = p.H / 8;
     const int64_t total = p.T * vecs_per_row;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -87,6 +96,7 @@ __global__ void __launch_bounds__(256) bulk_rs_kernel(const __grid_constant__ Bu
 // q-th chunk after the self rank (b / ctas_per_chunk), the self chunk last.
 __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ GatherParams p)
 {
+    pdl_enter();
     const int q = blockIdx.x / p.ctas_per_chunk + 1;  // 1..tp
     const int part = blockIdx.x - (q - 1) * p.ctas_per_chunk;
     const int r = (p.self_rank + q) % p.tp;
@@ -120,23 +130,24 @@ __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ Gat
 
 cudaError_t launch_gather(const GatherParams &p, cudaStream_t stream)
 {
-    gather_kernel<<<p.tp * p.ctas_per_chunk, 256, 0, stream>>>(p);
-    return cudaGetLastError();
+    cudaError_t e = launch_ex(gather_kernel, p, p.tp * p.ctas_per_chunk, 256, 0, 0, p.pdl != 0, stream);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_bulk_rs(const BulkRsParams &p, int grid, cudaStream_t stream)
 {
+    cudaError_t e;
     switch (p.tp) {
-    case 1: bulk_rs_kernel<1, 4><<<grid, 256, 0, stream>>>(p); break;
-    case 2: bulk_rs_kernel<2, 4><<<grid, 256, 0, stream>>>(p); break;
-    case 3: bulk_rs_kernel<3, 2><<<grid, 256, 0, stream>>>(p); break;
-    case 4: bulk_rs_kernel<4, 2><<<grid, 256, 0, stream>>>(p); break;
-    case 5: bulk_rs_kernel<5, 2><<<grid, 256, 0, stream>>>(p); break;
-    case 6: bulk_rs_kernel<6, 2><<<grid, 256, 0, stream>>>(p); break;
-    case 7: bulk_rs_kernel<7, 1><<<grid, 256, 0, stream>>>(p); break;
-    default: bulk_rs_kernel<8, 1><<<grid, 256, 0, stream>>>(p); break;
+    case 1: e = launch_ex(bulk_rs_kernel<1, 4>, p, grid, 256, 0, 0, p.pdl != 0, stream); break;
+    case 2: e = launch_ex(bulk_rs_kernel<2, 4>, p, grid, 256, 0, 0, p.pdl != 0, stream); break;
+    case 3: e = launch_ex(bulk_rs_kernel<3, 2>, p, grid, 256, 0, 0, p.pdl != 0, stream); break;
+    case 4: e = launch_ex(bulk_rs_kernel<4, 2>, p, grid, 256, 0, 0, p.pdl != 0, stream); break;
+    case 5: e = launch_ex(bulk_rs_kernel<5, 2>, p, grid, 256, 0, 0, p.pdl != 0, stream); break;
+    case 6: e = launch_ex(bulk_rs_kernel<6, 2>, p, grid, 256, 0, 0, p.pdl != 0, stream); break;
+    case 7: e = launch_ex(bulk_rs_kernel<7, 1>, p, grid, 256, 0, 0, p.pdl != 0, stream); break;
+    default: e = launch_ex(bulk_rs_kernel<8, 1>, p, grid, 256, 0, 0, p.pdl != 0, stream); break;
     }
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace ubk

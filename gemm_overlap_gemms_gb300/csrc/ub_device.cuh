@@ -91,6 +91,15 @@ __device__ __forceinline__ void fence_proxy_async_shared()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Programmatic dependent launch. `pdl_trigger` lets the next kernel on the stream start
+// launching once every CTA of this grid has reached it (all of them resident, so the
+// next grid's CTAs can only take SMs that are free); `pdl_wait` blocks until the grid
+// before this one has completed and its memory is visible. Without the launch
+// attribute both are no-ops. Every kernel here runs its prologue (barriers, TMEM,
+// tensor-map prefetch), then triggers, then waits before touching global memory.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

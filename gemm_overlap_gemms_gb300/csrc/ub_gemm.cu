@@ -214,6 +214,8 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_kernel(const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    pdl_trigger();
+    pdl_wait();
 
     if (warp == 0 && lane == 0) {
         // ---------------------------------------------------------- producer
@@ -531,6 +533,8 @@ __global__ void __maxnreg__(PAIR_MAX_REGS) ub_gemm_pair_kernel(const __grid_cons
     cluster_sync_all();  // barriers of both CTAs initialised before any cross-CTA signal
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    pdl_trigger();
+    pdl_wait();
 
     if (warp == 0 && lane == 0) {
         // ---------------------------------------------------------- producer (both CTAs)
@@ -932,23 +936,11 @@ int max_pair_clusters(int mode)
 
 cudaError_t launch_gemm_pair(const GemmParams &p, int mode, int clusters, cudaStream_t stream)
 {
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(2 * clusters, 1, 1);
-    cfg.blockDim = dim3(THREADS, 1, 1);
-    cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
     // MN-major operands only in the backward GEMMs' instantiations (never with SwiGLU)
     const bool mn = p.a_mn || p.b_mn;
-    auto go = [&](auto kernel) {
+    auto go = [&](void (*kernel)(GemmParams)) {
         cudaError_t e = raise_smem_limit(reinterpret_cast<const void *>(kernel), PAIR_SMEM_BYTES);
-        return e == cudaSuccess ? cudaLaunchKernelEx(&cfg, kernel, p) : e;
+        return e == cudaSuccess ? launch_ex(kernel, p, 2 * clusters, THREADS, PAIR_SMEM_BYTES, 2, p.pdl != 0, stream) : e;
     };
     cudaError_t e;
     if (mode == MODE_AG)
@@ -966,15 +958,18 @@ cudaError_t launch_gemm(const GemmParams &p, int mode, int grid, cudaStream_t st
     if (mode == MODE_AG_GLU) {
         e = raise_smem_limit(reinterpret_cast<const void *>(ub_gemm_kernel<MODE_AG_GLU>), SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        ub_gemm_kernel<MODE_AG_GLU><<<grid, THREADS, SMEM_BYTES, stream>>>(p);
+        e = launch_ex(ub_gemm_kernel<MODE_AG_GLU>, p, grid, THREADS, SMEM_BYTES, 0, p.pdl != 0, stream);
+        if (e != cudaSuccess) return e;
     } else if (mode == MODE_AG) {
         e = raise_smem_limit(reinterpret_cast<const void *>(ub_gemm_kernel<MODE_AG>), SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        ub_gemm_kernel<MODE_AG><<<grid, THREADS, SMEM_BYTES, stream>>>(p);
+        e = launch_ex(ub_gemm_kernel<MODE_AG>, p, grid, THREADS, SMEM_BYTES, 0, p.pdl != 0, stream);
+        if (e != cudaSuccess) return e;
     } else {
         e = raise_smem_limit(reinterpret_cast<const void *>(ub_gemm_kernel<MODE_RS>), SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        ub_gemm_kernel<MODE_RS><<<grid, THREADS, SMEM_BYTES, stream>>>(p);
+        e = launch_ex(ub_gemm_kernel<MODE_RS>, p, grid, THREADS, SMEM_BYTES, 0, p.pdl != 0, stream);
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }

@@ -123,6 +123,7 @@ struct GemmParams {
     int sk_split;                // k-pieces per tile; the last piece finishes the tile
     int sk_stages;               // shared-memory pipeline depth (<= SK_MAX_STAGES)
     int sk_units;                // n_tiles * sk_split
+    int pdl;                     // host: launch with programmatic stream serialization
 };
 
 // Launch the persistent GEMM (mode MODE_AG, MODE_AG_GLU or MODE_RS) with `grid` CTAs on
@@ -153,6 +154,7 @@ struct BulkRsParams {
     int64_t T;
     int64_t H;                 // multiple of 8
     int64_t c;
+    int pdl;                   // host: launch with programmatic stream serialization
 };
 cudaError_t launch_bulk_rs(const BulkRsParams &p, int grid, cudaStream_t stream);
 
@@ -170,11 +172,42 @@ struct GatherParams {
     int drop;                    // chunk whose flag is not published (-1: none)
     int ctas_per_chunk;
     int64_t chunk_vecs;          // 16-byte vectors per chunk = c * H / 8
+    int pdl;                     // host: launch with programmatic stream serialization
 };
 cudaError_t launch_gather(const GatherParams &p, cudaStream_t stream);
 
 // Record the message ub_last_error() returns on this host thread.
 void set_last_error(const char *msg);
+
+// Launch `kernel(params)` with `grid` x `threads`, `smem` dynamic shared memory, an
+// optional cluster of `cluster_x` CTAs, and programmatic stream serialization if `pdl`.
+template <typename P>
+inline cudaError_t launch_ex(void (*kernel)(P), const P &params, int grid, int threads, int smem, int cluster_x,
+                             bool pdl, cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (cluster_x > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = cluster_x;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kernel, params);
+}
 
 // Raise a kernel's dynamic shared memory limit to `bytes`, once per kernel and device
 // (the runtime call costs microseconds of host time, paid once instead of per launch).

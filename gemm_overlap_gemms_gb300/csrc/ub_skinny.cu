@@ -146,6 +146,8 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_skinny_kernel(const __grid
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    pdl_trigger();
+    pdl_wait();
 
     if (warp == 0 && lane == 0) {
         // ---------------------------------------------------------- producer
@@ -507,15 +509,18 @@ cudaError_t launch_gemm_skinny(const GemmParams &p, int mode, int grid, cudaStre
     if (mode == MODE_AG) {
         e = raise_smem_limit(reinterpret_cast<const void *>(ub_gemm_skinny_kernel<MODE_AG>), SK_SMEM_LIMIT);
         if (e != cudaSuccess) return e;
-        ub_gemm_skinny_kernel<MODE_AG><<<grid, THREADS, smem, stream>>>(p);
+        e = launch_ex(ub_gemm_skinny_kernel<MODE_AG>, p, grid, THREADS, smem, 0, p.pdl != 0, stream);
+        if (e != cudaSuccess) return e;
     } else if (mode == MODE_AG_GLU) {
         e = raise_smem_limit(reinterpret_cast<const void *>(ub_gemm_skinny_kernel<MODE_AG_GLU>), SK_SMEM_LIMIT);
         if (e != cudaSuccess) return e;
-        ub_gemm_skinny_kernel<MODE_AG_GLU><<<grid, THREADS, smem, stream>>>(p);
+        e = launch_ex(ub_gemm_skinny_kernel<MODE_AG_GLU>, p, grid, THREADS, smem, 0, p.pdl != 0, stream);
+        if (e != cudaSuccess) return e;
     } else {
         e = raise_smem_limit(reinterpret_cast<const void *>(ub_gemm_skinny_kernel<MODE_RS>), SK_SMEM_LIMIT);
         if (e != cudaSuccess) return e;
-        ub_gemm_skinny_kernel<MODE_RS><<<grid, THREADS, smem, stream>>>(p);
+        e = launch_ex(ub_gemm_skinny_kernel<MODE_RS>, p, grid, THREADS, smem, 0, p.pdl != 0, stream);
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }

@@ -93,12 +93,15 @@ enum {
                               own epilogue warps copy the chunks before their first tile and
                               publish the flags (tile kernels; the few-token kernel uses 1);
                               -1 (default): 1 for T <= 512, 0 above */
-    UB_OPT_SKINNY = 10     /* few-token kernel: weight rows on the MMA's M, tokens on its N, so
+    UB_OPT_SKINNY = 10,    /* few-token kernel: weight rows on the MMA's M, tokens on its N, so
                               the work follows T and the weight is read once. Usable while the
                               token columns (ag_gemm*: tp * roundup(T/tp, 16); gemm_rs*:
                               roundup(T, 16)) are <= 256. -1 (default) = used up to 128 columns
                               unless UB_OPT_CTA_PAIR forces a tile kernel; 0 = never; 1 =
                               whenever usable */
+    UB_OPT_PDL = 11        /* 1 (default): kernels are launched with programmatic stream
+                              serialization, so a kernel's launch and prologue overlap the end
+                              of the kernel before it on the stream; 0: plain launches */
 };
 
 /* Operation ids for ub_kernel_time. */
