@@ -232,10 +232,10 @@ GemmParams *cache_insert(ub_handle *h, std::vector<const void *> key, const Gemm
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 constexpr int64_t kGatherKernelMaxT = 512;  // UB_OPT_GATHER_KERNEL = -1: kernel up to this T
-// The gather inside the GEMM is not chosen automatically: on GB300 (tp 4, hidden 4096)
-// it measured even with the driver copies at T = 2048-4096 and 1-6 us slower at
-// T = 1024 and 8192 -- above T = 512 the copies already overlap the self chunk's tiles.
-constexpr bool kFusedGatherAuto = false;
+// ... and inside the GEMM above it: on GB300 (tp 4, hidden 4096) the whole AG call is
+// 2-8 % faster than with the driver copies at T = 1024-8192 (the chunks land sooner:
+// no copy launches, every SM copying; AG T = 2048: 73.2 vs 78.6 us).
+constexpr bool kFusedGatherAuto = true;
 
 // How many k-pieces the last wave's tiles are cut into: enough to give every pair one
 // piece, at most MAX_TAIL_SPLIT, each at least MIN_KBLOCKS_PER_PIECE k-blocks long.

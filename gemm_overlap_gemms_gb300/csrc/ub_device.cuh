@@ -315,7 +315,8 @@ __device__ __forceinline__ void st_release_u32(uint32_t *ptr, uint32_t v)
 // All-gather done by the GEMM's own epilogue warps (128 threads, named barrier 1) before
 // their first tile, while the producer already loads the self chunk's tiles: every CTA
 // copies its 1/gridDim.x share of each chunk in ring order after the self rank (the
-// self chunk last), with 16-byte loads that bypass L1, four in flight per thread; the
+// self chunk last), with 16-byte loads that bypass L1, sixteen in flight per thread
+// (about 5 MB in flight over the GPU: enough to keep HBM busy); the
 // CTA that completes a chunk's count resets the counter and publishes the chunk's
 // readiness flag with the call's epoch (no flag for chunk p.g_drop).
 __device__ void fused_gather(const GemmParams &p, int et)
@@ -329,16 +330,17 @@ __device__ void fused_gather(const GemmParams &p, int et)
         if (r >= p.tp) r -= p.tp;
         const uint4 *src = static_cast<const uint4 *>(p.g_src[r]);
         uint4 *dst = static_cast<uint4 *>(p.g_ub) + static_cast<int64_t>(r) * p.g_chunk_vecs;
-        for (int64_t v = v0 + et; v < v1; v += 4 * 128) {
-            uint4 x[4];
+        constexpr int U = 16;
+        for (int64_t v = v0 + et; v < v1; v += U * 128) {
+            uint4 x[U];
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+            for (int u = 0; u < U; ++u)
                 if (v + u * 128 < v1)
                     asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
                                  : "=r"(x[u].x), "=r"(x[u].y), "=r"(x[u].z), "=r"(x[u].w)
                                  : "l"(src + v + u * 128));
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+            for (int u = 0; u < U; ++u)
                 if (v + u * 128 < v1) dst[v + u * 128] = x[u];
         }
         asm volatile("bar.sync 1, 128;" ::: "memory");  // this CTA's share of chunk r is written

@@ -92,7 +92,8 @@ enum {
                               CTA finishes (fewer driver operations per call); 2: the GEMM's
                               own epilogue warps copy the chunks before their first tile and
                               publish the flags (tile kernels; the few-token kernel uses 1);
-                              -1 (default): 1 for T <= 512, 0 above */
+                              -1 (default): 1 for T <= 512, 2 above (the few-token kernel
+                              and ub_allgather use 1 or 0 instead of 2) */
     UB_OPT_SKINNY = 10,    /* few-token kernel: weight rows on the MMA's M, tokens on its N, so
                               the work follows T and the weight is read once. Usable while the
                               token columns (ag_gemm*: tp * roundup(T/tp, 16); gemm_rs*:
