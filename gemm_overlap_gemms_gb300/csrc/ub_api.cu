@@ -236,6 +236,10 @@ constexpr int64_t kGatherKernelMaxT = 512;  // UB_OPT_GATHER_KERNEL = -1: kernel
 // 2-8 % faster than with the driver copies at T = 1024-8192 (the chunks land sooner:
 // no copy launches, every SM copying; AG T = 2048: 73.2 vs 78.6 us).
 constexpr bool kFusedGatherAuto = true;
+// Not for the few-token kernel: there the chunks are tiny, the weight stream hides the
+// one-launch gather, and the gather inside the kernel measured 1-3 us slower per call
+// (AG and AG + SwiGLU, T = 4-128, GB300).
+constexpr bool kFusedGatherSkinnyAuto = false;
 
 // How many k-pieces the last wave's tiles are cut into: enough to give every pair one
 // piece, at most MAX_TAIL_SPLIT, each at least MIN_KBLOCKS_PER_PIECE k-blocks long.
@@ -376,12 +380,12 @@ int launch(ub_handle *h, GemmParams &p, int mode, int path, cudaStream_t s, int 
 // for chunk `drop`, a host-side fault injection). The copy streams first wait for the
 // work already queued on `s`.
 // Whether this AG call's gather runs inside the GEMM kernel (its epilogue warps copy the
-// chunks before their first tile; the tile kernels only): UB_OPT_GATHER_KERNEL = 2, or
-// the automatic choice above kGatherKernelMaxT tokens.
-bool gather_in_gemm(ub_handle *h, bool tile_kernel)
+// chunks before their first tile): UB_OPT_GATHER_KERNEL = 2, or the automatic choice.
+bool gather_in_gemm(ub_handle *h, bool skinny)
 {
-    if (!tile_kernel) return false;
-    return h->gather_kernel == 2 || (h->gather_kernel < 0 && kFusedGatherAuto && h->T > kGatherKernelMaxT);
+    if (h->gather_kernel == 2) return true;
+    if (h->gather_kernel >= 0) return false;
+    return skinny ? kFusedGatherSkinnyAuto : (kFusedGatherAuto && h->T > kGatherKernelMaxT);
 }
 
 int issue_gather(ub_handle *h, const void *const *shards, cudaStream_t s, uint32_t epoch, int64_t drop)
@@ -811,7 +815,7 @@ static int ag_gemm_impl(ub_handle_t h, const void *const *shards, const void *Wt
     const int64_t drop = h->drop_flag;
     h->drop_flag = -1;
 
-    const bool in_gemm = gather_in_gemm(h, !skinny);
+    const bool in_gemm = gather_in_gemm(h, skinny);
     p.fused_gather = in_gemm ? 1 : 0;
     if (in_gemm) {
         for (int r = 0; r < tp; ++r) p.g_src[r] = shards[r];
@@ -819,7 +823,7 @@ static int ag_gemm_impl(ub_handle_t h, const void *const *shards, const void *Wt
         p.g_counters = gather_counters_of(h);
         p.g_chunk_vecs = c * H / 8;
         p.g_drop = static_cast<int>(drop);
-        int rc = launch(h, p, mode, pair ? PATH_PAIR : PATH_SINGLE, s, prof_op);
+        int rc = launch(h, p, mode, skinny ? PATH_SKINNY : pair ? PATH_PAIR : PATH_SINGLE, s, prof_op);
         if (rc != UB_OK) return rc;
     } else {
         if (int rc = issue_gather(h, shards, s, epoch, drop)) return rc;

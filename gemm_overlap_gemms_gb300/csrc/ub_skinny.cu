@@ -297,6 +297,7 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_skinny_kernel(const __grid
         mbar_wait_drain(drain_bar, 0, p.timeout_ns);
     } else if (warp >= 2) {
         // ---------------------------------------------------------- epilogue
+        if (IS_AG && p.fused_gather) fused_gather(p, static_cast<int>(threadIdx.x) - 64);
         const int quarter = warp & 3;         // TMEM lanes this warp may read: 32*quarter ...
         const int row = quarter * 32 + lane;  // this thread's lane = weight row inside the tile
         const int T = p.tp * p.c;

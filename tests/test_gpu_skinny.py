@@ -28,15 +28,18 @@ def _make_buf(T, H, tp, skinny=1, extra=8):
 
 # (tp, c, H, N): chunks of 1..64 rows (token sub-tiles of 16..64 columns), one or many
 # weight tiles, N not a multiple of 128, K of 2..64 k-blocks (split into pieces or not).
+@pytest.mark.parametrize("gather", [-1, 2])
 @pytest.mark.parametrize("tp,c,H,N", [(4, 1, 256, 384), (4, 16, 256, 136), (4, 63, 512, 264),
                                       (2, 100, 256, 392), (1, 200, 320, 128), (8, 32, 1024, 1000),
                                       (4, 64, 4096, 3072), (1, 1, 72, 8)])
-def test_skinny_ag_matches_oracle(tp, c, H, N):
+def test_skinny_ag_matches_oracle(tp, c, H, N, gather):
+    """gather -1: the one-launch gather kernel; 2: the kernel's epilogue warps gather."""
     T = c * tp
     g = synth.generator(seed=101)
     shards = [synth.normal_bf16((c, H), 1.0, g) for _ in range(tp)]
     Wt = synth.normal_bf16((N, H), 1.0 / math.sqrt(H), g)
     with _make_buf(T, H, tp) as buf:
+        buf.set_option("gather_kernel", gather)
         Y = run_ag(buf, shards, Wt, y_rows=T + 5)
         assert buf.query_status() == ub.UB_OK
         G = buf.buffer()[:T].cpu()
@@ -166,7 +169,8 @@ def test_skinny_is_deterministic_and_agrees_with_the_tile_kernels():
         assert_close(Yrs[ridx], ref_rs, "RS " + name)
 
 
-def test_skinny_dropped_flag_times_out_and_the_handle_recovers():
+@pytest.mark.parametrize("gather", [-1, 2])
+def test_skinny_dropped_flag_times_out_and_the_handle_recovers(gather):
     """A chunk flag that is never written: the weight stream has started, the flag wait
     runs out, the call reports UB_ERR_TIMEOUT; the next call on the handle is clean."""
     tp, c, H, N = 4, 8, 1024, 2048
@@ -175,6 +179,7 @@ def test_skinny_dropped_flag_times_out_and_the_handle_recovers():
     shards = [synth.normal_bf16((c, H), 1.0, g) for _ in range(tp)]
     Wt = synth.normal_bf16((N, H), 1.0 / math.sqrt(H), g)
     with _make_buf(T, H, tp) as buf:
+        buf.set_option("gather_kernel", gather)
         buf.set_option("timeout_ns", 20_000_000)
         buf.set_option("drop_flag", 2)
         Y = run_ag(buf, shards, Wt)
