@@ -164,15 +164,22 @@ int ub_buffer(ub_handle_t h, void **dev_ptr, size_t *bytes);
  *     UB[r*c + i][:] = shards[r][i][:]            for r < tp, i < c
  *     Y[t][n]       = sum_h UB[t][h] * Wt[n][h]   for t < T, n < N.
  * shards: host array of tp device pointers, each [c, hidden]. Wt: device [N, hidden].
- * Y: device [T, N] (leading dimension N). The chunk copies are cudaMemcpyAsync calls on
- * the handle's side streams (the stand-in for copy-engine send/recv; on GB300 the
- * driver runs a same-device copy as a kernel on SMs, next to the GEMM, whose CTAs leave
- * room for it), each followed by a readiness-flag write; one persistent
- * GEMM kernel on `stream` walks the chunks in ring order starting at
- * UB_OPT_SELF_RANK (whose chunk it reads in place, without waiting), waits for each
- * other chunk's flag, and never reads or writes rows >= T. The side stream is joined
- * back into `stream` before return. A device wait that expires is reported by
- * ub_query_status (UB_ERR_TIMEOUT), never by a trap.
+ * Y: device [T, N] (leading dimension N). The chunks are landed in the buffer by one of
+ * three gathers (UB_OPT_GATHER_KERNEL): cudaMemcpyAsync calls on the handle's side
+ * streams (the stand-in for copy-engine send/recv; on GB300 the driver runs a
+ * same-device copy as a kernel on SMs, next to the GEMM, whose CTAs leave room for it),
+ * each followed by a readiness-flag write; one gather kernel on the side stream
+ * (default for T <= 512); or the GEMM kernel's own epilogue warps before their first
+ * tile (default above). One persistent GEMM kernel on `stream` walks the chunks in
+ * ring order starting at UB_OPT_SELF_RANK (whose chunk it reads in place, without
+ * waiting), waits for each other chunk's flag, and never reads or writes rows >= T.
+ * Side streams are joined back into `stream` before return. A device wait that expires
+ * is reported by ub_query_status (UB_ERR_TIMEOUT), never by a trap.
+ * Concurrency: the GEMM kernels size their grids to be resident at once (at most one
+ * CTA or CTA pair per SM) and some of their CTAs wait for others (the gather inside
+ * the GEMM, split k-ranges). Calls of one handle are stream-ordered by the caller;
+ * calls of this library that run at the same time on other streams must leave every
+ * SM the room of one such CTA, or a wait may run out (UB_ERR_TIMEOUT, never a hang).
  * Errors: UB_ERR_ARG, UB_ERR_ZERO (N <= 0), UB_ERR_ALIGN, UB_ERR_CUDA.
  */
 int ag_gemm(ub_handle_t h, const void *const *shards, const void *Wt, int64_t N, void *Y,
