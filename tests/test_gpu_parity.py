@@ -153,20 +153,26 @@ def test_deterministic_and_consistent_across_launch_shapes():
                (0, 0, -1, -1, 1)]
     outs = []
     with ub.UserBuffer([T, H], tp) as buf:
-        for self_rank, margin, pair, streamk, copy_streams in configs:
-            buf.set_option("self_rank", self_rank)
-            buf.set_option("sm_margin", margin)
-            buf.set_option("cta_pair", pair)
-            buf.set_option("streamk", streamk)
-            buf.set_option("copy_streams", copy_streams)
-            Y = run_ag(buf, shards, Wt)
-            R, _ = run_rs(buf, A, Bt)
-            outs.append((Y.view(torch.int16).clone(), [r.view(torch.int16).clone() for r in R]))
+        # the gather by driver copies, then inside the GEMM: it moves bytes only, so the
+        # same launch shape must give the same bits either way
+        for gather in (0, 2):
+            buf.set_option("gather_kernel", gather)
+            for self_rank, margin, pair, streamk, copy_streams in configs:
+                buf.set_option("self_rank", self_rank)
+                buf.set_option("sm_margin", margin)
+                buf.set_option("cta_pair", pair)
+                buf.set_option("streamk", streamk)
+                buf.set_option("copy_streams", copy_streams)
+                Y = run_ag(buf, shards, Wt)
+                R, _ = run_rs(buf, A, Bt)
+                outs.append((Y.view(torch.int16).clone(), [r.view(torch.int16).clone() for r in R]))
         assert buf.query_status() == ub.UB_OK
-    for i, j in [(0, 1), (4, 6)]:
+    n = len(configs)
+    for i, j in [(0, 1), (4, 6)] + [(k, k + n) for k in range(n)]:
         assert torch.equal(outs[i][0], outs[j][0])
         for a, b in zip(outs[i][1], outs[j][1]):
             assert torch.equal(a, b)
+    configs = configs + configs
     _, Yref = oracle_ag(shards, Wt)
     _, Yb = oracle_rs(A, Bt)
     for k, (Y, R) in enumerate(outs):
