@@ -75,6 +75,10 @@ def parse():
                     default=None,
                     help="time one op of the workload at one T only (small profiling case)")
     ap.add_argument("--case-T", type=int, default=8192)
+    ap.add_argument("--case-workload", choices=["swiglu", "qkv", "large"], default="swiglu",
+                    help="the shapes of --case: hidden, tp, AG N and RS K of this workload")
+    ap.add_argument("--case-N", type=int, default=0, help="AG output width of --case (0: the workload's)")
+    ap.add_argument("--case-K", type=int, default=0, help="RS K per shard of --case (0: the workload's)")
     ap.add_argument("--case-reps", type=int, default=3)
     ap.add_argument("--sm-margin", type=int, default=0)
     ap.add_argument("--gather-kernel", type=int, default=-1, choices=[-1, 0, 1, 2],
@@ -553,7 +557,7 @@ def run_ours(args):
                   "what": "same microbatches padded to max_tokens=%d (real tokens first, zeros "
                           "after); useful FLOPs only" % w.max_tokens}
     bulk = bulk_measure(wl, stream) if not args.no_bulk and rank == 0 else None
-    sweep = sweep_points(wl, stream) if args.sweep and rank == 0 else None
+    sweep = sweep_points(wl, stream) + sweep_other_configs(stream) if args.sweep and rank == 0 else None
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl, args.cpu_seconds)
@@ -650,6 +654,59 @@ def sweep_points(wl, stream):
     return out
 
 
+def sweep_other_configs(stream):
+    """The other throughput configs on their own handles: QKV (AG-GEMM, N = 3072, tp 4,
+    hidden 4096) and large (GEMM-RS, tp 8, hidden 8192, attention-out K = 1024 and fc2
+    K = 3584 per shard), one call each over a ladder of active T (20 calls per point)."""
+    from gemm_overlap_gemms_gb300 import ub
+    pk, _ = peaks()
+    tensor_peak = _peak_value(pk, "bf16_tflops_sustained", "bf16_tflops") or FALLBACK["bf16_tflops_sustained"]
+    hbm_peak = _peak_value(pk, "hbm_gbs") or FALLBACK["hbm_gbs"]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    g = synth.generator(dev, 7)
+    out = []
+
+    def point(name, T, fn, fl, nbytes):
+        ms = time_steps(fn, 20, 3, stream, 1) / 20
+        tf = fl / (ms / 1e3) / 1e12
+        out.append({"sweep": name, "T": T, "us": ms * 1e3, "tflops": tf, "frac_of_peak": tf / tensor_peak,
+                    "hbm_gbs": nbytes / (ms / 1e3) / 1e9, "hbm_frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak,
+                    "note": "includes the gather" if name.startswith("qkv") else ""})
+
+    w = synth.WORKLOADS["qkv"]
+    H, N, tp = w.hidden, w.ag_n[0], w.tp
+    Wq = synth.normal_bf16((N, H), 1.0 / math.sqrt(H), g, dev)
+    X = synth.normal_bf16((w.max_tokens, H), 1.0, g, dev)
+    Y = torch.empty((w.max_tokens, N), dtype=torch.bfloat16, device=dev)
+    buf = ub.UserBuffer([w.max_tokens, H], tp)
+    for T in (4, 64, 512, 1024, 2048, 4096, 8192):
+        c = T // tp
+        buf.set_active_shape([T, H])
+        shards = [X[r * c:(r + 1) * c] for r in range(tp)]
+        point("qkv_ag", T, lambda: buf.ag_gemm(shards, Wq, Y[:T], stream=stream), 2.0 * T * H * N,
+              2.0 * (N * H + 2 * T * H + T * N))
+    buf.close()
+    del Wq, X, Y
+
+    w = synth.WORKLOADS["large"]
+    H, tp = w.hidden, w.tp
+    buf = ub.UserBuffer([w.max_tokens, H], tp)
+    Yl = torch.empty((w.max_tokens, H), dtype=torch.bfloat16, device=dev)
+    for K in w.rs_k:
+        B = [synth.normal_bf16((H, K), 1.0 / math.sqrt(K), g, dev) for _ in range(tp)]
+        A = [synth.normal_bf16((w.max_tokens, K), 1.0, g, dev) for _ in range(tp)]
+        for T in (8, 512, 2048, 8192, 16384):
+            c = T // tp
+            buf.set_active_shape([T, H])
+            a_T = [a[:T] for a in A]
+            outs = [Yl[r * c:(r + 1) * c] for r in range(tp)]
+            point("large_rs_k%d" % K, T, lambda: buf.gemm_rs(a_T, B, outs, stream=stream), 2.0 * T * K * H * tp,
+                  2.0 * (tp * K * H + tp * T * K + T * H))
+        del A, B
+    buf.close()
+    return out
+
+
 # ---------------------------------------------------------------- reference arm (the oracle)
 
 def run_reference(args):
@@ -724,10 +781,12 @@ def run_case(args):
     """One op of the workload at one active T: a warm-up launch, then `case_reps`
     launches (the small case the profiler captures; holds well under 1 GB)."""
     from gemm_overlap_gemms_gb300 import ub
-    w = synth.WORKLOADS[WORKLOAD]
+    w = synth.WORKLOADS[args.case_workload]
     dev = torch.device("cuda", 0)
     T = args.case_T
-    H, N, K, tp = w.hidden, w.ag_n[0], w.rs_k[0], w.tp
+    H, tp = w.hidden, w.tp
+    N = args.case_N or (w.ag_n[0] if w.ag_n else 2 * H)
+    K = args.case_K or (w.rs_k[0] if w.rs_k else H)
     g = synth.generator(dev)
     buf = ub.UserBuffer([w.max_tokens, H], tp)
     buf.set_option("cta_pair", args.cta_pair)
@@ -838,7 +897,8 @@ def run_case(args):
     del graph
     status = buf.query_status()
     buf.close()
-    print(json.dumps({"case": args.case, "T": T, "cta_pair": args.cta_pair, "streamk": args.streamk,
+    print(json.dumps({"case": args.case, "workload": args.case_workload, "T": T, "N": N, "K": K,
+                      "cta_pair": args.cta_pair, "streamk": args.streamk,
                       "copy_streams": args.copy_streams, "sm_margin": args.sm_margin,
                       "gather_kernel": args.gather_kernel, "launches": n, "avg_us": 1e3 * ms / max(n, 1),
                       "tflops": flops * n / (ms / 1e3) / 1e12 if ms > 0 and flops else None,

@@ -241,16 +241,38 @@ constexpr bool kFusedGatherAuto = true;
 // (AG and AG + SwiGLU, T = 4-128, GB300).
 constexpr bool kFusedGatherSkinnyAuto = false;
 
-// How many k-pieces the last wave's tiles are cut into: enough to give every pair one
-// piece, at most MAX_TAIL_SPLIT, each at least MIN_KBLOCKS_PER_PIECE k-blocks long.
-int64_t tail_split_for(int64_t tiles, int64_t np, int64_t kb)
+// Cost of the last, partial wave's tiles when each is cut into s k-pieces, in units of
+// one whole tile on one pair: the longest piece, 1/s, plus the fix-up (the pieces'
+// fp32 partials published and added by the pair holding piece 0). Measured on GB300,
+// the fix-up costs about as much as kFixupKb0 + kFixupKb1 * (s - 1) k-blocks of a
+// 256 x 256 pair tile (9.5 us + 4.2 us per added piece, at 0.31 us per k-block), a fixed
+// time rather than a share of the tile: a split pays off for long K (GEMM-RS over tp
+// shards of K = 1024 .. 3584: 1-39 % faster) and loses for K = 4096 (AG: 1-16 % slower).
+constexpr double kFixupKb0 = 30.0;
+constexpr double kFixupKb1 = 13.5;
+double split_tail_cost(int64_t s, int64_t kb)
+{
+    if (s <= 1) return 1.0;
+    return 1.0 / static_cast<double>(s) + (kFixupKb0 + kFixupKb1 * static_cast<double>(s - 1)) / static_cast<double>(kb);
+}
+
+// How many k-pieces the last wave's tiles are cut into. At most one piece per idle pair,
+// MAX_TAIL_SPLIT pieces and MIN_KBLOCKS_PER_PIECE k-blocks per piece; within that the
+// cheapest cut by split_tail_cost (1 when no cut beats whole tiles), or with `widest`
+// the most pieces allowed (the split forced on).
+int64_t tail_split_for(int64_t tiles, int64_t np, int64_t kb, bool widest)
 {
     const int64_t rem = tiles % np;
     if (rem == 0) return 1;
-    int64_t s = np / rem;
-    if (s > ubk::MAX_TAIL_SPLIT) s = ubk::MAX_TAIL_SPLIT;
-    if (s > kb / ubk::MIN_KBLOCKS_PER_PIECE) s = kb / ubk::MIN_KBLOCKS_PER_PIECE;
-    return s < 1 ? 1 : s;
+    int64_t smax = np / rem;
+    if (smax > ubk::MAX_TAIL_SPLIT) smax = ubk::MAX_TAIL_SPLIT;
+    if (smax > kb / ubk::MIN_KBLOCKS_PER_PIECE) smax = kb / ubk::MIN_KBLOCKS_PER_PIECE;
+    if (smax < 1) return 1;
+    if (widest) return smax;
+    int64_t best = 1;
+    for (int64_t s = 2; s <= smax; ++s)
+        if (split_tail_cost(s, kb) < split_tail_cost(best, kb)) best = s;
+    return best;
 }
 
 // Launch shape of a pair-kernel call: whole tiles in strided waves, and (with the
@@ -259,7 +281,7 @@ void set_pairs(ub_handle *h, GemmParams &p, int mode, bool split)
 {
     const int64_t tiles = p.region_tile0[p.n_regions];
     int64_t np = clusters_for(h, mode, 1 << 30);
-    int64_t sp = split ? tail_split_for(tiles, np, p.k_blocks) : 1;
+    int64_t sp = split ? tail_split_for(tiles, np, p.k_blocks, h->streamk == 1) : 1;
     if (sp == 1 && np > tiles) np = tiles;
     if (np < 1) np = 1;
     p.num_pairs = static_cast<int>(np);
@@ -313,7 +335,7 @@ void set_skinny(ub_handle *h, GemmParams &p, int slot_mult, int w_bytes)
 // the time of one 128x256 tile on one SM, the same as one 256x256 tile on a pair):
 //   single CTAs, chunk-aligned 128-row tiles:    waves
 //   CTA pairs, whole tiles:                      0.91 * waves (a third less L2 traffic)
-//   CTA pairs, last wave split into s k-pieces:  0.91 * (full waves + 1.1 / s)
+//   CTA pairs, last wave split into s k-pieces:  0.91 * (full waves + split_tail_cost(s))
 // UB_OPT_CTA_PAIR / UB_OPT_STREAMK >= 0 force a choice. The choice depends only on the
 // shapes and the SM count, so results stay bitwise reproducible.
 void choose_path(ub_handle *h, int mode, int64_t single_tiles, int64_t pair_tiles, int64_t kb, bool &pair,
@@ -323,9 +345,8 @@ void choose_path(ub_handle *h, int mode, int64_t single_tiles, int64_t pair_tile
     const int64_t np = clusters_for(h, mode, 1 << 30);
     const double c_single = static_cast<double>(ceil_div(single_tiles, slots));
     const double c_dp = 0.91 * static_cast<double>(ceil_div(pair_tiles, np));
-    const int64_t s = tail_split_for(pair_tiles, np, kb);
-    const double c_split =
-        s > 1 ? 0.91 * (static_cast<double>(pair_tiles / np) + 1.1 / static_cast<double>(s)) : c_dp;
+    const int64_t s = tail_split_for(pair_tiles, np, kb, h->streamk == 1);
+    const double c_split = s > 1 ? 0.91 * (static_cast<double>(pair_tiles / np) + split_tail_cost(s, kb)) : c_dp;
     if (h->cta_pair == 0) {
         pair = false;
     } else if (h->cta_pair == 1) {
