@@ -297,6 +297,25 @@ def time_steps(fn, steps, warmup, stream, world):
     return e0.elapsed_time(e1)  # ms
 
 
+def time_calls(fn, calls, warmup, stream):
+    """Median and mean of `calls` individually timed calls (CUDA events on `stream`
+    around each call), after `warmup` untimed ones. Returns (median ms, mean ms)."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(calls + 1)]
+    ev[0].record(stream)
+    for i in range(calls):
+        fn()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(calls)]
+    return float(np.median(ms)), float(np.mean(ms))
+
+
+SWEEP_CALLS, SWEEP_WARMUP = 50, 10   # per point: median of 50 timed calls after 10 warm-ups
+
+
 def e2e_measure(wl, steps, warmup, stream, world):
     """Same step, with each microbatch's activations copied in from pinned host memory
     and its outputs copied back, inside the timed region. Copies run on their own
@@ -628,12 +647,11 @@ def sweep_points(wl, stream):
                 fn = lambda: wl.buf.ag_gemm_swiglu(shards, wl.W1, wl.Yz, stream=stream)
             else:
                 fn = lambda: wl.buf.gemm_rs(A, wl.B, outs, stream=stream)
-            reps = 20
             # the no-overlap comparator puts the gather copies on the GEMM's stream, ahead of it
             no_overlap = op == "ag_swiglu_no_overlap"
             wl.buf.set_option("copy_streams", 0 if no_overlap else 4)
             wl.buf.set_option("gather_kernel", 0 if no_overlap else -1)
-            ms = time_steps(fn, reps, 3, stream, 1) / reps
+            ms, ms_mean = time_calls(fn, SWEEP_CALLS, SWEEP_WARMUP, stream)
             wl.buf.set_option("copy_streams", 4)
             wl.buf.set_option("gather_kernel", -1)
             fl = 2.0 * T * H * N if op != "rs" else 2.0 * T * K * H * tp
@@ -645,7 +663,7 @@ def sweep_points(wl, stream):
             else:
                 n_out = N // 2 if op.startswith("ag_swiglu") else N
                 nbytes = 2.0 * (N * H + 2 * T * H + T * n_out)
-            out.append({"sweep": op, "T": T, "us": ms * 1e3, "tflops": tf,
+            out.append({"sweep": op, "T": T, "us": ms * 1e3, "us_mean": ms_mean * 1e3, "tflops": tf,
                         "frac_of_peak": tf / tensor_peak,
                         "hbm_gbs": nbytes / (ms / 1e3) / 1e9, "hbm_frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak,
                         "note": ("gather copies on the GEMM's stream, before it (no overlap)"
@@ -657,7 +675,7 @@ def sweep_points(wl, stream):
 def sweep_other_configs(stream):
     """The other throughput configs on their own handles: QKV (AG-GEMM, N = 3072, tp 4,
     hidden 4096) and large (GEMM-RS, tp 8, hidden 8192, attention-out K = 1024 and fc2
-    K = 3584 per shard), one call each over a ladder of active T (20 calls per point)."""
+    K = 3584 per shard), over a ladder of active T (median of 50 timed calls per point)."""
     from gemm_overlap_gemms_gb300 import ub
     pk, _ = peaks()
     tensor_peak = _peak_value(pk, "bf16_tflops_sustained", "bf16_tflops") or FALLBACK["bf16_tflops_sustained"]
@@ -667,9 +685,10 @@ def sweep_other_configs(stream):
     out = []
 
     def point(name, T, fn, fl, nbytes):
-        ms = time_steps(fn, 20, 3, stream, 1) / 20
+        ms, ms_mean = time_calls(fn, SWEEP_CALLS, SWEEP_WARMUP, stream)
         tf = fl / (ms / 1e3) / 1e12
-        out.append({"sweep": name, "T": T, "us": ms * 1e3, "tflops": tf, "frac_of_peak": tf / tensor_peak,
+        out.append({"sweep": name, "T": T, "us": ms * 1e3, "us_mean": ms_mean * 1e3, "tflops": tf,
+                    "frac_of_peak": tf / tensor_peak,
                     "hbm_gbs": nbytes / (ms / 1e3) / 1e9, "hbm_frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak,
                     "note": "includes the gather" if name.startswith("qkv") else ""})
 

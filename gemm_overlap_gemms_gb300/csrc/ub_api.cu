@@ -231,6 +231,54 @@ GemmParams *cache_insert(ub_handle *h, std::vector<const void *> key, const Gemm
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Row regions of the CTA-pair AG tiling, in ring order: the self chunk's first `head`
+// rows, read in place from its shard; the user-buffer rows from there to T (the rest of
+// the self chunk first, behind its readiness flag like the other chunks' rows); the
+// user-buffer rows before the self chunk. With head = c the self chunk is read wholly
+// in place; with head = its whole 256-row tiles only the second region ends in a partial
+// tile (self rank 0: ceil(T / 256) row tiles, one fewer whenever 256 does not divide c).
+struct AgRegion {
+    int64_t row0, rows;
+    const void *src;
+    int ub_backed;
+};
+int ag_pair_regions(int64_t T, int64_t c, int64_t H, int self, int64_t head, const void *self_shard, char *ub,
+                    AgRegion out[3])
+{
+    const int64_t row1 = self * c + head;
+    const AgRegion all[3] = {{self * c, head, self_shard, 0},
+                             {row1, T - row1, ub + row1 * H * 2, 1},
+                             {0, self * c, ub, 1}};
+    int n = 0;
+    for (const AgRegion &r : all)
+        if (r.rows > 0) out[n++] = r;
+    return n;
+}
+
+int64_t ag_pair_row_tiles(int64_t T, int64_t c, int self, int64_t head)
+{
+    AgRegion reg[3];
+    const int n = ag_pair_regions(T, c, 0, self, head, nullptr, nullptr, reg);
+    int64_t tiles = 0;
+    for (int i = 0; i < n; ++i) tiles += ceil_div(reg[i].rows, ubk::PAIR_BM);
+    return tiles;
+}
+
+// How many of the self chunk's rows the CTA-pair AG kernel reads in place: all of them,
+// unless reading only its whole 256-row tiles in place saves a wave of pairs. The rest
+// then waits for the gather, which copies those rows first (measured on GB300: AG +
+// SwiGLU at T = 1140 in two waves instead of three, 59 against 83 us; QKV at T = 1140,
+// one wave either way, 39.4 against 36.0 us had it always been done).
+int64_t ag_self_head(ub_handle *h, int mode, int64_t T, int64_t c, int self, int64_t n_tiles)
+{
+    const int64_t split = c / ubk::PAIR_BM * ubk::PAIR_BM;
+    if (split == c) return c;
+    const int64_t np = clusters_for(h, mode, 1 << 30);
+    const int64_t waves_split = ceil_div(ag_pair_row_tiles(T, c, self, split) * n_tiles, np);
+    const int64_t waves_whole = ceil_div(ag_pair_row_tiles(T, c, self, c) * n_tiles, np);
+    return waves_split < waves_whole ? split : c;
+}
+
 constexpr int64_t kGatherKernelMaxT = 512;  // UB_OPT_GATHER_KERNEL = -1: kernel up to this T
 // ... and inside the GEMM above it: on GB300 (tp 4, hidden 4096) the whole AG call is
 // 2-8 % faster than with the driver copies at T = 1024-8192 (the chunks land sooner:
@@ -409,7 +457,26 @@ bool gather_in_gemm(ub_handle *h, bool skinny)
     return skinny ? kFusedGatherSkinnyAuto : (kFusedGatherAuto && h->T > kGatherKernelMaxT);
 }
 
-int issue_gather(ub_handle *h, const void *const *shards, cudaStream_t s, uint32_t epoch, int64_t drop)
+// The copies of the all-gather in issue order: the self chunk's rows from `head` on (the
+// rows the GEMM reads from the buffer; flag after them), the other chunks in ring order
+// (flag after each), then the self chunk's first `head` rows (read in place by the GEMM;
+// flagged only when they are the whole chunk).
+struct GatherPart {
+    int r;
+    int64_t row_lo, row_hi;
+    bool flag;
+};
+int gather_parts(int tp, int self, int64_t c, int64_t head, GatherPart out[UB_MAX_TP + 1])
+{
+    int n = 0;
+    if (head < c) out[n++] = GatherPart{self, head, c, true};
+    for (int q = 1; q < tp; ++q) out[n++] = GatherPart{(self + q) % tp, 0, c, true};
+    if (head > 0) out[n++] = GatherPart{self, 0, head, head == c};
+    return n;
+}
+
+int issue_gather(ub_handle *h, const void *const *shards, cudaStream_t s, uint32_t epoch, int64_t drop,
+                 int64_t self_head)
 {
     const int tp = h->tp;
     const int64_t T = h->T, H = h->hidden, c = T / tp;
@@ -424,11 +491,15 @@ int issue_gather(ub_handle *h, const void *const *shards, cudaStream_t s, uint32
     if (h->copy_streams == 0 && !h->gather_by_kernel) {
         // In-stream: the copies and flag writes go on `s` itself, ahead of the GEMM,
         // which then finds every flag set (no overlap, no cross-stream hops).
-        for (int q = 1; q <= tp; ++q) {
-            const int r = (self + q) % tp;
-            UB_CUDA(cudaMemcpyAsync(ub + r * c * H * 2, shards[r], static_cast<size_t>(c * H * 2),
-                                    cudaMemcpyDeviceToDevice, s));
-            if (r != drop) {
+        GatherPart parts[UB_MAX_TP + 1];
+        const int np = gather_parts(tp, self, c, self_head, parts);
+        for (int i = 0; i < np; ++i) {
+            const GatherPart &pt = parts[i];
+            const int r = pt.r;
+            UB_CUDA(cudaMemcpyAsync(ub + (r * c + pt.row_lo) * H * 2,
+                                    static_cast<const char *>(shards[r]) + pt.row_lo * H * 2,
+                                    static_cast<size_t>((pt.row_hi - pt.row_lo) * H * 2), cudaMemcpyDeviceToDevice, s));
+            if (pt.flag && r != drop) {
                 CUresult cr = driver().write_value32(reinterpret_cast<CUstream>(s),
                                                      reinterpret_cast<CUdeviceptr>(flags_of(h) + r), epoch,
                                                      CU_STREAM_WRITE_VALUE_DEFAULT);
@@ -466,12 +537,16 @@ int issue_gather(ub_handle *h, const void *const *shards, cudaStream_t s, uint32
     auto copy_stream = [&](int i) { return i == 0 ? h->side : h->extra_side[i]; };
     UB_CUDA(cudaEventRecord(h->ev_fork, s));
     for (int i = 0; i < ncs; ++i) UB_CUDA(cudaStreamWaitEvent(copy_stream(i), h->ev_fork, 0));
-    for (int q = 1; q <= tp; ++q) {
-        const int r = (self + q) % tp;
-        cudaStream_t cs = copy_stream((q - 1) % ncs);
-        UB_CUDA(cudaMemcpyAsync(ub + r * c * H * 2, shards[r], static_cast<size_t>(c * H * 2),
-                                cudaMemcpyDeviceToDevice, cs));
-        if (r != drop) {
+    GatherPart parts[UB_MAX_TP + 1];
+    const int np = gather_parts(tp, self, c, self_head, parts);
+    for (int i = 0; i < np; ++i) {
+        const GatherPart &pt = parts[i];
+        const int r = pt.r;
+        cudaStream_t cs = copy_stream(i % ncs);
+        UB_CUDA(cudaMemcpyAsync(ub + (r * c + pt.row_lo) * H * 2,
+                                static_cast<const char *>(shards[r]) + pt.row_lo * H * 2,
+                                static_cast<size_t>((pt.row_hi - pt.row_lo) * H * 2), cudaMemcpyDeviceToDevice, cs));
+        if (pt.flag && r != drop) {
             CUresult cr = driver().write_value32(reinterpret_cast<CUstream>(cs),
                                                  reinterpret_cast<CUdeviceptr>(flags_of(h) + r), epoch,
                                                  CU_STREAM_WRITE_VALUE_DEFAULT);
@@ -711,9 +786,11 @@ static int ag_gemm_impl(ub_handle_t h, const void *const *shards, const void *Wt
     const int prof_op = glu ? UB_OP_AG_SWIGLU : (b_kn ? UB_OP_AG_KN : UB_OP_AG);
     const int64_t n_out = glu ? glu_f : N;                    // columns of Y
     const int64_t n_tiles = glu ? (glu_f + 127) / 128 : (N + ubk::BN - 1) / ubk::BN;
-    int64_t pair_rows_tiles = ceil_div(c, ubk::PAIR_BM);  // regions: self chunk, after it, before it
-    if (T - (self + 1) * c > 0) pair_rows_tiles += ceil_div(T - (self + 1) * c, ubk::PAIR_BM);
-    if (self * c > 0) pair_rows_tiles += ceil_div(self * c, ubk::PAIR_BM);
+    const int64_t self_head = ag_self_head(h, mode, T, c, self, n_tiles);
+    AgRegion regions[3];
+    const int n_regions = ag_pair_regions(T, c, H, self, self_head, shards[self], ub, regions);
+    int64_t pair_rows_tiles = 0;
+    for (int i = 0; i < n_regions; ++i) pair_rows_tiles += ceil_div(regions[i].rows, ubk::PAIR_BM);
     bool pair = false, streamk = false;
     choose_path(h, mode, tp * ceil_div(c, ubk::BM) * n_tiles, pair_rows_tiles * n_tiles,
                 (H + ubk::BK - 1) / ubk::BK, pair, streamk);
@@ -748,6 +825,7 @@ static int ag_gemm_impl(ub_handle_t h, const void *const *shards, const void *Wt
         p.n_tiles = static_cast<int>(n_tiles);
         p.num_tiles = tp * p.m_tiles * p.n_tiles;
         p.self_rank = self;
+        p.self_head = static_cast<int>(pair ? self_head : c);
         if (skinny) {
             // Token sub-tile r = chunk r (c rows, zero-filled to c16), the self chunk in place.
             for (int r = 0; r < tp; ++r) {
@@ -785,18 +863,9 @@ static int ag_gemm_impl(ub_handle_t h, const void *const *shards, const void *Wt
             }
             h->counters.tensor_map_encodes += 2 * tp;
         } else {
-            // Row regions in ring order: the self chunk (read in place), the chunks after
-            // it, the chunks before it (both from the user buffer).
-            struct {
-                int64_t row0, rows;
-                const void *src;
-                int ub_backed;
-            } reg[3] = {{self * c, c, shards[self], 0},
-                        {(self + 1) * c, T - (self + 1) * c, ub + (self + 1) * c * H * 2, 1},
-                        {0, self * c, ub, 1}};
             int nreg = 0;
-            for (auto &rgn : reg) {
-                if (rgn.rows <= 0) continue;
+            for (int i = 0; i < n_regions; ++i) {
+                const AgRegion &rgn = regions[i];
                 if (int rc = encode_2d(&p.tmA[nreg], rgn.src, H, rgn.rows, H * 2, ubk::BK, 128)) return rc;
                 if (int rc = encode_2d(&p.tmY[nreg], static_cast<char *>(Y) + rgn.row0 * n_out * 2, n_out,
                                        rgn.rows, n_out * 2, ubk::STORE_COLS, 32))
@@ -843,11 +912,12 @@ static int ag_gemm_impl(ub_handle_t h, const void *const *shards, const void *Wt
         p.g_ub = h->ub;
         p.g_counters = gather_counters_of(h);
         p.g_chunk_vecs = c * H / 8;
+        p.g_self_head_vecs = p.self_head * H / 8;
         p.g_drop = static_cast<int>(drop);
         int rc = launch(h, p, mode, skinny ? PATH_SKINNY : pair ? PATH_PAIR : PATH_SINGLE, s, prof_op);
         if (rc != UB_OK) return rc;
     } else {
-        if (int rc = issue_gather(h, shards, s, epoch, drop)) return rc;
+        if (int rc = issue_gather(h, shards, s, epoch, drop, p.self_head)) return rc;
         int rc = launch(h, p, mode, skinny ? PATH_SKINNY : pair ? PATH_PAIR : PATH_SINGLE, s, prof_op);
         // Join the copy streams back into `s` even if the launch failed.
         if (int jrc = join_gather(h, s)) return jrc;
@@ -1021,7 +1091,7 @@ int ub_allgather(ub_handle_t h, const void *const *shards, void *stream)
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint32_t epoch = 0;
     if (int rc = begin_call(h, s, epoch)) return rc;
-    if (int rc = issue_gather(h, shards, s, epoch, -1)) return rc;
+    if (int rc = issue_gather(h, shards, s, epoch, -1, h->T / h->tp)) return rc;
     if (int rc = join_gather(h, s)) return rc;
     h->counters.last_T = h->T;
     return UB_OK;

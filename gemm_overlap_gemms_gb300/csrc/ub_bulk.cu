@@ -92,13 +92,13 @@ __global__ void __launch_bounds__(256) bulk_rs_kernel(const __grid_constant__ Bu
     }
 }
 
-// One CTA group per chunk, ring order: block b copies part (b % ctas_per_chunk) of the
-// q-th chunk after the self rank (b / ctas_per_chunk), the self chunk last.
+// One CTA group per chunk, ring order: block b copies part (b % ctas_per_chunk) of chunk
+// self_rank + b / ctas_per_chunk (mod tp), the self chunk first.
 __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ GatherParams p)
 {
     pdl_enter();
-    const int q = blockIdx.x / p.ctas_per_chunk + 1;  // 1..tp
-    const int part = blockIdx.x - (q - 1) * p.ctas_per_chunk;
+    const int q = blockIdx.x / p.ctas_per_chunk;  // 0..tp-1
+    const int part = blockIdx.x - q * p.ctas_per_chunk;
     const int r = (p.self_rank + q) % p.tp;
     const uint4 *src = static_cast<const uint4 *>(p.src[r]);
     uint4 *dst = static_cast<uint4 *>(p.ub) + static_cast<int64_t>(r) * p.chunk_vecs;

@@ -313,21 +313,38 @@ __device__ __forceinline__ void st_release_u32(uint32_t *ptr, uint32_t v)
 }
 
 // All-gather done by the GEMM's own epilogue warps (128 threads, named barrier 1) before
-// their first tile, while the producer already loads the self chunk's tiles: every CTA
-// copies its 1/gridDim.x share of each chunk in ring order after the self rank (the
-// self chunk last), with 16-byte loads that bypass L1, sixteen in flight per thread
-// (about 5 MB in flight over the GPU: enough to keep HBM busy); the
-// CTA that completes a chunk's count resets the counter and publishes the chunk's
-// readiness flag with the call's epoch (no flag for chunk p.g_drop).
+// their first tile, while the producer already loads the self chunk's tiles. It copies
+// three kinds of parts, in this order: the self chunk's rows from g_self_head_vecs on
+// (the rows past its whole 256-row tiles, which the CTA-pair kernel reads from the
+// buffer), the other chunks in ring order after the self rank, then the self chunk's
+// first rows (read in place, so they need no flag unless they are the whole chunk).
+// Every CTA copies its 1/gridDim.x share of each part, with 16-byte loads that bypass
+// L1, sixteen in flight per thread (about 5 MB in flight over the GPU: enough to keep
+// HBM busy); the CTA that completes a flagged part's count resets the chunk's counter
+// and publishes its readiness flag with the call's epoch (no flag for chunk p.g_drop).
+// A chunk's counter serves one flagged part per call.
 __device__ void fused_gather(const GemmParams &p, int et)
 {
     const int G = static_cast<int>(gridDim.x);
-    const int64_t per = (p.g_chunk_vecs + G - 1) / G;
-    const int64_t v0 = static_cast<int64_t>(blockIdx.x) * per;
-    const int64_t v1 = v0 + per < p.g_chunk_vecs ? v0 + per : p.g_chunk_vecs;
-    for (int q = 1; q <= p.tp; ++q) {
-        int r = p.self_rank + q;
-        if (r >= p.tp) r -= p.tp;
+    const int64_t head = p.g_self_head_vecs;
+    for (int q = 0; q <= p.tp; ++q) {
+        int r = p.self_rank;
+        int64_t lo = 0, hi = p.g_chunk_vecs;
+        bool publish = true;
+        if (q == 0) {
+            lo = head;                  // the self chunk's last rows
+            if (lo >= hi) continue;
+        } else if (q < p.tp) {
+            r += q;                     // the other chunks
+            if (r >= p.tp) r -= p.tp;
+        } else {
+            hi = head;                  // the self chunk's first rows
+            publish = head >= p.g_chunk_vecs;
+            if (hi <= 0) continue;
+        }
+        const int64_t per = (hi - lo + G - 1) / G;
+        const int64_t v0 = lo + static_cast<int64_t>(blockIdx.x) * per;
+        const int64_t v1 = v0 + per < hi ? v0 + per : hi;
         const uint4 *src = static_cast<const uint4 *>(p.g_src[r]);
         uint4 *dst = static_cast<uint4 *>(p.g_ub) + static_cast<int64_t>(r) * p.g_chunk_vecs;
         constexpr int U = 16;
@@ -343,7 +360,8 @@ __device__ void fused_gather(const GemmParams &p, int et)
             for (int u = 0; u < U; ++u)
                 if (v + u * 128 < v1) dst[v + u * 128] = x[u];
         }
-        asm volatile("bar.sync 1, 128;" ::: "memory");  // this CTA's share of chunk r is written
+        if (!publish) continue;
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // this CTA's share of the part is written
         if (et == 0) {
             __threadfence();
             const uint32_t done = atomicAdd(p.g_counters + r, 1u) + 1u;

@@ -80,6 +80,8 @@ struct GemmParams {
     int n_tiles;                 // ceil(n_out / BN)
     int num_tiles;               // tp * m_tiles * n_tiles
     int self_rank;               // AG: chunk read in place, no flag wait
+    int self_head;               // AG: rows of the self chunk read in place (the CTA-pair
+                                 // kernel reads the rest from the buffer); c elsewhere
 
     // ---- CTA-pair kernel only: row regions and the stream-K split.
     // The pair kernel tiles rows by region instead of by chunk. RS has one region,
@@ -113,6 +115,7 @@ struct GemmParams {
     void *g_ub;                  // user buffer base
     uint32_t *g_counters;        // CTAs done per chunk (zero between calls)
     int64_t g_chunk_vecs;        // 16-byte vectors per chunk = c * hidden / 8
+    int64_t g_self_head_vecs;    // vectors of the self chunk's first self_head rows
 
     // ---- skinny kernel only (few tokens): weight rows on the MMA's M dimension, tokens
     // on its N dimension. Tiles are SK_BM weight rows (SwiGLU: SK_BM gate + SK_BM up rows)

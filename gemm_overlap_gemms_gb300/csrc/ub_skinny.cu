@@ -443,7 +443,7 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_skinny_kernel(const __grid
                                            static_cast<int64_t>(sb * p.c + i0) * p.ldy + n;
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            const float z = GLU ? a[i] / (1.0f + __expf(-a[i])) * b[i] : a[i];
+                            const float z = GLU ? __fdividef(a[i], 1.0f + __expf(-a[i])) * b[i] : a[i];
                             if (i0 + i < p.c) y[static_cast<int64_t>(i) * p.ldy] = __float2bfloat16_rn(z);
                         }
                     } else {
