@@ -269,14 +269,18 @@ int64_t ag_pair_row_tiles(int64_t T, int64_t c, int self, int64_t head)
 // then waits for the gather, which copies those rows first (measured on GB300: AG +
 // SwiGLU at T = 1140 in two waves instead of three, 59 against 83 us; QKV at T = 1140,
 // one wave either way, 39.4 against 36.0 us had it always been done).
-int64_t ag_self_head(ub_handle *h, int mode, int64_t T, int64_t c, int self, int64_t n_tiles)
+int64_t self_head_for(int64_t T, int64_t c, int self, int64_t n_tiles, int64_t np)
 {
     const int64_t split = c / ubk::PAIR_BM * ubk::PAIR_BM;
     if (split == c) return c;
-    const int64_t np = clusters_for(h, mode, 1 << 30);
     const int64_t waves_split = ceil_div(ag_pair_row_tiles(T, c, self, split) * n_tiles, np);
     const int64_t waves_whole = ceil_div(ag_pair_row_tiles(T, c, self, c) * n_tiles, np);
     return waves_split < waves_whole ? split : c;
+}
+
+int64_t ag_self_head(ub_handle *h, int mode, int64_t T, int64_t c, int self, int64_t n_tiles)
+{
+    return self_head_for(T, c, self, n_tiles, clusters_for(h, mode, 1 << 30));
 }
 
 constexpr int64_t kGatherKernelMaxT = 512;  // UB_OPT_GATHER_KERNEL = -1: kernel up to this T
@@ -386,29 +390,35 @@ void set_skinny(ub_handle *h, GemmParams &p, int slot_mult, int w_bytes)
 //   CTA pairs, last wave split into s k-pieces:  0.91 * (full waves + split_tail_cost(s))
 // UB_OPT_CTA_PAIR / UB_OPT_STREAMK >= 0 force a choice. The choice depends only on the
 // shapes and the SM count, so results stay bitwise reproducible.
-void choose_path(ub_handle *h, int mode, int64_t single_tiles, int64_t pair_tiles, int64_t kb, bool &pair,
-                 bool &split)
+void plan_path(int64_t slots, int64_t np, int cta_pair, int streamk, int64_t single_tiles, int64_t pair_tiles,
+               int64_t kb, bool &pair, bool &split)
 {
-    const int64_t slots = h->sm_count - h->sm_margin > 0 ? h->sm_count - h->sm_margin : 1;
-    const int64_t np = clusters_for(h, mode, 1 << 30);
     const double c_single = static_cast<double>(ceil_div(single_tiles, slots));
     const double c_dp = 0.91 * static_cast<double>(ceil_div(pair_tiles, np));
-    const int64_t s = tail_split_for(pair_tiles, np, kb, h->streamk == 1);
+    const int64_t s = tail_split_for(pair_tiles, np, kb, streamk == 1);
     const double c_split = s > 1 ? 0.91 * (static_cast<double>(pair_tiles / np) + split_tail_cost(s, kb)) : c_dp;
-    if (h->cta_pair == 0) {
+    if (cta_pair == 0) {
         pair = false;
-    } else if (h->cta_pair == 1) {
+    } else if (cta_pair == 1) {
         pair = true;
     } else {
         pair = (c_dp < c_single) || (c_split < c_single);
     }
     if (!pair) {
         split = false;
-    } else if (h->streamk >= 0) {
-        split = h->streamk != 0;
+    } else if (streamk >= 0) {
+        split = streamk != 0;
     } else {
         split = c_split < c_dp;
     }
+}
+
+void choose_path(ub_handle *h, int mode, int64_t single_tiles, int64_t pair_tiles, int64_t kb, bool &pair,
+                 bool &split)
+{
+    const int64_t slots = h->sm_count - h->sm_margin > 0 ? h->sm_count - h->sm_margin : 1;
+    plan_path(slots, clusters_for(h, mode, 1 << 30), static_cast<int>(h->cta_pair), static_cast<int>(h->streamk),
+              single_tiles, pair_tiles, kb, pair, split);
 }
 
 enum Path : int { PATH_SINGLE = 0, PATH_PAIR = 1, PATH_SKINNY = 2 };
@@ -755,6 +765,31 @@ int ub_grid_ctas(ub_handle_t h, int *ctas)
     DeviceGuard g(h->device);
     if (ctas) *ctas = h->cta_pair != 0 ? 2 * clusters_for(h, ubk::MODE_RS, 1 << 30) : grid_for(h, 1 << 30);
     return UB_OK;
+}
+
+int64_t ub_plan_tail_split(int64_t tiles, int64_t pairs, int64_t k_blocks, int widest)
+{
+    if (tiles < 1 || pairs < 1 || k_blocks < 1) return fail(UB_ERR_ARG, "ub_plan_tail_split: sizes must be >= 1");
+    return tail_split_for(tiles, pairs, k_blocks, widest != 0);
+}
+
+int ub_plan_path(int64_t single_tiles, int64_t pair_tiles, int64_t k_blocks, int64_t slots, int64_t pairs,
+                 int cta_pair, int streamk, int *pair, int *split)
+{
+    if (single_tiles < 1 || pair_tiles < 1 || k_blocks < 1 || slots < 1 || pairs < 1 || !pair || !split)
+        return fail(UB_ERR_ARG, "ub_plan_path: sizes must be >= 1 and outputs non-null");
+    bool pr = false, sp = false;
+    plan_path(slots, pairs, cta_pair, streamk, single_tiles, pair_tiles, k_blocks, pr, sp);
+    *pair = pr ? 1 : 0;
+    *split = sp ? 1 : 0;
+    return UB_OK;
+}
+
+int64_t ub_plan_ag_self_head(int64_t T, int tp, int self, int64_t n_tiles, int64_t pairs)
+{
+    if (tp < 1 || tp > UB_MAX_TP || T < tp || T % tp != 0 || self < 0 || self >= tp || n_tiles < 1 || pairs < 1)
+        return fail(UB_ERR_ARG, "ub_plan_ag_self_head: invalid shape");
+    return self_head_for(T, T / tp, self, n_tiles, pairs);
 }
 
 // AG-GEMM, optionally with the SwiGLU epilogue (glu_f > 0: Wt is [2 * glu_f, hidden],

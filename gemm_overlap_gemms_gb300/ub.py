@@ -37,7 +37,8 @@ EXPORTS = [
     "ub_buffer", "ag_gemm", "gemm_rs", "ub_set_option", "ub_get_option", "ub_query_status",
     "ub_clear_status", "ub_get_counters", "ub_kernel_time", "ub_grid_ctas", "ub_last_error",
     "ag_gemm_noalloc", "ag_gemm_swiglu", "ag_gemm_kn", "gemm_rs_kn", "ub_wgrad",
-    "ub_allgather", "ub_reduce_scatter",
+    "ub_allgather", "ub_reduce_scatter", "ub_plan_tail_split", "ub_plan_path",
+    "ub_plan_ag_self_head",
 ]
 NOALLOC_MAX_ELEMS = 16 * 1024 * 1024
 
@@ -96,17 +97,53 @@ def load():
         "ub_grid_ctas": [P, ctypes.POINTER(I)],
         "ub_last_error": [],
         "ag_gemm_noalloc": [PP, I, I64, I64, P, I64, P, P],
+        "ub_plan_tail_split": [I64, I64, I64, I],
+        "ub_plan_path": [I64, I64, I64, I64, I64, I, I, ctypes.POINTER(I), ctypes.POINTER(I)],
+        "ub_plan_ag_self_head": [I64, I, I, I64, I64],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
         fn.argtypes = args
-        fn.restype = ctypes.c_char_p if name == "ub_last_error" else ctypes.c_int
+        if name == "ub_last_error":
+            fn.restype = ctypes.c_char_p
+        elif name in ("ub_plan_tail_split", "ub_plan_ag_self_head"):
+            fn.restype = ctypes.c_int64
+        else:
+            fn.restype = ctypes.c_int
     _lib = L
     return L
 
 
 def last_error() -> str:
     return load().ub_last_error().decode(errors="replace")
+
+
+# ---------------------------------------------------------------- planning queries (host only)
+
+def _plan_check(v: int) -> int:
+    if v < 0:
+        _check(int(v))
+    return int(v)
+
+
+def plan_tail_split(tiles: int, pairs: int, k_blocks: int, widest: bool = False) -> int:
+    """k-pieces per tile of the CTA-pair kernel's last, partial wave (1: whole tiles)."""
+    return _plan_check(load().ub_plan_tail_split(tiles, pairs, k_blocks, 1 if widest else 0))
+
+
+def plan_path(single_tiles: int, pair_tiles: int, k_blocks: int, slots: int, pairs: int,
+              cta_pair: int = -1, streamk: int = -1) -> tuple:
+    """(pair, split) for a tile-kernel call: CTA pairs or single CTAs, split last wave."""
+    pr, sp = ctypes.c_int(0), ctypes.c_int(0)
+    rc = load().ub_plan_path(single_tiles, pair_tiles, k_blocks, slots, pairs, cta_pair, streamk,
+                             ctypes.byref(pr), ctypes.byref(sp))
+    _check(rc)
+    return bool(pr.value), bool(sp.value)
+
+
+def plan_ag_self_head(T: int, tp: int, self_rank: int, n_tiles: int, pairs: int) -> int:
+    """Rows of the self chunk the CTA-pair AG kernel reads in place."""
+    return _plan_check(load().ub_plan_ag_self_head(T, tp, self_rank, n_tiles, pairs))
 
 
 def _check(rc: int):

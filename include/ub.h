@@ -334,6 +334,37 @@ int ub_grid_ctas(ub_handle_t h, int *ctas);
 int ag_gemm_noalloc(const void *const *shards, int tp, int64_t T, int64_t hidden, const void *Wt,
                     int64_t N, void *Y, void *stream);
 
+/*
+ * Planning queries: the launch choices the library makes for a call, as pure functions
+ * of the shapes and the GPU's unit counts -- no handle, no device, no CUDA call. Tools
+ * use them to predict a call's launch; they are the same code the calls run.
+ *
+ * ub_plan_tail_split: into how many k-pieces the CTA-pair kernel cuts each tile of the
+ * last, partial wave. `tiles` 256 x 256 output tiles over `pairs` CTA pairs, `k_blocks`
+ * 64-wide k-blocks per tile (GEMM-RS: over all tp shards). At most one piece per idle
+ * pair, 8 pieces and 16 k-blocks per piece; within that, widest != 0 (the split forced
+ * on, UB_OPT_STREAMK = 1) gives the most pieces, else the cheapest cut by the fix-up
+ * cost model (the longest piece plus a fixed fix-up time per added piece, fitted on
+ * GB300). Returns the piece count (1 = whole tiles), or UB_ERR_ARG for sizes < 1.
+ *
+ * ub_plan_path: whether a tile-kernel call runs on CTA pairs (*pair = 1) or single CTAs
+ * (*pair = 0), and whether the pairs split the last wave (*split). `single_tiles`
+ * 128 x 256 tiles over `slots` SMs against `pair_tiles` 256 x 256 tiles over `pairs`
+ * pairs; `cta_pair` and `streamk` as UB_OPT_CTA_PAIR and UB_OPT_STREAMK (-1: chosen by
+ * the wave-count cost model; 0 / 1: forced). Returns UB_OK, or UB_ERR_ARG for sizes < 1
+ * or null outputs.
+ *
+ * ub_plan_ag_self_head: how many rows of the self chunk the CTA-pair AG kernel reads in
+ * place from its shard (the rest from the user buffer, behind the chunk's readiness
+ * flag): all c = T / tp rows, or only its whole 256-row tiles where that saves a wave of
+ * `pairs` pairs over `n_tiles` N tiles (self: the ring's start rank). Returns the row
+ * count, or UB_ERR_ARG for an invalid shape.
+ */
+int64_t ub_plan_tail_split(int64_t tiles, int64_t pairs, int64_t k_blocks, int widest);
+int ub_plan_path(int64_t single_tiles, int64_t pair_tiles, int64_t k_blocks, int64_t slots, int64_t pairs,
+                 int cta_pair, int streamk, int *pair, int *split);
+int64_t ub_plan_ag_self_head(int64_t T, int tp, int self, int64_t n_tiles, int64_t pairs);
+
 /* Message of the last failed call on this host thread ("" if none). */
 const char *ub_last_error(void);
 

@@ -1,0 +1,130 @@
+"""The launch planner through the C ABI's planning queries (host only, no GPU): the
+split-tail piece count, the CTA-pair / single-CTA choice and the self-chunk split of the
+CTA-pair AG tiling. The calls run this same code to pick their launch."""
+import math
+
+import pytest
+
+from gemm_overlap_gemms_gb300 import _build, ub
+
+PAIRS, SLOTS = 76, 152          # GB300: 152 SMs, 76 CTA pairs
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    _build.build()
+    return ub.load()
+
+
+def _allowed(tiles, pairs, kb):
+    rem = tiles % pairs
+    if rem == 0:
+        return 1
+    return max(1, min(pairs // rem, 8, kb // 16))
+
+
+@pytest.mark.parametrize("pairs", [1, 3, 37, 76])
+@pytest.mark.parametrize("kb", [1, 15, 16, 40, 64, 128, 224, 448, 1000])
+def test_tail_split_stays_within_its_limits(pairs, kb):
+    for tiles in range(1, 3 * pairs + 2):
+        s = ub.plan_tail_split(tiles, pairs, kb)
+        w = ub.plan_tail_split(tiles, pairs, kb, widest=True)
+        rem = tiles % pairs
+        assert 1 <= s <= w == _allowed(tiles, pairs, kb), (tiles, pairs, kb, s, w)
+        if rem == 0:
+            assert s == 1                       # whole waves: nothing to share
+        if s > 1:
+            assert rem * s <= pairs             # one piece per idle pair at most
+            assert kb // s >= 16                # pieces of at least 16 k-blocks
+
+
+def test_tail_split_grows_with_k():
+    """The fix-up is a fixed time per added piece, so longer tiles afford more pieces."""
+    for tiles in (80, 96, 112, 256, 300, 384):
+        prev = 1
+        for kb in (16, 32, 64, 96, 128, 224, 448, 896):
+            s = ub.plan_tail_split(tiles, PAIRS, kb)
+            assert s >= prev, (tiles, kb, s, prev)
+            prev = s
+
+
+@pytest.mark.parametrize("what,tiles,kb,split", [
+    # measured on GB300, whole tiles against a split last wave (bench.py --case ... --streamk 0|1)
+    ("QKV AG T=2048: 46.2 us whole, 55.0 split in 3", 96, 64, False),
+    ("SwiGLU fc1 AG T=1024: 52.8 us whole, 55.9 split in 2", 112, 64, False),
+    ("SwiGLU fc1 AG T=512: 47.0 us whole, 51.8 split in 2", 112, 64, False),
+    ("SwiGLU fc2 RS T=512: 72.3 us whole, 52.0 split in 2", 32, 224, True),
+    ("SwiGLU fc2 RS T=1536: 140.7 us whole, 114.1 split in 3", 96, 224, True),
+    ("SwiGLU fc2 RS T=4096: 292.0 us whole, 272.9 split in 2", 256, 224, True),
+    ("large RS K=3584 T=2048: 601.6 us whole, 561.3 split in 2", 256, 448, True),
+])
+def test_tail_split_follows_the_measured_winner(what, tiles, kb, split):
+    assert (ub.plan_tail_split(tiles, PAIRS, kb) > 1) == split, what
+
+
+def test_plan_path_respects_forced_options():
+    for single, pair_tiles, kb in [(96, 48, 64), (192, 96, 64), (1024, 512, 224), (7, 4, 8)]:
+        assert ub.plan_path(single, pair_tiles, kb, SLOTS, PAIRS, cta_pair=0) == (False, False)
+        assert ub.plan_path(single, pair_tiles, kb, SLOTS, PAIRS, cta_pair=1, streamk=0) == (True, False)
+        assert ub.plan_path(single, pair_tiles, kb, SLOTS, PAIRS, cta_pair=1, streamk=1) == (True, True)
+
+
+def test_plan_path_cost_model_choices():
+    # whole waves of pair tiles: pairs, no split (nothing left to share)
+    assert ub.plan_path(2 * 2 * PAIRS, 2 * PAIRS, 224, SLOTS, PAIRS) == (True, False)
+    # the SwiGLU fc2 RS at T = 4096 (256 pair tiles, 224 k-blocks): pairs, last wave split
+    assert ub.plan_path(512, 256, 224, SLOTS, PAIRS) == (True, True)
+    # QKV AG at T = 2048 (96 pair tiles, 64 k-blocks): pairs, whole tiles
+    assert ub.plan_path(192, 96, 64, SLOTS, PAIRS) == (True, False)
+    # one wave either way: pairs (a third less L2 traffic per tile)
+    assert ub.plan_path(8, 4, 2, SLOTS, PAIRS) == (True, False)
+    # AG at T = 512 (N = 7168): 112 chunk-aligned single tiles in one wave against 84
+    # pair tiles in two, too short to split (64 k-blocks): single CTAs
+    assert ub.plan_path(112, 84, 64, SLOTS, PAIRS) == (False, False)
+
+
+def _row_tiles(T, c, self_rank, head):
+    parts = [head, T - self_rank * c - head, self_rank * c]
+    return sum(math.ceil(r / 256) for r in parts if r > 0)
+
+
+@pytest.mark.parametrize("tp", [1, 2, 4, 8])
+@pytest.mark.parametrize("n_tiles", [12, 28])
+def test_self_head_split_only_when_it_saves_a_wave(tp, n_tiles):
+    for T in list(range(tp * 8, 8193, tp * 52)) + [1140, 1316, 2280, 2956, 8192]:
+        T -= T % tp
+        c = T // tp
+        for self_rank in sorted({0, tp - 1, tp // 2}):
+            head = ub.plan_ag_self_head(T, tp, self_rank, n_tiles, PAIRS)
+            whole = c // 256 * 256
+            assert head in (c, whole), (T, tp, self_rank, head)
+            waves = lambda h: math.ceil(_row_tiles(T, c, self_rank, h) * n_tiles / PAIRS)
+            if head != c:
+                assert waves(head) < waves(c), (T, tp, self_rank)
+            elif whole != c:
+                assert waves(whole) >= waves(c), (T, tp, self_rank)
+
+
+def test_self_head_cases():
+    # AG + SwiGLU at T = 1140 (28 N tiles): 140 tiles in two waves instead of 168 in three
+    assert ub.plan_ag_self_head(1140, 4, 0, 28, PAIRS) == 256
+    # QKV at T = 1140 (12 N tiles): one wave either way, the self chunk stays in place
+    assert ub.plan_ag_self_head(1140, 4, 0, 12, PAIRS) == 285
+    # 256 divides c: nothing to split
+    assert ub.plan_ag_self_head(8192, 4, 0, 28, PAIRS) == 2048
+
+
+@pytest.mark.parametrize("call", [
+    lambda: ub.plan_tail_split(0, PAIRS, 64),
+    lambda: ub.plan_tail_split(10, 0, 64),
+    lambda: ub.plan_tail_split(10, PAIRS, 0),
+    lambda: ub.plan_path(0, 1, 1, SLOTS, PAIRS),
+    lambda: ub.plan_path(1, 1, 1, 0, PAIRS),
+    lambda: ub.plan_ag_self_head(1142, 4, 0, 28, PAIRS),     # T % tp != 0
+    lambda: ub.plan_ag_self_head(1140, 4, 4, 28, PAIRS),     # self outside the ring
+    lambda: ub.plan_ag_self_head(1140, 9, 0, 28, PAIRS),     # tp above the maximum
+])
+def test_planning_queries_reject_bad_arguments(call):
+    with pytest.raises(ub.UbError) as ei:
+        call()
+    assert ei.value.name == "UB_ERR_ARG"
