@@ -297,23 +297,38 @@ def time_steps(fn, steps, warmup, stream, world):
     return e0.elapsed_time(e1)  # ms
 
 
-def time_calls(fn, calls, warmup, stream):
-    """Median and mean of `calls` individually timed calls (CUDA events on `stream`
-    around each call), after `warmup` untimed ones. Returns (median ms, mean ms)."""
-    for _ in range(warmup):
-        fn()
+def time_calls(fn, calls, warmup, stream, graph=True):
+    """Time one call, `fn(st)` issuing it on stream `st`. Returns (median ms, mean ms,
+    eager ms): with `graph`, the call is captured once into a CUDA graph and replayed
+    `calls` times on `stream`, each replay between CUDA events, after `warmup` replays --
+    what the call costs the GPU, with no host work (argument marshalling, launch calls)
+    between calls to starve it; eager = `calls` calls issued back to back from Python,
+    events at both ends only (a host slower than the GPU shows up here). Without
+    `graph`, median and mean are None."""
+    fn(stream)
     torch.cuda.synchronize()
+    eager = time_steps(lambda: fn(stream), calls, 3, stream, 1) / calls
+    if not graph:
+        return None, None, eager
+    cap = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cap):
+        fn(cap)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(calls + 1)]
-    ev[0].record(stream)
-    for i in range(calls):
-        fn()
-        ev[i + 1].record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            g.replay()
+        ev[0].record(stream)
+        for i in range(calls):
+            g.replay()
+            ev[i + 1].record(stream)
     torch.cuda.synchronize()
     ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(calls)]
-    return float(np.median(ms)), float(np.mean(ms))
+    del g
+    return float(np.median(ms)), float(np.mean(ms)), eager
 
 
-SWEEP_CALLS, SWEEP_WARMUP = 50, 10   # per point: median of 50 timed calls after 10 warm-ups
+SWEEP_CALLS, SWEEP_WARMUP = 50, 10   # per point: median of 50 timed graph replays after 10 warm-ups
 
 
 def e2e_measure(wl, steps, warmup, stream, world):
@@ -642,18 +657,21 @@ def sweep_points(wl, stream):
         wl.buf.set_active_shape([T, H])
         for op in ("ag", "ag_swiglu", "ag_swiglu_no_overlap", "rs"):
             if op == "ag":
-                fn = lambda: wl.buf.ag_gemm(shards, wl.W1, wl.Y1, stream=stream)
+                fn = lambda st: wl.buf.ag_gemm(shards, wl.W1, wl.Y1, stream=st)
             elif op.startswith("ag_swiglu"):
-                fn = lambda: wl.buf.ag_gemm_swiglu(shards, wl.W1, wl.Yz, stream=stream)
+                fn = lambda st: wl.buf.ag_gemm_swiglu(shards, wl.W1, wl.Yz, stream=st)
             else:
-                fn = lambda: wl.buf.gemm_rs(A, wl.B, outs, stream=stream)
-            # the no-overlap comparator puts the gather copies on the GEMM's stream, ahead of it
+                fn = lambda st: wl.buf.gemm_rs(A, wl.B, outs, stream=st)
+            # the no-overlap comparator puts the gather copies on the GEMM's stream, ahead
+            # of it (driver copies and stream flag writes: timed eagerly, no graph)
             no_overlap = op == "ag_swiglu_no_overlap"
             wl.buf.set_option("copy_streams", 0 if no_overlap else 4)
             wl.buf.set_option("gather_kernel", 0 if no_overlap else -1)
-            ms, ms_mean = time_calls(fn, SWEEP_CALLS, SWEEP_WARMUP, stream)
+            ms, ms_mean, eager = time_calls(fn, SWEEP_CALLS, SWEEP_WARMUP, stream, graph=not no_overlap)
             wl.buf.set_option("copy_streams", 4)
             wl.buf.set_option("gather_kernel", -1)
+            if ms is None:
+                ms = eager
             fl = 2.0 * T * H * N if op != "rs" else 2.0 * T * K * H * tp
             tf = fl / (ms / 1e3) / 1e12
             # algorithmic HBM bytes: weights once, activations in, results out (AG: the
@@ -663,8 +681,10 @@ def sweep_points(wl, stream):
             else:
                 n_out = N // 2 if op.startswith("ag_swiglu") else N
                 nbytes = 2.0 * (N * H + 2 * T * H + T * n_out)
-            out.append({"sweep": op, "T": T, "us": ms * 1e3, "us_mean": ms_mean * 1e3, "tflops": tf,
-                        "frac_of_peak": tf / tensor_peak,
+            out.append({"sweep": op, "T": T, "us": ms * 1e3,
+                        "us_mean": ms_mean * 1e3 if ms_mean is not None else None,
+                        "us_eager": eager * 1e3, "timing": "eager" if no_overlap else "graph replay",
+                        "tflops": tf, "frac_of_peak": tf / tensor_peak,
                         "hbm_gbs": nbytes / (ms / 1e3) / 1e9, "hbm_frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak,
                         "note": ("gather copies on the GEMM's stream, before it (no overlap)"
                                  if op == "ag_swiglu_no_overlap" else
@@ -675,7 +695,7 @@ def sweep_points(wl, stream):
 def sweep_other_configs(stream):
     """The other throughput configs on their own handles: QKV (AG-GEMM, N = 3072, tp 4,
     hidden 4096) and large (GEMM-RS, tp 8, hidden 8192, attention-out K = 1024 and fc2
-    K = 3584 per shard), over a ladder of active T (median of 50 timed calls per point)."""
+    K = 3584 per shard), over a ladder of active T (median of 50 graph replays per point)."""
     from gemm_overlap_gemms_gb300 import ub
     pk, _ = peaks()
     tensor_peak = _peak_value(pk, "bf16_tflops_sustained", "bf16_tflops") or FALLBACK["bf16_tflops_sustained"]
@@ -685,10 +705,10 @@ def sweep_other_configs(stream):
     out = []
 
     def point(name, T, fn, fl, nbytes):
-        ms, ms_mean = time_calls(fn, SWEEP_CALLS, SWEEP_WARMUP, stream)
+        ms, ms_mean, eager = time_calls(fn, SWEEP_CALLS, SWEEP_WARMUP, stream)
         tf = fl / (ms / 1e3) / 1e12
-        out.append({"sweep": name, "T": T, "us": ms * 1e3, "us_mean": ms_mean * 1e3, "tflops": tf,
-                    "frac_of_peak": tf / tensor_peak,
+        out.append({"sweep": name, "T": T, "us": ms * 1e3, "us_mean": ms_mean * 1e3, "us_eager": eager * 1e3,
+                    "timing": "graph replay", "tflops": tf, "frac_of_peak": tf / tensor_peak,
                     "hbm_gbs": nbytes / (ms / 1e3) / 1e9, "hbm_frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak,
                     "note": "includes the gather" if name.startswith("qkv") else ""})
 
@@ -702,7 +722,7 @@ def sweep_other_configs(stream):
         c = T // tp
         buf.set_active_shape([T, H])
         shards = [X[r * c:(r + 1) * c] for r in range(tp)]
-        point("qkv_ag", T, lambda: buf.ag_gemm(shards, Wq, Y[:T], stream=stream), 2.0 * T * H * N,
+        point("qkv_ag", T, lambda st: buf.ag_gemm(shards, Wq, Y[:T], stream=st), 2.0 * T * H * N,
               2.0 * (N * H + 2 * T * H + T * N))
     buf.close()
     del Wq, X, Y
@@ -719,7 +739,7 @@ def sweep_other_configs(stream):
             buf.set_active_shape([T, H])
             a_T = [a[:T] for a in A]
             outs = [Yl[r * c:(r + 1) * c] for r in range(tp)]
-            point("large_rs_k%d" % K, T, lambda: buf.gemm_rs(a_T, B, outs, stream=stream), 2.0 * T * K * H * tp,
+            point("large_rs_k%d" % K, T, lambda st: buf.gemm_rs(a_T, B, outs, stream=st), 2.0 * T * K * H * tp,
                   2.0 * (tp * K * H + tp * T * K + T * H))
         del A, B
     buf.close()
