@@ -94,7 +94,7 @@ def parse():
     ap.add_argument("--skinny", type=int, default=-1, choices=[-1, 0, 1],
                     help="few-token kernel: -1 whenever usable (default), 0 never, 1 whenever usable")
     ap.add_argument("--streamk", type=int, default=-1, choices=[-1, 0, 1],
-                    help="-1: chosen per call (default); 1: stream-K over all pairs; 0: whole tiles")
+                    help="-1: chosen per call (default); 1: the last wave of pair tiles cut into k-pieces; 0: whole tiles")
     return ap.parse_args()
 
 

@@ -131,7 +131,7 @@ struct ub_handle {
     int tp = 1;
     int64_t T = 0;  // active tokens
     void *ub = nullptr;      // [max_tokens, hidden] bf16
-    uint32_t *ctrl = nullptr;  // flags[UB_MAX_TP] | abort | status | ... | stream-K flags (from word 64)
+    uint32_t *ctrl = nullptr;  // flags[UB_MAX_TP] | abort | status | ... | partial-tile flags (from word 64)
     size_t ctrl_bytes = 0;
     float *ws = nullptr;       // partial tiles of split work: ws_slots x PARTIAL_FLOATS fp32
     int ws_slots = 0;          // 2 per SM: pair kernel (pair, rank) slots, skinny-kernel pieces

@@ -83,7 +83,7 @@ struct GemmParams {
     int self_head;               // AG: rows of the self chunk read in place (the CTA-pair
                                  // kernel reads the rest from the buffer); c elsewhere
 
-    // ---- CTA-pair kernel only: row regions and the stream-K split.
+    // ---- CTA-pair kernel only: row regions and the split last wave.
     // The pair kernel tiles rows by region instead of by chunk. RS has one region,
     // [0, T): its tiles may span chunks, and the epilogue splits stores at chunk ends.
     // AG has one region per source of A rows, in ring order: the self chunk (read in

@@ -140,9 +140,9 @@ def test_active_shape_equals_exact_allocation_bitwise():
 
 def test_deterministic_and_consistent_across_launch_shapes():
     """Bitwise run-to-run determinism for a fixed launch shape; the same values (within
-    tolerance of the oracle) for every ring start, SM margin and tile shape. Stream-K
-    splits depend on the number of CTA pairs, so different launch shapes may round
-    differently."""
+    tolerance of the oracle) for every ring start, SM margin and tile shape. The k-pieces
+    of a split last wave depend on the number of CTA pairs, so different launch shapes
+    may round differently."""
     tp, H, N, K = 4, 256, 512, 256
     T = 4 * 260
     g = synth.generator(seed=15)
