@@ -89,6 +89,10 @@ def parse():
     ap.add_argument("--cta-pair", type=int, default=-1, choices=[-1, 0, 1],
                     help="-1: chosen per call (default); 1: 256x256 tiles on CTA pairs; 0: single CTAs")
     ap.add_argument("--copy-streams", type=int, default=4)
+    ap.add_argument("--gather-ahead", type=int, default=0, choices=[0, 1],
+                    help="1: each microbatch's all-gather runs on a second stream beside the previous "
+                         "microbatch's GEMM-RS, and its fc1 runs on the gathered buffer "
+                         "(ag_gemm_from_buffer); 0: fc1 gathers inside its own call (default)")
     ap.add_argument("--pdl", type=int, default=1, choices=[0, 1],
                     help="1: kernels launched with programmatic dependent launch (default); 0: plain")
     ap.add_argument("--skinny", type=int, default=-1, choices=[-1, 0, 1],
@@ -276,8 +280,39 @@ class SwigluWorkload:
         self.buf.gemm_rs(self.A[i], self.B, self.out_shards(i), stream=stream)
 
     def step(self, stream):
+        if GATHER_AHEAD:
+            self.step_gather_ahead(stream)
+            return
         for i in range(len(self.Ts)):
             self.run_mb(i, stream)
+
+    def step_gather_ahead(self, stream):
+        """The same microbatches with each all-gather moved off fc1's critical path: it
+        runs on a second stream once the previous fc1 has read the buffer, beside the
+        previous microbatch's GEMM-RS, and fc1 then reads the gathered buffer."""
+        if not hasattr(self, "side"):
+            self.side = torch.cuda.Stream(stream.device)
+            self.ev_read = [torch.cuda.Event() for _ in self.Ts]
+            self.ev_landed = [torch.cuda.Event() for _ in self.Ts]
+        H, n = self.w.hidden, len(self.Ts)
+        self.buf.set_active_shape([self.Ts[0], H])
+        self.buf.allgather(self.shards(0), stream=stream)
+        for i in range(n):
+            self.buf.set_active_shape([self.Ts[i], H])
+            if i > 0:
+                stream.wait_event(self.ev_landed[i])
+            if MLP == "fused":
+                self.buf.ag_gemm_from_buffer(self.W1, self.A[i][0], swiglu=True, stream=stream)
+            else:
+                self.buf.ag_gemm_from_buffer(self.W1, self.Y1, stream=stream)
+            self.ev_read[i].record(stream)
+            if i + 1 < n:
+                self.buf.set_active_shape([self.Ts[i + 1], H])
+                self.side.wait_event(self.ev_read[i])
+                self.buf.allgather(self.shards(i + 1), stream=self.side)
+                self.ev_landed[i + 1].record(self.side)
+                self.buf.set_active_shape([self.Ts[i], H])
+            self.buf.gemm_rs(self.A[i], self.B, self.out_shards(i), stream=stream)
 
 
 def time_steps(fn, steps, warmup, stream, world):
@@ -607,6 +642,8 @@ def run_ours(args):
                                "fc1 AG-GEMM N=7168 + fc2 GEMM-RS K=3584",
                    "mlp": ("fc1 with fused SwiGLU epilogue writes virtual rank 0's fc2 input"
                            if MLP == "fused" else "fc1 output [T, 7168] unfused"),
+                   "gather": ("each all-gather beside the previous microbatch's GEMM-RS, fc1 on the "
+                              "gathered buffer" if GATHER_AHEAD else "inside each fc1 AG-GEMM call"),
                    "tp": w.tp, "hidden": w.hidden, "max_tokens": w.max_tokens,
                    "microbatches": len(wl.Ts), "tokens_per_step": int(sum(wl.Ts)),
                    "parallelism": "replicas" if world > 1 else "single GPU",
@@ -952,11 +989,13 @@ CTA_PAIR = -1
 STREAMK = -1
 PDL = 1
 MLP = "fused"
+GATHER_AHEAD = 0
 
 
 def main():
-    global CTA_PAIR, STREAMK, PDL, MLP
+    global CTA_PAIR, STREAMK, PDL, MLP, GATHER_AHEAD
     args = parse()
+    GATHER_AHEAD = args.gather_ahead
     CTA_PAIR = args.cta_pair
     STREAMK = args.streamk
     PDL = args.pdl

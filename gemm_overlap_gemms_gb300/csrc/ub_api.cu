@@ -1241,6 +1241,68 @@ int ub_wgrad(ub_handle_t h, const void *D, int64_t M, int ub_is_a, void *out, vo
     return UB_OK;
 }
 
+int ag_gemm_from_buffer(ub_handle_t h, const void *Wt, int64_t N, int64_t glu_f, void *Y, void *stream)
+{
+    if (int rc = check_handle(h)) return rc;
+    if (!Wt || !Y) return fail(UB_ERR_ARG, "ag_gemm_from_buffer: null pointer argument");
+    if (N <= 0) return fail(UB_ERR_ZERO, "ag_gemm_from_buffer: N = %lld", (long long)N);
+    if (N % 8 != 0) return fail(UB_ERR_ALIGN, "ag_gemm_from_buffer: N = %lld is not a multiple of 8", (long long)N);
+    if (glu_f < 0 || (glu_f > 0 && (N != 2 * glu_f || glu_f % 8 != 0)))
+        return fail(UB_ERR_ARG, "ag_gemm_from_buffer: SwiGLU needs N = 2 * F with F a multiple of 8");
+    if (N > (int64_t(1) << 24)) return fail(UB_ERR_ARG, "ag_gemm_from_buffer: N = %lld too large", (long long)N);
+    if (!aligned16(Wt) || !aligned16(Y)) return fail(UB_ERR_ALIGN, "ag_gemm_from_buffer: Wt / Y not 16-byte aligned");
+    DeviceGuard g(h->device);
+    if (!g.ok) return fail(UB_ERR_CUDA, "ag_gemm_from_buffer: cannot select the handle's device");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t T = h->T, H = h->hidden;
+    const bool glu = glu_f > 0;
+    const int mode = glu ? ubk::MODE_AG_GLU : ubk::MODE_AG;
+    const int64_t n_out = glu ? glu_f : N;
+    std::vector<const void *> key = {reinterpret_cast<const void *>(uintptr_t(200 + (glu ? 1 : 0))),
+                                     reinterpret_cast<const void *>(uintptr_t(T)),
+                                     reinterpret_cast<const void *>(uintptr_t(N)), Wt, Y};
+    GemmParams *pp = cache_lookup(h, key);
+    if (!pp) {
+        GemmParams p;
+        memset(&p, 0, sizeof p);
+        // One region: all T rows of the buffer, no readiness flags (already gathered).
+        if (int rc = encode_2d(&p.tmA[0], h->ub, H, T, H * 2, ubk::BK, 128)) return rc;
+        if (int rc = encode_2d(&p.tmB[0], Wt, H, N, H * 2, ubk::BK, ubk::BN / 2)) return rc;
+        if (int rc = encode_2d(&p.tmY[0], Y, n_out, T, n_out * 2, ubk::STORE_COLS, 32)) return rc;
+        h->counters.tensor_map_encodes += 3;
+        p.tp = h->tp;
+        p.c = static_cast<int>(T / h->tp);
+        p.n_out = static_cast<int>(n_out);
+        p.glu_f = static_cast<int>(glu_f);
+        p.k_blocks = static_cast<int>((H + ubk::BK - 1) / ubk::BK);
+        p.k_blocks_per_shard = p.k_blocks;
+        p.n_tiles = static_cast<int>(glu ? (glu_f + 127) / 128 : (N + ubk::BN - 1) / ubk::BN);
+        p.self_head = static_cast<int>(T / h->tp);
+        p.n_regions = 1;
+        p.region_row0[0] = 0;
+        p.region_rows[0] = static_cast<int>(T);
+        p.region_ub[0] = 0;
+        p.region_tile0[1] = static_cast<int>((T + ubk::PAIR_BM - 1) / ubk::PAIR_BM) * p.n_tiles;
+        pp = cache_insert(h, std::move(key), p);
+    }
+    GemmParams &p = *pp;
+    p.flags = flags_of(h);
+    p.abort_word = abort_of(h);
+    p.status = status_of(h);
+    p.timeout_ns = static_cast<uint64_t>(h->timeout_ns);
+    bool pair = true, split = false;
+    choose_path(h, mode, 1 << 30, p.region_tile0[1], p.k_blocks, pair, split);
+    set_pairs(h, p, mode, split);
+    uint32_t epoch = 0;
+    if (int rc = begin_call(h, s, epoch)) return rc;
+    p.epoch = epoch;
+    p.fused_gather = 0;
+    if (int rc = launch(h, p, mode, PATH_PAIR, s, glu ? UB_OP_AG_SWIGLU : UB_OP_AG)) return rc;
+    ++h->counters.ag_calls;
+    h->counters.last_T = T;
+    return UB_OK;
+}
+
 int ub_set_option(ub_handle_t h, int key, int64_t val)
 {
     if (int rc = check_handle(h)) return rc;

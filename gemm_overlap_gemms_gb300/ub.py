@@ -38,7 +38,7 @@ EXPORTS = [
     "ub_clear_status", "ub_get_counters", "ub_kernel_time", "ub_grid_ctas", "ub_last_error",
     "ag_gemm_noalloc", "ag_gemm_swiglu", "ag_gemm_kn", "gemm_rs_kn", "ub_wgrad",
     "ub_allgather", "ub_reduce_scatter", "ub_plan_tail_split", "ub_plan_path",
-    "ub_plan_ag_self_head",
+    "ub_plan_ag_self_head", "ag_gemm_from_buffer",
 ]
 NOALLOC_MAX_ELEMS = 16 * 1024 * 1024
 
@@ -97,6 +97,7 @@ def load():
         "ub_grid_ctas": [P, ctypes.POINTER(I)],
         "ub_last_error": [],
         "ag_gemm_noalloc": [PP, I, I64, I64, P, I64, P, P],
+        "ag_gemm_from_buffer": [P, P, I64, I64, P, P],
         "ub_plan_tail_split": [I64, I64, I64, I],
         "ub_plan_path": [I64, I64, I64, I64, I64, I, I, ctypes.POINTER(I), ctypes.POINTER(I)],
         "ub_plan_ag_self_head": [I64, I, I, I64, I64],
@@ -393,6 +394,27 @@ class UserBuffer:
         _check(load().ub_wgrad(self._h, ctypes.c_void_p(D.data_ptr()), M, int(bool(ub_is_a)),
                                ctypes.c_void_p(out.data_ptr()), _stream_ptr(stream)))
         return out
+
+    def ag_gemm_from_buffer(self, Wt: torch.Tensor, Y: torch.Tensor | None = None, swiglu: bool = False,
+                            stream=None):
+        """Y[T, N] = UB[:T] @ Wt.T over the buffer as it stands (no gather, no flag wait);
+        with swiglu, Wt is [2F, hidden] (gate rows first) and Y[T, F] = silu(gate) * up.
+        The buffer must already hold the chunks: an allgather() of this active shape on
+        this handle, ordered before this call (same stream, or an event)."""
+        T, H = self.active_shape
+        _bf16_cuda(Wt, "Wt")
+        if Wt.dim() != 2 or Wt.shape[1] != H or (swiglu and Wt.shape[0] % 2):
+            raise ValueError("Wt must be [%s, %d], got %s" % ("2F" if swiglu else "N", H, tuple(Wt.shape)))
+        N = Wt.shape[0]
+        n_out = N // 2 if swiglu else N
+        if Y is None:
+            Y = torch.empty((T, n_out), dtype=torch.bfloat16, device=Wt.device)
+        _bf16_cuda(Y, "Y")
+        if Y.dim() != 2 or Y.shape[0] < T or Y.shape[1] != n_out:
+            raise ValueError("Y must be [>=%d, %d], got %s" % (T, n_out, tuple(Y.shape)))
+        _check(load().ag_gemm_from_buffer(self._h, ctypes.c_void_p(Wt.data_ptr()), N, n_out if swiglu else 0,
+                                          ctypes.c_void_p(Y.data_ptr()), _stream_ptr(stream)))
+        return Y
 
     def allgather(self, shards, stream=None):
         """Bulk all-gather: UB[r*c + i] = shards[r][i] for the active shape, no GEMM."""

@@ -270,6 +270,23 @@ int ub_wgrad(ub_handle_t h, const void *D, int64_t M, int ub_is_a, void *out, vo
 int ub_allgather(ub_handle_t h, const void *const *shards, void *stream);
 int ub_reduce_scatter(ub_handle_t h, const void *const *P, void *const *Y_shards, void *stream);
 
+/*
+ * AG-GEMM over the user buffer as it stands: Y[t, :] = UB[t, :] . Wt^T for t < T (the
+ * active shape), with no gather and no readiness-flag wait -- for a caller that landed
+ * the chunks ahead of time with ub_allgather on this handle, for the same active shape
+ * and shards, and ordered that call before this one (same stream, or an event), e.g.
+ * the next microbatch's all-gather run beside the current GEMM-RS (the pages' "bulk"
+ * overlap feeding the column-parallel GEMM). Nothing checks that the buffer holds the
+ * chunks: an unordered or missing gather gives undefined results.
+ *  - Wt: device [N, hidden] (out x in); Y: device [T, N] (rows >= T untouched).
+ *  - glu_f > 0: the SwiGLU epilogue of ag_gemm_swiglu: N = 2 * glu_f (gate rows first),
+ *    Y is [T, glu_f]; 0: plain.
+ *  - Runs on CTA pairs, all T rows as one region (ceil(T / 256) row tiles).
+ *  - Errors: UB_ERR_ARG (null pointers, bad glu_f), UB_ERR_ZERO, UB_ERR_ALIGN (N or glu_f
+ *    not a multiple of 8, pointers not 16-byte aligned), UB_ERR_CUDA.
+ */
+int ag_gemm_from_buffer(ub_handle_t h, const void *Wt, int64_t N, int64_t glu_f, void *Y, void *stream);
+
 /* Options (UB_OPT_*). UB_ERR_ARG for an unknown key or an out-of-range value. */
 int ub_set_option(ub_handle_t h, int key, int64_t val);
 int ub_get_option(ub_handle_t h, int key, int64_t *val);

@@ -106,3 +106,81 @@ def test_bulk_collectives_beside_gemms_on_other_streams():
     Yref = oracle.reduce_scatter([_u16(x) for x in P])
     for r in range(tp):
         assert_close(Ys[r], Yref[r], "bulk RS block %d" % r)
+
+
+# ---------------------------------------------------------------- gather ahead, GEMM from the buffer
+
+@pytest.mark.parametrize("swiglu", [False, True])
+@pytest.mark.parametrize("T", [4 * 300, 4 * 64, 2048])
+def test_ag_gemm_from_buffer_after_allgather(T, swiglu):
+    """ub_allgather lands the chunks; ag_gemm_from_buffer then computes the AG-GEMM (or
+    AG + SwiGLU) over the buffer as it stands: the same values as the oracle."""
+    tp, H, N = 4, 1024, 896
+    g = synth.generator(seed=141)
+    shards, Wt = synth.ag_inputs(T, H, N, tp, g)
+    Gref = np.concatenate([synth.to_u16(s) for s in shards])
+    with ub.UserBuffer([T + 64, H], tp) as buf:
+        buf.set_active_shape([T, H])
+        buf.allgather([s.to(dev()) for s in shards])
+        n_out = N // 2 if swiglu else N
+        Y = sentinel((T + 5, n_out))
+        buf.ag_gemm_from_buffer(Wt.to(dev()), Y[:T], swiglu=swiglu)
+        torch.cuda.synchronize()
+        assert buf.query_status() == ub.UB_OK
+        np.testing.assert_array_equal(synth.to_u16(buf.buffer()[:T]), Gref)
+    ref = oracle.gemm_rows(Gref, synth.to_u16(Wt), np.arange(T))
+    if swiglu:
+        ref = oracle.swiglu(ref)
+    assert_close(Y[:T], ref, "from buffer T=%d swiglu=%s" % (T, swiglu))
+    assert is_sentinel(Y[T:]), "rows past T touched"
+
+
+def test_gather_ahead_pipeline_matches_the_oracle():
+    """Three microbatches of different T: each all-gather on a second stream once the
+    previous fc1 has read the buffer, beside the previous GEMM-RS; fc1 (AG + SwiGLU) on
+    the gathered buffer, fc2 GEMM-RS on the main stream. Every output against the oracle
+    on sampled rows."""
+    tp, H, F, K = 4, 1024, 256, 512
+    Ts = [4 * 260, 4 * 96, 4 * 400]
+    g = synth.generator(dev(), seed=142)
+    W1 = synth.normal_bf16((2 * F, H), H ** -0.5, g, dev())
+    Bt = [synth.normal_bf16((H, K), K ** -0.5, g, dev()) for _ in range(tp)]
+    X = [synth.normal_bf16((T, H), 1.0, g, dev()) for T in Ts]
+    A = [[synth.normal_bf16((T, K), 1.0, g, dev()) for _ in range(tp)] for T in Ts]
+    Z = [torch.empty((T, F), dtype=torch.bfloat16, device=dev()) for T in Ts]
+    R = [torch.empty((T, H), dtype=torch.bfloat16, device=dev()) for T in Ts]
+    main, side = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_read = [torch.cuda.Event() for _ in Ts]
+    ev_landed = [torch.cuda.Event() for _ in Ts]
+
+    def shards(i):
+        c = Ts[i] // tp
+        return [X[i][r * c:(r + 1) * c] for r in range(tp)]
+
+    with ub.UserBuffer([max(Ts), H], tp) as buf:
+        buf.set_active_shape([Ts[0], H])
+        buf.allgather(shards(0), stream=main)
+        for i, T in enumerate(Ts):
+            buf.set_active_shape([T, H])
+            if i > 0:
+                main.wait_event(ev_landed[i])
+            buf.ag_gemm_from_buffer(W1, Z[i], swiglu=True, stream=main)
+            ev_read[i].record(main)
+            if i + 1 < len(Ts):
+                buf.set_active_shape([Ts[i + 1], H])
+                side.wait_event(ev_read[i])
+                buf.allgather(shards(i + 1), stream=side)
+                ev_landed[i + 1].record(side)
+                buf.set_active_shape([T, H])
+            c = T // tp
+            buf.gemm_rs(A[i], Bt, [R[i][r * c:(r + 1) * c] for r in range(tp)], stream=main)
+        torch.cuda.synchronize()
+        assert buf.query_status() == ub.UB_OK
+    for i, T in enumerate(Ts):
+        c = T // tp
+        rows = np.unique(np.array([0, c - 1, c, T // 2, T - 1]))
+        ridx = torch.as_tensor(rows, device=dev())
+        Xu = synth.to_u16(X[i])
+        assert_close(Z[i][ridx], oracle.swiglu(oracle.gemm_rows(Xu, synth.to_u16(W1), rows)), "fc1 mb %d" % i)
+        ref = sum(oracle.gemm_rows(synth.to_u16(A[i][j]), synth.to_u16(Bt[j]), rows) for j in range(tp))
+        assert_close(R[i][ridx], ref, "fc2 mb %d" % i)
