@@ -785,6 +785,23 @@ int ub_plan_path(int64_t single_tiles, int64_t pair_tiles, int64_t k_blocks, int
     return UB_OK;
 }
 
+int ub_plan_gather_parts(int tp, int self, int64_t c, int64_t head, int *chunk, int64_t *row_lo,
+                         int64_t *row_hi, int *flag)
+{
+    if (tp < 1 || tp > UB_MAX_TP || self < 0 || self >= tp || c < 1 || head < 0 || head > c || !chunk ||
+        !row_lo || !row_hi || !flag)
+        return fail(UB_ERR_ARG, "ub_plan_gather_parts: invalid arguments");
+    GatherPart parts[UB_MAX_TP + 1];
+    const int n = gather_parts(tp, self, c, head, parts);
+    for (int i = 0; i < n; ++i) {
+        chunk[i] = parts[i].r;
+        row_lo[i] = parts[i].row_lo;
+        row_hi[i] = parts[i].row_hi;
+        flag[i] = parts[i].flag ? 1 : 0;
+    }
+    return n;
+}
+
 int64_t ub_plan_ag_self_head(int64_t T, int tp, int self, int64_t n_tiles, int64_t pairs)
 {
     if (tp < 1 || tp > UB_MAX_TP || T < tp || T % tp != 0 || self < 0 || self >= tp || n_tiles < 1 || pairs < 1)

@@ -38,7 +38,7 @@ EXPORTS = [
     "ub_clear_status", "ub_get_counters", "ub_kernel_time", "ub_grid_ctas", "ub_last_error",
     "ag_gemm_noalloc", "ag_gemm_swiglu", "ag_gemm_kn", "gemm_rs_kn", "ub_wgrad",
     "ub_allgather", "ub_reduce_scatter", "ub_plan_tail_split", "ub_plan_path",
-    "ub_plan_ag_self_head", "ag_gemm_from_buffer",
+    "ub_plan_ag_self_head", "ag_gemm_from_buffer", "ub_plan_gather_parts",
 ]
 NOALLOC_MAX_ELEMS = 16 * 1024 * 1024
 
@@ -101,6 +101,8 @@ def load():
         "ub_plan_tail_split": [I64, I64, I64, I],
         "ub_plan_path": [I64, I64, I64, I64, I64, I, I, ctypes.POINTER(I), ctypes.POINTER(I)],
         "ub_plan_ag_self_head": [I64, I, I, I64, I64],
+        "ub_plan_gather_parts": [I, I, I64, I64, ctypes.POINTER(I), ctypes.POINTER(I64), ctypes.POINTER(I64),
+                                 ctypes.POINTER(I)],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -140,6 +142,19 @@ def plan_path(single_tiles: int, pair_tiles: int, k_blocks: int, slots: int, pai
                              ctypes.byref(pr), ctypes.byref(sp))
     _check(rc)
     return bool(pr.value), bool(sp.value)
+
+
+def plan_gather_parts(tp: int, self_rank: int, c: int, head: int) -> list:
+    """The gather's copies in issue order: (chunk, row_lo, row_hi, publishes_flag)."""
+    n_max = MAX_TP + 1
+    ch = (ctypes.c_int * n_max)()
+    lo = (ctypes.c_int64 * n_max)()
+    hi = (ctypes.c_int64 * n_max)()
+    fl = (ctypes.c_int * n_max)()
+    n = load().ub_plan_gather_parts(tp, self_rank, c, head, ch, lo, hi, fl)
+    if n < 0:
+        _check(n)
+    return [(ch[i], lo[i], hi[i], bool(fl[i])) for i in range(n)]
 
 
 def plan_ag_self_head(T: int, tp: int, self_rank: int, n_tiles: int, pairs: int) -> int:

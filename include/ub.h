@@ -382,6 +382,20 @@ int ub_plan_path(int64_t single_tiles, int64_t pair_tiles, int64_t k_blocks, int
                  int cta_pair, int streamk, int *pair, int *split);
 int64_t ub_plan_ag_self_head(int64_t T, int tp, int self, int64_t n_tiles, int64_t pairs);
 
+/*
+ * ub_plan_gather_parts: the copies of an ag_gemm gather by driver copies, in issue
+ * order, for tp chunks of c rows, ring start `self`, of which the CTA-pair kernel reads
+ * the self chunk's first `head` rows in place (ub_plan_ag_self_head; c elsewhere).
+ * Part i copies rows [row_lo[i], row_hi[i]) of chunk chunk[i] into the buffer and, when
+ * flag[i] is 1, then publishes that chunk's readiness flag: the self chunk's rows from
+ * `head` on (if any) first, the other chunks in ring order, then the self chunk's first
+ * `head` rows (flagged only when they are the whole chunk). The gather inside the GEMM
+ * copies in the same order. Outputs hold UB_MAX_TP + 1 entries. Returns the part count,
+ * or UB_ERR_ARG.
+ */
+int ub_plan_gather_parts(int tp, int self, int64_t c, int64_t head, int *chunk, int64_t *row_lo,
+                         int64_t *row_hi, int *flag);
+
 /* Message of the last failed call on this host thread ("" if none). */
 const char *ub_last_error(void);
 

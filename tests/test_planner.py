@@ -1,6 +1,6 @@
 """The launch planner through the C ABI's planning queries (host only, no GPU): the
-split-tail piece count, the CTA-pair / single-CTA choice and the self-chunk split of the
-CTA-pair AG tiling. The calls run this same code to pick their launch."""
+split-tail piece count, the CTA-pair / single-CTA choice, the self-chunk split of the
+CTA-pair AG tiling and the gather's copy order. The calls run this same code."""
 import math
 
 import pytest
@@ -123,8 +123,52 @@ def test_self_head_cases():
     lambda: ub.plan_ag_self_head(1142, 4, 0, 28, PAIRS),     # T % tp != 0
     lambda: ub.plan_ag_self_head(1140, 4, 4, 28, PAIRS),     # self outside the ring
     lambda: ub.plan_ag_self_head(1140, 9, 0, 28, PAIRS),     # tp above the maximum
+    lambda: ub.plan_gather_parts(4, 0, 285, 286),            # head past the chunk
+    lambda: ub.plan_gather_parts(4, 4, 285, 256),            # self outside the ring
+    lambda: ub.plan_gather_parts(0, 0, 285, 256),
 ])
 def test_planning_queries_reject_bad_arguments(call):
     with pytest.raises(ub.UbError) as ei:
         call()
     assert ei.value.name == "UB_ERR_ARG"
+
+
+@pytest.mark.parametrize("tp", [1, 2, 3, 4, 8])
+def test_gather_parts_cover_every_row_once_and_flag_after_what_the_gemm_reads(tp):
+    for c in (1, 100, 255, 256, 257, 285, 570, 2048):
+        heads = sorted({c, c // 256 * 256})
+        for self_rank in range(tp):
+            for head in heads:
+                parts = ub.plan_gather_parts(tp, self_rank, c, head)
+                rows = {r: [] for r in range(tp)}
+                flags = {r: [] for r in range(tp)}
+                for i, (r, lo, hi, flag) in enumerate(parts):
+                    assert 0 <= lo < hi <= c
+                    rows[r].append((lo, hi))
+                    if flag:
+                        flags[r].append(i)
+                for r in range(tp):
+                    cover = sorted(rows[r])
+                    assert cover[0][0] == 0 and cover[-1][1] == c
+                    assert all(a[1] == b[0] for a, b in zip(cover, cover[1:]))   # no gap, no overlap
+                    assert len(flags[r]) == 1                                    # one flag per chunk
+                # the other chunks in ring order after the self rank
+                others = [r for r, *_ in parts if r != self_rank]
+                assert others == [(self_rank + q) % tp for q in range(1, tp)]
+                fi = flags[self_rank][0]
+                if head < c:
+                    # the rows the GEMM reads from the buffer go first, flagged
+                    assert parts[0] == (self_rank, head, c, True)
+                    assert fi == 0
+                else:
+                    # read wholly in place: copied last, flagged after its last row
+                    assert parts[-1] == (self_rank, 0, c, True)
+
+
+def test_gather_parts_follow_the_planned_self_head():
+    # AG + SwiGLU at T = 1140 on 76 pairs: the self chunk's last 29 rows go first
+    head = ub.plan_ag_self_head(1140, 4, 0, 28, PAIRS)
+    assert ub.plan_gather_parts(4, 0, 285, head)[0] == (0, 256, 285, True)
+    # QKV at T = 1140: the self chunk stays in place and is copied last
+    head = ub.plan_ag_self_head(1140, 4, 0, 12, PAIRS)
+    assert ub.plan_gather_parts(4, 0, 285, head)[-1] == (0, 0, 285, True)
