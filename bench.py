@@ -213,24 +213,31 @@ class ClockSampler:
         lines = [l.strip() for l in self.out.read().splitlines() if l.strip()]
         self.out.close()
         os.unlink(self.out.name)
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for l in lines:
-            f = [x.strip() for x in l.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
-            return None
-        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
-                "samples": len(sm), "reasons": sorted(reasons)}
+        return parse_clocks(lines)
+
+
+def parse_clocks(lines):
+    """Summary of nvidia-smi samples in ClockSampler.FIELDS order (csv, no header, no
+    units): median SM clock, the highest max clock, and the throttle reasons seen
+    active in any sample; None without a usable sample."""
+    sm, mx, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for l in lines:
+        f = [x.strip() for x in l.split(",")]
+        if len(f) < 9:
+            continue
+        try:
+            sm.append(float(f[1]))
+            mx.append(float(f[2]))
+        except ValueError:
+            continue
+        for n, v in zip(names, f[5:9]):
+            if v.lower().startswith("active"):
+                reasons.add(n)
+    if not sm:
+        return None
+    return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
+            "samples": len(sm), "reasons": sorted(reasons)}
 
 
 # ---------------------------------------------------------------- our arm

@@ -1,0 +1,70 @@
+"""Host-side helpers of bench.py on CPU: the clock-sample summary that decides whether a
+run is kept, the DRAM-traffic record keyed to the kernel source, the FLOP count of a
+step and the choice of the peak a fraction is taken against."""
+import hashlib
+import os
+import sys
+
+import pytest
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+import bench  # noqa: E402
+from gemm_overlap_gemms_gb300 import synth  # noqa: E402
+
+
+def _line(sm, mx, hw="Not Active", hw_th="Not Active", sw_th="Not Active", cap="Not Active"):
+    # index, clocks.sm, clocks.max.sm, power.draw, reasons.active, then the four reasons
+    return "0, %s, %s, 1012.5, 0x0000000000000004, %s, %s, %s, %s" % (sm, mx, hw, hw_th, sw_th, cap)
+
+
+def test_clock_summary_median_max_and_reasons():
+    lines = [_line(2070, 2070), _line(1995, 2070, cap="Active"), _line(2032, 2070),
+             "garbage", "0, [N/A], 2070, 1, 0, Not Active, Not Active, Not Active, Not Active"]
+    c = bench.parse_clocks(lines)
+    assert c == {"sm_mhz": 2032.0, "sm_max_mhz": 2070.0, "samples": 3, "reasons": ["sw_power_cap"]}
+
+
+def test_clock_summary_reports_every_slowdown_it_saw():
+    lines = [_line(1600, 2070, hw="Active"), _line(1500, 2070, hw_th="Active"),
+             _line(1700, 2070, sw_th="Active")]
+    c = bench.parse_clocks(lines)
+    assert c["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"]
+    assert c["sm_mhz"] == 1600.0
+
+
+def test_clock_summary_without_samples():
+    assert bench.parse_clocks([]) is None
+    assert bench.parse_clocks(["a, b", "0, x, y, 1, 0, A, A, A, A"]) is None
+
+
+def test_traffic_record_follows_the_kernel_source(monkeypatch):
+    sha = hashlib.sha256(open(bench.KERNEL_SRC, "rb").read()).hexdigest()[:16]
+    rec = {"sha256_16": sha, "bytes": 1.0e9, "T": 8192, "source": "profiles/x.md"}
+    monkeypatch.setattr(bench, "NCU_TRAFFIC", {"rs": rec})
+    t = bench.kernel_traffic("rs", 4096.0)
+    assert t["bytes_per_launch"] == pytest.approx(0.5e9)      # scaled by the launches' mean T
+    assert t["captured_T"] == 8192 and t["scaled_to_mean_T"] == 4096.0
+    assert bench.kernel_traffic("ag_swiglu", 4096.0) is None  # no record
+    monkeypatch.setattr(bench, "NCU_TRAFFIC", {"rs": dict(rec, sha256_16="0" * 16)})
+    assert bench.kernel_traffic("rs", 4096.0) is None         # stale once the source changed
+
+
+def test_step_flops_are_the_algorithmic_counts():
+    w = synth.WORKLOADS["swiglu"]
+    ag, rs = bench.step_flops([1024, 2048], w)
+    H, N, K, tp = w.hidden, w.ag_n[0], w.rs_k[0], w.tp
+    assert ag == 2.0 * 3072 * H * N
+    assert rs == 2.0 * 3072 * K * H * tp
+
+
+def test_peak_values_measured_or_fallback(monkeypatch, tmp_path):
+    assert bench._peak_value({"bf16_tflops_sustained": 1650}, "bf16_tflops_sustained") == 1650.0
+    assert bench._peak_value({"hbm_gbs": {"median": 7100.5}}, "hbm_gbs") == 7100.5
+    assert bench._peak_value({"bf16_tflops": 1900.0}, "bf16_tflops_sustained", "bf16_tflops") == 1900.0
+    assert bench._peak_value({}, "hbm_gbs") is None
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    d, src = bench.peaks()
+    assert src == "fallback" and d == bench.FALLBACK
+    (tmp_path / "MEASURED_PEAKS.json").write_text('{"hbm_gbs": 7000.0}')
+    d, src = bench.peaks()
+    assert src == "measured" and d["hbm_gbs"] == 7000.0
