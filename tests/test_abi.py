@@ -108,3 +108,21 @@ def test_create_without_a_device_fails_cleanly(lib):
     assert lib.ub_create(512, 256, 2, 0, ctypes.byref(h)) == C["UB_ERR_CUDA"]
     assert h.value is None
     assert "cuda" in ub.last_error().lower() or "driver" in ub.last_error().lower()
+
+
+def _header_enum(prefix):
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    return {name: int(val) for name, val in re.findall(r"\b(%s[A-Z_]*)\s*=\s*(-?\d+)" % prefix, text)}
+
+
+def test_binding_constants_match_the_header():
+    """Error codes, option keys and operation ids of the binding are the header's."""
+    errs = _header_enum("UB_ERR_")
+    assert errs == ub.CODES
+    assert _header_enum("UB_OK") == {"UB_OK": ub.UB_OK}
+    opts = {k[len("UB_OPT_"):].lower(): v for k, v in _header_enum("UB_OPT_").items()}
+    assert opts == ub.OPTIONS
+    ops = {k[len("UB_OP_"):].lower(): v for k, v in _header_enum("UB_OP_").items()}
+    assert ops == ub.OPS
+    m = re.search(r"#define UB_MAX_TP (\d+)", open(HEADER).read())
+    assert int(m.group(1)) == ub.MAX_TP
