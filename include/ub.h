@@ -172,7 +172,9 @@ int ub_buffer(ub_handle_t h, void **dev_ptr, size_t *bytes);
  * (default for T <= 512); or the GEMM kernel's own epilogue warps before their first
  * tile (default above). One persistent GEMM kernel on `stream` walks the chunks in
  * ring order starting at UB_OPT_SELF_RANK (whose chunk it reads in place, without
- * waiting), waits for each other chunk's flag, and never reads or writes rows >= T.
+ * waiting -- on CTA pairs, where that saves a wave, only the chunk's whole 256-row
+ * tiles, its last rows from the buffer behind its flag, see ub_plan_ag_self_head),
+ * waits for each other chunk's flag, and never reads or writes rows >= T.
  * Side streams are joined back into `stream` before return. A device wait that expires
  * is reported by ub_query_status (UB_ERR_TIMEOUT), never by a trap.
  * Concurrency: the GEMM kernels size their grids to be resident at once (at most one
