@@ -13,9 +13,12 @@ weights are shared. FLOPs are algorithmic: 2*T*H*N for AG, 2*T*K*H*tp for RS.
 
   python bench.py [--steps K] [--warmup W] [--gpus N] [--impl ours|reference] [--sweep]
 
-Prints one JSON line (rank 0). ``--impl reference`` times the CPU oracle instead, on a
-bounded row sample of the same workload. ``--sweep`` additionally prints one JSON line
-per (op, T) point of the active-T sweep.
+Prints one JSON line (rank 0); its ``sweep`` key holds the active-T sweep of the metric
+(fc1 / fc2 of the SwiGLU MLP, the QKV projection and the large configuration's GEMM-RS
+at a ladder of T, each point one whole call with L2 flushed before it, against the
+roofline). ``--impl reference`` times the CPU oracle instead, on a bounded row sample
+of the same workload. ``--sweep`` additionally prints one JSON line per (op, T) point
+of a longer ladder.
 """
 from __future__ import annotations
 
@@ -59,7 +62,10 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="also print one JSON line per point of the extended active-T ladder")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="leave the active-T sweep out of the JSON line")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--mlp", choices=["fused", "unfused"], default="fused",
@@ -372,6 +378,140 @@ def time_calls(fn, calls, warmup, stream, graph=True):
 
 SWEEP_CALLS, SWEEP_WARMUP = 50, 10   # per point: median of 50 timed graph replays after 10 warm-ups
 
+# The active-T sweep carried in the default JSON line: (name, workload, op, T ladder).
+# fc1 / fc2 of the SwiGLU MLP, the QKV projection, and the large configuration's two
+# GEMM-RS (attention-out K = 1024, fc2 K = 3584 per shard).
+DEFAULT_SWEEP = (
+    ("fc1_ag_swiglu", "swiglu", "ag_swiglu", (4, 64, 128, 512, 1024, 2048, 4096, 8192)),
+    ("fc2_rs", "swiglu", "rs", (4, 64, 128, 512, 1024, 2048, 4096, 8192)),
+    ("qkv_ag", "qkv", "ag", (4, 512, 1024, 2048, 4096, 8192)),
+    ("large_rs_k1024", "large", "rs", (8, 2048, 16384)),
+    ("large_rs_k3584", "large", "rs", (8, 2048, 16384)),
+)
+DEFAULT_SWEEP_CALLS, DEFAULT_SWEEP_WARMUP = 20, 5
+L2_FLUSH_BYTES = 256 << 20   # written before every timed call: twice the 129 MB L2
+
+
+def op_flops_bytes(op, T, H, tp, N=0, K=0):
+    """Algorithmic FLOPs and HBM bytes of one call. AG: 2*T*H*N FLOPs; bytes = the weight
+    once, the shards read, the gathered buffer written, Y written (SwiGLU: N/2 columns).
+    RS: 2*T*K*H*tp FLOPs; bytes = the tp weights once, the tp A_j read, the tp row blocks
+    written."""
+    if op == "rs":
+        return 2.0 * T * K * H * tp, 2.0 * (tp * K * H + tp * T * K + T * H)
+    n_out = N // 2 if op == "ag_swiglu" else N
+    return 2.0 * T * H * N, 2.0 * (N * H + 2 * T * H + T * n_out)
+
+
+def roofline_point(flops, nbytes, sec, tensor_peak, hbm_peak):
+    """TFLOP/s and GB/s of one call against the roofline min(tensor peak, I * HBM peak),
+    I = FLOPs / byte: `bound` names the roof that limits this shape."""
+    tf = flops / sec / 1e12
+    gbs = nbytes / sec / 1e9
+    intensity = flops / nbytes
+    attainable = min(tensor_peak, intensity * hbm_peak / 1e3)
+    return {"tflops": tf, "frac_of_peak": tf / tensor_peak, "hbm_gbs": gbs, "hbm_frac": gbs / hbm_peak,
+            "flop_per_byte": intensity, "bound": "tensor" if attainable >= tensor_peak else "hbm",
+            "frac_of_roofline": tf / attainable}
+
+
+def time_graph_flushed(fn, stream, flush, calls, warmup):
+    """Median and minimum time of one call, `fn(st)` issuing it on stream `st`: the call is
+    captured once into a CUDA graph and replayed `calls` times on `stream`, each replay
+    between CUDA events and preceded by a write of `flush` (larger than L2) outside the
+    events, after `warmup` replays."""
+    fn(stream)
+    torch.cuda.synchronize()
+    cap = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cap):
+        fn(cap)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(calls)]
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            g.replay()
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in ev]
+    del g
+    return float(np.median(ms)), float(np.min(ms))
+
+
+def default_sweep(stream):
+    """The active-T sweep of the metric ("TFLOP/s and % of bf16 peak vs active token
+    count T"): every point is one whole call (AG: the gather, its flag waits and joins
+    included) on a handle registered at the workload's capacity, timed as the median of
+    DEFAULT_SWEEP_CALLS graph replays with L2 flushed before each, with the kernel path
+    the library took. Fractions are of the measured burst bf16 peak (an isolated call)
+    and of the measured HBM bandwidth (algorithmic bytes)."""
+    from gemm_overlap_gemms_gb300 import ub
+    pk, src = peaks()
+    tensor_peak = _peak_value(pk, "bf16_tflops") or FALLBACK["bf16_tflops"]
+    hbm_peak = _peak_value(pk, "hbm_gbs") or FALLBACK["hbm_gbs"]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    points = []
+    t_start = time.perf_counter()
+    for wname in ("swiglu", "qkv", "large"):
+        w = synth.WORKLOADS[wname]
+        H, tp, cap = w.hidden, w.tp, w.max_tokens
+        g = synth.generator(dev, 31)
+        buf = ub.UserBuffer([cap, H], tp)
+        X = synth.normal_bf16((cap, H), 1.0, g, dev)
+        Yrs = torch.empty((cap, H), dtype=torch.bfloat16, device=dev)
+        for name, wl_name, op, Ts in DEFAULT_SWEEP:
+            if wl_name != wname:
+                continue
+            if op == "rs":
+                K = int(name.rsplit("_k", 1)[1]) if "_k" in name else w.rs_k[0]
+                A = [synth.normal_bf16((cap, K), 1.0, g, dev) for _ in range(tp)]
+                Bt = [synth.normal_bf16((H, K), 1.0 / math.sqrt(K), g, dev) for _ in range(tp)]
+                N = 0
+            else:
+                N, K = w.ag_n[0], 0
+                Wt = synth.normal_bf16((N, H), 1.0 / math.sqrt(H), g, dev)
+                Y = torch.empty((cap, N // 2 if op == "ag_swiglu" else N), dtype=torch.bfloat16, device=dev)
+            for T in Ts:
+                c = T // tp
+                buf.set_active_shape([T, H])
+                if op == "rs":
+                    a_T = [a[:T] for a in A]
+                    outs = [Yrs[r * c:(r + 1) * c] for r in range(tp)]
+                    fn = lambda st, a_T=a_T, outs=outs: buf.gemm_rs(a_T, Bt, outs, stream=st)
+                else:
+                    shards = [X[r * c:(r + 1) * c] for r in range(tp)]
+                    call = buf.ag_gemm_swiglu if op == "ag_swiglu" else buf.ag_gemm
+                    fn = lambda st, shards=shards, call=call: call(shards, Wt, Y, stream=st)
+                med, best = time_graph_flushed(fn, stream, flush, DEFAULT_SWEEP_CALLS, DEFAULT_SWEEP_WARMUP)
+                cnt = buf.counters()
+                flops, nbytes = op_flops_bytes(op, T, H, tp, N, K)
+                pt = {"op": name, "T": T, "us": med * 1e3, "us_min": best * 1e3}
+                pt.update(roofline_point(flops, nbytes, med / 1e3, tensor_peak, hbm_peak))
+                pt["kernel"] = ub.KERNELS.get(cnt["last_kernel"], "?")
+                pt["k_pieces"] = cnt["last_pieces"]
+                if op != "rs":
+                    pt["gather"] = ub.GATHERS.get(cnt["last_gather"], "?")
+                points.append(pt)
+            if op == "rs":
+                del A, Bt
+            else:
+                del Wt, Y
+        assert buf.query_status() == ub.UB_OK, "device status %d" % buf.query_status()
+        buf.close()
+        del X, Yrs
+    del flush
+    return {"points": points, "timing": "median of %d CUDA-graph replays of one whole call, L2 flushed (%d MiB "
+                                        "written) before each, after %d warm-up replays"
+                                        % (DEFAULT_SWEEP_CALLS, L2_FLUSH_BYTES >> 20, DEFAULT_SWEEP_WARMUP),
+            "peaks": {"bf16_tflops": tensor_peak, "hbm_gbs": hbm_peak,
+                      "source": "%s burst bf16 and HBM copy (%s)" % (src, "MEASURED_PEAKS.json" if src == "measured"
+                                                                      else "recipe fallback")},
+            "seconds": time.perf_counter() - t_start}
+
 
 def e2e_measure(wl, steps, warmup, stream, world):
     """Same step, with each microbatch's activations copied in from pinned host memory
@@ -633,6 +773,7 @@ def run_ours(args):
                   "what": "same microbatches padded to max_tokens=%d (real tokens first, zeros "
                           "after); useful FLOPs only" % w.max_tokens}
     bulk = bulk_measure(wl, stream) if not args.no_bulk and rank == 0 else None
+    active_sweep = default_sweep(stream) if not args.no_sweep and rank == 0 else None
     sweep = sweep_points(wl, stream) + sweep_other_configs(stream) if args.sweep and rank == 0 else None
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -663,6 +804,7 @@ def run_ours(args):
         "e2e": e2e,
         "padded_comparator": padded,
         "bulk_overlap": bulk,
+        "sweep": active_sweep,
         "clocks": clk,
         "flops_per_step": {"ag": ag_flops, "rs": rs_flops},
     }

@@ -14,6 +14,7 @@
 // register cap of the pair kernel), and every flag wait is bounded.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
@@ -445,6 +446,9 @@ int launch(ub_handle *h, GemmParams &p, int mode, int path, cudaStream_t s, int 
                     : path == PATH_SKINNY ? ubk::launch_gemm_skinny(p, mode, grid, s)
                                           : ubk::launch_gemm(p, mode, grid, s);
     if (e != cudaSuccess) return cuda_fail(e, "GEMM kernel launch");
+    h->counters.last_kernel = path == PATH_PAIR ? UB_KERNEL_PAIR : path == PATH_SKINNY ? UB_KERNEL_FEW_TOKEN : UB_KERNEL_SINGLE;
+    h->counters.last_pieces = path == PATH_PAIR ? p.tail_split : path == PATH_SKINNY ? p.sk_split : 1;
+    h->counters.last_gather = -1;  // an AG call sets it after the launch
     if (timed) {
         UB_CUDA(cudaEventRecord(ring.stop[ring.count], s));
         ++ring.count;
@@ -597,6 +601,19 @@ int begin_call(ub_handle *h, cudaStream_t s, uint32_t &epoch)
     }
     return UB_OK;
 }
+
+// An NVTX range around one ABI call, named with the call and its active T, so that a
+// timeline shows which GPU work each call issued and what of it stays exposed. Without
+// an attached tool the push and pop cost a few nanoseconds.
+struct NvtxRange {
+    NvtxRange(const char *name, int64_t T)
+    {
+        char msg[64];
+        snprintf(msg, sizeof msg, "%s T=%lld", name, static_cast<long long>(T));
+        nvtxRangePushA(msg);
+    }
+    ~NvtxRange() { nvtxRangePop(); }
+};
 
 int check_handle(ub_handle *h)
 {
@@ -828,6 +845,7 @@ static int ag_gemm_impl(ub_handle_t h, const void *const *shards, const void *Wt
     }
     DeviceGuard g(h->device);
     if (!g.ok) return fail(UB_ERR_CUDA, "ag_gemm: cannot select the handle's device");
+    NvtxRange range(glu_f > 0 ? "ag_gemm_swiglu" : b_kn ? "ag_gemm_kn" : "ag_gemm", h->T);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int64_t T = h->T, H = h->hidden, c = T / tp;
     const int self = static_cast<int>(h->self_rank);
@@ -975,6 +993,7 @@ static int ag_gemm_impl(ub_handle_t h, const void *const *shards, const void *Wt
         if (int jrc = join_gather(h, s)) return jrc;
         if (rc != UB_OK) return rc;
     }
+    h->counters.last_gather = in_gemm ? 2 : h->gather_by_kernel ? 1 : 0;
     ++h->counters.ag_calls;
     h->counters.last_T = T;
     return UB_OK;
@@ -1014,6 +1033,7 @@ static int gemm_rs_impl(ub_handle_t h, const void *const *A, const void *const *
     }
     DeviceGuard g(h->device);
     if (!g.ok) return fail(UB_ERR_CUDA, "gemm_rs: cannot select the handle's device");
+    NvtxRange range(b_kn ? "gemm_rs_kn" : "gemm_rs", h->T);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int64_t T = h->T, H = h->hidden, c = T / tp;
 
@@ -1140,6 +1160,7 @@ int ub_allgather(ub_handle_t h, const void *const *shards, void *stream)
     }
     DeviceGuard g(h->device);
     if (!g.ok) return fail(UB_ERR_CUDA, "ub_allgather: cannot select the handle's device");
+    NvtxRange range("ub_allgather", h->T);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint32_t epoch = 0;
     if (int rc = begin_call(h, s, epoch)) return rc;
@@ -1165,6 +1186,7 @@ int ub_reduce_scatter(ub_handle_t h, const void *const *P, void *const *Y_shards
     }
     DeviceGuard g(h->device);
     if (!g.ok) return fail(UB_ERR_CUDA, "ub_reduce_scatter: cannot select the handle's device");
+    NvtxRange range("ub_reduce_scatter", h->T);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     p.tp = tp;
     p.T = h->T;
@@ -1209,6 +1231,7 @@ int ub_wgrad(ub_handle_t h, const void *D, int64_t M, int ub_is_a, void *out, vo
     if (ub_is_a != 0 && ub_is_a != 1) return fail(UB_ERR_ARG, "ub_wgrad: ub_is_a must be 0 or 1");
     DeviceGuard g(h->device);
     if (!g.ok) return fail(UB_ERR_CUDA, "ub_wgrad: cannot select the handle's device");
+    NvtxRange range("ub_wgrad", h->T);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int64_t T = h->T, H = h->hidden;
     // out = A^T B over the T active rows; A and B are [T, .] row-major (MN-major operands)
@@ -1270,6 +1293,7 @@ int ag_gemm_from_buffer(ub_handle_t h, const void *Wt, int64_t N, int64_t glu_f,
     if (!aligned16(Wt) || !aligned16(Y)) return fail(UB_ERR_ALIGN, "ag_gemm_from_buffer: Wt / Y not 16-byte aligned");
     DeviceGuard g(h->device);
     if (!g.ok) return fail(UB_ERR_CUDA, "ag_gemm_from_buffer: cannot select the handle's device");
+    NvtxRange range("ag_gemm_from_buffer", h->T);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int64_t T = h->T, H = h->hidden;
     const bool glu = glu_f > 0;

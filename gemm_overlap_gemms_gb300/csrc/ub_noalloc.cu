@@ -14,6 +14,7 @@
 // library.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
@@ -134,6 +135,10 @@ extern "C" int ag_gemm_noalloc(const void *const *shards, int tp, int64_t T, int
     if (e != cudaSuccess) return fail(UB_ERR_CUDA, "ag_gemm_noalloc: cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
 
     std::lock_guard<std::mutex> lock(g_mu);
+    nvtxRangePushA("ag_gemm_noalloc");
+    struct Pop {
+        ~Pop() { nvtxRangePop(); }
+    } pop;
     DeviceScratch &ds = g_dev[dev];
     if (!ds.ready) {
         // Set-up, once per device, with that device current: the host-side name of
@@ -181,8 +186,9 @@ extern "C" int ag_gemm_noalloc(const void *const *shards, int tp, int64_t T, int
     if (e != cudaSuccess) return fail(UB_ERR_CUDA, "ag_gemm_noalloc: clearing status: %s", cudaGetErrorString(e));
     // Chunk copies and their flags on the caller's stream (no side stream is created
     // here), in ring order after rank 0; they therefore complete before the kernel.
-    for (int q = 1; q <= tp; ++q) {
-        const int r = q % tp;
+    // Chunk 0 is not copied: the kernel reads it in place from its shard and never
+    // waits for its flag, and nothing else reads the scratch.
+    for (int r = 1; r < tp; ++r) {
         e = cudaMemcpyAsync(ub + r * c * H * 2, shards[r], static_cast<size_t>(c * H * 2), cudaMemcpyDeviceToDevice,
                             s);
         if (e != cudaSuccess) return fail(UB_ERR_CUDA, "ag_gemm_noalloc: cudaMemcpyAsync: %s", cudaGetErrorString(e));

@@ -53,7 +53,12 @@ class UbError(RuntimeError):
 class Counters(ctypes.Structure):
     _fields_ = [("ag_calls", ctypes.c_int64), ("rs_calls", ctypes.c_int64),
                 ("device_allocations", ctypes.c_int64), ("last_T", ctypes.c_int64),
-                ("tensor_map_encodes", ctypes.c_int64)]
+                ("tensor_map_encodes", ctypes.c_int64), ("last_kernel", ctypes.c_int64),
+                ("last_pieces", ctypes.c_int64), ("last_gather", ctypes.c_int64)]
+
+
+KERNELS = {0: "single", 1: "pair", 2: "few_token"}
+GATHERS = {-1: "none", 0: "copies", 1: "gather_kernel", 2: "in_gemm"}
 
 
 def lib_path() -> str:
@@ -184,11 +189,13 @@ def _ptrs(tensors):
     return (ctypes.c_void_p * len(tensors))(*[t.data_ptr() for t in tensors])
 
 
-def _bf16_cuda(t: torch.Tensor, name: str, shape=None):
+def _bf16_cuda(t: torch.Tensor, name: str, shape=None, device=None):
     if not isinstance(t, torch.Tensor):
         raise TypeError("%s must be a torch.Tensor" % name)
     if t.dtype != torch.bfloat16 or not t.is_cuda:
         raise TypeError("%s must be a CUDA bfloat16 tensor, got %s on %s" % (name, t.dtype, t.device))
+    if device is not None and t.device != device:
+        raise ValueError("%s is on %s, the user buffer on %s" % (name, t.device, device))
     if not t.is_contiguous():
         raise ValueError("%s must be contiguous" % name)
     if shape is not None and tuple(t.shape) != tuple(shape):
@@ -313,14 +320,14 @@ class UserBuffer:
             raise ValueError("expected %d shards, got %d" % (self.tp, len(shards)))
         c = T // self.tp
         for r, s in enumerate(shards):
-            _bf16_cuda(s, "shards[%d]" % r, (c, H))
-        _bf16_cuda(Wt, "Wt")
+            _bf16_cuda(s, "shards[%d]" % r, (c, H), device=self.device)
+        _bf16_cuda(Wt, "Wt", device=self.device)
         if Wt.dim() != 2 or Wt.shape[1] != H:
             raise ValueError("Wt must be [N, %d], got %s" % (H, tuple(Wt.shape)))
         N = Wt.shape[0]
         if Y is None:
             Y = torch.empty((T, N), dtype=torch.bfloat16, device=Wt.device)
-        _bf16_cuda(Y, "Y")
+        _bf16_cuda(Y, "Y", device=self.device)
         if Y.dim() != 2 or Y.shape[0] < T or Y.shape[1] != N:
             raise ValueError("Y must be [>=%d, %d], got %s" % (T, N, tuple(Y.shape)))
         _check(load().ag_gemm(self._h, _ptrs(shards), ctypes.c_void_p(Wt.data_ptr()), N,
@@ -335,14 +342,14 @@ class UserBuffer:
             raise ValueError("expected %d shards, got %d" % (self.tp, len(shards)))
         c = T // self.tp
         for r, s in enumerate(shards):
-            _bf16_cuda(s, "shards[%d]" % r, (c, H))
-        _bf16_cuda(Wt, "Wt")
+            _bf16_cuda(s, "shards[%d]" % r, (c, H), device=self.device)
+        _bf16_cuda(Wt, "Wt", device=self.device)
         if Wt.dim() != 2 or Wt.shape[1] != H or Wt.shape[0] % 2:
             raise ValueError("Wt must be [2F, %d], got %s" % (H, tuple(Wt.shape)))
         F = Wt.shape[0] // 2
         if Z is None:
             Z = torch.empty((T, F), dtype=torch.bfloat16, device=Wt.device)
-        _bf16_cuda(Z, "Z")
+        _bf16_cuda(Z, "Z", device=self.device)
         if Z.dim() != 2 or Z.shape[0] < T or Z.shape[1] != F:
             raise ValueError("Z must be [>=%d, %d], got %s" % (T, F, tuple(Z.shape)))
         _check(load().ag_gemm_swiglu(self._h, _ptrs(shards), ctypes.c_void_p(Wt.data_ptr()), F,
@@ -357,14 +364,14 @@ class UserBuffer:
             raise ValueError("expected %d shards, got %d" % (self.tp, len(shards)))
         c = T // self.tp
         for r, s in enumerate(shards):
-            _bf16_cuda(s, "shards[%d]" % r, (c, H))
-        _bf16_cuda(W, "W")
+            _bf16_cuda(s, "shards[%d]" % r, (c, H), device=self.device)
+        _bf16_cuda(W, "W", device=self.device)
         if W.dim() != 2 or W.shape[0] != H:
             raise ValueError("W must be [%d, N], got %s" % (H, tuple(W.shape)))
         N = W.shape[1]
         if Y is None:
             Y = torch.empty((T, N), dtype=torch.bfloat16, device=W.device)
-        _bf16_cuda(Y, "Y")
+        _bf16_cuda(Y, "Y", device=self.device)
         if Y.dim() != 2 or Y.shape[0] < T or Y.shape[1] != N:
             raise ValueError("Y must be [>=%d, %d], got %s" % (T, N, tuple(Y.shape)))
         _check(load().ag_gemm_kn(self._h, _ptrs(shards), ctypes.c_void_p(W.data_ptr()), N,
@@ -379,14 +386,14 @@ class UserBuffer:
             raise ValueError("expected %d A and B operands" % self.tp)
         K = A[0].shape[1] if A[0].dim() == 2 else -1
         for j in range(self.tp):
-            _bf16_cuda(A[j], "A[%d]" % j, (T, K))
-            _bf16_cuda(B[j], "B[%d]" % j, (K, H))
+            _bf16_cuda(A[j], "A[%d]" % j, (T, K), device=self.device)
+            _bf16_cuda(B[j], "B[%d]" % j, (K, H), device=self.device)
         c = T // self.tp
         if Y_shards is None:
             Y_shards = [torch.empty((c, H), dtype=torch.bfloat16, device=A[0].device)
                         for _ in range(self.tp)]
         for r, y in enumerate(Y_shards):
-            _bf16_cuda(y, "Y_shards[%d]" % r)
+            _bf16_cuda(y, "Y_shards[%d]" % r, device=self.device)
             if y.dim() != 2 or y.shape[0] < c or y.shape[1] != H:
                 raise ValueError("Y_shards[%d] must be [>=%d, %d]" % (r, c, H))
         _check(load().gemm_rs_kn(self._h, _ptrs(A), _ptrs(B), K, _ptrs(Y_shards),
@@ -398,14 +405,14 @@ class UserBuffer:
         """Weight gradient over the T active rows of the gathered buffer G:
         ub_is_a=False -> out [M, hidden] = D.T @ G; ub_is_a=True -> out [hidden, M] = G.T @ D."""
         T, H = self.active_shape
-        _bf16_cuda(D, "D")
+        _bf16_cuda(D, "D", device=self.device)
         if D.dim() != 2 or D.shape[0] != T:
             raise ValueError("D must be [%d, M], got %s" % (T, tuple(D.shape)))
         M = D.shape[1]
         shape = (H, M) if ub_is_a else (M, H)
         if out is None:
             out = torch.empty(shape, dtype=torch.bfloat16, device=D.device)
-        _bf16_cuda(out, "out", shape)
+        _bf16_cuda(out, "out", shape, device=self.device)
         _check(load().ub_wgrad(self._h, ctypes.c_void_p(D.data_ptr()), M, int(bool(ub_is_a)),
                                ctypes.c_void_p(out.data_ptr()), _stream_ptr(stream)))
         return out
@@ -417,14 +424,14 @@ class UserBuffer:
         The buffer must already hold the chunks: an allgather() of this active shape on
         this handle, ordered before this call (same stream, or an event)."""
         T, H = self.active_shape
-        _bf16_cuda(Wt, "Wt")
+        _bf16_cuda(Wt, "Wt", device=self.device)
         if Wt.dim() != 2 or Wt.shape[1] != H or (swiglu and Wt.shape[0] % 2):
             raise ValueError("Wt must be [%s, %d], got %s" % ("2F" if swiglu else "N", H, tuple(Wt.shape)))
         N = Wt.shape[0]
         n_out = N // 2 if swiglu else N
         if Y is None:
             Y = torch.empty((T, n_out), dtype=torch.bfloat16, device=Wt.device)
-        _bf16_cuda(Y, "Y")
+        _bf16_cuda(Y, "Y", device=self.device)
         if Y.dim() != 2 or Y.shape[0] < T or Y.shape[1] != n_out:
             raise ValueError("Y must be [>=%d, %d], got %s" % (T, n_out, tuple(Y.shape)))
         _check(load().ag_gemm_from_buffer(self._h, ctypes.c_void_p(Wt.data_ptr()), N, n_out if swiglu else 0,
@@ -438,7 +445,7 @@ class UserBuffer:
             raise ValueError("expected %d shards, got %d" % (self.tp, len(shards)))
         c = T // self.tp
         for r, s in enumerate(shards):
-            _bf16_cuda(s, "shards[%d]" % r, (c, H))
+            _bf16_cuda(s, "shards[%d]" % r, (c, H), device=self.device)
         _check(load().ub_allgather(self._h, _ptrs(shards), _stream_ptr(stream)))
 
     def reduce_scatter(self, P, Y_shards=None, stream=None):
@@ -447,13 +454,13 @@ class UserBuffer:
         if len(P) != self.tp:
             raise ValueError("expected %d partials" % self.tp)
         for j, x in enumerate(P):
-            _bf16_cuda(x, "P[%d]" % j, (T, H))
+            _bf16_cuda(x, "P[%d]" % j, (T, H), device=self.device)
         c = T // self.tp
         if Y_shards is None:
             Y_shards = [torch.empty((c, H), dtype=torch.bfloat16, device=P[0].device)
                         for _ in range(self.tp)]
         for r, y in enumerate(Y_shards):
-            _bf16_cuda(y, "Y_shards[%d]" % r)
+            _bf16_cuda(y, "Y_shards[%d]" % r, device=self.device)
             if y.dim() != 2 or y.shape[0] < c or y.shape[1] != H:
                 raise ValueError("Y_shards[%d] must be [>=%d, %d]" % (r, c, H))
         _check(load().ub_reduce_scatter(self._h, _ptrs(P), _ptrs(Y_shards), _stream_ptr(stream)))
@@ -466,8 +473,8 @@ class UserBuffer:
             raise ValueError("expected %d A and Bt operands" % self.tp)
         K = A[0].shape[1] if A[0].dim() == 2 else -1
         for j in range(self.tp):
-            _bf16_cuda(A[j], "A[%d]" % j, (T, K))
-            _bf16_cuda(Bt[j], "Bt[%d]" % j, (H, K))
+            _bf16_cuda(A[j], "A[%d]" % j, (T, K), device=self.device)
+            _bf16_cuda(Bt[j], "Bt[%d]" % j, (H, K), device=self.device)
         c = T // self.tp
         if Y_shards is None:
             Y_shards = [torch.empty((c, H), dtype=torch.bfloat16, device=A[0].device)
@@ -475,7 +482,7 @@ class UserBuffer:
         if len(Y_shards) != self.tp:
             raise ValueError("expected %d output shards" % self.tp)
         for r, y in enumerate(Y_shards):
-            _bf16_cuda(y, "Y_shards[%d]" % r)
+            _bf16_cuda(y, "Y_shards[%d]" % r, device=self.device)
             if y.dim() != 2 or y.shape[0] < c or y.shape[1] != H:
                 raise ValueError("Y_shards[%d] must be [>=%d, %d]" % (r, c, H))
         _check(load().gemm_rs(self._h, _ptrs(A), _ptrs(Bt), K, _ptrs(Y_shards),
@@ -486,19 +493,38 @@ class UserBuffer:
 def ag_gemm_noalloc(shards, Wt: torch.Tensor, Y: torch.Tensor | None = None, stream=None):
     """AG-GEMM through the allocation-free entry point (no handle): for callers that
     cannot allocate device memory. Uses the library's fixed 32 MiB device scratch, so
-    T * hidden <= NOALLOC_MAX_ELEMS, and calls on one device must not overlap."""
+    T * hidden <= NOALLOC_MAX_ELEMS, and calls on one device must not overlap.
+
+    The C entry point cannot see tensor sizes (it builds its tensor maps from T, hidden
+    and N alone), so every shape and the device of every tensor are checked here, and
+    the call runs with the tensors' device current: the library picks that device's
+    copy of the scratch and launches there."""
     tp = len(shards)
+    if not 1 <= tp <= MAX_TP:
+        raise ValueError("expected 1..%d shards, got %d" % (MAX_TP, tp))
+    _bf16_cuda(shards[0], "shards[0]")
+    if shards[0].dim() != 2:
+        raise ValueError("shards[0] must be [c, hidden], got %s" % (tuple(shards[0].shape),))
     c, H = shards[0].shape
     for r, s in enumerate(shards):
         _bf16_cuda(s, "shards[%d]" % r, (c, H))
     _bf16_cuda(Wt, "Wt")
+    if Wt.dim() != 2 or Wt.shape[1] != H:
+        raise ValueError("Wt must be [N, %d], got %s" % (H, tuple(Wt.shape)))
     N = Wt.shape[0]
     T = c * tp
+    device = Wt.device
     if Y is None:
-        Y = torch.empty((T, N), dtype=torch.bfloat16, device=Wt.device)
+        Y = torch.empty((T, N), dtype=torch.bfloat16, device=device)
     _bf16_cuda(Y, "Y")
-    _check(load().ag_gemm_noalloc(_ptrs(shards), tp, T, H, ctypes.c_void_p(Wt.data_ptr()), N,
-                                  ctypes.c_void_p(Y.data_ptr()), _stream_ptr(stream)))
+    if Y.dim() != 2 or Y.shape[0] < T or Y.shape[1] != N:
+        raise ValueError("Y must be [>=%d, %d], got %s" % (T, N, tuple(Y.shape)))
+    for name, t in [("shards[%d]" % r, s) for r, s in enumerate(shards)] + [("Y", Y)]:
+        if t.device != device:
+            raise ValueError("%s is on %s, Wt on %s: all tensors must share one device" % (name, t.device, device))
+    with torch.cuda.device(device):
+        _check(load().ag_gemm_noalloc(_ptrs(shards), tp, T, H, ctypes.c_void_p(Wt.data_ptr()), N,
+                                      ctypes.c_void_p(Y.data_ptr()), _stream_ptr(stream)))
     return Y
 
 

@@ -32,7 +32,12 @@
  *    (UB_ERR_ALIGN otherwise): rows are moved by the tensor memory accelerator.
  *  - `stream` is a cudaStream_t (NULL = legacy default stream). Calls are
  *    asynchronous on it; the caller keeps every buffer alive until the stream has
- *    passed the call. Results are deterministic run to run (no split-K, no atomics).
+ *    passed the call. Results are deterministic run to run for a given launch shape:
+ *    where a tile's K range is split over several CTAs (the last wave of the CTA-pair
+ *    kernel, the few-token kernel) the fp32 partials are added in a fixed piece order,
+ *    and atomics only count finished gather copies and record the status word; no
+ *    result is accumulated atomically. The split depends only on the shapes and the
+ *    SM count.
  *  - Every function returns UB_OK (0) or a negative UB_ERR_* code; on error the
  *    state of the handle is unchanged and ub_last_error() describes the failure.
  *  - A handle is used from one host thread at a time.
@@ -129,7 +134,9 @@ enum {
  */
 int ub_create(int64_t max_tokens, int64_t hidden, int tp, ub_dtype_t dtype, ub_handle_t *out);
 
-/* Release everything the handle owns. Synchronises the handle's side stream. */
+/* Release everything the handle owns. Synchronises the handle's side stream. An
+ * addition of this library: [P2] registers a buffer once and never releases it within
+ * the run, so it names no release call. */
 int ub_destroy(ub_handle_t h);
 
 /*
@@ -155,7 +162,10 @@ int ub_get_capacity(ub_handle_t h, int64_t *max_tokens, int64_t *hidden);
 int ub_get_tp(ub_handle_t h, int *tp);
 
 /* Device address and byte size of the registered buffer. After ag_gemm its first T
- * rows hold the gathered input concat_r X_r (rows >= T are never touched). */
+ * rows hold the gathered input concat_r X_r (rows >= T are never touched): [P1]'s point
+ * that the buffer stages the communicated activation [S, hidden]. The accessor itself is
+ * an addition of this library (the pages expose the buffer only through the overlap
+ * calls). */
 int ub_buffer(ub_handle_t h, void **dev_ptr, size_t *bytes);
 
 /*
@@ -240,6 +250,9 @@ int gemm_rs_kn(ub_handle_t h, const void *const *A, const void *const *B, int64_
                void *const *Y_shards, void *stream);
 
 /*
+ * An addition of this library, for the backward pass of [P1]'s two layers (the pages
+ * show only the forward diagrams): the buffer still holds the communicated activation
+ * after the all-gather, so the weight gradient reads it instead of gathering again.
  * Weight gradient over the active tokens, reading the gathered rows G = UB[0:T] that
  * the last ag_gemm / ag_gemm_kn / ag_gemm_swiglu of this handle left in the buffer:
  *   ub_is_a = 0:  out[m][h] = sum_{t<T} D[t][m] * G[t][h]   (out [M, hidden]: dWt of the
@@ -273,6 +286,9 @@ int ub_allgather(ub_handle_t h, const void *const *shards, void *stream);
 int ub_reduce_scatter(ub_handle_t h, const void *const *P, void *const *Y_shards, void *stream);
 
 /*
+ * An addition of this library, the column-parallel half of [P3]'s "bulk" method: the
+ * all-gather is done ahead by ub_allgather, beside other work, and this call computes
+ * from its result.
  * AG-GEMM over the user buffer as it stands: Y[t, :] = UB[t, :] . Wt^T for t < T (the
  * active shape), with no gather and no readiness-flag wait -- for a caller that landed
  * the chunks ahead of time with ub_allgather on this handle, for the same active shape
@@ -294,6 +310,8 @@ int ub_set_option(ub_handle_t h, int key, int64_t val);
 int ub_get_option(ub_handle_t h, int key, int64_t *val);
 
 /*
+ * Additions of this library (failure reporting of the bounded device waits; the pages
+ * define none).
  * Sticky device status: UB_OK, or the first UB_ERR_* a kernel of this handle raised
  * (UB_ERR_TIMEOUT when a readiness flag or pipeline barrier wait ran out). Reads the
  * device word through the handle's side stream; call it after the stream of the
@@ -304,24 +322,36 @@ int ub_query_status(ub_handle_t h);
 int ub_clear_status(ub_handle_t h);
 
 /* Counters of the handle: calls made, device allocations made (constant after
- * ub_create), last active T used by a GEMM call. */
+ * ub_create), last active T used by a GEMM call, and how the last GEMM call ran:
+ * which kernel (UB_KERNEL_*), into how many k-pieces it cut a tile (the CTA-pair
+ * kernel: the tiles of its last, partial wave; the few-token kernel: every weight tile;
+ * 1 = whole tiles) and which all-gather fed it (a UB_OPT_GATHER_KERNEL value: 0 driver
+ * copies, 1 one gather kernel, 2 inside the GEMM; -1 none, e.g. GEMM-RS). An addition
+ * of this library; the pages define no counters. */
+enum { UB_KERNEL_SINGLE = 0, UB_KERNEL_PAIR = 1, UB_KERNEL_FEW_TOKEN = 2 };
 typedef struct {
     int64_t ag_calls;
     int64_t rs_calls;
     int64_t device_allocations;
     int64_t last_T;
     int64_t tensor_map_encodes;
+    int64_t last_kernel;
+    int64_t last_pieces;
+    int64_t last_gather;
 } ub_counters_t;
 int ub_get_counters(ub_handle_t h, ub_counters_t *out);
 
 /*
- * With UB_OPT_PROFILE = 1, every GEMM kernel launch of operation `op` (a UB_OP_* id) is bracketed by CUDA events on its launch stream (up to 4096 launches are
- * kept). This call waits for the last recorded launch, returns the summed kernel time
- * in milliseconds and the launch count, and clears the record.
+ * An addition of this library (kernel timing for the benchmark; the pages define none).
+ * With UB_OPT_PROFILE = 1, every GEMM kernel launch of operation `op` (a UB_OP_* id) is
+ * bracketed by CUDA events on its launch stream (up to 4096 launches are kept). This
+ * call waits for the last recorded launch, returns the summed kernel time in
+ * milliseconds and the launch count, and clears the record.
  */
 int ub_kernel_time(ub_handle_t h, int op, double *total_ms, int64_t *launches);
 
-/* Grid size a GEMM call of this handle launches (SM count minus the margin). */
+/* Grid size a GEMM call of this handle launches (SM count minus the margin of [P3]'s
+ * "num_sm" / "set_sm_margin"). The query is an addition of this library. */
 int ub_grid_ctas(ub_handle_t h, int *ctas);
 
 /*
@@ -336,8 +366,13 @@ int ub_grid_ctas(ub_handle_t h, int *ctas);
  * the same kernel. Instead of a handle's user buffer and control block it uses one
  * file-scope device array of UB_NOALLOC_MAX_ELEMS bf16 elements (32 MiB) plus 256
  * bytes, which every GPU that loads the library holds until the process exits. It
- * calls no cudaMalloc or cudaFree and creates no stream or event: the chunk copies and
- * their readiness flags are issued on `stream` itself, ahead of the kernel.
+ * calls no cudaMalloc or cudaFree and creates no stream or event: the copies of chunks
+ * 1 .. tp-1 and their readiness flags are issued on `stream` itself, ahead of the kernel
+ * (chunk 0 is read in place from its shard and not copied).
+ *  - Every pointer and `stream` must belong to the current device: the scratch used is
+ *    that device's copy of the array, and the kernel is launched there. The function
+ *    cannot see the sizes behind the pointers: Y must hold T x N elements and Wt
+ *    N x hidden, or the kernel reads or writes past them.
  *  - T * hidden must not exceed UB_NOALLOC_MAX_ELEMS (UB_ERR_CAPACITY otherwise);
  *    T % tp == 0 (UB_ERR_DIVISIBLE); hidden, N multiples of 8 and pointers 16-byte
  *    aligned (UB_ERR_ALIGN); 1 <= tp <= UB_MAX_TP (UB_ERR_ARG).
@@ -354,9 +389,10 @@ int ag_gemm_noalloc(const void *const *shards, int tp, int64_t T, int64_t hidden
                     int64_t N, void *Y, void *stream);
 
 /*
- * Planning queries: the launch choices the library makes for a call, as pure functions
- * of the shapes and the GPU's unit counts -- no handle, no device, no CUDA call. Tools
- * use them to predict a call's launch; they are the same code the calls run.
+ * Planning queries, additions of this library (the pages define no launch planning):
+ * the launch choices the library makes for a call, as pure functions of the shapes and
+ * the GPU's unit counts -- no handle, no device, no CUDA call. Tools use them to predict
+ * a call's launch; they are the same code the calls run.
  *
  * ub_plan_tail_split: into how many k-pieces the CTA-pair kernel cuts each tile of the
  * last, partial wave. `tiles` 256 x 256 output tiles over `pairs` CTA pairs, `k_blocks`

@@ -68,3 +68,40 @@ def test_peak_values_measured_or_fallback(monkeypatch, tmp_path):
     (tmp_path / "MEASURED_PEAKS.json").write_text('{"hbm_gbs": 7000.0}')
     d, src = bench.peaks()
     assert src == "measured" and d["hbm_gbs"] == 7000.0
+
+
+def test_sweep_counts_are_algorithmic():
+    # AG: 2*T*H*N FLOPs; bytes = weight once + shards read + buffer written + Y written
+    fl, nb = bench.op_flops_bytes("ag", 512, 4096, 4, N=3072)
+    assert fl == 2.0 * 512 * 4096 * 3072
+    assert nb == 2.0 * (3072 * 4096 + 2 * 512 * 4096 + 512 * 3072)
+    # SwiGLU writes half the columns
+    _, nb_glu = bench.op_flops_bytes("ag_swiglu", 512, 4096, 4, N=7168)
+    assert nb_glu == 2.0 * (7168 * 4096 + 2 * 512 * 4096 + 512 * 3584)
+    # RS: 2*T*K*H*tp FLOPs; bytes = tp weights + tp A_j + the T output rows
+    fl, nb = bench.op_flops_bytes("rs", 64, 4096, 4, K=3584)
+    assert fl == 2.0 * 64 * 3584 * 4096 * 4
+    assert nb == 2.0 * (4 * 3584 * 4096 + 4 * 64 * 3584 + 64 * 4096)
+
+
+def test_roofline_point_names_the_limiting_roof():
+    # 1 GFLOP over 10 MB (100 FLOP/B) in 1 ms against 2000 TFLOP/s and 8000 GB/s:
+    # the ridge is 250 FLOP/B, so HBM bounds it at 100 * 8000 GB/s = 800 TFLOP/s
+    p = bench.roofline_point(1e9, 1e7, 1e-3, 2000.0, 8000.0)
+    assert p["bound"] == "hbm"
+    assert p["tflops"] == pytest.approx(1.0)
+    assert p["hbm_gbs"] == pytest.approx(10.0)
+    assert p["frac_of_roofline"] == pytest.approx(1.0 / 800.0)
+    # far right of the ridge: the tensor peak bounds it
+    q = bench.roofline_point(1e12, 1e8, 1e-3, 2000.0, 8000.0)
+    assert q["bound"] == "tensor" and q["frac_of_roofline"] == pytest.approx(1000.0 / 2000.0)
+    assert q["frac_of_peak"] == pytest.approx(0.5)
+
+
+def test_default_sweep_covers_the_metric_ladder():
+    names = {n: Ts for n, _, _, Ts in bench.DEFAULT_SWEEP}
+    assert set(names) == {"fc1_ag_swiglu", "fc2_rs", "qkv_ag", "large_rs_k1024", "large_rs_k3584"}
+    for n, Ts in names.items():
+        w = synth.WORKLOADS[dict((a, b) for a, b, _, _ in bench.DEFAULT_SWEEP)[n]]
+        assert all(T % w.tp == 0 and w.tp <= T <= w.max_tokens for T in Ts), n
+    assert min(names["fc2_rs"]) == 4 and max(names["large_rs_k3584"]) == 16384
