@@ -103,8 +103,8 @@ def parse():
                     help="1: kernels launched with programmatic dependent launch (default); 0: plain")
     ap.add_argument("--skinny", type=int, default=-1, choices=[-1, 0, 1],
                     help="few-token kernel: -1 whenever usable (default), 0 never, 1 whenever usable")
-    ap.add_argument("--streamk", type=int, default=-1, choices=[-1, 0, 1],
-                    help="-1: chosen per call (default); 1: the last wave of pair tiles cut into k-pieces; 0: whole tiles")
+    ap.add_argument("--streamk", type=int, default=-1, choices=[-1, 0, 1, 2, 3, 4, 5, 6, 7, 8],
+                    help="-1: chosen per call (default); 1: the last wave of pair tiles cut into as many k-pieces as allowed; 2..8: at most that many; 0: whole tiles")
     return ap.parse_args()
 
 

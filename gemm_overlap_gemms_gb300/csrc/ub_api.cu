@@ -295,25 +295,38 @@ constexpr bool kFusedGatherAuto = true;
 constexpr bool kFusedGatherSkinnyAuto = false;
 
 // Cost of the last, partial wave's tiles when each is cut into s k-pieces, in units of
-// one whole tile on one pair: the longest piece, 1/s, plus the fix-up (the pieces'
-// fp32 partials published and added by the pair holding piece 0). Measured on GB300,
-// the fix-up costs about as much as kFixupKb0 + kFixupKb1 * (s - 1) k-blocks of a
-// 256 x 256 pair tile (9.5 us + 4.2 us per added piece, at 0.31 us per k-block), a fixed
-// time rather than a share of the tile: a split pays off for long K (GEMM-RS over tp
-// shards of K = 1024 .. 3584: 1-39 % faster) and loses for K = 4096 (AG: 1-16 % slower).
+// one whole tile on one pair: the longest piece, 1/s, plus the fix-up (each piece
+// publishes its fp32 partial of the columns it does not own and adds the others' partials
+// of its own). The fix-up is a fixed time rather than a share of the tile, fitted on
+// GB300 in k-blocks of a 256 x 256 pair tile (0.34 us each) by running the same shapes
+// whole and split in 2..8 pieces (bench.py --case ... --streamk 0 | n):
+//  - GEMM-RS: kFixupKb0 + kFixupKb1 * (s - 1), about 10 us + 4.6 us per added piece; a
+//    split pays off for its long K (tp shards of K = 1024 .. 3584: 2-27 % faster).
+//  - AG-GEMM behind the gather (`gathered`): kFixupAgKb0 + kFixupAgKb1 * (s - 1), about
+//    3.4 us + 2.6 us per added piece (K = 4096: QKV at T = 5120 90.5 us in 4 pieces against
+//    96.1 whole, AG + SwiGLU at T = 3072 119.3 in 2 against 124.0). Its tail tiles are the
+//    last rows of the gather, so with fewer than kMinWavesAg whole waves before them they
+//    wait for the gather whatever their length, and a split only adds its fix-up (QKV at
+//    T = 2048, one whole wave: 55.8 us in 2 pieces, 62.0 in 3, against 53.8 whole).
 constexpr double kFixupKb0 = 30.0;
 constexpr double kFixupKb1 = 13.5;
-double split_tail_cost(int64_t s, int64_t kb)
+constexpr double kFixupAgKb0 = 10.0;
+constexpr double kFixupAgKb1 = 7.5;
+constexpr int64_t kMinWavesAg = 2;
+double split_tail_cost(int64_t s, int64_t kb, bool gathered)
 {
     if (s <= 1) return 1.0;
-    return 1.0 / static_cast<double>(s) + (kFixupKb0 + kFixupKb1 * static_cast<double>(s - 1)) / static_cast<double>(kb);
+    const double f = gathered ? kFixupAgKb0 + kFixupAgKb1 * static_cast<double>(s - 1)
+                              : kFixupKb0 + kFixupKb1 * static_cast<double>(s - 1);
+    return 1.0 / static_cast<double>(s) + f / static_cast<double>(kb);
 }
 
 // How many k-pieces the last wave's tiles are cut into. At most one piece per idle pair,
 // MAX_TAIL_SPLIT pieces and MIN_KBLOCKS_PER_PIECE k-blocks per piece; within that the
-// cheapest cut by split_tail_cost (1 when no cut beats whole tiles), or with `widest`
-// the most pieces allowed (the split forced on).
-int64_t tail_split_for(int64_t tiles, int64_t np, int64_t kb, bool widest)
+// cheapest cut by split_tail_cost (1 when no cut beats whole tiles, or for a gathered
+// AG-GEMM with fewer than kMinWavesAg whole waves), or with `force` = 1 the most pieces
+// allowed (the split forced on), with `force` = n >= 2 at most n pieces.
+int64_t tail_split_for(int64_t tiles, int64_t np, int64_t kb, int64_t force, bool gathered)
 {
     const int64_t rem = tiles % np;
     if (rem == 0) return 1;
@@ -321,21 +334,25 @@ int64_t tail_split_for(int64_t tiles, int64_t np, int64_t kb, bool widest)
     if (smax > ubk::MAX_TAIL_SPLIT) smax = ubk::MAX_TAIL_SPLIT;
     if (smax > kb / ubk::MIN_KBLOCKS_PER_PIECE) smax = kb / ubk::MIN_KBLOCKS_PER_PIECE;
     if (smax < 1) return 1;
-    if (widest) return smax;
+    if (force == 1) return smax;
+    if (force >= 2) return force < smax ? force : smax;
+    if (gathered && tiles / np < kMinWavesAg) return 1;
     int64_t best = 1;
     for (int64_t s = 2; s <= smax; ++s)
-        if (split_tail_cost(s, kb) < split_tail_cost(best, kb)) best = s;
+        if (split_tail_cost(s, kb, gathered) < split_tail_cost(best, kb, gathered)) best = s;
     return best;
 }
 
 // Launch shape of a pair-kernel call: whole tiles in strided waves, and (with the
-// split on) the last, partial wave's tiles cut into k-pieces over the idle pairs.
-void set_pairs(ub_handle *h, GemmParams &p, int mode, bool split)
+// split on) the last, partial wave's tiles cut into k-pieces over the idle pairs. With
+// `every_pair` (the gather runs inside the GEMM) every pair is launched even when there
+// are fewer tiles, so that every SM copies its share of the gather.
+void set_pairs(ub_handle *h, GemmParams &p, int mode, bool split, bool every_pair = false, bool gathered = false)
 {
     const int64_t tiles = p.region_tile0[p.n_regions];
     int64_t np = clusters_for(h, mode, 1 << 30);
-    int64_t sp = split ? tail_split_for(tiles, np, p.k_blocks, h->streamk == 1) : 1;
-    if (sp == 1 && np > tiles) np = tiles;
+    int64_t sp = split ? tail_split_for(tiles, np, p.k_blocks, h->streamk > 0 ? h->streamk : 0, gathered) : 1;
+    if (sp == 1 && np > tiles && !every_pair) np = tiles;
     if (np < 1) np = 1;
     p.num_pairs = static_cast<int>(np);
     p.dp_tiles = static_cast<int>((tiles / np) * np);
@@ -366,7 +383,7 @@ void set_skinny(ub_handle *h, GemmParams &p, int slot_mult, int w_bytes)
     int64_t s = slots / p.n_tiles;
     if (s > ubk::SK_MAX_SPLIT) s = ubk::SK_MAX_SPLIT;
     if (s > p.k_blocks / ubk::SK_MIN_KBLOCKS) s = p.k_blocks / ubk::SK_MIN_KBLOCKS;
-    const int64_t ws_cap = 1 + h->ws_slots / (static_cast<int64_t>(p.n_tiles) * slot_mult);
+    const int64_t ws_cap = h->ws_slots / (static_cast<int64_t>(p.n_tiles) * slot_mult);  // every piece publishes
     if (s > ws_cap) s = ws_cap;
     if (s < 1) s = 1;
     p.sk_split = static_cast<int>(s);
@@ -392,12 +409,13 @@ void set_skinny(ub_handle *h, GemmParams &p, int slot_mult, int w_bytes)
 // UB_OPT_CTA_PAIR / UB_OPT_STREAMK >= 0 force a choice. The choice depends only on the
 // shapes and the SM count, so results stay bitwise reproducible.
 void plan_path(int64_t slots, int64_t np, int cta_pair, int streamk, int64_t single_tiles, int64_t pair_tiles,
-               int64_t kb, bool &pair, bool &split)
+               int64_t kb, bool gathered, bool &pair, bool &split)
 {
     const double c_single = static_cast<double>(ceil_div(single_tiles, slots));
     const double c_dp = 0.91 * static_cast<double>(ceil_div(pair_tiles, np));
-    const int64_t s = tail_split_for(pair_tiles, np, kb, streamk == 1);
-    const double c_split = s > 1 ? 0.91 * (static_cast<double>(pair_tiles / np) + split_tail_cost(s, kb)) : c_dp;
+    const int64_t s = tail_split_for(pair_tiles, np, kb, streamk > 0 ? streamk : 0, gathered);
+    const double c_split =
+        s > 1 ? 0.91 * (static_cast<double>(pair_tiles / np) + split_tail_cost(s, kb, gathered)) : c_dp;
     if (cta_pair == 0) {
         pair = false;
     } else if (cta_pair == 1) {
@@ -414,12 +432,12 @@ void plan_path(int64_t slots, int64_t np, int cta_pair, int streamk, int64_t sin
     }
 }
 
-void choose_path(ub_handle *h, int mode, int64_t single_tiles, int64_t pair_tiles, int64_t kb, bool &pair,
-                 bool &split)
+void choose_path(ub_handle *h, int mode, int64_t single_tiles, int64_t pair_tiles, int64_t kb, bool gathered,
+                 bool &pair, bool &split)
 {
     const int64_t slots = h->sm_count - h->sm_margin > 0 ? h->sm_count - h->sm_margin : 1;
     plan_path(slots, clusters_for(h, mode, 1 << 30), static_cast<int>(h->cta_pair), static_cast<int>(h->streamk),
-              single_tiles, pair_tiles, kb, pair, split);
+              single_tiles, pair_tiles, kb, gathered, pair, split);
 }
 
 enum Path : int { PATH_SINGLE = 0, PATH_PAIR = 1, PATH_SKINNY = 2 };
@@ -427,7 +445,10 @@ enum Path : int { PATH_SINGLE = 0, PATH_PAIR = 1, PATH_SKINNY = 2 };
 int launch(ub_handle *h, GemmParams &p, int mode, int path, cudaStream_t s, int prof_op)
 {
     p.pdl = static_cast<int>(h->pdl);
-    const int grid = path == PATH_PAIR ? p.num_pairs : grid_for(h, path == PATH_SKINNY ? p.sk_units : p.num_tiles);
+    // single CTAs: one per tile, or one per SM when the gather runs inside the GEMM
+    const int grid = path == PATH_PAIR ? p.num_pairs
+                                       : grid_for(h, path == PATH_SKINNY ? p.sk_units
+                                                                         : (p.fused_gather ? 1 << 30 : p.num_tiles));
     if (path == PATH_SKINNY && p.sk_split > 1 && grid < p.sk_units)
         return fail(UB_ERR_ARG, "skinny launch: %d split units on %d CTAs", p.sk_units, grid);
     ProfileRing &ring = h->prof[prof_op];
@@ -584,11 +605,12 @@ int join_gather(ub_handle *h, cudaStream_t s)
     return UB_OK;
 }
 
-// A new call's epoch. When `s` is being captured into a CUDA graph, the epoch becomes a
-// constant of the graph, so every replay would find the readiness flags, the partial-tile
-// flags and the abort word still holding it from the replay before. The captured call
-// therefore starts, in stream order, by clearing them (never the sticky status word).
-// An uncaptured call pays nothing: epochs only grow there.
+// A new call's epoch, unique per handle: every wait compares a flag for equality with
+// it, so words left by other calls never match. When `s` is being captured into a CUDA
+// graph the epoch becomes a constant of the graph, so every replay would find the
+// readiness flags, the partial-tile flags and the abort word still holding it from the
+// replay before. The captured call therefore starts, in stream order, by clearing them
+// (never the sticky status word). An uncaptured call pays nothing.
 int begin_call(ub_handle *h, cudaStream_t s, uint32_t &epoch)
 {
     epoch = ++h->epoch;
@@ -784,19 +806,19 @@ int ub_grid_ctas(ub_handle_t h, int *ctas)
     return UB_OK;
 }
 
-int64_t ub_plan_tail_split(int64_t tiles, int64_t pairs, int64_t k_blocks, int widest)
+int64_t ub_plan_tail_split(int64_t tiles, int64_t pairs, int64_t k_blocks, int widest, int gathered)
 {
     if (tiles < 1 || pairs < 1 || k_blocks < 1) return fail(UB_ERR_ARG, "ub_plan_tail_split: sizes must be >= 1");
-    return tail_split_for(tiles, pairs, k_blocks, widest != 0);
+    return tail_split_for(tiles, pairs, k_blocks, widest != 0 ? 1 : 0, gathered != 0);
 }
 
 int ub_plan_path(int64_t single_tiles, int64_t pair_tiles, int64_t k_blocks, int64_t slots, int64_t pairs,
-                 int cta_pair, int streamk, int *pair, int *split)
+                 int cta_pair, int streamk, int gathered, int *pair, int *split)
 {
     if (single_tiles < 1 || pair_tiles < 1 || k_blocks < 1 || slots < 1 || pairs < 1 || !pair || !split)
         return fail(UB_ERR_ARG, "ub_plan_path: sizes must be >= 1 and outputs non-null");
     bool pr = false, sp = false;
-    plan_path(slots, pairs, cta_pair, streamk, single_tiles, pair_tiles, k_blocks, pr, sp);
+    plan_path(slots, pairs, cta_pair, streamk, single_tiles, pair_tiles, k_blocks, gathered != 0, pr, sp);
     *pair = pr ? 1 : 0;
     *split = sp ? 1 : 0;
     return UB_OK;
@@ -863,7 +885,7 @@ static int ag_gemm_impl(ub_handle_t h, const void *const *shards, const void *Wt
     for (int i = 0; i < n_regions; ++i) pair_rows_tiles += ceil_div(regions[i].rows, ubk::PAIR_BM);
     bool pair = false, streamk = false;
     choose_path(h, mode, tp * ceil_div(c, ubk::BM) * n_tiles, pair_rows_tiles * n_tiles,
-                (H + ubk::BK - 1) / ubk::BK, pair, streamk);
+                (H + ubk::BK - 1) / ubk::BK, true, pair, streamk);
     const int64_t c16 = ceil_div(c, 16) * 16;  // token columns of one chunk in the skinny kernel
     const bool skinny = use_skinny(h, tp * c16);
     if (skinny) pair = false;
@@ -967,15 +989,15 @@ static int ag_gemm_impl(ub_handle_t h, const void *const *shards, const void *Wt
     p.abort_word = abort_of(h);
     p.status = status_of(h);
     p.timeout_ns = static_cast<uint64_t>(h->timeout_ns);
+    const bool in_gemm = gather_in_gemm(h, skinny);
     if (skinny) set_skinny(h, p, glu ? 2 : 1, glu ? 2 * ubk::SK_W_BYTES : ubk::SK_W_BYTES);
-    else if (pair) set_pairs(h, p, mode, streamk);
+    else if (pair) set_pairs(h, p, mode, streamk, in_gemm, true);
     uint32_t epoch = 0;
     if (int rc = begin_call(h, s, epoch)) return rc;
     p.epoch = epoch;
     const int64_t drop = h->drop_flag;
     h->drop_flag = -1;
 
-    const bool in_gemm = gather_in_gemm(h, skinny);
     p.fused_gather = in_gemm ? 1 : 0;
     if (in_gemm) {
         for (int r = 0; r < tp; ++r) p.g_src[r] = shards[r];
@@ -1040,7 +1062,7 @@ static int gemm_rs_impl(ub_handle_t h, const void *const *A, const void *const *
     const int64_t n_tiles = (H + ubk::BN - 1) / ubk::BN;
     bool pair = false, streamk = false;
     choose_path(h, ubk::MODE_RS, tp * ceil_div(c, ubk::BM) * n_tiles, ceil_div(T, ubk::PAIR_BM) * n_tiles,
-                tp * ((K + ubk::BK - 1) / ubk::BK), pair, streamk);
+                tp * ((K + ubk::BK - 1) / ubk::BK), false, pair, streamk);
     const int64_t T16 = ceil_div(T, 16) * 16;  // token columns in the skinny kernel
     const bool skinny = use_skinny(h, T16);
     if (skinny) pair = false;
@@ -1193,8 +1215,8 @@ int ub_reduce_scatter(ub_handle_t h, const void *const *P, void *const *Y_shards
     p.H = h->hidden;
     p.c = h->T / tp;
     p.pdl = static_cast<int>(h->pdl);
-    // Small CTAs, four per SM: two fit beside a persistent GEMM CTA on the same SM (the
-    // rest start as GEMM CTAs leave); alone, all four keep enough loads in flight.
+    // Small CTAs, four per SM: alone, they keep enough loads in flight to stream HBM; beside
+    // a persistent GEMM CTA one of them fits on each SM (the rest start as GEMM CTAs leave).
     const int64_t vecs = p.T * (p.H / 8);
     int64_t grid = 4 * static_cast<int64_t>(h->sm_count);
     if (grid > (vecs + 255) / 256) grid = (vecs + 255) / 256;
@@ -1271,7 +1293,7 @@ int ub_wgrad(ub_handle_t h, const void *D, int64_t M, int ub_is_a, void *out, vo
     p.status = status_of(h);
     p.timeout_ns = static_cast<uint64_t>(h->timeout_ns);
     bool pair = true, split = false;
-    choose_path(h, ubk::MODE_AG, 1 << 30, p.region_tile0[1], p.k_blocks, pair, split);
+    choose_path(h, ubk::MODE_AG, 1 << 30, p.region_tile0[1], p.k_blocks, false, pair, split);
     set_pairs(h, p, ubk::MODE_AG, split);
     uint32_t epoch = 0;
     if (int rc = begin_call(h, s, epoch)) return rc;
@@ -1332,7 +1354,7 @@ int ag_gemm_from_buffer(ub_handle_t h, const void *Wt, int64_t N, int64_t glu_f,
     p.status = status_of(h);
     p.timeout_ns = static_cast<uint64_t>(h->timeout_ns);
     bool pair = true, split = false;
-    choose_path(h, mode, 1 << 30, p.region_tile0[1], p.k_blocks, pair, split);
+    choose_path(h, mode, 1 << 30, p.region_tile0[1], p.k_blocks, false, pair, split);
     set_pairs(h, p, mode, split);
     uint32_t epoch = 0;
     if (int rc = begin_call(h, s, epoch)) return rc;
@@ -1373,7 +1395,8 @@ int ub_set_option(ub_handle_t h, int key, int64_t val)
         h->cta_pair = val;
         return UB_OK;
     case UB_OPT_STREAMK:
-        if (val < -1 || val > 1) return fail(UB_ERR_ARG, "streamk must be -1, 0 or 1");
+        if (val < -1 || val > ubk::MAX_TAIL_SPLIT)
+            return fail(UB_ERR_ARG, "streamk must be -1, 0, 1 or a piece count 2..%d", ubk::MAX_TAIL_SPLIT);
         h->streamk = val;
         return UB_OK;
     case UB_OPT_SKINNY:

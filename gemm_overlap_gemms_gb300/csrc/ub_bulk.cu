@@ -8,7 +8,11 @@
 // The work is HBM-bound: (tp + 1) * T * hidden * 2 bytes for tp * T * hidden adds. Each
 // thread owns 8 consecutive columns of one row (16-byte loads and stores, coalesced
 // across the warp); a grid-stride loop covers the active rows only. The CTAs are small
-// (256 threads, no shared memory) so that they fit on SMs beside a persistent GEMM CTA.
+// (256 threads, no shared memory), four per SM, so that together they keep enough loads
+// in flight to stream HBM, and one fits on an SM beside a persistent GEMM CTA. Beside a
+// GEMM that streams its operands at full rate, the reduce-scatter's loads queue behind
+// the GEMM's (measured: it runs at about a fifth of its speed alone), which limits how
+// much of it the bulk overlap hides.
 #include <cuda_bf16.h>
 
 #include "ub_internal.h"

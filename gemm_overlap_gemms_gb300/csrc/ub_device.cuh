@@ -289,15 +289,26 @@ __device__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t timeout_
     return true;
 }
 
-// Wait until the readiness flag of a chunk has reached this call's epoch (wrap-safe),
-// then order the tensor-memory-accelerator reads that follow after it.
-__device__ bool wait_flag(const uint32_t *flag, const WaitCtx &w)
+// Wait until the readiness flag of every chunk in `mask` holds this call's epoch, then
+// order the tensor-memory-accelerator reads that follow after them. Epochs are unique per
+// handle (a call captured into a graph clears the flags in stream order before it
+// starts), so a flag left by any other call never matches. Every flag still pending is
+// read with an acquire load on each pass, the passes 512 ns apart: every producer thread
+// of the grid polls the same few words, and faster polling queues on the L2 slice that
+// holds them, in front of the operand loads (measured on GB300: polling every 128 ns made
+// the AG-GEMM 1-2 % slower at T = 1024-4096). Once all are set, one proxy fence orders the
+// async-proxy (TMA) reads of the chunks after the acquires.
+__device__ bool wait_flags(const uint32_t *flags, uint32_t mask, const WaitCtx &w)
 {
     WaitClock clk;
     for (uint32_t n = 0;; ++n) {
-        uint32_t v;
-        asm volatile("ld.acquire.sys.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
-        if (static_cast<int32_t>(v - w.epoch) >= 0) {
+        for (uint32_t m = mask; m != 0u; m &= m - 1u) {
+            const int r = __ffs(static_cast<int>(m)) - 1;
+            uint32_t v;
+            asm volatile("ld.acquire.sys.global.u32 %0, [%1];" : "=r"(v) : "l"(flags + r) : "memory");
+            if (v == w.epoch) mask &= ~(1u << r);
+        }
+        if (mask == 0u) {
             asm volatile("fence.proxy.async.global;" ::: "memory");
             return true;
         }
@@ -306,6 +317,8 @@ __device__ bool wait_flag(const uint32_t *flag, const WaitCtx &w)
     }
 }
 
+// The same for one chunk's flag.
+__device__ __forceinline__ bool wait_flag(const uint32_t *flag, const WaitCtx &w) { return wait_flags(flag, 1u, w); }
 
 __device__ __forceinline__ void st_release_u32(uint32_t *ptr, uint32_t v)
 {

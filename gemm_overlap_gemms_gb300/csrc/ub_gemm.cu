@@ -679,20 +679,33 @@ __global__ void __maxnreg__(PAIR_MAX_REGS) ub_gemm_pair_kernel(const __grid_cons
             const int lrow0 = x.m * PAIR_BM + static_cast<int>(rank) * 128 + quarter * 32;  // inside the region
             const int prow = quarter * 32 + lane;  // this thread's row inside the CTA's 128
 
-            if (k0 > 0) {
-                // Not the tile's first piece: publish the fp32 partial for the finisher.
+            // A tile of the split last wave: its k-pieces are held by pairs p0 .. p0 + sp - 1
+            // (piece q here), and each piece owns an equal share of the tile's output
+            // units (64-column groups; with SwiGLU, 64-feature groups of gate and up
+            // columns). A piece publishes its fp32 partial of the units it does not own,
+            // then adds the other pieces' partials of its own units (own accumulator
+            // first, then the pieces in order: deterministic for a given launch shape) and
+            // stores them, so the fix-up of a tile is shared by its pairs. Whole tiles own
+            // every unit and publish nothing.
+            constexpr int UNITS = GLU ? 2 : BN / STORE_COLS;
+            const bool split_seg = k1 - k0 < KB;
+            const int sp = split_seg ? p.tail_split : 1;
+            const int q = split_seg ? pair % sp : 0;
+            const int p0 = pair - q;
+            const int u_lo = q * UNITS / sp, u_hi = (q + 1) * UNITS / sp;
+            auto owned = [&](int sub) {  // 64-column group `sub` of the accumulator (0..3)
+                const int u = GLU ? (sub & 1) : sub;
+                return u >= u_lo && u < u_hi;
+            };
+            if (split_seg) {
                 float4 *dst = reinterpret_cast<float4 *>(p.ws + static_cast<size_t>(pair * 2 + rank) * PARTIAL_FLOATS);
 #pragma unroll 1
                 for (int sub = 0; sub < BN / STORE_COLS; ++sub) {
+                    if (owned(sub)) continue;
                     uint32_t v[STORE_COLS];
                     tmem_ld32(trow + sub * STORE_COLS, v);
                     tmem_ld32(trow + sub * STORE_COLS + 32, v + 32);
                     tmem_wait_ld();
-                    if (sub == BN / STORE_COLS - 1) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
-                    }
 #pragma unroll
                     for (int i = 0; i < STORE_COLS / 4; ++i)
                         __stcg(dst + (sub * (STORE_COLS / 4) + i) * 128 + prow,
@@ -704,25 +717,22 @@ __global__ void __maxnreg__(PAIR_MAX_REGS) ub_gemm_pair_kernel(const __grid_cons
                     __threadfence();
                     st_release_u32(p.ws_flags + my_slot, p.epoch);
                 }
-                continue;
-            }
-
-            // This pair holds piece 0 of the tile: collect the partials of the pairs that
-            // hold its other pieces (pair + 1 ... pair + split - 1, in order).
-            int n_contrib = 0;
-            if (k1 < KB) {
+                if (u_lo == u_hi) {
+                    // Nothing to store here: release the accumulator.
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
+                    continue;
+                }
                 bool okw = true;
-                for (int cp = pair + 1; cp < pair + p.tail_split && cp < p.num_pairs; ++cp) {
+                for (int k = 0; okw && k < sp; ++k) {
+                    if (k == q || p0 + k >= p.num_pairs) continue;
                     int got = 1;
                     if (lane == 0) {
-                        const uint32_t *f = p.ws_flags + (cp * 2 + static_cast<int>(rank)) * EPI_WARPS + quarter;
+                        const uint32_t *f = p.ws_flags + ((p0 + k) * 2 + static_cast<int>(rank)) * EPI_WARPS + quarter;
                         got = wait_partial(f, w) ? 1 : 0;
                     }
-                    if (!__shfl_sync(0xffffffffu, got, 0)) {
-                        okw = false;
-                        break;
-                    }
-                    ++n_contrib;
+                    okw = __shfl_sync(0xffffffffu, got, 0) != 0;
                 }
                 if (!okw) {
                     // Abort: release the accumulator so the MMA side is not left waiting.
@@ -732,6 +742,10 @@ __global__ void __maxnreg__(PAIR_MAX_REGS) ub_gemm_pair_kernel(const __grid_cons
                     break;
                 }
             }
+            // The partials added into an owned unit: the other pieces' slots, in piece order.
+            auto contrib = [&](int k) -> const float4 * {
+                return reinterpret_cast<const float4 *>(p.ws + static_cast<size_t>((p0 + k) * 2 + rank) * PARTIAL_FLOATS);
+            };
 
             if constexpr (GLU) {
                 // Two output groups of 64 columns: gate columns [64h, 64h + 64) and up
@@ -741,7 +755,7 @@ __global__ void __maxnreg__(PAIR_MAX_REGS) ub_gemm_pair_kernel(const __grid_cons
                 // the IEEE division the epilogue slowed the whole call by 3-9 % on GB300
                 // (T = 2048: 80.9 against 74.2 us).
 #pragma unroll 1
-                for (int hs = 0; hs < 2; ++hs) {
+                for (int hs = u_lo; hs < u_hi; ++hs) {
                     // 32 columns at a time keeps the live registers low enough for the
                     // kernel's register cap.
                     uint32_t pk[STORE_COLS / 2];
@@ -752,14 +766,14 @@ __global__ void __maxnreg__(PAIR_MAX_REGS) ub_gemm_pair_kernel(const __grid_cons
                         tmem_ld32(trow + c0, g);
                         tmem_ld32(trow + 128 + c0, u);
                         tmem_wait_ld();
-                        if (hs == 1 && hf == 1) {
+                        if (hs == u_hi - 1 && hf == 1) {
                             tc_fence_before();
                             __syncwarp();
                             if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
                         }
-                        for (int ci = 1; ci <= n_contrib; ++ci) {
-                            const float4 *src = reinterpret_cast<const float4 *>(
-                                p.ws + static_cast<size_t>((pair + ci) * 2 + rank) * PARTIAL_FLOATS);
+                        for (int k = 0; k < sp; ++k) {
+                            if (k == q) continue;
+                            const float4 *src = contrib(k);
 #pragma unroll
                             for (int i = 0; i < 8; ++i) {
                                 const float4 a = __ldcg(src + (c0 / 4 + i) * 128 + prow);
@@ -802,19 +816,19 @@ __global__ void __maxnreg__(PAIR_MAX_REGS) ub_gemm_pair_kernel(const __grid_cons
                 }
             } else {
 #pragma unroll 1
-                for (int sub = 0; sub < BN / STORE_COLS; ++sub) {
+                for (int sub = u_lo; sub < u_hi; ++sub) {
                     uint32_t v[STORE_COLS];
                     tmem_ld32(trow + sub * STORE_COLS, v);
                     tmem_ld32(trow + sub * STORE_COLS + 32, v + 32);
                     tmem_wait_ld();
-                    if (sub == BN / STORE_COLS - 1) {
+                    if (sub == u_hi - 1) {
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
                     }
-                    for (int ci = 1; ci <= n_contrib; ++ci) {
-                        const float4 *src = reinterpret_cast<const float4 *>(
-                            p.ws + static_cast<size_t>((pair + ci) * 2 + rank) * PARTIAL_FLOATS);
+                    for (int k = 0; k < sp; ++k) {
+                        if (k == q) continue;
+                        const float4 *src = contrib(k);
 #pragma unroll
                         for (int i = 0; i < STORE_COLS / 4; ++i) {
                             const float4 q = __ldcg(src + (sub * (STORE_COLS / 4) + i) * 128 + prow);

@@ -178,7 +178,8 @@ extern "C" int ag_gemm_noalloc(const void *const *shards, int tp, int64_t T, int
     p.n_tiles = static_cast<int>((N + ubk::BN - 1) / ubk::BN);
     p.num_tiles = tp * p.m_tiles * p.n_tiles;
     p.self_rank = 0;
-    const uint32_t epoch = ++ds.epoch;  // flags are never reset: epochs only grow
+    uint32_t epoch = ++ds.epoch;  // flags are never reset: epochs only grow
+    if (epoch == 0) epoch = ++ds.epoch;  // 0 is what a cleared flag holds
     p.epoch = epoch;
 
     // The status word keeps the previous call's value: clear it for this call.

@@ -12,10 +12,11 @@
 //
 // with N = the tokens rounded up to 16: the MMA work follows T, and the weight is read
 // from HBM exactly once per call. The K range of each weight panel is cut into pieces
-// so that about one work unit (panel, piece) runs per SM; the unit holding the last
-// piece of a panel adds the other pieces' fp32 partials (published in the workspace
-// with the call's epoch, added in piece order: deterministic for a given launch shape)
-// and writes the outputs.
+// so that about one work unit (panel, piece) runs per SM. Each piece owns an equal
+// share of the token columns: it publishes its fp32 partial of the other columns in the
+// workspace (with the call's epoch), adds the other pieces' partials of its own columns
+// in a fixed order (deterministic for a given launch shape) and writes their outputs,
+// so the pieces of a panel share its fix-up.
 //
 //  * AG (column-parallel, QKV / fc1): the tokens are the gathered chunks. Sub-tile r of
 //    the token tile holds chunk r's c rows (the self chunk read in place from its shard,
@@ -84,7 +85,7 @@ __device__ __forceinline__ Unit unit_at(int u, const GemmParams &p)
     return x;
 }
 
-// Workspace slot of a unit that is not its tile's last piece (SwiGLU units take two).
+// Workspace slot of a unit's published partial (SwiGLU units take two slots' room).
 __device__ __forceinline__ int partial_slot(const Unit &x, const GemmParams &p) { return x.piece * p.n_tiles + x.tile; }
 
 template <int MODE>
@@ -215,8 +216,8 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_skinny_kernel(const __grid
                     // The weight ran ahead as far as the stages allow (or the piece
                     // ended); now the chunks must have landed. Then the token loads of
                     // the stages issued so far (AG: k-blocks pend_kb .. kb).
-                    for (int r = 0; ok && r < p.tp; ++r)
-                        if (r != p.self_rank && !wait_flag(p.flags + r, w)) ok = false;
+                    const uint32_t others = ((1u << p.tp) - 1u) & ~(1u << p.self_rank);
+                    if (!wait_flags(p.flags, others, w)) ok = false;
                     if (!ok) break;
                     ready = true;
                     for (int q = pend_kb; q <= kb; ++q) {
@@ -315,12 +316,22 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_skinny_kernel(const __grid
 
             constexpr int HALVES = GLU ? 2 : 1;
             constexpr int COLS4 = (GLU ? 2 * SK_MAX_COLS : SK_MAX_COLS) / 4;  // float4 columns of a slot
-            if (x.piece != p.sk_split - 1) {
-                // Not the tile's last piece: publish the fp32 partial for the finisher.
+            // With the tile's K range cut into s pieces, piece q owns the token columns of
+            // the 16-column groups [q * g16 / s, (q + 1) * g16 / s): it publishes its fp32
+            // partial of every other column for the pieces that own them, then adds the
+            // other pieces' partials of its own columns and writes their outputs, so the
+            // fix-up of a tile is shared by its s CTAs (all resident: one unit per CTA).
+            const int nsplit = p.sk_split;
+            const int q = x.piece;
+            const int g16 = acc_cols / 16;
+            const int c_lo = q * g16 / nsplit * 16, c_hi = (q + 1) * g16 / nsplit * 16;
+            const int np = nsplit - 1;  // partials added into the own columns
+            if (np > 0) {
                 float4 *dst = reinterpret_cast<float4 *>(p.ws + static_cast<size_t>(partial_slot(x, p)) * SLOT_FLOATS) +
                               quarter * COLS4 * 32 + lane;
 #pragma unroll 1
                 for (int c0 = 0; c0 < acc_cols; c0 += 16) {
+                    if (c0 >= c_lo && c0 < c_hi) continue;
 #pragma unroll
                     for (int h = 0; h < HALVES; ++h) {
                         const int tc = h * p.sk_stride + c0;
@@ -334,25 +345,21 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_skinny_kernel(const __grid
                                                __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])));
                     }
                 }
-                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(tempty_bar(acc));
                     __threadfence();
                     st_release_u32(p.ws_flags + partial_slot(x, p) * EPI_WARPS + quarter, p.epoch);
                 }
-                continue;
             }
 
-            // The last piece finishes the tile. The other pieces' partials of this warp's
-            // rows are streamed into this warp's part of the (now idle) stage buffers by
-            // bulk copies, a chunk of columns at a time, two chunks in flight; the sums
-            // run in a fixed order (own accumulator, then pieces 0, 1, ...).
-            const int np = p.sk_split - 1;
+            // The other pieces' partials of the own columns are streamed into this warp's
+            // part of the (now idle) stage buffers by bulk copies, a chunk of columns at a
+            // time, two chunks in flight; the sums run in a fixed order (own accumulator,
+            // then the other pieces in piece order).
             int okw = 1;
-            if (np > 0 && lane == 0) {
-                for (int pc = 0; okw && pc < np; ++pc)
-                    okw = wait_partial(p.ws_flags + (pc * p.n_tiles + x.tile) * EPI_WARPS + quarter, w) ? 1 : 0;
+            if (np > 0 && c_hi > c_lo && lane == 0) {
+                for (int pc = 0; okw && pc < nsplit; ++pc)
+                    if (pc != q) okw = wait_partial(p.ws_flags + (pc * p.n_tiles + x.tile) * EPI_WARPS + quarter, w) ? 1 : 0;
                 asm volatile("fence.proxy.async.global;" ::: "memory");  // bulk copies read what was acquired
             }
             if (!__shfl_sync(0xffffffffu, okw, 0)) {
@@ -363,25 +370,26 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_skinny_kernel(const __grid
             }
             constexpr int CH = FIX_CHUNK_COLS / HALVES;  // columns per chunk
             const uint32_t fbuf = smem_u32(base) + static_cast<uint32_t>((warp - 2) * 2 * FIX_BUF_BYTES);
-            const int n_chunks = (acc_cols + CH - 1) / CH;
+            const int n_chunks = (c_hi - c_lo + CH - 1) / CH;
             auto issue_chunk = [&](int ci) {
-                const int c_lo = ci * CH;
-                const int cols = acc_cols - c_lo < CH ? acc_cols - c_lo : CH;
+                const int ca = c_lo + ci * CH;
+                const int cols = c_hi - ca < CH ? c_hi - ca : CH;
                 const uint32_t bytes = static_cast<uint32_t>(cols) * 128u;
                 const uint32_t bar = fix_bar(warp - 2, ci & 1);
                 const uint32_t dst0 = fbuf + static_cast<uint32_t>((ci & 1) * FIX_BUF_BYTES);
                 mbar_arrive_expect_tx(bar, bytes * static_cast<uint32_t>(np * HALVES));
-                for (int pc = 0; pc < np; ++pc) {
+                for (int k = 0; k < np; ++k) {
+                    const int pc = k < q ? k : k + 1;
                     const float4 *src = reinterpret_cast<const float4 *>(
                                             p.ws + static_cast<size_t>(pc * p.n_tiles + x.tile) * SLOT_FLOATS) +
                                         quarter * COLS4 * 32;
                     for (int h = 0; h < HALVES; ++h)
-                        bulk_load(dst0 + static_cast<uint32_t>((pc * HALVES + h) * CH * 128),
-                                  src + ((h * p.sk_stride + c_lo) / 4) * 32, bytes, bar);
+                        bulk_load(dst0 + static_cast<uint32_t>((k * HALVES + h) * CH * 128),
+                                  src + ((h * p.sk_stride + ca) / 4) * 32, bytes, bar);
                 }
             };
             if (np > 0 && lane == 0) {
-                issue_chunk(0);
+                if (n_chunks > 0) issue_chunk(0);
                 if (n_chunks > 1) issue_chunk(1);
             }
             const int n = x.tile * SK_BM + row;  // output column (feature) of this thread
@@ -398,9 +406,10 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_skinny_kernel(const __grid
                     }
                 }
                 const uint32_t buf = fbuf + static_cast<uint32_t>((ci & 1) * FIX_BUF_BYTES);
-                const int c_hi = (ci + 1) * CH < acc_cols ? (ci + 1) * CH : acc_cols;
+                const int ca = c_lo + ci * CH;
+                const int cb = ca + CH < c_hi ? ca + CH : c_hi;
 #pragma unroll 1
-                for (int c0 = ci * CH; c0 < c_hi; c0 += 16) {
+                for (int c0 = ca; c0 < cb; c0 += 16) {
                     float a[16], b[16];
                     {
                         uint32_t v[16];
@@ -415,22 +424,22 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_skinny_kernel(const __grid
                             for (int i = 0; i < 16; ++i) b[i] = __uint_as_float(v[i]);
                         }
                     }
-                    for (int pc = 0; pc < np; ++pc) {
+                    for (int k = 0; k < np; ++k) {
 #pragma unroll
                         for (int h = 0; h < HALVES; ++h) {
                             float *acc_h = h == 0 ? a : b;
                             const uint32_t src =
-                                buf + static_cast<uint32_t>((pc * HALVES + h) * CH * 128 + (c0 - ci * CH) * 128) + lane * 16u;
+                                buf + static_cast<uint32_t>((k * HALVES + h) * CH * 128 + (c0 - ca) * 128) + lane * 16u;
 #pragma unroll
                             for (int i = 0; i < 4; ++i) {
-                                float4 q;
+                                float4 f;
                                 asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                                             : "=f"(q.x), "=f"(q.y), "=f"(q.z), "=f"(q.w)
+                                             : "=f"(f.x), "=f"(f.y), "=f"(f.z), "=f"(f.w)
                                              : "r"(src + i * 512u));
-                                acc_h[4 * i] += q.x;
-                                acc_h[4 * i + 1] += q.y;
-                                acc_h[4 * i + 2] += q.z;
-                                acc_h[4 * i + 3] += q.w;
+                                acc_h[4 * i] += f.x;
+                                acc_h[4 * i + 1] += f.y;
+                                acc_h[4 * i + 2] += f.z;
+                                acc_h[4 * i + 3] += f.w;
                             }
                         }
                     }

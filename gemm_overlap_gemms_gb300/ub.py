@@ -103,8 +103,8 @@ def load():
         "ub_last_error": [],
         "ag_gemm_noalloc": [PP, I, I64, I64, P, I64, P, P],
         "ag_gemm_from_buffer": [P, P, I64, I64, P, P],
-        "ub_plan_tail_split": [I64, I64, I64, I],
-        "ub_plan_path": [I64, I64, I64, I64, I64, I, I, ctypes.POINTER(I), ctypes.POINTER(I)],
+        "ub_plan_tail_split": [I64, I64, I64, I, I],
+        "ub_plan_path": [I64, I64, I64, I64, I64, I, I, I, ctypes.POINTER(I), ctypes.POINTER(I)],
         "ub_plan_ag_self_head": [I64, I, I, I64, I64],
         "ub_plan_gather_parts": [I, I, I64, I64, ctypes.POINTER(I), ctypes.POINTER(I64), ctypes.POINTER(I64),
                                  ctypes.POINTER(I)],
@@ -134,17 +134,18 @@ def _plan_check(v: int) -> int:
     return int(v)
 
 
-def plan_tail_split(tiles: int, pairs: int, k_blocks: int, widest: bool = False) -> int:
-    """k-pieces per tile of the CTA-pair kernel's last, partial wave (1: whole tiles)."""
-    return _plan_check(load().ub_plan_tail_split(tiles, pairs, k_blocks, 1 if widest else 0))
+def plan_tail_split(tiles: int, pairs: int, k_blocks: int, widest: bool = False, gathered: bool = False) -> int:
+    """k-pieces per tile of the CTA-pair kernel's last, partial wave (1: whole tiles);
+    `gathered` for an AG-GEMM whose rows come through the all-gather."""
+    return _plan_check(load().ub_plan_tail_split(tiles, pairs, k_blocks, 1 if widest else 0, 1 if gathered else 0))
 
 
 def plan_path(single_tiles: int, pair_tiles: int, k_blocks: int, slots: int, pairs: int,
-              cta_pair: int = -1, streamk: int = -1) -> tuple:
+              cta_pair: int = -1, streamk: int = -1, gathered: bool = False) -> tuple:
     """(pair, split) for a tile-kernel call: CTA pairs or single CTAs, split last wave."""
     pr, sp = ctypes.c_int(0), ctypes.c_int(0)
     rc = load().ub_plan_path(single_tiles, pair_tiles, k_blocks, slots, pairs, cta_pair, streamk,
-                             ctypes.byref(pr), ctypes.byref(sp))
+                             1 if gathered else 0, ctypes.byref(pr), ctypes.byref(sp))
     _check(rc)
     return bool(pr.value), bool(sp.value)
 

@@ -85,8 +85,9 @@ enum {
                               128x256 tiles on single CTAs */
     UB_OPT_STREAMK = 7,    /* pair tiles only. -1 (default) = chosen per call; 1 = the last,
                               partial wave's tiles are cut into equal k-pieces spread over the
-                              idle pairs (fixed-order fp32 fix-up: deterministic); 0 = whole
-                              tiles only */
+                              idle pairs, as many as allowed (fixed-order fp32 fix-up:
+                              deterministic); 2..8 = the same with at most that many pieces;
+                              0 = whole tiles only */
     UB_OPT_COPY_STREAMS = 8, /* side streams the ag_gemm chunk copies are dealt over
                               (round-robin in ring order), 1..UB_MAX_TP; default min(tp, 4).
                               0 = no overlap: the copies and flag writes go on the call's own
@@ -396,18 +397,21 @@ int ag_gemm_noalloc(const void *const *shards, int tp, int64_t T, int64_t hidden
  *
  * ub_plan_tail_split: into how many k-pieces the CTA-pair kernel cuts each tile of the
  * last, partial wave. `tiles` 256 x 256 output tiles over `pairs` CTA pairs, `k_blocks`
- * 64-wide k-blocks per tile (GEMM-RS: over all tp shards). At most one piece per idle
- * pair, 8 pieces and 16 k-blocks per piece; within that, widest != 0 (the split forced
- * on, UB_OPT_STREAMK = 1) gives the most pieces, else the cheapest cut by the fix-up
- * cost model (the longest piece plus a fixed fix-up time per added piece, fitted on
- * GB300). Returns the piece count (1 = whole tiles), or UB_ERR_ARG for sizes < 1.
+ * 64-wide k-blocks per tile (GEMM-RS: over all tp shards); `gathered` != 0 for an
+ * AG-GEMM whose rows come through the all-gather. At most one piece per idle pair, 8
+ * pieces and 16 k-blocks per piece; within that, widest != 0 (the split forced on,
+ * UB_OPT_STREAMK = 1) gives the most pieces, else the cheapest cut by the fix-up cost
+ * model (the longest piece plus a fixed fix-up time per added piece, fitted on GB300
+ * separately for GEMM-RS and for a gathered AG-GEMM, which also needs two whole waves
+ * before its last). Returns the piece count (1 = whole tiles), or UB_ERR_ARG for sizes
+ * < 1.
  *
  * ub_plan_path: whether a tile-kernel call runs on CTA pairs (*pair = 1) or single CTAs
  * (*pair = 0), and whether the pairs split the last wave (*split). `single_tiles`
  * 128 x 256 tiles over `slots` SMs against `pair_tiles` 256 x 256 tiles over `pairs`
  * pairs; `cta_pair` and `streamk` as UB_OPT_CTA_PAIR and UB_OPT_STREAMK (-1: chosen by
- * the wave-count cost model; 0 / 1: forced). Returns UB_OK, or UB_ERR_ARG for sizes < 1
- * or null outputs.
+ * the wave-count cost model; 0 / 1: forced); `gathered` as for ub_plan_tail_split.
+ * Returns UB_OK, or UB_ERR_ARG for sizes < 1 or null outputs.
  *
  * ub_plan_ag_self_head: how many rows of the self chunk the CTA-pair AG kernel reads in
  * place from its shard (the rest from the user buffer, behind the chunk's readiness
@@ -415,9 +419,9 @@ int ag_gemm_noalloc(const void *const *shards, int tp, int64_t T, int64_t hidden
  * `pairs` pairs over `n_tiles` N tiles (self: the ring's start rank). Returns the row
  * count, or UB_ERR_ARG for an invalid shape.
  */
-int64_t ub_plan_tail_split(int64_t tiles, int64_t pairs, int64_t k_blocks, int widest);
+int64_t ub_plan_tail_split(int64_t tiles, int64_t pairs, int64_t k_blocks, int widest, int gathered);
 int ub_plan_path(int64_t single_tiles, int64_t pair_tiles, int64_t k_blocks, int64_t slots, int64_t pairs,
-                 int cta_pair, int streamk, int *pair, int *split);
+                 int cta_pair, int streamk, int gathered, int *pair, int *split);
 int64_t ub_plan_ag_self_head(int64_t T, int tp, int self, int64_t n_tiles, int64_t pairs);
 
 /*

@@ -1,7 +1,11 @@
 """GPU parity at the full workload sizes, in the launch configuration the benchmark
 times: every row of the gathered buffer and every capacity tail is checked exactly;
-the GEMM outputs are checked on sampled rows (every chunk's first, last and tile-edge
-rows, plus seeded random rows) against the oracle computed row by row."""
+the GEMM outputs are checked on sampled rows against the oracle computed row by row.
+The rows: every chunk's first, last and tile-edge rows, one seeded random row in every
+64-row window of the active prefix (so every output tile of every call is hit, whatever
+tiling the call chose: 256-row pair tiles by region, 128-row chunk-aligned tiles, the
+split last wave, the partial tiles at region and chunk ends), plus seeded random rows.
+A sampled row is compared across all of its columns."""
 import math
 
 import numpy as np
@@ -15,18 +19,24 @@ from gpu_helpers import assert_close, dev, is_sentinel, sentinel
 pytestmark = pytest.mark.gpu
 
 
-def sample_rows(T: int, tp: int, n_random: int, rng: np.random.Generator) -> np.ndarray:
+WINDOW = 64  # one sampled row per this many active rows
+
+
+def sample_rows(T: int, tp: int, n_random: int, rng: np.random.Generator, window: int | None = WINDOW) -> np.ndarray:
     c = T // tp
     rows = set()
     for r in range(tp):
         for i in (0, 1, 127, 128, 255, 256, c - 1):
             if 0 <= i < c:
                 rows.add(r * c + i)
+    if window:
+        for lo in range(0, T, window):
+            rows.add(int(rng.integers(lo, min(lo + window, T))))
     rows.update(int(x) for x in rng.integers(0, T, size=n_random))
     return np.array(sorted(rows), dtype=np.int64)
 
 
-def check_ag(buf, T, N, g, rng, Wt=None, n_random=24):
+def check_ag(buf, T, N, g, rng, Wt=None, n_random=24, window=WINDOW):
     """One AG-GEMM at active T with fresh shards; returns Wt for reuse."""
     tp, H, cap = buf.tp, buf.hidden, buf.max_tokens
     c = T // tp
@@ -47,13 +57,13 @@ def check_ag(buf, T, N, g, rng, Wt=None, n_random=24):
     np.testing.assert_array_equal(synth.to_u16(whole[:T]), G, err_msg="gather T=%d" % T)
     assert is_sentinel(whole[T:]), "buffer rows >= %d touched" % T
     assert is_sentinel(Y[T:]), "Y rows >= %d touched" % T
-    rows = sample_rows(T, tp, n_random, rng)
+    rows = sample_rows(T, tp, n_random, rng, window)
     ref = oracle.gemm_rows(G, synth.to_u16(Wt), rows)
     assert_close(Y[torch.as_tensor(rows, device=dev())], ref, "AG T=%d N=%d" % (T, N))
     return Wt
 
 
-def check_rs(buf, T, K, g, rng, Bt=None, n_random=16):
+def check_rs(buf, T, K, g, rng, Bt=None, n_random=16, window=WINDOW):
     tp, H = buf.tp, buf.hidden
     c = T // tp
     buf.set_active_shape([T, H])
@@ -68,7 +78,7 @@ def check_rs(buf, T, K, g, rng, Bt=None, n_random=16):
     assert buf.query_status() == ub.UB_OK
     for r in range(tp):
         assert is_sentinel(big[r * (c + pad) + c:(r + 1) * (c + pad)]), "guard after block %d" % r
-    rows = sample_rows(T, tp, n_random, rng)
+    rows = sample_rows(T, tp, n_random, rng, window)
     ridx = torch.as_tensor(rows, device=dev())
     ref, owner, local = oracle.gemm_rs_rows([synth.to_u16(a[ridx]) for a in A],
                                             [synth.to_u16(b) for b in Bt], rows, T)
@@ -110,7 +120,7 @@ def test_large_workload():
         B = {K: None for K in w.rs_k}
         for T in Ts[:2] + [w.max_tokens]:
             for K in w.rs_k:
-                B[K] = check_rs(buf, T, K, g, rng, B[K], n_random=8)
+                B[K] = check_rs(buf, T, K, g, rng, B[K], n_random=8, window=128)
 
 
 def test_active_shape_stress_64_microbatches():
@@ -123,8 +133,9 @@ def test_active_shape_stress_64_microbatches():
         ptr = buf.buffer_ptr()
         Wt = Bt = None
         for T in Ts:
-            Wt = check_ag(buf, T, w.ag_n[0], g, rng, Wt, n_random=4)
-            Bt = check_rs(buf, T, w.rs_k[0], g, rng, Bt, n_random=2)
+            # 16 seeded random rows per call on top of every chunk's edge rows
+            Wt = check_ag(buf, T, w.ag_n[0], g, rng, Wt, n_random=16, window=None)
+            Bt = check_rs(buf, T, w.rs_k[0], g, rng, Bt, n_random=16, window=None)
         c = buf.counters()
         assert c["device_allocations"] == 3
         assert c["ag_calls"] == 64 and c["rs_calls"] == 64

@@ -48,18 +48,29 @@ def test_tail_split_grows_with_k():
             prev = s
 
 
-@pytest.mark.parametrize("what,tiles,kb,split", [
-    # measured on GB300, whole tiles against a split last wave (bench.py --case ... --streamk 0|1)
-    ("QKV AG T=2048: 46.2 us whole, 55.0 split in 3", 96, 64, False),
-    ("SwiGLU fc1 AG T=1024: 52.8 us whole, 55.9 split in 2", 112, 64, False),
-    ("SwiGLU fc1 AG T=512: 47.0 us whole, 51.8 split in 2", 112, 64, False),
-    ("SwiGLU fc2 RS T=512: 72.3 us whole, 52.0 split in 2", 32, 224, True),
-    ("SwiGLU fc2 RS T=1536: 140.7 us whole, 114.1 split in 3", 96, 224, True),
-    ("SwiGLU fc2 RS T=4096: 292.0 us whole, 272.9 split in 2", 256, 224, True),
-    ("large RS K=3584 T=2048: 601.6 us whole, 561.3 split in 2", 256, 448, True),
+@pytest.mark.parametrize("what,tiles,kb,gathered,split", [
+    # measured on GB300, whole tiles against a split last wave (one call from a CUDA graph,
+    # L2 flushed before it, median of 20; bench.py --case ... --streamk 0|n gives the same)
+    ("QKV AG T=2048 (one whole wave): 53.8 us whole, 55.8 split in 2, 62.0 in 3", 96, 64, True, False),
+    ("SwiGLU fc1 AG+SwiGLU T=1024 (one whole wave): 62.5 us whole, 64.1 split in 2", 112, 64, True, False),
+    ("QKV AG T=5120 (three whole waves): 96.1 us whole, 90.5 split in 4", 240, 64, True, True),
+    ("SwiGLU fc1 AG+SwiGLU T=3072 (four whole waves): 124.0 us whole, 119.3 split in 2", 336, 64, True, True),
+    ("SwiGLU fc2 RS T=512: 78.4 us whole, 57.9 split in 2", 32, 224, False, True),
+    ("SwiGLU fc2 RS T=1536: 144.6 us whole, 113.2 split in 3", 96, 224, False, True),
+    ("SwiGLU fc2 RS T=4096: 292.6 us whole, 268.8 split in 2", 256, 224, False, True),
+    ("large RS K=1024 T=2048: 180.7 us whole, 168.4 split in 2", 256, 128, False, True),
+    ("large RS K=3584 T=2048: 614.2 us whole, 561.7 split in 2", 256, 448, False, True),
 ])
-def test_tail_split_follows_the_measured_winner(what, tiles, kb, split):
-    assert (ub.plan_tail_split(tiles, PAIRS, kb) > 1) == split, what
+def test_tail_split_follows_the_measured_winner(what, tiles, kb, gathered, split):
+    assert (ub.plan_tail_split(tiles, PAIRS, kb, gathered=gathered) > 1) == split, what
+
+
+def test_gathered_ag_splits_only_after_two_whole_waves():
+    for tiles in range(1, 6 * PAIRS):
+        s = ub.plan_tail_split(tiles, PAIRS, 64, gathered=True)
+        if tiles // PAIRS < 2:
+            assert s == 1, tiles
+        assert s <= ub.plan_tail_split(tiles, PAIRS, 64, widest=True, gathered=True)
 
 
 def test_plan_path_respects_forced_options():
@@ -75,7 +86,9 @@ def test_plan_path_cost_model_choices():
     # the SwiGLU fc2 RS at T = 4096 (256 pair tiles, 224 k-blocks): pairs, last wave split
     assert ub.plan_path(512, 256, 224, SLOTS, PAIRS) == (True, True)
     # QKV AG at T = 2048 (96 pair tiles, 64 k-blocks): pairs, whole tiles
-    assert ub.plan_path(192, 96, 64, SLOTS, PAIRS) == (True, False)
+    assert ub.plan_path(192, 96, 64, SLOTS, PAIRS, gathered=True) == (True, False)
+    # QKV AG at T = 5120 (240 pair tiles): pairs, last wave split
+    assert ub.plan_path(480, 240, 64, SLOTS, PAIRS, gathered=True) == (True, True)
     # one wave either way: pairs (a third less L2 traffic per tile)
     assert ub.plan_path(8, 4, 2, SLOTS, PAIRS) == (True, False)
     # AG at T = 512 (N = 7168): 112 chunk-aligned single tiles in one wave against 84
