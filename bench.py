@@ -44,7 +44,8 @@ from gemm_overlap_gemms_gb300 import synth  # noqa: E402
 METRIC = "AG-GEMM / GEMM-RS TFLOP/s and % of GB300 bf16 peak vs active token count T"
 WORKLOAD = "swiglu"
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_SRC = os.path.join(ROOT, "gemm_overlap_gemms_gb300", "csrc", "ub_gemm.cu")
+# the sources of the tile kernels: the kernels and their device-side building blocks
+KERNEL_SRC = [os.path.join(ROOT, "gemm_overlap_gemms_gb300", "csrc", f) for f in ("ub_gemm.cu", "ub_device.cuh")]
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one ncu capture per op,
 # per active token of the captured launch, and the kernel source they were taken on.
 # Traffic is reported as null once the kernel source no longer matches.
@@ -135,15 +136,22 @@ def kernel_traffic(op: str, avg_T: float):
     """ncu DRAM traffic of one launch of `op`, scaled from the captured launch to the
     mean active T of the benchmark's launches (traffic grows with T: A and Y are
     proportional, and the weight re-reads follow the number of M-tile waves)."""
-    import hashlib
     rec = NCU_TRAFFIC.get(op)
-    if not rec or not os.path.exists(KERNEL_SRC):
+    if not rec or not all(os.path.exists(f) for f in KERNEL_SRC):
         return None
-    sha = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()[:16]
-    if sha != rec["sha256_16"]:
+    if kernel_src_sha() != rec["sha256_16"]:
         return None
     return {"bytes_per_launch": rec["bytes"] * avg_T / rec["T"], "captured_T": rec["T"],
             "scaled_to_mean_T": avg_T, "source": rec["source"]}
+
+
+def kernel_src_sha() -> str:
+    """sha256 prefix of the tile kernels' sources, concatenated in KERNEL_SRC order."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SRC:
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
 
 
 def step_flops(Ts, w):

@@ -164,11 +164,16 @@ struct ub_handle {
 
 namespace {
 
+// Control block, in 32-bit words: the readiness flags [0, UB_MAX_TP), the partial-tile
+// flags [UB_MAX_TP, UB_MAX_TP + W) with W = ws_slots * EPI_WARPS, then the abort word, the
+// status word and the gather's per-chunk counters (zero between calls). The words a
+// captured call clears (flags and partial-tile flags) are one contiguous run.
+size_t ws_flag_words(const ub_handle *h) { return static_cast<size_t>(h->ws_slots) * ubk::EPI_WARPS; }
 uint32_t *flags_of(ub_handle *h) { return h->ctrl; }
-uint32_t *abort_of(ub_handle *h) { return h->ctrl + UB_MAX_TP; }
-int32_t *status_of(ub_handle *h) { return reinterpret_cast<int32_t *>(h->ctrl + UB_MAX_TP + 1); }
-uint32_t *ws_flags_of(ub_handle *h) { return h->ctrl + 64; }
-uint32_t *gather_counters_of(ub_handle *h) { return h->ctrl + 16; }  // UB_MAX_TP words, zero between calls
+uint32_t *ws_flags_of(ub_handle *h) { return h->ctrl + UB_MAX_TP; }
+uint32_t *abort_of(ub_handle *h) { return h->ctrl + UB_MAX_TP + ws_flag_words(h); }
+int32_t *status_of(ub_handle *h) { return reinterpret_cast<int32_t *>(abort_of(h) + 1); }
+uint32_t *gather_counters_of(ub_handle *h) { return abort_of(h) + 8; }  // UB_MAX_TP words
 
 // Makes the handle's device current for the duration of a call.
 struct DeviceGuard {
@@ -607,19 +612,23 @@ int join_gather(ub_handle *h, cudaStream_t s)
 
 // A new call's epoch, unique per handle: every wait compares a flag for equality with
 // it, so words left by other calls never match. When `s` is being captured into a CUDA
-// graph the epoch becomes a constant of the graph, so every replay would find the
-// readiness flags, the partial-tile flags and the abort word still holding it from the
-// replay before. The captured call therefore starts, in stream order, by clearing them
-// (never the sticky status word). An uncaptured call pays nothing.
-int begin_call(ub_handle *h, cudaStream_t s, uint32_t &epoch)
+// graph the epoch becomes a constant of the graph, so every replay would find the words
+// it waits on still holding it from the replay before. The captured call therefore
+// starts, in stream order, by clearing the ones it uses -- the readiness flags (`gathered`:
+// the call waits for chunk flags) and the partial-tile flags (`split`: tiles cut into
+// k-pieces) -- in one memset of the contiguous run that covers them; a call that uses
+// neither clears nothing. The abort word, which a timeout sets to the call's epoch, is
+// cleared by ub_clear_status. An uncaptured call pays nothing.
+int begin_call(ub_handle *h, cudaStream_t s, uint32_t &epoch, bool gathered, bool split)
 {
     epoch = ++h->epoch;
     if (epoch == 0) epoch = ++h->epoch;  // 0 is what a cleared word holds
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     UB_CUDA(cudaStreamIsCapturing(s, &cs));
-    if (cs == cudaStreamCaptureStatusActive) {
-        UB_CUDA(cudaMemsetAsync(h->ctrl, 0, (UB_MAX_TP + 1) * sizeof(uint32_t), s));  // flags, abort word
-        UB_CUDA(cudaMemsetAsync(ws_flags_of(h), 0, h->ctrl_bytes - 64 * sizeof(uint32_t), s));
+    if (cs == cudaStreamCaptureStatusActive && (gathered || split)) {
+        const size_t lo = gathered ? 0 : UB_MAX_TP;
+        const size_t hi = split ? UB_MAX_TP + ws_flag_words(h) : static_cast<size_t>(h->tp);
+        UB_CUDA(cudaMemsetAsync(h->ctrl + lo, 0, (hi - lo) * sizeof(uint32_t), s));
     }
     return UB_OK;
 }
@@ -705,7 +714,7 @@ int ub_create(int64_t max_tokens, int64_t hidden, int tp, ub_dtype_t dtype, ub_h
     ++h->counters.device_allocations;
     h->max_pairs = h->sm_count / 2 > 0 ? h->sm_count / 2 : 1;
     h->ws_slots = 2 * (h->sm_count > 0 ? h->sm_count : 1);
-    h->ctrl_bytes = 256 + static_cast<size_t>(h->ws_slots) * ubk::EPI_WARPS * sizeof(uint32_t);
+    h->ctrl_bytes = (UB_MAX_TP + ws_flag_words(h) + 8 + UB_MAX_TP) * sizeof(uint32_t);
     e = cudaMalloc(reinterpret_cast<void **>(&h->ctrl), h->ctrl_bytes);
     if (e != cudaSuccess) return cleanup(cuda_fail(e, "cudaMalloc(control block)"));
     ++h->counters.device_allocations;
@@ -993,12 +1002,15 @@ static int ag_gemm_impl(ub_handle_t h, const void *const *shards, const void *Wt
     if (skinny) set_skinny(h, p, glu ? 2 : 1, glu ? 2 * ubk::SK_W_BYTES : ubk::SK_W_BYTES);
     else if (pair) set_pairs(h, p, mode, streamk, in_gemm, true);
     uint32_t epoch = 0;
-    if (int rc = begin_call(h, s, epoch)) return rc;
+    if (int rc = begin_call(h, s, epoch, true, pair ? p.tail_split > 1 : skinny && p.sk_split > 1)) return rc;
     p.epoch = epoch;
     const int64_t drop = h->drop_flag;
     h->drop_flag = -1;
 
-    p.fused_gather = in_gemm ? 1 : 0;
+    // one wave of tiles: the gather end to end (every chunk needed at once), else part by
+    // part (the chunks land in ring order, the first wave's soonest)
+    const bool one_wave = pair ? p.region_tile0[p.n_regions] <= p.num_pairs : p.num_tiles <= grid_for(h, 1 << 30);
+    p.fused_gather = in_gemm ? (one_wave ? 2 : 1) : 0;
     if (in_gemm) {
         for (int r = 0; r < tp; ++r) p.g_src[r] = shards[r];
         p.g_ub = h->ub;
@@ -1150,7 +1162,7 @@ static int gemm_rs_impl(ub_handle_t h, const void *const *A, const void *const *
     if (skinny) set_skinny(h, p, 1, ubk::SK_W_BYTES);
     else if (pair) set_pairs(h, p, ubk::MODE_RS, streamk);
     uint32_t epoch = 0;
-    if (int rc = begin_call(h, s, epoch)) return rc;
+    if (int rc = begin_call(h, s, epoch, false, pair ? p.tail_split > 1 : skinny && p.sk_split > 1)) return rc;
     p.epoch = epoch;
     if (int rc = launch(h, p, ubk::MODE_RS, skinny ? PATH_SKINNY : pair ? PATH_PAIR : PATH_SINGLE, s,
                         b_kn ? UB_OP_RS_KN : UB_OP_RS))
@@ -1185,7 +1197,7 @@ int ub_allgather(ub_handle_t h, const void *const *shards, void *stream)
     NvtxRange range("ub_allgather", h->T);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint32_t epoch = 0;
-    if (int rc = begin_call(h, s, epoch)) return rc;
+    if (int rc = begin_call(h, s, epoch, false, false)) return rc;
     if (int rc = issue_gather(h, shards, s, epoch, -1, h->T / h->tp)) return rc;
     if (int rc = join_gather(h, s)) return rc;
     h->counters.last_T = h->T;
@@ -1296,7 +1308,7 @@ int ub_wgrad(ub_handle_t h, const void *D, int64_t M, int ub_is_a, void *out, vo
     choose_path(h, ubk::MODE_AG, 1 << 30, p.region_tile0[1], p.k_blocks, false, pair, split);
     set_pairs(h, p, ubk::MODE_AG, split);
     uint32_t epoch = 0;
-    if (int rc = begin_call(h, s, epoch)) return rc;
+    if (int rc = begin_call(h, s, epoch, false, p.tail_split > 1)) return rc;
     p.epoch = epoch;
     if (int rc = launch(h, p, ubk::MODE_AG, PATH_PAIR, s, UB_OP_WGRAD)) return rc;
     h->counters.last_T = T;
@@ -1357,7 +1369,7 @@ int ag_gemm_from_buffer(ub_handle_t h, const void *Wt, int64_t N, int64_t glu_f,
     choose_path(h, mode, 1 << 30, p.region_tile0[1], p.k_blocks, false, pair, split);
     set_pairs(h, p, mode, split);
     uint32_t epoch = 0;
-    if (int rc = begin_call(h, s, epoch)) return rc;
+    if (int rc = begin_call(h, s, epoch, false, p.tail_split > 1)) return rc;
     p.epoch = epoch;
     p.fused_gather = 0;
     if (int rc = launch(h, p, mode, PATH_PAIR, s, glu ? UB_OP_AG_SWIGLU : UB_OP_AG)) return rc;
@@ -1460,7 +1472,7 @@ int ub_clear_status(ub_handle_t h)
 {
     if (int rc = check_handle(h)) return rc;
     DeviceGuard g(h->device);
-    UB_CUDA(cudaMemsetAsync(status_of(h), 0, sizeof(int32_t), h->side));
+    UB_CUDA(cudaMemsetAsync(abort_of(h), 0, 2 * sizeof(uint32_t), h->side));  // abort and status words
     UB_CUDA(cudaStreamSynchronize(h->side));
     return UB_OK;
 }

@@ -326,18 +326,134 @@ __device__ __forceinline__ void st_release_u32(uint32_t *ptr, uint32_t v)
 }
 
 // All-gather done by the GEMM's own epilogue warps (128 threads, named barrier 1) before
-// their first tile, while the producer already loads the self chunk's tiles. It copies
-// three kinds of parts, in this order: the self chunk's rows from g_self_head_vecs on
+// their first tile, while the producer already loads the self chunk's tiles. The parts
+// to copy, in issue order (gather_part): the self chunk's rows from g_self_head_vecs on
 // (the rows past its whole 256-row tiles, which the CTA-pair kernel reads from the
 // buffer), the other chunks in ring order after the self rank, then the self chunk's
 // first rows (read in place, so they need no flag unless they are the whole chunk).
-// Every CTA copies its 1/gridDim.x share of each part, with 16-byte loads that bypass
-// L1, sixteen in flight per thread (about 5 MB in flight over the GPU: enough to keep
-// HBM busy); the CTA that completes a flagged part's count resets the chunk's counter
-// and publishes its readiness flag with the call's epoch (no flag for chunk p.g_drop).
-// A chunk's counter serves one flagged part per call.
+// Two orders, chosen per call by the host:
+//  - part by part (p.fused_gather == 1): every CTA copies its 1/gridDim.x share of each
+//    part in turn, so the chunks land in ring order, the first soonest: for calls of
+//    several waves of tiles, whose first wave needs only the first chunks;
+//  - end to end (p.fused_gather == 2): the parts laid end to end and every CTA copies one
+//    contiguous 1/gridDim.x of the whole, two batches of loads in flight per thread, so
+//    a CTA pays the memory latency a few times instead of once per part and every chunk
+//    lands sooner on average, but all at about the same time: for one wave of tiles,
+//    which all start together (QKV at T = 1024 on GB300: 45.8 against 51.7 us a call).
+// 16-byte loads bypass L1. A flagged part is complete when every CTA whose share meets it
+// has counted it (after a CTA barrier and a fence); the CTA that completes the count
+// resets the chunk's counter and publishes its readiness flag with the call's epoch (no
+// flag for chunk p.g_drop). A chunk's counter serves one flagged part per call.
+struct GatherPart {
+    int r;           // chunk
+    int64_t lo, hi;  // its vectors [lo, hi)
+    bool flag;       // publishes the chunk's readiness flag once complete
+};
+__device__ __forceinline__ int gather_n_parts(const GemmParams &p)
+{
+    return (p.g_self_head_vecs < p.g_chunk_vecs) + (p.tp - 1) + (p.g_self_head_vecs > 0);
+}
+__device__ __forceinline__ GatherPart gather_part(const GemmParams &p, int i)
+{
+    const int64_t head = p.g_self_head_vecs, cv = p.g_chunk_vecs;
+    const int k0 = head < cv ? 1 : 0;
+    if (i < k0) return GatherPart{p.self_rank, head, cv, true};
+    if (i < k0 + p.tp - 1) {
+        int r = p.self_rank + 1 + (i - k0);
+        if (r >= p.tp) r -= p.tp;
+        return GatherPart{r, 0, cv, true};
+    }
+    return GatherPart{p.self_rank, 0, head, head >= cv};
+}
+
+__device__ __forceinline__ uint4 ld_nc_v4(const uint4 *p)
+{
+    uint4 x;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(x.x), "=r"(x.y), "=r"(x.z), "=r"(x.w)
+                 : "l"(p));
+    return x;
+}
+
+// Copy n 16-byte vectors src -> dst with the 128 threads et = 0..127 (vector i to thread
+// i % 128): two batches of 8 loads per thread in flight, the next batch's loads issued
+// before the current batch is stored.
+__device__ __forceinline__ void copy_vecs(const uint4 *__restrict__ src, uint4 *__restrict__ dst, int64_t n, int et)
+{
+    constexpr int U = 8;
+    constexpr int64_t STEP = U * 128;
+    uint4 a[U], b[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+        if (et + u * 128 < n) a[u] = ld_nc_v4(src + et + u * 128);
+    for (int64_t v = et; v < n; v += 2 * STEP) {
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (v + STEP + u * 128 < n) b[u] = ld_nc_v4(src + v + STEP + u * 128);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (v + u * 128 < n) dst[v + u * 128] = a[u];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (v + 2 * STEP + u * 128 < n) a[u] = ld_nc_v4(src + v + 2 * STEP + u * 128);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (v + STEP + u * 128 < n) dst[v + STEP + u * 128] = b[u];
+    }
+}
+
+// The end-to-end order (p.fused_gather == 2).
+__device__ void fused_gather_end_to_end(const GemmParams &p, int et)
+{
+    const int64_t G = gridDim.x;
+    const int np = gather_n_parts(p);
+    int64_t total = 0;
+    for (int i = 0; i < np; ++i) {
+        const GatherPart g = gather_part(p, i);
+        total += g.hi - g.lo;
+    }
+    const int64_t per = (total + G - 1) / G;
+    const int64_t a = static_cast<int64_t>(blockIdx.x) * per;
+    const int64_t b = a + per < total ? a + per : total;
+    int64_t s0 = 0;
+    for (int i = 0; i < np; ++i) {
+        const GatherPart g = gather_part(p, i);
+        const int64_t s1 = s0 + g.hi - g.lo;
+        const int64_t lo = a > s0 ? a : s0, hi = b < s1 ? b : s1;
+        if (lo < hi) {
+            const int64_t v0 = g.lo + (lo - s0);
+            copy_vecs(static_cast<const uint4 *>(p.g_src[g.r]) + v0,
+                      static_cast<uint4 *>(p.g_ub) + static_cast<int64_t>(g.r) * p.g_chunk_vecs + v0, hi - lo, et);
+        }
+        s0 = s1;
+    }
+    asm volatile("bar.sync 1, 128;" ::: "memory");  // this CTA's share is written
+    if (et != 0) return;
+    __threadfence();
+    s0 = 0;
+    for (int i = 0; i < np; ++i) {
+        const GatherPart g = gather_part(p, i);
+        const int64_t s1 = s0 + g.hi - g.lo;
+        // the CTAs whose shares meet part [s0, s1): s0 / per .. (s1 - 1) / per
+        if (g.flag && s1 > s0 && blockIdx.x >= s0 / per && blockIdx.x <= (s1 - 1) / per) {
+            const uint32_t done = atomicAdd(p.g_counters + g.r, 1u) + 1u;
+            if (done == static_cast<uint32_t>((s1 - 1) / per - s0 / per + 1)) {
+                p.g_counters[g.r] = 0u;  // zero again for the next call
+                __threadfence();
+                if (g.r != p.g_drop) st_release_u32(const_cast<uint32_t *>(p.flags) + g.r, p.epoch);
+            }
+        }
+        s0 = s1;
+    }
+}
+
+// The part-by-part order (p.fused_gather == 1).
 __device__ void fused_gather(const GemmParams &p, int et)
 {
+    if (p.fused_gather == 2) {
+        fused_gather_end_to_end(p, et);
+        return;
+    }
     const int G = static_cast<int>(gridDim.x);
     const int64_t head = p.g_self_head_vecs;
     for (int q = 0; q <= p.tp; ++q) {

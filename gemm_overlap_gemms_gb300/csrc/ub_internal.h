@@ -109,7 +109,8 @@ struct GemmParams {
 
     // ---- fused gather (tile kernels, AG modes): the epilogue warps copy the chunks into
     // the user buffer before their first tile and publish each chunk's readiness flag
-    int fused_gather;            // 1: on; the host then issues no copies for the call
+    int fused_gather;            // 1: chunk by chunk; 2: the chunks end to end, one range per
+                                 // CTA (one wave of tiles); the host then issues no copies
     int g_drop;                  // chunk whose flag is not published (-1: none)
     const void *g_src[UB_MAX_TP];  // shard r ([c, hidden])
     void *g_ub;                  // user buffer base

@@ -319,7 +319,10 @@ int ub_get_option(ub_handle_t h, int key, int64_t *val);
  * calls of interest has been synchronised. Returns UB_ERR_CUDA if the read fails.
  */
 int ub_query_status(ub_handle_t h);
-/* Reset the sticky device status to UB_OK (stream-ordered on the side stream). */
+/* Reset the sticky device status to UB_OK, and the word through which a call whose wait
+ * ran out stops the rest of its CTAs (stream-ordered on the side stream). A call replayed
+ * from a CUDA graph keeps the epoch it was captured with, so after one replay has timed
+ * out the later replays of that graph give up at once until this is called. */
 int ub_clear_status(ub_handle_t h);
 
 /* Counters of the handle: calls made, device allocations made (constant after

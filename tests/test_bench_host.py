@@ -38,7 +38,8 @@ def test_clock_summary_without_samples():
 
 
 def test_traffic_record_follows_the_kernel_source(monkeypatch):
-    sha = hashlib.sha256(open(bench.KERNEL_SRC, "rb").read()).hexdigest()[:16]
+    sha = bench.kernel_src_sha()
+    assert sha == hashlib.sha256(b"".join(open(f, "rb").read() for f in bench.KERNEL_SRC)).hexdigest()[:16]
     rec = {"sha256_16": sha, "bytes": 1.0e9, "T": 8192, "source": "profiles/x.md"}
     monkeypatch.setattr(bench, "NCU_TRAFFIC", {"rs": rec})
     t = bench.kernel_traffic("rs", 4096.0)

@@ -20,10 +20,12 @@ def _u16(t):
 
 
 # T = 64: the few-token kernel with split pieces; T = 2048: CTA pairs, the gather
-# overlapped with the GEMM (chunks of 512 rows that land while the self chunk computes).
-@pytest.mark.parametrize("T", [64, 2048])
-def test_captured_step_replays_with_new_inputs(T):
-    tp, H, N, K = 4, 1024, 768, 512
+# overlapped with the GEMM (chunks of 512 rows that land while the self chunk computes);
+# streamk = 1: the pairs' last wave cut into k-pieces, whose partial-tile flags a replay
+# must not find set by the replay before (the captured call clears them).
+@pytest.mark.parametrize("T,H,N,streamk", [(64, 1024, 768, -1), (2048, 1024, 768, -1), (1024, 2048, 512, 1)])
+def test_captured_step_replays_with_new_inputs(T, H, N, streamk):
+    tp, K = 4, 512
     c = T // tp
     d = dev()
     g = synth.generator(d, seed=121)
@@ -43,12 +45,17 @@ def test_captured_step_replays_with_new_inputs(T):
 
     with ub.UserBuffer([T, H], tp) as buf:
         buf.set_active_shape([T, H])
+        buf.set_option("streamk", streamk)
         s = torch.cuda.Stream(d)
         refill()
         torch.cuda.synchronize()
         with torch.cuda.stream(s):  # warm-up outside the capture
             buf.ag_gemm(shards, Wt, Y, stream=s)
+            if streamk == 1:
+                assert buf.counters()["last_pieces"] > 1, "the AG call did not split its last wave"
             buf.gemm_rs(A, Bt, outs, stream=s)
+            if streamk == 1:
+                assert buf.counters()["last_pieces"] > 1, "the RS call did not split its last wave"
         torch.cuda.synchronize()
         assert buf.query_status() == ub.UB_OK
         graph = torch.cuda.CUDAGraph()
