@@ -449,13 +449,29 @@ def time_graph_flushed(fn, stream, flush, calls, warmup):
     return float(np.median(ms)), float(np.min(ms))
 
 
+READ_FLOOR_MAX_T = 512  # few-token points: the weight read is the work
+
+
+def read_floor(buf, weights, stream, flush):
+    """Median time of one plain read of the weight bytes (`ub_stream_read`: one kernel,
+    one CTA per SM, bulk copies into shared memory, nothing computed), timed exactly as a
+    sweep call is (graph replay, L2 flushed before each): what reading the same bytes in
+    one isolated kernel costs on this GPU, launch and ramp included."""
+    med, _ = time_graph_flushed(lambda st: buf.stream_read(weights, stream=st), stream, flush,
+                                DEFAULT_SWEEP_CALLS, DEFAULT_SWEEP_WARMUP)
+    return med
+
+
 def default_sweep(stream):
     """The active-T sweep of the metric ("TFLOP/s and % of bf16 peak vs active token
     count T"): every point is one whole call (AG: the gather, its flag waits and joins
     included) on a handle registered at the workload's capacity, timed as the median of
     DEFAULT_SWEEP_CALLS graph replays with L2 flushed before each, with the kernel path
     the library took. Fractions are of the measured burst bf16 peak (an isolated call)
-    and of the measured HBM bandwidth (algorithmic bytes)."""
+    and of the measured HBM bandwidth (algorithmic bytes). Few-token points (T <= 512)
+    also carry the time a bare streaming kernel takes to read the same weight bytes
+    under the same timing (`read_floor_us`, `ub_stream_read`): the floor an isolated call
+    of that size meets before any GEMM work."""
     from gemm_overlap_gemms_gb300 import ub
     pk, src = peaks()
     tensor_peak = _peak_value(pk, "bf16_tflops") or FALLBACK["bf16_tflops"]
@@ -477,12 +493,16 @@ def default_sweep(stream):
             if op == "rs":
                 K = int(name.rsplit("_k", 1)[1]) if "_k" in name else w.rs_k[0]
                 A = [synth.normal_bf16((cap, K), 1.0, g, dev) for _ in range(tp)]
-                Bt = [synth.normal_bf16((H, K), 1.0 / math.sqrt(K), g, dev) for _ in range(tp)]
+                B_all = synth.normal_bf16((tp * H, K), 1.0 / math.sqrt(K), g, dev)  # the tp weights, end to end
+                Bt = list(B_all.split(H))
                 N = 0
+                weights = B_all
             else:
                 N, K = w.ag_n[0], 0
                 Wt = synth.normal_bf16((N, H), 1.0 / math.sqrt(H), g, dev)
+                weights = Wt
                 Y = torch.empty((cap, N // 2 if op == "ag_swiglu" else N), dtype=torch.bfloat16, device=dev)
+            floor = None
             for T in Ts:
                 c = T // tp
                 buf.set_active_shape([T, H])
@@ -503,11 +523,16 @@ def default_sweep(stream):
                 pt["k_pieces"] = cnt["last_pieces"]
                 if op != "rs":
                     pt["gather"] = ub.GATHERS.get(cnt["last_gather"], "?")
+                if T <= READ_FLOOR_MAX_T:
+                    if floor is None:
+                        floor = read_floor(buf, weights, stream, flush)
+                    pt["read_floor_us"] = floor * 1e3
+                    pt["frac_of_read_floor"] = floor / med
                 points.append(pt)
             if op == "rs":
-                del A, Bt
+                del A, Bt, B_all, weights
             else:
-                del Wt, Y
+                del Wt, Y, weights
         assert buf.query_status() == ub.UB_OK, "device status %d" % buf.query_status()
         buf.close()
         del X, Yrs

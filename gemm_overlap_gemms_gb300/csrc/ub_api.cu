@@ -290,13 +290,18 @@ int64_t ag_self_head(ub_handle *h, int mode, int64_t T, int64_t c, int self, int
 }
 
 constexpr int64_t kGatherKernelMaxT = 512;  // UB_OPT_GATHER_KERNEL = -1: kernel up to this T
-// ... and inside the GEMM above it: on GB300 (tp 4, hidden 4096) the whole AG call is
-// 2-8 % faster than with the driver copies at T = 1024-8192 (the chunks land sooner:
-// no copy launches, every SM copying; AG T = 2048: 73.2 vs 78.6 us).
+// ... and inside the GEMM above it when the call has more than one wave of tiles: on
+// GB300 (tp 4, hidden 4096) the whole AG call is 2-8 % faster than with the driver copies
+// at T = 1024-8192 (the chunks land sooner: no copy launches, every SM copying; AG
+// T = 2048: 73.2 vs 78.6 us). A call whose tiles fit one wave leaves SMs without a tile,
+// and there the gather kernel, whose CTAs run on them, lands the chunks sooner than the
+// GEMM's own epilogue warps: QKV (N = 3072) at T = 576-1536 37.0-41.5 against 39.4-45.6 us,
+// tp 8 / hidden 8192 at T = 576-1024 55.8-61.9 against 60.2-64.5; with more than one wave
+// the GEMM's warps win (QKV T = 2048: 51.7 against 61.6 us).
 constexpr bool kFusedGatherAuto = true;
 // Not for the few-token kernel: there the chunks are tiny, the weight stream hides the
-// one-launch gather, and the gather inside the kernel measured 1-3 us slower per call
-// (AG and AG + SwiGLU, T = 4-128, GB300).
+// one-launch gather, and the gather inside the kernel (each chunk by its own few CTAs)
+// measured 2-5 us slower per call (AG, AG + SwiGLU and QKV at T = 4-128, GB300).
 constexpr bool kFusedGatherSkinnyAuto = false;
 
 // Cost of the last, partial wave's tiles when each is cut into s k-pieces, in units of
@@ -490,11 +495,11 @@ int launch(ub_handle *h, GemmParams &p, int mode, int path, cudaStream_t s, int 
 // work already queued on `s`.
 // Whether this AG call's gather runs inside the GEMM kernel (its epilogue warps copy the
 // chunks before their first tile): UB_OPT_GATHER_KERNEL = 2, or the automatic choice.
-bool gather_in_gemm(ub_handle *h, bool skinny)
+bool gather_in_gemm(ub_handle *h, bool skinny, bool one_wave)
 {
     if (h->gather_kernel == 2) return true;
     if (h->gather_kernel >= 0) return false;
-    return skinny ? kFusedGatherSkinnyAuto : (kFusedGatherAuto && h->T > kGatherKernelMaxT);
+    return skinny ? kFusedGatherSkinnyAuto : (kFusedGatherAuto && h->T > kGatherKernelMaxT && !one_wave);
 }
 
 // The copies of the all-gather in issue order: the self chunk's rows from `head` on (the
@@ -516,7 +521,7 @@ int gather_parts(int tp, int self, int64_t c, int64_t head, GatherPart out[UB_MA
 }
 
 int issue_gather(ub_handle *h, const void *const *shards, cudaStream_t s, uint32_t epoch, int64_t drop,
-                 int64_t self_head)
+                 int64_t self_head, bool one_wave = false)
 {
     const int tp = h->tp;
     const int64_t T = h->T, H = h->hidden, c = T / tp;
@@ -527,7 +532,7 @@ int issue_gather(ub_handle *h, const void *const *shards, cudaStream_t s, uint32
     // the call (GB300, tp 4: AG at T <= 512 takes 26-33 us with the kernel, 39-44 us with
     // the copies), while for many tokens the copies are as fast or faster.
     h->gather_by_kernel = h->gather_kernel == 1 || h->gather_kernel == 2 ||
-                          (h->gather_kernel < 0 && T <= kGatherKernelMaxT);
+                          (h->gather_kernel < 0 && (T <= kGatherKernelMaxT || one_wave));
     if (h->copy_streams == 0 && !h->gather_by_kernel) {
         // In-stream: the copies and flag writes go on `s` itself, ahead of the GEMM,
         // which then finds every flag set (no overlap, no cross-stream hops).
@@ -998,7 +1003,9 @@ static int ag_gemm_impl(ub_handle_t h, const void *const *shards, const void *Wt
     p.abort_word = abort_of(h);
     p.status = status_of(h);
     p.timeout_ns = static_cast<uint64_t>(h->timeout_ns);
-    const bool in_gemm = gather_in_gemm(h, skinny);
+    const bool fits_one_wave = pair ? pair_rows_tiles * n_tiles <= clusters_for(h, mode, 1 << 30)
+                                    : tp * ceil_div(c, ubk::BM) * n_tiles <= grid_for(h, 1 << 30);
+    const bool in_gemm = gather_in_gemm(h, skinny, fits_one_wave);
     if (skinny) set_skinny(h, p, glu ? 2 : 1, glu ? 2 * ubk::SK_W_BYTES : ubk::SK_W_BYTES);
     else if (pair) set_pairs(h, p, mode, streamk, in_gemm, true);
     uint32_t epoch = 0;
@@ -1011,6 +1018,16 @@ static int ag_gemm_impl(ub_handle_t h, const void *const *shards, const void *Wt
     // part (the chunks land in ring order, the first wave's soonest)
     const bool one_wave = pair ? p.region_tile0[p.n_regions] <= p.num_pairs : p.num_tiles <= grid_for(h, 1 << 30);
     p.fused_gather = in_gemm ? (one_wave ? 2 : 1) : 0;
+    if (in_gemm && skinny) {
+        // few tokens: each chunk copied by its own group of CTAs, at most 32 KB per CTA
+        // (the self chunk is a part too); with fewer CTAs than chunks, one CTA per group
+        // and some groups copy several chunks
+        const int64_t grid = grid_for(h, p.sk_units), parts = tp;
+        int64_t gs = (c * H / 8 + 2047) / 2048;
+        if (gs > grid / parts) gs = grid / parts;
+        p.fused_gather = 3;
+        p.g_group = static_cast<int>(gs < 1 ? 1 : gs);
+    }
     if (in_gemm) {
         for (int r = 0; r < tp; ++r) p.g_src[r] = shards[r];
         p.g_ub = h->ub;
@@ -1021,7 +1038,7 @@ static int ag_gemm_impl(ub_handle_t h, const void *const *shards, const void *Wt
         int rc = launch(h, p, mode, skinny ? PATH_SKINNY : pair ? PATH_PAIR : PATH_SINGLE, s, prof_op);
         if (rc != UB_OK) return rc;
     } else {
-        if (int rc = issue_gather(h, shards, s, epoch, drop, p.self_head)) return rc;
+        if (int rc = issue_gather(h, shards, s, epoch, drop, p.self_head, fits_one_wave)) return rc;
         int rc = launch(h, p, mode, skinny ? PATH_SKINNY : pair ? PATH_PAIR : PATH_SINGLE, s, prof_op);
         // Join the copy streams back into `s` even if the launch failed.
         if (int jrc = join_gather(h, s)) return jrc;
@@ -1201,6 +1218,33 @@ int ub_allgather(ub_handle_t h, const void *const *shards, void *stream)
     if (int rc = issue_gather(h, shards, s, epoch, -1, h->T / h->tp)) return rc;
     if (int rc = join_gather(h, s)) return rc;
     h->counters.last_T = h->T;
+    return UB_OK;
+}
+
+int ub_stream_read(ub_handle_t h, const void *src, int64_t bytes, void *stream)
+{
+    if (int rc = check_handle(h)) return rc;
+    if (!src || bytes < 0) return fail(UB_ERR_ARG, "ub_stream_read: null source or negative size");
+    if (!aligned16(src) || bytes % 16 != 0)
+        return fail(UB_ERR_ALIGN, "ub_stream_read: source or size not a multiple of 16 bytes");
+    if (bytes == 0) return UB_OK;
+    DeviceGuard g(h->device);
+    if (!g.ok) return fail(UB_ERR_CUDA, "ub_stream_read: cannot select the handle's device");
+    NvtxRange range("ub_stream_read", bytes);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t epoch = 0;
+    if (int rc = begin_call(h, s, epoch, false, false)) return rc;
+    ubk::StreamReadParams p;
+    memset(&p, 0, sizeof p);
+    p.src = static_cast<const char *>(src);
+    p.bytes = bytes;
+    p.abort_word = abort_of(h);
+    p.status = status_of(h);
+    p.timeout_ns = static_cast<uint64_t>(h->timeout_ns);
+    p.epoch = epoch;
+    p.pdl = static_cast<int>(h->pdl);
+    cudaError_t e = ubk::launch_stream_read(p, h->sm_count, s);
+    if (e != cudaSuccess) return cuda_fail(e, "stream-read kernel launch");
     return UB_OK;
 }
 

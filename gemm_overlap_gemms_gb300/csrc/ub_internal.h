@@ -110,7 +110,9 @@ struct GemmParams {
     // ---- fused gather (tile kernels, AG modes): the epilogue warps copy the chunks into
     // the user buffer before their first tile and publish each chunk's readiness flag
     int fused_gather;            // 1: chunk by chunk; 2: the chunks end to end, one range per
-                                 // CTA (one wave of tiles); the host then issues no copies
+                                 // CTA (one wave of tiles); 3: each chunk by its own group of
+                                 // g_group CTAs (few tokens); the host then issues no copies
+    int g_group;                 // fused_gather 3: CTAs per chunk
     int g_drop;                  // chunk whose flag is not published (-1: none)
     const void *g_src[UB_MAX_TP];  // shard r ([c, hidden])
     void *g_ub;                  // user buffer base
@@ -149,6 +151,20 @@ cudaError_t launch_gemm_skinny(const GemmParams &p, int mode, int grid, cudaStre
 
 // Dynamic shared memory of the skinny kernel for a pipeline of `stages`.
 int skinny_smem_bytes(int stages, int w_bytes, int x_bytes);
+
+// Calibration read (ub_skinny.cu): `bytes` of `src` streamed into shared memory by bulk
+// copies, one contiguous share per CTA, and discarded: the cost of reading those bytes
+// once in one kernel, which a few-token call (whose work is its weight read) cannot beat.
+struct StreamReadParams {
+    const char *src;
+    int64_t bytes;               // multiple of 16
+    uint32_t *abort_word;
+    int32_t *status;
+    uint64_t timeout_ns;
+    uint32_t epoch;
+    int pdl;                     // host: launch with programmatic stream serialization
+};
+cudaError_t launch_stream_read(const StreamReadParams &p, int grid, cudaStream_t stream);
 
 // Standalone reduce-scatter (ub_bulk.cu): Y[r][i][:] = sum_j P[j][r*c + i][:].
 struct BulkRsParams {

@@ -88,6 +88,44 @@ __device__ __forceinline__ Unit unit_at(int u, const GemmParams &p)
 // Workspace slot of a unit's published partial (SwiGLU units take two slots' room).
 __device__ __forceinline__ int partial_slot(const Unit &x, const GemmParams &p) { return x.piece * p.n_tiles + x.tile; }
 
+// The gather inside this kernel (UB_OPT_GATHER_KERNEL = 2; p.fused_gather == 3): the
+// CTAs form groups of g_group; group k alone copies parts k, k + groups, ... (gather_part),
+// each member a share, and CTAs past the last whole group copy nothing. A few-token
+// call's chunks are small (T = 4, tp = 4: 8 KB), so a chunk is one CTA's or a few CTAs'
+// work and its flag waits for no count across the grid (the tile kernels' part-by-part
+// order, every CTA a share of every part, took 2-4 us longer here). The one-launch
+// gather kernel on the side stream is still faster, by 2-5 us a call at T = 4-128 on
+// GB300, and stays the default.
+__device__ void fused_gather_grouped(const GemmParams &p, int et)
+{
+    const int gs = p.g_group;                           // 1 <= gs <= gridDim.x
+    const int ng = static_cast<int>(gridDim.x) / gs;    // groups; group k copies parts k, k + ng, ...
+    const int grp = static_cast<int>(blockIdx.x) / gs;
+    if (grp >= ng) return;
+    const int m = static_cast<int>(blockIdx.x) - grp * gs;
+    const int np = gather_n_parts(p);
+    for (int i = grp; i < np; i += ng) {
+        const GatherPart g = gather_part(p, i);
+        const int64_t per = (g.hi - g.lo + gs - 1) / gs;
+        const int64_t v0 = g.lo + m * per;
+        const int64_t v1 = v0 + per < g.hi ? v0 + per : g.hi;
+        if (v1 > v0)
+            copy_vecs(static_cast<const uint4 *>(p.g_src[g.r]) + v0,
+                      static_cast<uint4 *>(p.g_ub) + static_cast<int64_t>(g.r) * p.g_chunk_vecs + v0, v1 - v0, et);
+        if (!g.flag) continue;
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // this CTA's share is written
+        if (et != 0) continue;
+        __threadfence();
+        if (gs > 1) {
+            const uint32_t done = atomicAdd(p.g_counters + g.r, 1u) + 1u;
+            if (done != static_cast<uint32_t>(gs)) continue;
+            p.g_counters[g.r] = 0u;  // zero again for the next call
+            __threadfence();
+        }
+        if (g.r != p.g_drop) st_release_u32(const_cast<uint32_t *>(p.flags) + g.r, p.epoch);
+    }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1) ub_gemm_skinny_kernel(const __grid_constant__ GemmParams p)
 {
@@ -298,7 +336,7 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_skinny_kernel(const __grid
         mbar_wait_drain(drain_bar, 0, p.timeout_ns);
     } else if (warp >= 2) {
         // ---------------------------------------------------------- epilogue
-        if (IS_AG && p.fused_gather) fused_gather(p, static_cast<int>(threadIdx.x) - 64);
+        if (IS_AG && p.fused_gather) fused_gather_grouped(p, static_cast<int>(threadIdx.x) - 64);
         const int quarter = warp & 3;         // TMEM lanes this warp may read: 32*quarter ...
         const int row = quarter * 32 + lane;  // this thread's lane = weight row inside the tile
         const int T = p.tp * p.c;
@@ -503,7 +541,69 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_skinny_kernel(const __grid
     }
 }
 
+// Calibration read: each CTA streams one contiguous share of the bytes through a ring of
+// SR_STAGES shared-memory buffers with 32 KB bulk copies (thread 0 issues, thread 32
+// frees), the pipeline a few-token weight stream would use with nothing else to do.
+constexpr int SR_STAGES = 6;
+constexpr uint32_t SR_CHUNK = 32768;
+constexpr int SR_SMEM = 128 + SR_STAGES * static_cast<int>(SR_CHUNK) + 2 * SR_STAGES * 8;
+
+__global__ void __launch_bounds__(64, 1) stream_read_kernel(const __grid_constant__ StreamReadParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    const uint32_t buf0 = smem_u32(base);
+    const uint32_t bar0 = buf0 + SR_STAGES * SR_CHUNK;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (SR_STAGES + s); };
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < SR_STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+    pdl_trigger();
+    pdl_wait();
+    const WaitCtx w{p.abort_word, p.status, p.timeout_ns, p.epoch};
+    const int64_t vecs = p.bytes / 16;
+    const int64_t per = (vecs + gridDim.x - 1) / gridDim.x * 16;
+    const int64_t lo = static_cast<int64_t>(blockIdx.x) * per;
+    const int64_t hi = lo + per < p.bytes ? lo + per : p.bytes;
+    const int n = hi > lo ? static_cast<int>((hi - lo + SR_CHUNK - 1) / SR_CHUNK) : 0;
+    if (threadIdx.x == 0) {
+        int issued = 0;
+        for (int i = 0; i < n; ++i) {
+            const int s = i % SR_STAGES;
+            if (!mbar_wait(empty_bar(s), ((i / SR_STAGES) & 1u) ^ 1u, w)) break;
+            const int64_t o = lo + static_cast<int64_t>(i) * SR_CHUNK;
+            const uint32_t bytes = static_cast<uint32_t>(hi - o < SR_CHUNK ? hi - o : SR_CHUNK);
+            mbar_arrive_expect_tx(full_bar(s), bytes);
+            bulk_load(buf0 + s * SR_CHUNK, p.src + o, bytes, full_bar(s));
+            ++issued;
+        }
+        // the copies in flight must land before the CTA may exit
+        for (int i = issued > SR_STAGES ? issued - SR_STAGES : 0; i < issued; ++i)
+            mbar_wait_drain(full_bar(i % SR_STAGES), static_cast<uint32_t>(i / SR_STAGES) & 1u, p.timeout_ns);
+    } else if (threadIdx.x == 32) {
+        for (int i = 0; i < n; ++i) {
+            const int s = i % SR_STAGES;
+            if (!mbar_wait(full_bar(s), static_cast<uint32_t>(i / SR_STAGES) & 1u, w)) break;
+            mbar_arrive(empty_bar(s));
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_stream_read(const StreamReadParams &p, int grid, cudaStream_t stream)
+{
+    cudaError_t e = raise_smem_limit(reinterpret_cast<const void *>(stream_read_kernel), SR_SMEM);
+    if (e != cudaSuccess) return e;
+    e = launch_ex(stream_read_kernel, p, grid, 64, SR_SMEM, 0, p.pdl != 0, stream);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
 
 int skinny_smem_bytes(int stages, int w_bytes, int x_bytes)
 {

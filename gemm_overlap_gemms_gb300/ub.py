@@ -38,7 +38,7 @@ EXPORTS = [
     "ub_clear_status", "ub_get_counters", "ub_kernel_time", "ub_grid_ctas", "ub_last_error",
     "ag_gemm_noalloc", "ag_gemm_swiglu", "ag_gemm_kn", "gemm_rs_kn", "ub_wgrad",
     "ub_allgather", "ub_reduce_scatter", "ub_plan_tail_split", "ub_plan_path",
-    "ub_plan_ag_self_head", "ag_gemm_from_buffer", "ub_plan_gather_parts",
+    "ub_plan_ag_self_head", "ag_gemm_from_buffer", "ub_plan_gather_parts", "ub_stream_read",
 ]
 NOALLOC_MAX_ELEMS = 16 * 1024 * 1024
 
@@ -92,6 +92,7 @@ def load():
         "ub_wgrad": [P, P, I64, I, P, P],
         "ub_allgather": [P, PP, P],
         "ub_reduce_scatter": [P, PP, PP, P],
+        "ub_stream_read": [P, P, I64, P],
         "gemm_rs": [P, PP, PP, I64, PP, P],
         "ub_set_option": [P, I, I64],
         "ub_get_option": [P, I, ctypes.POINTER(I64)],
@@ -466,6 +467,16 @@ class UserBuffer:
                 raise ValueError("Y_shards[%d] must be [>=%d, %d]" % (r, c, H))
         _check(load().ub_reduce_scatter(self._h, _ptrs(P), _ptrs(Y_shards), _stream_ptr(stream)))
         return Y_shards
+
+    def stream_read(self, t: torch.Tensor, stream=None):
+        """Read the bytes of contiguous CUDA tensor `t` once and discard them (ub_stream_read:
+        the cost of one kernel reading them, the floor of a call whose work is that read)."""
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous():
+            raise TypeError("t must be a contiguous CUDA tensor")
+        if t.device != self.device:
+            raise ValueError("t is on %s, the user buffer on %s" % (t.device, self.device))
+        _check(load().ub_stream_read(self._h, ctypes.c_void_p(t.data_ptr()), t.numel() * t.element_size(),
+                                     _stream_ptr(stream)))
 
     def gemm_rs(self, A, Bt, Y_shards=None, stream=None):
         """Y_shards[r] = rows [r*c, (r+1)*c) of sum_j A[j] @ Bt[j].T (c = T / tp)."""

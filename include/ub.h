@@ -97,9 +97,10 @@ enum {
                               chunk in ring order and publishes each chunk's flag as its last
                               CTA finishes (fewer driver operations per call); 2: the GEMM's
                               own epilogue warps copy the chunks before their first tile and
-                              publish the flags (tile kernels; the few-token kernel uses 1);
-                              -1 (default): 1 for T <= 512, 2 above (the few-token kernel
-                              and ub_allgather use 1 or 0 instead of 2) */
+                              publish the flags (the few-token kernel: each chunk by its own
+                              few CTAs); -1 (default): the tile kernels 2 when T > 512 and
+                              the call has more than one wave of tiles, else 1; the
+                              few-token kernel 1 (ub_allgather uses 1 or 0 instead of 2) */
     UB_OPT_SKINNY = 10,    /* few-token kernel: weight rows on the MMA's M, tokens on its N, so
                               the work follows T and the weight is read once. Usable while the
                               token columns (ag_gemm*: tp * roundup(T/tp, 16); gemm_rs*:
@@ -180,8 +181,10 @@ int ub_buffer(ub_handle_t h, void **dev_ptr, size_t *bytes);
  * streams (the stand-in for copy-engine send/recv; on GB300 the driver runs a
  * same-device copy as a kernel on SMs, next to the GEMM, whose CTAs leave room for it),
  * each followed by a readiness-flag write; one gather kernel on the side stream
- * (default for T <= 512); or the GEMM kernel's own epilogue warps before their first
- * tile (default above). One persistent GEMM kernel on `stream` walks the chunks in
+ * (default for the few-token kernel, and for the tile kernels at T <= 512 or when the
+ * tiles fit one wave, so that the gather's CTAs run on the SMs no tile holds); or the
+ * GEMM kernel's own epilogue warps before their first tile (default for tile-kernel
+ * calls of more than one wave). One persistent GEMM kernel on `stream` walks the chunks in
  * ring order starting at UB_OPT_SELF_RANK (whose chunk it reads in place, without
  * waiting -- on CTA pairs, where that saves a wave, only the chunk's whole 256-row
  * tiles, its last rows from the buffer behind its flag, see ub_plan_ag_self_head),
@@ -305,6 +308,18 @@ int ub_reduce_scatter(ub_handle_t h, const void *const *P, void *const *Y_shards
  *    not a multiple of 8, pointers not 16-byte aligned), UB_ERR_CUDA.
  */
 int ag_gemm_from_buffer(ub_handle_t h, const void *Wt, int64_t N, int64_t glu_f, void *Y, void *stream);
+
+/*
+ * An addition of this library for measurement (the pages define no such call): read
+ * `bytes` of device memory at `src` once and discard them -- one kernel on `stream`, one
+ * CTA per SM, each streaming a contiguous share into shared memory with bulk copies. Its
+ * time is what reading those bytes costs in one isolated kernel on this GPU (launch, ramp
+ * and drain included): the floor of a few-token call, whose work is its weight read.
+ *  - src: device pointer, 16-byte aligned; bytes: a multiple of 16 (0: nothing launched).
+ *  - Errors: UB_ERR_ARG (null src, negative bytes), UB_ERR_ALIGN, UB_ERR_CUDA; a bounded
+ *    wait that runs out is reported by ub_query_status (UB_ERR_TIMEOUT).
+ */
+int ub_stream_read(ub_handle_t h, const void *src, int64_t bytes, void *stream);
 
 /* Options (UB_OPT_*). UB_ERR_ARG for an unknown key or an out-of-range value. */
 int ub_set_option(ub_handle_t h, int key, int64_t val);

@@ -33,7 +33,8 @@ def _make_buf(T, H, tp, skinny=1, extra=8):
                                       (2, 100, 256, 392), (1, 200, 320, 128), (8, 32, 1024, 1000),
                                       (4, 64, 4096, 3072), (1, 1, 72, 8)])
 def test_skinny_ag_matches_oracle(tp, c, H, N, gather):
-    """gather -1: the one-launch gather kernel; 2: the kernel's epilogue warps gather."""
+    """gather -1: the one-launch gather kernel; 2: the kernel's epilogue warps gather,
+    each chunk by its own group of CTAs (N tiles fewer than the chunks included)."""
     T = c * tp
     g = synth.generator(seed=101)
     shards = [synth.normal_bf16((c, H), 1.0, g) for _ in range(tp)]
