@@ -11,8 +11,9 @@
 // (256 threads, no shared memory), four per SM, so that together they keep enough loads
 // in flight to stream HBM, and one fits on an SM beside a persistent GEMM CTA. Beside a
 // GEMM that streams its operands at full rate, the reduce-scatter's loads queue behind
-// the GEMM's (measured: it runs at about a fifth of its speed alone), which limits how
-// much of it the bulk overlap hides.
+// the GEMM's (measured on GB300 beside the weight-gradient GEMM: a third of its speed
+// alone at best, and in some runs no overlap at all), which limits how much of it the
+// bulk overlap hides.
 #include <cuda_bf16.h>
 
 #include "ub_internal.h"
