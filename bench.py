@@ -641,12 +641,13 @@ def padded_measure(wl, steps, warmup, stream, world):
     return ms
 
 
-def bulk_measure(wl, stream, T=4096, reps=10):
+def bulk_measure(wl, stream, T=4096, reps=20):
     """The "bulk" method at one microbatch of the workload: an independent collective on
-    a second stream beside an unrelated GEMM. fc1 backward: its input-gradient GEMM
-    (gemm_rs_kn over dZ_j Wt_j) beside the bulk all-gather of its input X (needed by its
-    weight gradient); then its weight-gradient GEMM beside a bulk reduce-scatter of tp
-    bf16 partials [T, hidden]. Times are ms per pair of operations."""
+    a second stream beside an unrelated GEMM, the GEMM issued first. fc1 backward: its
+    input-gradient GEMM (gemm_rs_kn over dZ_j Wt_j) beside the bulk all-gather of its
+    input X (needed by its weight gradient); then its weight-gradient GEMM beside a bulk
+    reduce-scatter of tp bf16 partials [T, hidden]. Times are ms per pair of operations,
+    each the median of three timings."""
     w = wl.w
     H, F, tp = w.hidden, w.rs_k[0], w.tp
     dev = wl.W1.device
@@ -668,7 +669,9 @@ def bulk_measure(wl, stream, T=4096, reps=10):
     buf.allgather(shards, stream=stream)      # the buffer holds X for the wgrad runs
 
     def timed(fn):
-        return time_steps(fn, reps, 2, stream, 1) / reps
+        # median of three timings of `reps` back-to-back runs: single timings of a pair
+        # of kernels on two streams vary by several us from run to run
+        return float(np.median([time_steps(fn, reps, 2, stream, 1) / reps for _ in range(3)]))
 
     def both(gemm, coll):
         def fn():
@@ -861,8 +864,9 @@ def sweep_points(wl, stream):
     Amax = wl.A[int(np.argmax(wl.Ts))]
     Tmax = max(wl.Ts)
     pk, src = peaks()
-    tensor_peak = _peak_value(pk, "bf16_tflops_sustained", "bf16_tflops") or FALLBACK["bf16_tflops_sustained"]
+    tensor_peak = _peak_value(pk, "bf16_tflops") or FALLBACK["bf16_tflops"]
     hbm_peak = _peak_value(pk, "hbm_gbs") or FALLBACK["hbm_gbs"]
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=Xmax.device)
     for T in (4, 64, 128, 256, 512, 1024, 2048, 4096, 6144, 8192):
         if T > Tmax:
             X = synth.normal_bf16((T, H), 1.0, synth.generator(Xmax.device, 5), Xmax.device)
@@ -886,11 +890,10 @@ def sweep_points(wl, stream):
             no_overlap = op == "ag_swiglu_no_overlap"
             wl.buf.set_option("copy_streams", 0 if no_overlap else 4)
             wl.buf.set_option("gather_kernel", 0 if no_overlap else -1)
-            ms, ms_mean, eager = time_calls(fn, SWEEP_CALLS, SWEEP_WARMUP, stream, graph=not no_overlap)
+            _, _, eager = time_calls(fn, SWEEP_CALLS, SWEEP_WARMUP, stream, graph=False)
+            ms = eager if no_overlap else time_graph_flushed(fn, stream, flush, SWEEP_CALLS, SWEEP_WARMUP)[0]
             wl.buf.set_option("copy_streams", 4)
             wl.buf.set_option("gather_kernel", -1)
-            if ms is None:
-                ms = eager
             fl = 2.0 * T * H * N if op != "rs" else 2.0 * T * K * H * tp
             tf = fl / (ms / 1e3) / 1e12
             # algorithmic HBM bytes: weights once, activations in, results out (AG: the
@@ -900,34 +903,37 @@ def sweep_points(wl, stream):
             else:
                 n_out = N // 2 if op.startswith("ag_swiglu") else N
                 nbytes = 2.0 * (N * H + 2 * T * H + T * n_out)
-            out.append({"sweep": op, "T": T, "us": ms * 1e3,
-                        "us_mean": ms_mean * 1e3 if ms_mean is not None else None,
-                        "us_eager": eager * 1e3, "timing": "eager" if no_overlap else "graph replay",
+            out.append({"sweep": op, "T": T, "us": ms * 1e3, "us_eager": eager * 1e3,
+                        "timing": "eager, back to back" if no_overlap else "graph replay, L2 flushed",
                         "tflops": tf, "frac_of_peak": tf / tensor_peak,
                         "hbm_gbs": nbytes / (ms / 1e3) / 1e9, "hbm_frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak,
                         "note": ("gather copies on the GEMM's stream, before it (no overlap)"
                                  if op == "ag_swiglu_no_overlap" else
                                  "includes the gather copies, overlapped" if op != "rs" else "")})
+    del flush
     return out
 
 
 def sweep_other_configs(stream):
     """The other throughput configs on their own handles: QKV (AG-GEMM, N = 3072, tp 4,
     hidden 4096) and large (GEMM-RS, tp 8, hidden 8192, attention-out K = 1024 and fc2
-    K = 3584 per shard), over a ladder of active T (median of 50 graph replays per point)."""
+    K = 3584 per shard), over a ladder of active T (median of 50 graph replays per point,
+    L2 flushed before each; and 50 calls back to back)."""
     from gemm_overlap_gemms_gb300 import ub
     pk, _ = peaks()
-    tensor_peak = _peak_value(pk, "bf16_tflops_sustained", "bf16_tflops") or FALLBACK["bf16_tflops_sustained"]
+    tensor_peak = _peak_value(pk, "bf16_tflops") or FALLBACK["bf16_tflops"]
     hbm_peak = _peak_value(pk, "hbm_gbs") or FALLBACK["hbm_gbs"]
     dev = torch.device("cuda", torch.cuda.current_device())
     g = synth.generator(dev, 7)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     out = []
 
     def point(name, T, fn, fl, nbytes):
-        ms, ms_mean, eager = time_calls(fn, SWEEP_CALLS, SWEEP_WARMUP, stream)
+        _, _, eager = time_calls(fn, SWEEP_CALLS, SWEEP_WARMUP, stream, graph=False)
+        ms = time_graph_flushed(fn, stream, flush, SWEEP_CALLS, SWEEP_WARMUP)[0]
         tf = fl / (ms / 1e3) / 1e12
-        out.append({"sweep": name, "T": T, "us": ms * 1e3, "us_mean": ms_mean * 1e3, "us_eager": eager * 1e3,
-                    "timing": "graph replay", "tflops": tf, "frac_of_peak": tf / tensor_peak,
+        out.append({"sweep": name, "T": T, "us": ms * 1e3, "us_eager": eager * 1e3,
+                    "timing": "graph replay, L2 flushed", "tflops": tf, "frac_of_peak": tf / tensor_peak,
                     "hbm_gbs": nbytes / (ms / 1e3) / 1e9, "hbm_frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak,
                     "note": "includes the gather" if name.startswith("qkv") else ""})
 
