@@ -117,7 +117,12 @@ __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ Gat
         if (two) dst[v + stride] = b2;
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0 && p.ctas_per_chunk == 1) {
+        // the whole chunk is this CTA's: its release store publishes every thread's
+        // copies (ordered before it by the CTA barrier), no count needed
+        if (r != p.drop)
+            asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p.flags + r), "r"(p.epoch) : "memory");
+    } else if (threadIdx.x == 0) {
         __threadfence();
         const uint32_t done = atomicAdd(p.counters + r, 1u) + 1u;
         if (done == static_cast<uint32_t>(p.ctas_per_chunk)) {
