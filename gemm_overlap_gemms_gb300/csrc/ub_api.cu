@@ -315,9 +315,11 @@ constexpr bool kFusedGatherSkinnyAuto = false;
 //  - AG-GEMM behind the gather (`gathered`): kFixupAgKb0 + kFixupAgKb1 * (s - 1), about
 //    3.4 us + 2.6 us per added piece (K = 4096: QKV at T = 5120 90.5 us in 4 pieces against
 //    96.1 whole, AG + SwiGLU at T = 3072 119.3 in 2 against 124.0). Its tail tiles are the
-//    last rows of the gather, so with fewer than kMinWavesAg whole waves before them they
-//    wait for the gather whatever their length, and a split only adds its fix-up (QKV at
-//    T = 2048, one whole wave: 55.8 us in 2 pieces, 62.0 in 3, against 53.8 whole).
+//    last rows of the gather, so with one whole wave before them they wait for the
+//    gather whatever their length, and a split only adds its fix-up (QKV at T = 2048, one
+//    whole wave: 55.8 us in 2 pieces, 62.0 in 3, against 53.8 whole). With no whole wave
+//    (fewer tiles than pairs) every tile is in the split and spreads over idle pairs: QKV
+//    at T = 256 31.7 us in 3 pieces against 34.5 whole, at T = 512 33.3 in 2 against 35.0.
 constexpr double kFixupKb0 = 30.0;
 constexpr double kFixupKb1 = 13.5;
 constexpr double kFixupAgKb0 = 10.0;
@@ -334,7 +336,8 @@ double split_tail_cost(int64_t s, int64_t kb, bool gathered)
 // How many k-pieces the last wave's tiles are cut into. At most one piece per idle pair,
 // MAX_TAIL_SPLIT pieces and MIN_KBLOCKS_PER_PIECE k-blocks per piece; within that the
 // cheapest cut by split_tail_cost (1 when no cut beats whole tiles, or for a gathered
-// AG-GEMM with fewer than kMinWavesAg whole waves), or with `force` = 1 the most pieces
+// AG-GEMM with at least one but fewer than kMinWavesAg whole waves), or with `force` = 1
+// the most pieces
 // allowed (the split forced on), with `force` = n >= 2 at most n pieces.
 int64_t tail_split_for(int64_t tiles, int64_t np, int64_t kb, int64_t force, bool gathered)
 {
@@ -346,7 +349,7 @@ int64_t tail_split_for(int64_t tiles, int64_t np, int64_t kb, int64_t force, boo
     if (smax < 1) return 1;
     if (force == 1) return smax;
     if (force >= 2) return force < smax ? force : smax;
-    if (gathered && tiles / np < kMinWavesAg) return 1;
+    if (gathered && tiles >= np && tiles / np < kMinWavesAg) return 1;
     int64_t best = 1;
     for (int64_t s = 2; s <= smax; ++s)
         if (split_tail_cost(s, kb, gathered) < split_tail_cost(best, kb, gathered)) best = s;

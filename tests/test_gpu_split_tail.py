@@ -114,3 +114,29 @@ def test_swiglu_split_tail():
         torch.cuda.synchronize()
         assert buf.query_status() == ub.UB_OK
     assert_close(Z, ref, "SwiGLU split")
+
+
+@pytest.mark.parametrize("T", [256, 512])
+def test_ag_with_fewer_tiles_than_pairs_splits_by_default_and_matches(T):
+    """The QKV projection at T = 256 / 512 (12 / 24 pair tiles on 76 pairs, no whole wave):
+    by default every tile is cut into k-pieces over the idle pairs, behind the gather
+    kernel's chunk flags; integer inputs make the sums exact, so the result equals the
+    oracle's rounded to bf16 bit for bit, and the gathered buffer equals its
+    concatenation."""
+    tp, H, N = 4, 4096, 3072
+    c = T // tp
+    g = synth.generator(seed=307)
+    shards = [synth.small_int_bf16((c, H), -2, 2, g) for _ in range(tp)]
+    Wt = synth.small_int_bf16((N, H), -2, 2, g)
+    with ub.UserBuffer([8192, H], tp) as buf:
+        buf.set_active_shape([T, H])
+        Y = run_ag(buf, shards, Wt)
+        cnt = buf.counters()
+        assert ub.KERNELS[cnt["last_kernel"]] == "pair" and cnt["last_pieces"] > 1, cnt
+        assert ub.GATHERS[cnt["last_gather"]] == "gather_kernel", cnt
+        assert buf.query_status() == ub.UB_OK
+        G = buf.buffer()[:T].cpu()
+    Gref, Yref = oracle_ag(shards, Wt)
+    np.testing.assert_array_equal(synth.to_u16(G), Gref)
+    assert np.abs(Yref).max() < 2 ** 24
+    np.testing.assert_array_equal(synth.to_u16(Y), _round_bf16(Yref))

@@ -65,12 +65,19 @@ def test_tail_split_follows_the_measured_winner(what, tiles, kb, gathered, split
     assert (ub.plan_tail_split(tiles, PAIRS, kb, gathered=gathered) > 1) == split, what
 
 
-def test_gathered_ag_splits_only_after_two_whole_waves():
+def test_gathered_ag_splits_with_no_whole_wave_or_after_two():
+    """One whole wave in front: the tail waits for the gather's last rows, no split. No
+    whole wave: every tile is split over the idle pairs when the fix-up pays."""
     for tiles in range(1, 6 * PAIRS):
         s = ub.plan_tail_split(tiles, PAIRS, 64, gathered=True)
-        if tiles // PAIRS < 2:
+        if tiles // PAIRS == 1:
             assert s == 1, tiles
         assert s <= ub.plan_tail_split(tiles, PAIRS, 64, widest=True, gathered=True)
+    # QKV at T = 256 / 512 (12 / 24 pair tiles, 64 k-blocks): split
+    assert ub.plan_tail_split(12, PAIRS, 64, gathered=True) > 1
+    assert ub.plan_tail_split(24, PAIRS, 64, gathered=True) > 1
+    # QKV at T = 2048 (96 tiles, one whole wave): whole tiles
+    assert ub.plan_tail_split(96, PAIRS, 64, gathered=True) == 1
 
 
 def test_plan_path_respects_forced_options():
