@@ -289,6 +289,11 @@ int64_t ag_self_head(ub_handle *h, int mode, int64_t T, int64_t c, int self, int
     return self_head_for(T, c, self, n_tiles, clusters_for(h, mode, 1 << 30));
 }
 
+// GEMM-RS on CTA pairs: tile rows walked in groups of kGroupM (rows fastest inside a
+// group) when the weights exceed this many bytes, else N fastest.
+constexpr int64_t kGroupedOrderBytes = int64_t(256) << 20;
+constexpr int kGroupM = 8;
+
 constexpr int64_t kGatherKernelMaxT = 512;  // UB_OPT_GATHER_KERNEL = -1: kernel up to this T
 // ... and inside the GEMM above it when the call has more than one wave of tiles: on
 // GB300 (tp 4, hidden 4096) the whole AG call is 2-8 % faster than with the driver copies
@@ -1181,6 +1186,9 @@ static int gemm_rs_impl(ub_handle_t h, const void *const *A, const void *const *
     p.timeout_ns = static_cast<uint64_t>(h->timeout_ns);
     if (skinny) set_skinny(h, p, 1, ubk::SK_W_BYTES);
     else if (pair) set_pairs(h, p, ubk::MODE_RS, streamk);
+    // weight panels that together exceed L2 several times over (the large RS at K = 3584:
+    // 470 MB) would be re-read from HBM by every wave walked N fastest
+    p.group_m = pair && static_cast<int64_t>(tp) * K * H * 2 > kGroupedOrderBytes ? kGroupM : 0;
     uint32_t epoch = 0;
     if (int rc = begin_call(h, s, epoch, false, pair ? p.tail_split > 1 : skinny && p.sk_split > 1)) return rc;
     p.epoch = epoch;

@@ -473,6 +473,20 @@ __device__ __forceinline__ PTile pair_tile_at(int t, const GemmParams &p)
     const int rem = t - p.region_tile0[q];
     PTile x;
     x.q = q;
+    if (p.group_m > 1) {
+        // groups of group_m tile rows (the last group may be shorter), rows fastest: a
+        // wave of P tiles spans group_m activation panels and about P / group_m weight
+        // panels instead of every weight panel
+        const int mt = (p.region_tile0[q + 1] - p.region_tile0[q]) / p.n_tiles;
+        const int per_group = p.group_m * p.n_tiles;
+        const int g = rem / per_group;
+        const int m0 = g * p.group_m;
+        const int gm = mt - m0 < p.group_m ? mt - m0 : p.group_m;
+        const int r = rem - g * per_group;
+        x.n = r / gm;
+        x.m = m0 + (r - x.n * gm);
+        return x;
+    }
     x.m = rem / p.n_tiles;
     x.n = rem - x.m * p.n_tiles;
     return x;

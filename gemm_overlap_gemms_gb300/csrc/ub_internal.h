@@ -99,6 +99,9 @@ struct GemmParams {
     int dp_tiles;                // tiles [0, dp_tiles) go whole to pairs in strided order
                                  // (pair p: p, p + num_pairs, ...)
     int tail_split;              // the remaining tiles are cut into this many k-pieces
+    int group_m;                 // > 1: tiles walked in groups of this many 256-row tile rows,
+                                 // rows fastest inside a group (RS whose weight panels
+                                 // together exceed L2); else N fastest
     int ldy;                     // RS: leading dimension of Y_shards (= hidden)
     void *y_ptr[UB_MAX_TP];      // RS: Y_shards[r], for stores that cross a chunk end
     int glu_f;                   // MODE_AG_GLU: F, the width of each half (gate, up) of Wt

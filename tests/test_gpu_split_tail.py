@@ -140,3 +140,28 @@ def test_ag_with_fewer_tiles_than_pairs_splits_by_default_and_matches(T):
     np.testing.assert_array_equal(synth.to_u16(G), Gref)
     assert np.abs(Yref).max() < 2 ** 24
     np.testing.assert_array_equal(synth.to_u16(Y), _round_bf16(Yref))
+
+
+def test_rs_grouped_tile_order_integer_inputs_exact():
+    """Weights above 256 MB (tp 8 x [4096, 4096]): the pair kernel walks tile rows in
+    groups of eight, rows fastest, with the split last wave; integer inputs make the sums
+    exact, so every sampled row -- two in each 256-row tile row, all 4096 columns --
+    equals the oracle's rounded to bf16 bit for bit."""
+    tp, H, K, T = 8, 4096, 4096, 2048
+    g = synth.generator(seed=309)
+    A = [synth.small_int_bf16((T, K), -1, 1, g) for _ in range(tp)]
+    Bt = [synth.small_int_bf16((H, K), -1, 1, g) for _ in range(tp)]
+    c = T // tp
+    with ub.UserBuffer([T, H], tp) as buf:
+        buf.set_active_shape([T, H])
+        Ys, _ = run_rs(buf, [a.cpu() for a in A], [b.cpu() for b in Bt])
+        cnt = buf.counters()
+        assert ub.KERNELS[cnt["last_kernel"]] == "pair", cnt
+        assert buf.query_status() == ub.UB_OK
+    rows = np.unique(np.concatenate([np.arange(0, T, 256), np.arange(255, T, 256), [1, T - 2]]))
+    ridx = torch.as_tensor(rows)
+    ref, owner, local = oracle.gemm_rs_rows([synth.to_u16(a.cpu()[ridx]) for a in A],
+                                            [synth.to_u16(b.cpu()) for b in Bt], rows, T)
+    assert np.abs(ref).max() < 2 ** 24
+    got = torch.stack([Ys[int(o)][int(i)] for o, i in zip(owner, local)])
+    np.testing.assert_array_equal(synth.to_u16(got), _round_bf16(ref))
