@@ -108,13 +108,16 @@ __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ Gat
     const uint4 *src = static_cast<const uint4 *>(p.src[r]);
     uint4 *dst = static_cast<uint4 *>(p.ub) + static_cast<int64_t>(r) * p.chunk_vecs;
     const int64_t stride = static_cast<int64_t>(p.ctas_per_chunk) * blockDim.x;
-    for (int64_t v = static_cast<int64_t>(part) * blockDim.x + threadIdx.x; v < p.chunk_vecs; v += 2 * stride) {
-        const uint4 a = ld_stream(src + v);
-        const bool two = v + stride < p.chunk_vecs;
-        uint4 b2;
-        if (two) b2 = ld_stream(src + v + stride);
-        dst[v] = a;
-        if (two) dst[v + stride] = b2;
+    // eight 16-byte loads in flight per thread before the first store
+    constexpr int U = 8;
+    for (int64_t v = static_cast<int64_t>(part) * blockDim.x + threadIdx.x; v < p.chunk_vecs; v += U * stride) {
+        uint4 x[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (v + u * stride < p.chunk_vecs) x[u] = ld_stream(src + v + u * stride);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (v + u * stride < p.chunk_vecs) dst[v + u * stride] = x[u];
     }
     __syncthreads();
     if (threadIdx.x == 0 && p.ctas_per_chunk == 1) {
