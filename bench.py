@@ -660,12 +660,14 @@ def padded_measure(wl, steps, warmup, stream, world):
 
 
 def bulk_measure(wl, stream, T=4096, reps=20):
-    """The "bulk" method at one microbatch of the workload: an independent collective on
-    a second stream beside an unrelated GEMM, the GEMM issued first. fc1 backward: its
-    input-gradient GEMM (gemm_rs_kn over dZ_j Wt_j) beside the bulk all-gather of its
-    input X (needed by its weight gradient); then its weight-gradient GEMM beside a bulk
-    reduce-scatter of tp bf16 partials [T, hidden]. Times are ms per pair of operations,
-    each the median of three timings."""
+    """The "bulk" method at one microbatch of the workload: an independent collective
+    beside an unrelated GEMM. fc1 backward: its input-gradient GEMM (gemm_rs_kn over
+    dZ_j Wt_j) beside the bulk all-gather of its input X (needed by its weight gradient);
+    then its weight-gradient GEMM beside a bulk reduce-scatter of tp bf16 partials
+    [T, hidden]. `overlapped_ms`: beside mode (UB_OPT_BULK_BESIDE: the collective on the
+    GEMM's stream right after it, launched once the GEMM's CTAs hold their SMs);
+    `two_streams_overlapped_ms`: the collective on a second stream, the GEMM issued
+    first. Times are ms per pair of operations, each the median of three timings."""
     w = wl.w
     H, F, tp = w.hidden, w.rs_k[0], w.tp
     dev = wl.W1.device
@@ -699,6 +701,19 @@ def bulk_measure(wl, stream, T=4096, reps=20):
             stream.wait_stream(side)
         return fn
 
+    def beside(gemm, coll):
+        def fn():
+            gemm()
+            coll()
+        return fn
+
+    def timed_beside(fn):
+        buf.set_option("bulk_beside", 1)
+        try:
+            return timed(fn)
+        finally:
+            buf.set_option("bulk_beside", 0)
+
     dgrad = lambda: buf.gemm_rs_kn(dZ, Wt, outs, stream=stream)
     ag_side = lambda: buf.allgather(shards, stream=side)
     ag_alone = lambda: buf.allgather(shards, stream=stream)
@@ -711,9 +726,12 @@ def bulk_measure(wl, stream, T=4096, reps=20):
             ("reduce_scatter_beside_wgrad", wgrad, rs_side, rs_alone, (tp + 1) * T * H * 2)):
         t_g = timed(gemm)
         t_c = timed(coll_alone)
-        t_b = timed(both(gemm, coll_side))
+        t_b = timed_beside(beside(gemm, coll_alone))
+        t_2 = timed(both(gemm, coll_side))
+        hidden = lambda t: (t_g + t_c - t) / t_c if t_c > 0 else None
         res[name] = {"gemm_ms": t_g, "collective_ms": t_c, "sequential_ms": t_g + t_c,
-                     "overlapped_ms": t_b, "hidden_fraction": (t_g + t_c - t_b) / t_c if t_c > 0 else None,
+                     "overlapped_ms": t_b, "hidden_fraction": hidden(t_b),
+                     "two_streams_overlapped_ms": t_2, "two_streams_hidden_fraction": hidden(t_2),
                      "collective_gbs": coll_bytes / (t_c / 1e3) / 1e9}
     assert buf.query_status() == 0
     return res

@@ -155,6 +155,7 @@ struct ub_handle {
     int64_t streamk = -1;   // -1 = chosen per call
     int64_t skinny = -1;    // -1 = whenever the few-token kernel is usable
     int64_t pdl = 1;        // programmatic dependent launch of every kernel
+    int64_t bulk_beside = 0; // 1: ub_allgather / ub_reduce_scatter beside the kernel before them
     int pair_clusters[3] = {-1, -1, -1};  // resident clusters of the pair kernel, per mode
     ub_counters_t counters{};
     std::vector<CacheEntry> cache;
@@ -528,6 +529,31 @@ int gather_parts(int tp, int self, int64_t c, int64_t head, GatherPart out[UB_MA
     return n;
 }
 
+// The gather kernel's launch parameters for the handle's active shape: about one CTA
+// per SM in all (ceil(SMs / tp) per chunk, fewer for small chunks), ring order from the
+// self rank, each chunk's flag published at `epoch` unless it is `drop`.
+ubk::GatherParams gather_kernel_params(ub_handle *h, const void *const *shards, uint32_t epoch, int64_t drop)
+{
+    const int tp = h->tp;
+    ubk::GatherParams g;
+    memset(&g, 0, sizeof g);
+    for (int r = 0; r < tp; ++r) g.src[r] = shards[r];
+    g.ub = h->ub;
+    g.flags = flags_of(h);
+    g.counters = gather_counters_of(h);
+    g.epoch = epoch;
+    g.tp = tp;
+    g.self_rank = static_cast<int>(h->self_rank);
+    g.drop = static_cast<int>(drop);
+    g.chunk_vecs = (h->T / tp) * h->hidden / 8;
+    int64_t per = (h->sm_count + tp - 1) / tp;
+    const int64_t need = (g.chunk_vecs + 511) / 512;  // at least two vectors per thread
+    if (per > need) per = need;
+    g.ctas_per_chunk = static_cast<int>(per < 1 ? 1 : per);
+    g.pdl = static_cast<int>(h->pdl);
+    return g;
+}
+
 int issue_gather(ub_handle *h, const void *const *shards, cudaStream_t s, uint32_t epoch, int64_t drop,
                  int64_t self_head, bool one_wave = false)
 {
@@ -564,22 +590,7 @@ int issue_gather(ub_handle *h, const void *const *shards, cudaStream_t s, uint32
     if (h->gather_by_kernel) {
         // One launch on the side stream: small CTAs (they fit beside the GEMM's), about
         // one per SM per chunk, each chunk's flag published by its last CTA.
-        ubk::GatherParams g;
-        memset(&g, 0, sizeof g);
-        for (int r = 0; r < tp; ++r) g.src[r] = shards[r];
-        g.ub = h->ub;
-        g.flags = flags_of(h);
-        g.counters = gather_counters_of(h);
-        g.epoch = epoch;
-        g.tp = tp;
-        g.self_rank = self;
-        g.drop = static_cast<int>(drop);
-        g.chunk_vecs = c * H / 8;
-        int64_t per = (h->sm_count + tp - 1) / tp;
-        const int64_t need = (g.chunk_vecs + 511) / 512;  // at least two vectors per thread
-        if (per > need) per = need;
-        g.ctas_per_chunk = static_cast<int>(per < 1 ? 1 : per);
-        g.pdl = static_cast<int>(h->pdl);
+        ubk::GatherParams g = gather_kernel_params(h, shards, epoch, drop);
         UB_CUDA(cudaEventRecord(h->ev_fork, s));
         UB_CUDA(cudaStreamWaitEvent(h->side, h->ev_fork, 0));
         cudaError_t e = ubk::launch_gather(g, h->side);
@@ -1226,6 +1237,17 @@ int ub_allgather(ub_handle_t h, const void *const *shards, void *stream)
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint32_t epoch = 0;
     if (int rc = begin_call(h, s, epoch, false, false)) return rc;
+    if (h->bulk_beside) {
+        // the gather kernel on `stream` itself, a programmatic dependent of the kernel
+        // before it: about one CTA per SM, in the room that kernel's CTAs leave
+        ubk::GatherParams g = gather_kernel_params(h, shards, epoch, -1);
+        g.pdl = 1;
+        g.beside = 1;
+        cudaError_t e = ubk::launch_gather(g, s);
+        if (e != cudaSuccess) return cuda_fail(e, "gather kernel launch");
+        h->counters.last_T = h->T;
+        return UB_OK;
+    }
     if (int rc = issue_gather(h, shards, s, epoch, -1, h->T / h->tp)) return rc;
     if (int rc = join_gather(h, s)) return rc;
     h->counters.last_T = h->T;
@@ -1284,8 +1306,12 @@ int ub_reduce_scatter(ub_handle_t h, const void *const *P, void *const *Y_shards
     p.pdl = static_cast<int>(h->pdl);
     // Small CTAs, four per SM: alone, they keep enough loads in flight to stream HBM; beside
     // a persistent GEMM CTA one of them fits on each SM (the rest start as GEMM CTAs leave).
+    // Beside mode: one per SM, all of them running beside the kernel before it on `s`
+    // (a CTA that waits for that kernel at its exit would hold back any CTA queued behind).
+    p.beside = h->bulk_beside ? 1 : 0;
+    if (p.beside) p.pdl = 1;
     const int64_t vecs = p.T * (p.H / 8);
-    int64_t grid = 4 * static_cast<int64_t>(h->sm_count);
+    int64_t grid = (p.beside ? 1 : 4) * static_cast<int64_t>(h->sm_count);
     if (grid > (vecs + 255) / 256) grid = (vecs + 255) / 256;
     ProfileRing &ring = h->prof[UB_OP_REDUCE_SCATTER];
     const bool timed = h->profile != 0 && ring.count < kMaxProfiled;
@@ -1474,6 +1500,10 @@ int ub_set_option(ub_handle_t h, int key, int64_t val)
         if (val != 0 && val != 1) return fail(UB_ERR_ARG, "UB_OPT_PDL must be 0 or 1");
         h->pdl = val;
         return UB_OK;
+    case UB_OPT_BULK_BESIDE:
+        if (val != 0 && val != 1) return fail(UB_ERR_ARG, "UB_OPT_BULK_BESIDE must be 0 or 1");
+        h->bulk_beside = val;
+        return UB_OK;
     case UB_OPT_GATHER_KERNEL:
         if (val < -1 || val > 2) return fail(UB_ERR_ARG, "gather_kernel must be -1, 0, 1 or 2");
         h->gather_kernel = val;
@@ -1509,6 +1539,7 @@ int ub_get_option(ub_handle_t h, int key, int64_t *val)
     case UB_OPT_GATHER_KERNEL: *val = h->gather_kernel; return UB_OK;
     case UB_OPT_SKINNY: *val = h->skinny; return UB_OK;
     case UB_OPT_PDL: *val = h->pdl; return UB_OK;
+    case UB_OPT_BULK_BESIDE: *val = h->bulk_beside; return UB_OK;
     default: return fail(UB_ERR_ARG, "unknown option %d", key);
     }
 }

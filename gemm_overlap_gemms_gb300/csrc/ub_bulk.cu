@@ -21,12 +21,23 @@
 namespace ubk {
 namespace {
 
-// Programmatic dependent launch (see ub_device.cuh): let the next kernel launch, then
-// wait for the previous one before touching memory.
-__device__ __forceinline__ void pdl_enter()
+// Programmatic dependent launch (see ub_device.cuh). A plain launch waits for the grid
+// before it, then lets the next kernel launch. Beside mode (`beside`, the host launches
+// the kernel as a programmatic dependent of the GEMM issued just before it): no wait at
+// entry -- the kernel launches once every CTA of the GEMM holds its SM (the GEMM triggers
+// only after its own wait, so every grid before the GEMM is complete and the inputs are
+// in memory), runs in the room the GEMM's CTAs leave, and waits for the GEMM at exit, so
+// that it completes only after the GEMM and work behind it on the stream sees both.
+__device__ __forceinline__ void pdl_enter(int beside)
 {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (beside) return;
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_leave(int beside)
+{
+    if (beside) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 __device__ __forceinline__ uint4 ld_stream(const void *p)
@@ -57,7 +68,7 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi)
 template <int TP, int U>
 __global__ void __launch_bounds__(256) bulk_rs_kernel(const __grid_constant__ BulkRsParams p)
 {
-    pdl_enter();
+    pdl_enter(p.beside);
     const int64_t vecs_per_row = p.H / 8;
     const int64_t total = p.T * vecs_per_row;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -95,13 +106,14 @@ __global__ void __launch_bounds__(256) bulk_rs_kernel(const __grid_constant__ Bu
             *dst = make_uint4(pack2(a[0], a[1]), pack2(a[2], a[3]), pack2(a[4], a[5]), pack2(a[6], a[7]));
         }
     }
+    pdl_leave(p.beside);
 }
 
 // One CTA group per chunk, ring order: block b copies part (b % ctas_per_chunk) of chunk
 // self_rank + b / ctas_per_chunk (mod tp), the self chunk first.
 __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ GatherParams p)
 {
-    pdl_enter();
+    pdl_enter(p.beside);
     const int q = blockIdx.x / p.ctas_per_chunk;  // 0..tp-1
     const int part = blockIdx.x - q * p.ctas_per_chunk;
     const int r = (p.self_rank + q) % p.tp;
@@ -137,6 +149,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const __grid_constant__ Gat
                 asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p.flags + r), "r"(p.epoch) : "memory");
         }
     }
+    pdl_leave(p.beside);
 }
 
 }  // namespace

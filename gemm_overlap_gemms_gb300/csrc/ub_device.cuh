@@ -91,12 +91,14 @@ __device__ __forceinline__ void fence_proxy_async_shared()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Programmatic dependent launch. `pdl_trigger` lets the next kernel on the stream start
-// launching once every CTA of this grid has reached it (all of them resident, so the
-// next grid's CTAs can only take SMs that are free); `pdl_wait` blocks until the grid
-// before this one has completed and its memory is visible. Without the launch
-// attribute both are no-ops. Every kernel here runs its prologue (barriers, TMEM,
-// tensor-map prefetch), then triggers, then waits before touching global memory.
+// Programmatic dependent launch. `pdl_wait` blocks until the grid before this one has
+// completed and its memory is visible; `pdl_trigger` lets the next kernel on the stream
+// start launching once every CTA of this grid has reached it (all of them resident, so
+// the next grid's CTAs can only take SMs that are free). Without the launch attribute
+// both are no-ops. Every kernel here runs its prologue (barriers, TMEM, tensor-map
+// prefetch), waits, and only then triggers: a grid launched on the trigger finds every
+// earlier grid on the stream complete, which a bulk collective launched beside a GEMM
+// (ub_bulk.cu, no wait of its own at entry) relies on for its inputs.
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 

@@ -214,8 +214,8 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_kernel(const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    pdl_trigger();
     pdl_wait();
+    pdl_trigger();
 
     if (warp == 0 && lane == 0) {
         // ---------------------------------------------------------- producer
@@ -548,8 +548,8 @@ __global__ void __maxnreg__(PAIR_MAX_REGS) ub_gemm_pair_kernel(const __grid_cons
     cluster_sync_all();  // barriers of both CTAs initialised before any cross-CTA signal
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    pdl_trigger();
     pdl_wait();
+    pdl_trigger();
 
     if (warp == 0 && lane == 0) {
         // ---------------------------------------------------------- producer (both CTAs)

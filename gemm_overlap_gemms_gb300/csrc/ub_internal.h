@@ -178,6 +178,7 @@ struct BulkRsParams {
     int64_t H;                 // multiple of 8
     int64_t c;
     int pdl;                   // host: launch with programmatic stream serialization
+    int beside;                // launched beside the GEMM before it: no entry wait, wait at exit
 };
 cudaError_t launch_bulk_rs(const BulkRsParams &p, int grid, cudaStream_t stream);
 
@@ -196,6 +197,7 @@ struct GatherParams {
     int ctas_per_chunk;
     int64_t chunk_vecs;          // 16-byte vectors per chunk = c * H / 8
     int pdl;                     // host: launch with programmatic stream serialization
+    int beside;                  // launched beside the GEMM before it: no entry wait, wait at exit
 };
 cudaError_t launch_gather(const GatherParams &p, cudaStream_t stream);
 

@@ -185,8 +185,8 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_skinny_kernel(const __grid
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    pdl_trigger();
     pdl_wait();
+    pdl_trigger();
 
     if (warp == 0 && lane == 0) {
         // ---------------------------------------------------------- producer
@@ -564,8 +564,8 @@ __global__ void __launch_bounds__(64, 1) stream_read_kernel(const __grid_constan
         fence_mbar_init();
     }
     __syncthreads();
-    pdl_trigger();
     pdl_wait();
+    pdl_trigger();
     const WaitCtx w{p.abort_word, p.status, p.timeout_ns, p.epoch};
     const int64_t vecs = p.bytes / 16;
     const int64_t per = (vecs + gridDim.x - 1) / gridDim.x * 16;

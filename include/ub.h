@@ -107,9 +107,15 @@ enum {
                               roundup(T, 16)) are <= 256. -1 (default) = used up to 128 columns
                               unless UB_OPT_CTA_PAIR forces a tile kernel; 0 = never; 1 =
                               whenever usable */
-    UB_OPT_PDL = 11        /* 1 (default): kernels are launched with programmatic stream
+    UB_OPT_PDL = 11,       /* 1 (default): kernels are launched with programmatic stream
                               serialization, so a kernel's launch and prologue overlap the end
-                              of the kernel before it on the stream; 0: plain launches */
+                              of the kernel before it on the stream; 0: plain launches. Every
+                              kernel lets the next one launch only after its own wait for the
+                              grid before it, so a grid launched early finds every earlier
+                              grid on the stream complete */
+    UB_OPT_BULK_BESIDE = 12 /* 1: ub_allgather and ub_reduce_scatter run beside the kernel
+                              issued just before them on their stream (see ub_allgather);
+                              0 (default): they wait for the work before them, as any call */
 };
 
 /* Operation ids for ub_kernel_time. */
@@ -271,19 +277,37 @@ int ub_wgrad(ub_handle_t h, const void *D, int64_t M, int ub_is_a, void *out, vo
 
 /*
  * The "bulk" method of [P3] ("Overlap GEMM with an independent bulk all-gather or
- * reduce-scatter"): the collective alone, to run on one stream while an unrelated GEMM
- * runs on another (for example, gather a layer's input for its weight gradient while
- * its input-gradient GEMM runs, or reduce the input-gradient partials while the
- * weight-gradient GEMM runs).
+ * reduce-scatter"): the collective alone, to run beside an unrelated GEMM (for example,
+ * gather a layer's input for its weight gradient while its input-gradient GEMM runs, or
+ * reduce the input-gradient partials while the weight-gradient GEMM runs).
+ *
+ * Two ways to run it beside the GEMM:
+ *  - on a second stream (UB_OPT_BULK_BESIDE = 0). The GPU then decides which grid it
+ *    places first: the GEMM first, the collective's CTAs fill the room beside the GEMM's;
+ *    the collective first, its CTAs take the SMs and the two run one after the other.
+ *  - beside mode (UB_OPT_BULK_BESIDE = 1): call it on the GEMM's own stream directly
+ *    after the GEMM call. Its kernel is launched as a programmatic dependent of the GEMM:
+ *    it starts once every GEMM CTA holds its SM, runs one CTA per SM in the room they
+ *    leave, and completes only after the GEMM (it waits for it at exit), so work behind
+ *    it on the stream sees both results. It does not wait for the GEMM at entry: what it
+ *    reads must be complete before the GEMM starts, which holds for anything written
+ *    before the GEMM on the stream when that GEMM is a call of this library (its kernels
+ *    let the next grid launch only after their own wait). After a kernel of another
+ *    library, which may let the next grid launch before its own predecessors finish,
+ *    leave the option at 0. After a non-kernel operation (a copy, an event wait) the
+ *    collective simply runs after it. The collective must not write what the GEMM reads
+ *    (ub_allgather writes the user buffer: not beside an AG-GEMM of the same handle).
  *
  * ub_allgather: the all-gather of ag_gemm without the GEMM -- UB[r*c + i] = shards[r][i]
  * for the active shape, copies and readiness flags on the handle's side streams, joined
- * back into `stream`. A following ub_wgrad on `stream` reads the gathered rows.
+ * back into `stream` (beside mode: the gather kernel on `stream` itself). A following
+ * ub_wgrad on `stream` reads the gathered rows.
  *
  * ub_reduce_scatter: Y_shards[r][i][n] = bf16(sum_{j<tp} P[j][r*c + i][n]) for the
  * active shape (P: tp device pointers [T, hidden]; Y_shards: tp pointers [c, hidden]);
  * fp32 sum in j order, one small HBM-bound kernel on `stream` whose CTAs fit beside a
- * persistent GEMM CTA. Rows >= T of P and rows >= c of each Y_shards[r] are untouched.
+ * persistent GEMM CTA (four per SM; beside mode one). Rows >= T of P and rows >= c of
+ * each Y_shards[r] are untouched.
  * Errors: UB_ERR_ARG, UB_ERR_ALIGN (pointers not 16-byte aligned), UB_ERR_CUDA.
  */
 int ub_allgather(ub_handle_t h, const void *const *shards, void *stream);

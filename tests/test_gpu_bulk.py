@@ -1,5 +1,6 @@
 """The "bulk" method: an all-gather or reduce-scatter run on its own, alone and beside an
-unrelated GEMM on another stream, against the oracle."""
+unrelated GEMM (on another stream, or in beside mode on the GEMM's own stream), against
+the oracle."""
 import math
 
 import numpy as np
@@ -106,6 +107,126 @@ def test_bulk_collectives_beside_gemms_on_other_streams():
     Yref = oracle.reduce_scatter([_u16(x) for x in P])
     for r in range(tp):
         assert_close(Ys[r], Yref[r], "bulk RS block %d" % r)
+
+
+# ---------------------------------------------------------------- beside mode (UB_OPT_BULK_BESIDE)
+
+def test_bulk_collectives_in_beside_mode_on_the_gemms_stream():
+    """The same column-parallel backward with every call on one stream, each collective
+    launched beside the GEMM just before it: its inputs written just before that GEMM by
+    another kernel, its results and the GEMM's read right after it by another kernel on
+    the stream (ordering), all against the oracle."""
+    tp, H, F, T = 4, 2048, 1024, 2048
+    c = T // tp
+    d = dev()
+    g = synth.generator(d, seed=95)
+    X = synth.normal_bf16((T, H), 1.0, g, d)
+    dZ = [synth.normal_bf16((T, F), 1.0, g, d) for _ in range(tp)]
+    Wt = [synth.normal_bf16((F, H), 1.0 / math.sqrt(H), g, d) for _ in range(tp)]
+    P = [synth.normal_bf16((T, H), 1.0, g, d) for _ in range(tp)]
+    s1 = torch.cuda.Stream(d)
+    torch.cuda.synchronize()
+    with ub.UserBuffer([T, H], tp) as buf:
+        buf.set_active_shape([T, H])
+        buf.set_option("bulk_beside", 1)
+        assert buf.get_option("bulk_beside") == 1
+        with torch.cuda.stream(s1):
+            Xs = torch.empty_like(X)
+            Xs.copy_(X)                       # the gather's input, written just before the GEMM
+            Pn = [torch.empty_like(x) for x in P]
+            for j in range(tp):
+                torch.add(P[j], 0.0, out=Pn[j])   # the reduce-scatter's inputs, likewise
+        dX = buf.gemm_rs_kn(dZ, Wt, stream=s1)                                # GEMM ...
+        buf.allgather([Xs[r * c:(r + 1) * c] for r in range(tp)], stream=s1)  # ... beside it
+        dW = buf.wgrad(dZ[0], stream=s1)     # reads the gathered buffer: after the gather
+        Ys = buf.reduce_scatter(Pn, stream=s1)                              # beside the wgrad
+        with torch.cuda.stream(s1):
+            dW_after = dW.clone()             # read by the next kernel on the stream
+            Y_after = [y.clone() for y in Ys]
+            G_after = buf.buffer()[:T].clone()
+        torch.cuda.synchronize()
+        assert buf.query_status() == ub.UB_OK
+    rng = np.random.default_rng(4)
+    rows = np.unique(np.concatenate([[0, c - 1, c, T - 1], rng.integers(0, T, 16)]))
+    ridx = torch.as_tensor(rows, device=d)
+    S = sum(oracle.gemm_xw_rows(_u16(dZ[j]), _u16(Wt[j]), rows) for j in range(tp))
+    assert_close(torch.cat(dX)[ridx], S, "dgrad with the gather beside it")
+    np.testing.assert_array_equal(_u16(G_after), _u16(X))
+    ms = np.array([0, 5, F // 2, F - 1])
+    ref = oracle.gemm_tn(np.ascontiguousarray(_u16(dZ[0])[:, ms]), _u16(X))
+    assert_close(dW_after[torch.as_tensor(ms, device=d)], ref, "wgrad with the reduce-scatter beside it")
+    Yref = oracle.reduce_scatter([_u16(x) for x in P])
+    for r in range(tp):
+        assert_close(Y_after[r], Yref[r], "beside RS block %d" % r)
+
+
+def test_beside_mode_integer_inputs_exact_alone_and_after_a_gemm():
+    """Beside mode with nothing before it on a fresh stream (runs as a plain launch) and
+    directly after a GEMM: bit-exact sums of small integers, and every row past c of the
+    output blocks untouched."""
+    tp, c, H, M = 4, 96, 512, 256
+    T = c * tp
+    g = synth.generator(seed=96)
+    P = [synth.small_int_bf16((T, H), -20, 20, g).to(dev()) for _ in range(tp)]
+    D = synth.normal_bf16((T, M), 1.0, g).to(dev())
+    Yref = oracle.reduce_scatter([_u16(x) for x in P])
+    with ub.UserBuffer([T, H], tp) as buf:
+        buf.set_active_shape([T, H])
+        buf.buffer().zero_()
+        buf.set_option("bulk_beside", 1)
+        for after_gemm in (False, True):
+            st = torch.cuda.Stream()
+            pad = 3
+            big = sentinel((tp * (c + pad), H))
+            Ys = [big[r * (c + pad): r * (c + pad) + c] for r in range(tp)]
+            torch.cuda.synchronize()
+            if after_gemm:
+                buf.wgrad(D, stream=st)
+            buf.reduce_scatter(P, Ys, stream=st)
+            torch.cuda.synchronize()
+            assert buf.query_status() == ub.UB_OK
+            for r in range(tp):
+                np.testing.assert_array_equal(Ys[r].float().cpu().numpy(), Yref[r])
+                assert is_sentinel(big[r * (c + pad) + c:(r + 1) * (c + pad)])
+
+
+def test_beside_mode_replays_from_a_cuda_graph():
+    """A weight-gradient GEMM with the reduce-scatter beside it, captured once and
+    replayed: the programmatic edge holds in the graph, and each replay gives the
+    oracle's values for new inputs copied in before it."""
+    tp, c, H, M = 4, 256, 1024, 512
+    T = c * tp
+    g = synth.generator(dev(), seed=97)
+    D = synth.normal_bf16((T, M), 1.0, g, dev())
+    X = synth.normal_bf16((T, H), 1.0, g, dev())
+    P = [torch.empty((T, H), dtype=torch.bfloat16, device=dev()) for _ in range(tp)]
+    dW = torch.empty((M, H), dtype=torch.bfloat16, device=dev())
+    with ub.UserBuffer([T, H], tp) as buf:
+        buf.set_active_shape([T, H])
+        buf.allgather([X[r * c:(r + 1) * c] for r in range(tp)])
+        buf.set_option("bulk_beside", 1)
+        st = torch.cuda.Stream()
+        Ys = [torch.empty((c, H), dtype=torch.bfloat16, device=dev()) for _ in range(tp)]
+        for x in P:
+            x.zero_()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=st):
+            buf.wgrad(D, out=dW, stream=st)
+            buf.reduce_scatter(P, Ys, stream=st)
+        for rep in range(2):
+            src = [synth.normal_bf16((T, H), 1.0, synth.generator(seed=200 + 10 * rep + j)) for j in range(tp)]
+            for x, y in zip(P, src):
+                x.copy_(y)
+            graph.replay()
+            torch.cuda.synchronize()
+            assert buf.query_status() == ub.UB_OK
+            Yref = oracle.reduce_scatter([_u16(x) for x in src])
+            for r in range(tp):
+                assert_close(Ys[r], Yref[r], "graph replay %d block %d" % (rep, r))
+        ms = np.array([0, 7, M - 1])
+        ref = oracle.gemm_tn(np.ascontiguousarray(_u16(D)[:, ms]), _u16(X))
+        assert_close(dW[torch.as_tensor(ms, device=dev())], ref, "wgrad in the graph")
 
 
 # ---------------------------------------------------------------- gather ahead, GEMM from the buffer
