@@ -546,7 +546,7 @@ def default_sweep(stream):
             "seconds": time.perf_counter() - t_start}
 
 
-def e2e_measure(wl, steps, warmup, stream, world):
+def e2e_measure(wl, steps, warmup, stream, world, reps=3):
     """Same step, with each microbatch's activations copied in from pinned host memory
     and its outputs copied back, inside the timed region. Copies run on their own
     streams so that microbatch i+1's inputs and microbatch i-1's outputs move while
@@ -554,7 +554,10 @@ def e2e_measure(wl, steps, warmup, stream, world):
     input copy waits only until the previous step has computed that microbatch, so the
     host link streams without a break from one timed step to the next, as a training
     loop's prefetch would; no copy of the timed steps starts before the timer's start
-    event, and the timer stops after the last output has landed in host memory."""
+    event, and the timer stops after the last output has landed in host memory. The
+    timed region runs `reps` times (ms of each returned): the host link and the host
+    thread that issues the copies see other work on the machine, so one region can be
+    slow for reasons outside the step."""
     fused = MLP == "fused"
     a0 = 1 if fused else 0      # fused: A[i][0] is produced on the device by fc1
     hX = [x.cpu().pin_memory() for x in wl.X]
@@ -607,20 +610,23 @@ def e2e_measure(wl, steps, warmup, stream, world):
         s_in.wait_stream(stream)
         step()
         stream.wait_stream(s_out)
-    torch.cuda.synchronize()
-    barrier(world)
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    s_in.wait_event(e0)            # nothing of the timed steps starts before the timer
-    for _ in range(steps):
-        step()
-    stream.wait_stream(s_out)      # the last outputs are in host memory
-    e1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    return e0.elapsed_time(e1), h2d, d2h
+    times = []
+    for _ in range(reps):
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        s_in.wait_event(e0)            # nothing of the timed steps starts before the timer
+        for _ in range(steps):
+            step()
+        stream.wait_stream(s_out)      # the last outputs are in host memory
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        times.append(e0.elapsed_time(e1))
+    return times, h2d, d2h
 
 
 def padded_measure(wl, steps, warmup, stream, world):
@@ -667,7 +673,8 @@ def bulk_measure(wl, stream, T=4096, reps=20):
     [T, hidden]. `overlapped_ms`: beside mode (UB_OPT_BULK_BESIDE: the collective on the
     GEMM's stream right after it, launched once the GEMM's CTAs hold their SMs);
     `two_streams_overlapped_ms`: the collective on a second stream, the GEMM issued
-    first. Times are ms per pair of operations, each the median of three timings."""
+    first. Times are ms per pair of operations (20 back to back per timing), each the
+    median of three timings interleaved with the others'."""
     w = wl.w
     H, F, tp = w.hidden, w.rs_k[0], w.tp
     dev = wl.W1.device
@@ -689,9 +696,7 @@ def bulk_measure(wl, stream, T=4096, reps=20):
     buf.allgather(shards, stream=stream)      # the buffer holds X for the wgrad runs
 
     def timed(fn):
-        # median of three timings of `reps` back-to-back runs: single timings of a pair
-        # of kernels on two streams vary by several us from run to run
-        return float(np.median([time_steps(fn, reps, 2, stream, 1) / reps for _ in range(3)]))
+        return time_steps(fn, reps, 2, stream, 1) / reps
 
     def both(gemm, coll):
         def fn():
@@ -714,6 +719,13 @@ def bulk_measure(wl, stream, T=4096, reps=20):
         finally:
             buf.set_option("bulk_beside", 0)
 
+    def medians(*fns):
+        # the timings interleaved, three rounds, the median of each: single timings of a
+        # pair of kernels vary by several us, and a GEMM's time drifts with the clocks
+        # over a run, which would bias whichever timing came first
+        rounds = [[f() for f in fns] for _ in range(3)]
+        return [float(np.median([r[i] for r in rounds])) for i in range(len(fns))]
+
     dgrad = lambda: buf.gemm_rs_kn(dZ, Wt, outs, stream=stream)
     ag_side = lambda: buf.allgather(shards, stream=side)
     ag_alone = lambda: buf.allgather(shards, stream=stream)
@@ -724,10 +736,9 @@ def bulk_measure(wl, stream, T=4096, reps=20):
     for name, gemm, coll_side, coll_alone, coll_bytes in (
             ("allgather_beside_dgrad", dgrad, ag_side, ag_alone, 2 * T * H * 2),
             ("reduce_scatter_beside_wgrad", wgrad, rs_side, rs_alone, (tp + 1) * T * H * 2)):
-        t_g = timed(gemm)
-        t_c = timed(coll_alone)
-        t_b = timed_beside(beside(gemm, coll_alone))
-        t_2 = timed(both(gemm, coll_side))
+        t_g, t_c, t_b, t_2 = medians(lambda: timed(gemm), lambda: timed(coll_alone),
+                                     lambda: timed_beside(beside(gemm, coll_alone)),
+                                     lambda: timed(both(gemm, coll_side)))
         hidden = lambda t: (t_g + t_c - t) / t_c if t_c > 0 else None
         res[name] = {"gemm_ms": t_g, "collective_ms": t_c, "sequential_ms": t_g + t_c,
                      "overlapped_ms": t_b, "hidden_fraction": hidden(t_b),
@@ -830,11 +841,14 @@ def run_ours(args):
     e2e = None
     if not args.no_e2e:
         e_steps = max(2, min(args.steps, 10))
-        e_ms, h2d, d2h = e2e_measure(wl, e_steps, 1, stream, world)
-        e_ms = max_over_ranks(e_ms, world)
+        e_all, h2d, d2h = e2e_measure(wl, e_steps, max(3, args.warmup), stream, world)
+        e_all = [max_over_ranks(t, world) for t in e_all]
+        e_ms = float(np.median(e_all))
         e2e = {"value": flops * e_steps * world / (e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": e_ms / e_steps}
+               "ms_per_step": e_ms / e_steps,
+               "timed_regions": "median of %d regions of %d steps each: %s ms per step" % (
+                   len(e_all), e_steps, ", ".join("%.2f" % (t / e_steps) for t in e_all))}
 
     padded = None
     if not args.no_padded:

@@ -8,12 +8,20 @@
 // The work is HBM-bound: (tp + 1) * T * hidden * 2 bytes for tp * T * hidden adds. Each
 // thread owns 8 consecutive columns of one row (16-byte loads and stores, coalesced
 // across the warp); a grid-stride loop covers the active rows only. The CTAs are small
-// (256 threads, no shared memory), four per SM, so that together they keep enough loads
-// in flight to stream HBM, and one fits on an SM beside a persistent GEMM CTA. Beside a
-// GEMM that streams its operands at full rate, the reduce-scatter's loads queue behind
-// the GEMM's (measured on GB300 beside the weight-gradient GEMM: a third of its speed
-// alone at best, and in some runs no overlap at all), which limits how much of it the
-// bulk overlap hides.
+// (256 threads, no shared memory, under 88 registers a thread), four per SM alone, so
+// that together they keep enough loads in flight to stream HBM. One fits on an SM beside
+// a persistent GEMM CTA of the pair kernel: that CTA leaves about 1 KB of the SM's shared
+// memory, and in each of the SM's four register files room for two more warps of at
+// most 88 registers (a reduce-scatter of more loads in flight per thread, 98 registers
+// and up, ran only after the GEMM).
+//
+// Beside a GEMM on a second stream, which grid the GPU places first decides the overlap
+// (GB300, beside the weight-gradient GEMM: per run either about a third hidden or none,
+// the collective's four CTAs per SM then keeping the GEMM's out). Beside mode (`beside`)
+// removes the choice: the host launches the kernel on the GEMM's stream as its
+// programmatic dependent, one CTA per SM, so it starts only once every GEMM CTA holds
+// its SM. What it then hides is bounded by HBM: its 168 MB (T = 4096, tp 4, hidden 4096)
+// beside the GEMM's own traffic slow the GEMM by some microseconds.
 #include <cuda_bf16.h>
 
 #include "ub_internal.h"
