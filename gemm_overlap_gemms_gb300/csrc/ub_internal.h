@@ -101,7 +101,8 @@ struct GemmParams {
     int tail_split;              // the remaining tiles are cut into this many k-pieces
     int group_m;                 // > 1: tiles walked in groups of this many 256-row tile rows,
                                  // rows fastest inside a group (RS whose weight panels
-                                 // together exceed L2); else N fastest
+                                 // together exceed L2; AG with chunks of >= 2 tile rows);
+                                 // else N fastest
     int ldy;                     // RS: leading dimension of Y_shards (= hidden)
     void *y_ptr[UB_MAX_TP];      // RS: Y_shards[r], for stores that cross a chunk end
     int glu_f;                   // MODE_AG_GLU: F, the width of each half (gate, up) of Wt
