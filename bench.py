@@ -50,9 +50,9 @@ KERNEL_SRC = [os.path.join(ROOT, "gemm_overlap_gemms_gb300", "csrc", f) for f in
 # per active token of the captured launch, and the kernel source they were taken on.
 # Traffic is reported as null once the kernel source no longer matches.
 NCU_TRAFFIC = {
-    "rs": {"sha256_16": "9781cd3deec9d0d3", "bytes": 1154.16e6, "T": 8192,
+    "rs": {"sha256_16": "3c6d7d174032b015", "bytes": 1154.37e6, "T": 8192,
            "source": "profiles/ub_gemm_pair_kernel_rs_swiglu_fc2_T8192.md"},
-    "ag_swiglu": {"sha256_16": "9781cd3deec9d0d3", "bytes": 653.89e6, "T": 8192,
+    "ag_swiglu": {"sha256_16": "3c6d7d174032b015", "bytes": 482.46e6, "T": 8192,
                   "source": "profiles/ub_gemm_pair_kernel_ag_glu_swiglu_fc1_T8192.md"},
 }
 
@@ -423,11 +423,14 @@ def roofline_point(flops, nbytes, sec, tensor_peak, hbm_peak):
             "frac_of_roofline": tf / attainable}
 
 
-def time_graph_flushed(fn, stream, flush, calls, warmup):
+def time_graph_flushed(fn, stream, flush, calls, warmup, clean=False):
     """Median and minimum time of one call, `fn(st)` issuing it on stream `st`: the call is
     captured once into a CUDA graph and replayed `calls` times on `stream`, each replay
     between CUDA events and preceded by a write of `flush` (larger than L2) outside the
-    events, after `warmup` replays."""
+    events, after `warmup` replays. The write leaves L2 full of dirty lines, which the
+    call then writes back to HBM as it evicts them; with `clean`, `flush` is also read
+    back after the write (outside the events), so that the call starts from a cold L2 of
+    clean lines, as after a kernel that read rather than wrote."""
     fn(stream)
     torch.cuda.synchronize()
     cap = torch.cuda.Stream()
@@ -438,8 +441,11 @@ def time_graph_flushed(fn, stream, flush, calls, warmup):
     with torch.cuda.stream(stream):
         for _ in range(warmup):
             g.replay()
+        sink = torch.empty((), dtype=flush.dtype, device=flush.device)
         for a, b in ev:
             flush.zero_()
+            if clean:
+                torch.sum(flush, dim=0, out=sink)
             a.record(stream)
             g.replay()
             b.record(stream)
@@ -452,13 +458,13 @@ def time_graph_flushed(fn, stream, flush, calls, warmup):
 READ_FLOOR_MAX_T = 512  # few-token points: the weight read is the work
 
 
-def read_floor(buf, weights, stream, flush):
+def read_floor(buf, weights, stream, flush, clean=False):
     """Median time of one plain read of the weight bytes (`ub_stream_read`: one kernel,
     one CTA per SM, bulk copies into shared memory, nothing computed), timed exactly as a
     sweep call is (graph replay, L2 flushed before each): what reading the same bytes in
     one isolated kernel costs on this GPU, launch and ramp included."""
     med, _ = time_graph_flushed(lambda st: buf.stream_read(weights, stream=st), stream, flush,
-                                DEFAULT_SWEEP_CALLS, DEFAULT_SWEEP_WARMUP)
+                                DEFAULT_SWEEP_CALLS, DEFAULT_SWEEP_WARMUP, clean)
     return med
 
 
@@ -526,8 +532,17 @@ def default_sweep(stream):
                 if T <= READ_FLOOR_MAX_T:
                     if floor is None:
                         floor = read_floor(buf, weights, stream, flush)
+                        floor_clean = read_floor(buf, weights, stream, flush, clean=True)
                     pt["read_floor_us"] = floor * 1e3
                     pt["frac_of_read_floor"] = floor / med
+                    # the same call and floor after a flush that leaves L2 clean (written,
+                    # then read back): a few-token call writes back the flush's dirty lines
+                    # as it streams its weights, which a call after a read-only kernel
+                    # would not
+                    med_c, _ = time_graph_flushed(fn, stream, flush, DEFAULT_SWEEP_CALLS, DEFAULT_SWEEP_WARMUP,
+                                                  clean=True)
+                    pt["clean_l2"] = {"us": med_c * 1e3, "hbm_frac": nbytes / (med_c / 1e3) / 1e9 / hbm_peak,
+                                      "read_floor_us": floor_clean * 1e3, "frac_of_read_floor": floor_clean / med_c}
                 points.append(pt)
             if op == "rs":
                 del A, Bt, B_all, weights
@@ -538,8 +553,10 @@ def default_sweep(stream):
         del X, Yrs
     del flush
     return {"points": points, "timing": "median of %d CUDA-graph replays of one whole call, L2 flushed (%d MiB "
-                                        "written) before each, after %d warm-up replays"
-                                        % (DEFAULT_SWEEP_CALLS, L2_FLUSH_BYTES >> 20, DEFAULT_SWEEP_WARMUP),
+                                        "written) before each, after %d warm-up replays; `clean_l2` (T <= %d): "
+                                        "the same with the flush buffer read back after the write, so that L2 "
+                                        "holds clean lines" % (DEFAULT_SWEEP_CALLS, L2_FLUSH_BYTES >> 20,
+                                                               DEFAULT_SWEEP_WARMUP, READ_FLOOR_MAX_T),
             "peaks": {"bf16_tflops": tensor_peak, "hbm_gbs": hbm_peak,
                       "source": "%s burst bf16 and HBM copy (%s)" % (src, "MEASURED_PEAKS.json" if src == "measured"
                                                                       else "recipe fallback")},
