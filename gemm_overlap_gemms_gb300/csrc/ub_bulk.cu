@@ -35,11 +35,13 @@ namespace {
 // entry -- the kernel launches once every CTA of the GEMM holds its SM (the GEMM triggers
 // only after its own wait, so every grid before the GEMM is complete and the inputs are
 // in memory), runs in the room the GEMM's CTAs leave, and waits for the GEMM at exit, so
-// that it completes only after the GEMM and work behind it on the stream sees both.
+// that it completes only after the GEMM and work behind it on the stream sees both. It
+// lets the next kernel launch at once: that kernel's CTAs take SMs as the GEMM's leave
+// and wait for this one (so for the GEMM too) before touching memory, so its launch and
+// prologue overlap the GEMM's end instead of following this kernel's exit.
 __device__ __forceinline__ void pdl_enter(int beside)
 {
-    if (beside) return;
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (!beside) asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 

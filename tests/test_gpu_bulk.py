@@ -256,11 +256,12 @@ def test_ag_gemm_from_buffer_after_allgather(T, swiglu):
     assert is_sentinel(Y[T:]), "rows past T touched"
 
 
-def test_gather_ahead_pipeline_matches_the_oracle():
-    """Three microbatches of different T: each all-gather on a second stream once the
-    previous fc1 has read the buffer, beside the previous GEMM-RS; fc1 (AG + SwiGLU) on
-    the gathered buffer, fc2 GEMM-RS on the main stream. Every output against the oracle
-    on sampled rows."""
+@pytest.mark.parametrize("beside", [False, True])
+def test_gather_ahead_pipeline_matches_the_oracle(beside):
+    """Three microbatches of different T: each all-gather beside the previous GEMM-RS --
+    on a second stream once the previous fc1 has read the buffer, or (beside mode) on the
+    main stream right after the GEMM-RS; fc1 (AG + SwiGLU) on the gathered buffer, fc2
+    GEMM-RS on the main stream. Every output against the oracle on sampled rows."""
     tp, H, F, K = 4, 1024, 256, 512
     Ts = [4 * 260, 4 * 96, 4 * 400]
     g = synth.generator(dev(), seed=142)
@@ -287,7 +288,7 @@ def test_gather_ahead_pipeline_matches_the_oracle():
                 main.wait_event(ev_landed[i])
             buf.ag_gemm_from_buffer(W1, Z[i], swiglu=True, stream=main)
             ev_read[i].record(main)
-            if i + 1 < len(Ts):
+            if i + 1 < len(Ts) and not beside:
                 buf.set_active_shape([Ts[i + 1], H])
                 side.wait_event(ev_read[i])
                 buf.allgather(shards(i + 1), stream=side)
@@ -295,6 +296,12 @@ def test_gather_ahead_pipeline_matches_the_oracle():
                 buf.set_active_shape([T, H])
             c = T // tp
             buf.gemm_rs(A[i], Bt, [R[i][r * c:(r + 1) * c] for r in range(tp)], stream=main)
+            if i + 1 < len(Ts) and beside:
+                buf.set_active_shape([Ts[i + 1], H])
+                buf.set_option("bulk_beside", 1)
+                buf.allgather(shards(i + 1), stream=main)   # beside the GEMM-RS just issued
+                buf.set_option("bulk_beside", 0)
+                ev_landed[i + 1].record(main)
         torch.cuda.synchronize()
         assert buf.query_status() == ub.UB_OK
     for i, T in enumerate(Ts):
