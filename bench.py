@@ -843,23 +843,37 @@ def run_ours(args):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    clocks.start()
-    # The headline: K steps with nothing on the stream but the step's own work.
-    ms = time_steps(step, args.steps, 0, stream, world)
-    # The per-kernel durations for the roofline: K more steps, now with a CUDA event
+    # The headline: K steps with nothing on the stream but the step's own work. The
+    # per-kernel durations for the roofline come from K more steps with a CUDA event
     # recorded on the stream before and after every GEMM launch (UB_OPT_PROFILE). An event
     # between two kernels removes their programmatic launch (the second kernel's launch
     # and prologue no longer overlap the end of the first; ~1.5 % of the step on GB300),
-    # so the events stay out of the headline region.
-    wl.buf.set_option("profile", 1)
-    wl.buf.kernel_time(ag_op)
-    wl.buf.kernel_time("rs")
-    ms_events = time_steps(step, args.steps, 0, stream, world)
+    # so the events stay out of the headline region; they run in two halves, just before
+    # and just after it, so that their kernels see the GPU's clocks and power state on
+    # both sides of the headline (under the power cap, the clocks drift over a run).
+    k_before = args.steps // 2
+    k_after = args.steps - k_before
+    ag_ms = rs_ms = ms_events = 0.0
+    ag_n = rs_n = 0
+    clocks.start()
+
+    def events_region(k):
+        nonlocal ag_ms, rs_ms, ms_events, ag_n, rs_n
+        if k == 0:
+            return
+        wl.buf.set_option("profile", 1)
+        wl.buf.kernel_time(ag_op)
+        wl.buf.kernel_time("rs")
+        ms_events += max_over_ranks(time_steps(step, k, 0, stream, world), world)
+        a, an = wl.buf.kernel_time(ag_op)
+        r, rn = wl.buf.kernel_time("rs")
+        ag_ms, ag_n, rs_ms, rs_n = ag_ms + a, ag_n + an, rs_ms + r, rs_n + rn
+        wl.buf.set_option("profile", 0)
+
+    events_region(k_before)
+    ms = time_steps(step, args.steps, 0, stream, world)
+    events_region(k_after)
     clk = clocks.stop()
-    ag_ms, ag_n = wl.buf.kernel_time(ag_op)
-    rs_ms, rs_n = wl.buf.kernel_time("rs")
-    wl.buf.set_option("profile", 0)
-    ms_events = max_over_ranks(ms_events, world)
     assert wl.buf.query_status() == ub.UB_OK, "device status %d" % wl.buf.query_status()
     ms = max_over_ranks(ms, world)
     total_flops = flops * args.steps * world
@@ -872,9 +886,9 @@ def run_ours(args):
                "tflops": (ag_flops * args.steps) / (ag_ms / 1e3) / 1e12 if ag_ms > 0 else None},
         "rs": {"launches": rs_n, "avg_us": 1e3 * rs_ms / max(rs_n, 1),
                "tflops": (rs_flops * args.steps) / (rs_ms / 1e3) / 1e12 if rs_ms > 0 else None},
-        "timed_region": "a second region of the same %d steps right after the headline's, with a CUDA "
+        "timed_region": "%d + %d steps just before and just after the headline's %d, with a CUDA "
                         "event before and after every GEMM launch on its stream: %.3f ms per step there"
-                        % (args.steps, ms_events / args.steps),
+                        % (k_before, k_after, args.steps, ms_events / args.steps),
     }
     dom = "rs" if rs_ms >= ag_ms else "ag"
     achieved = kernels[dom]["tflops"]
