@@ -173,6 +173,10 @@ def test_beside_mode_integer_inputs_exact_alone_and_after_a_gemm():
     with ub.UserBuffer([T, H], tp) as buf:
         buf.set_active_shape([T, H])
         buf.buffer().zero_()
+        assert buf.get_option("bulk_beside") == 0           # off by default
+        with pytest.raises(ub.UbError) as ei:
+            buf.set_option("bulk_beside", 2)
+        assert ei.value.name == "UB_ERR_ARG"
         buf.set_option("bulk_beside", 1)
         for after_gemm in (False, True):
             st = torch.cuda.Stream()
