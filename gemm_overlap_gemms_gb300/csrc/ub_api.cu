@@ -143,6 +143,7 @@ struct ub_handle {
     int64_t copy_streams = 1;  // raised to min(tp, 4) at creation
     int64_t gather_kernel = -1; // 0: driver copies; 1: one kernel launch; 2: inside the GEMM; -1: by T
     bool gather_by_kernel = false;  // what the last issue_gather chose (join_gather follows it)
+    bool gather_chained = false;    // ... and whether its kernel went on the call's own stream
     cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
     uint32_t epoch = 0;
     // options
@@ -156,6 +157,7 @@ struct ub_handle {
     int64_t skinny = -1;    // -1 = whenever the few-token kernel is usable
     int64_t pdl = 1;        // programmatic dependent launch of every kernel
     int64_t bulk_beside = 0; // 1: ub_allgather / ub_reduce_scatter beside the kernel before them
+    int64_t gather_chain = 1; // 1: the gather kernel on the call's stream, the GEMM its dependent
     int pair_clusters[3] = {-1, -1, -1};  // resident clusters of the pair kernel, per mode
     ub_counters_t counters{};
     std::vector<CacheEntry> cache;
@@ -605,10 +607,22 @@ int issue_gather(ub_handle *h, const void *const *shards, cudaStream_t s, uint32
         }
         return UB_OK;
     }
+    h->gather_chained = false;
     if (h->gather_by_kernel) {
-        // One launch on the side stream: small CTAs (they fit beside the GEMM's), about
-        // one per SM per chunk, each chunk's flag published by its last CTA.
+        // One launch: small CTAs (they fit beside the GEMM's), about one per SM per chunk,
+        // each chunk's flag published by its last CTA.
         ubk::GatherParams g = gather_kernel_params(h, shards, epoch, drop);
+        if (h->gather_chain && h->pdl) {
+            // On the call's own stream: the kernel waits for the work before it, then lets
+            // the next launch, so a GEMM launched next as its programmatic dependent starts
+            // once every gather CTA holds its SM (the flags it waits on are then certain to
+            // come) and finds every grid before the gather complete.
+            cudaError_t e = ubk::launch_gather(g, s);
+            if (e != cudaSuccess) return cuda_fail(e, "gather kernel launch");
+            h->gather_chained = true;
+            return UB_OK;
+        }
+        // On the side stream, forked from and joined back into the call's stream.
         UB_CUDA(cudaEventRecord(h->ev_fork, s));
         UB_CUDA(cudaStreamWaitEvent(h->side, h->ev_fork, 0));
         cudaError_t e = ubk::launch_gather(g, h->side);
@@ -642,6 +656,7 @@ int issue_gather(ub_handle *h, const void *const *shards, cudaStream_t s, uint32
 int join_gather(ub_handle *h, cudaStream_t s)
 {
     if (h->copy_streams == 0 && !h->gather_by_kernel) return UB_OK;  // in-stream: nothing to join
+    if (h->gather_chained) return UB_OK;  // the gather kernel ran on the call's stream
     const int ncs = h->gather_by_kernel ? 1 : static_cast<int>(h->copy_streams < h->tp ? h->copy_streams : h->tp);
     UB_CUDA(cudaEventRecord(h->ev_join, h->side));
     UB_CUDA(cudaStreamWaitEvent(s, h->ev_join, 0));
@@ -1073,10 +1088,15 @@ static int ag_gemm_impl(ub_handle_t h, const void *const *shards, const void *Wt
         p.g_chunk_vecs = c * H / 8;
         p.g_self_head_vecs = p.self_head * H / 8;
         p.g_drop = static_cast<int>(drop);
+        p.after_gather = 0;
         int rc = launch(h, p, mode, skinny ? PATH_SKINNY : pair ? PATH_PAIR : PATH_SINGLE, s, prof_op);
         if (rc != UB_OK) return rc;
     } else {
         if (int rc = issue_gather(h, shards, s, epoch, drop, p.self_head, fits_one_wave)) return rc;
+        // chained: the GEMM is the gather kernel's programmatic dependent (no wait at entry:
+        // the chunk flags order its reads of the buffer; one thread waits for the gather at
+        // exit, so that the call completes only after both)
+        p.after_gather = h->gather_chained ? 1 : 0;
         int rc = launch(h, p, mode, skinny ? PATH_SKINNY : pair ? PATH_PAIR : PATH_SINGLE, s, prof_op);
         // Join the copy streams back into `s` even if the launch failed.
         if (int jrc = join_gather(h, s)) return jrc;
@@ -1524,6 +1544,10 @@ int ub_set_option(ub_handle_t h, int key, int64_t val)
         if (val != 0 && val != 1) return fail(UB_ERR_ARG, "UB_OPT_BULK_BESIDE must be 0 or 1");
         h->bulk_beside = val;
         return UB_OK;
+    case UB_OPT_GATHER_CHAIN:
+        if (val != 0 && val != 1) return fail(UB_ERR_ARG, "UB_OPT_GATHER_CHAIN must be 0 or 1");
+        h->gather_chain = val;
+        return UB_OK;
     case UB_OPT_GATHER_KERNEL:
         if (val < -1 || val > 2) return fail(UB_ERR_ARG, "gather_kernel must be -1, 0, 1 or 2");
         h->gather_kernel = val;
@@ -1560,6 +1584,7 @@ int ub_get_option(ub_handle_t h, int key, int64_t *val)
     case UB_OPT_SKINNY: *val = h->skinny; return UB_OK;
     case UB_OPT_PDL: *val = h->pdl; return UB_OK;
     case UB_OPT_BULK_BESIDE: *val = h->bulk_beside; return UB_OK;
+    case UB_OPT_GATHER_CHAIN: *val = h->gather_chain; return UB_OK;
     default: return fail(UB_ERR_ARG, "unknown option %d", key);
     }
 }

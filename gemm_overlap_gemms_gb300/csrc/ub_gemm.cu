@@ -214,7 +214,7 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_kernel(const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    pdl_wait();
+    if (!p.after_gather) pdl_wait();
     pdl_trigger();
 
     if (warp == 0 && lane == 0) {
@@ -416,6 +416,7 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_kernel(const __grid_consta
         tc_fence_after();
         tmem_dealloc(tmem_base, TMEM_COLS);
     }
+    if (p.after_gather && threadIdx.x == 0) pdl_wait();  // complete only after the gather
 }
 
 
@@ -548,7 +549,7 @@ __global__ void __maxnreg__(PAIR_MAX_REGS) ub_gemm_pair_kernel(const __grid_cons
     cluster_sync_all();  // barriers of both CTAs initialised before any cross-CTA signal
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    pdl_wait();
+    if (!p.after_gather) pdl_wait();
     pdl_trigger();
 
     if (warp == 0 && lane == 0) {
@@ -915,6 +916,7 @@ __global__ void __maxnreg__(PAIR_MAX_REGS) ub_gemm_pair_kernel(const __grid_cons
         tc_fence_after();
         tmem_dealloc_pair(tmem_base, TMEM_COLS);
     }
+    if (p.after_gather && threadIdx.x == 0) pdl_wait();  // complete only after the gather
 }
 
 }  // namespace

@@ -134,6 +134,9 @@ struct GemmParams {
     int sk_stages;               // shared-memory pipeline depth (<= SK_MAX_STAGES)
     int sk_units;                // n_tiles * sk_split
     int pdl;                     // host: launch with programmatic stream serialization
+    int after_gather;            // AG launched as the programmatic dependent of its gather kernel:
+                                 // no wait at entry (the chunk flags order the buffer reads), one
+                                 // thread waits for the gather at exit
 };
 
 // Launch the persistent GEMM (mode MODE_AG, MODE_AG_GLU or MODE_RS) with `grid` CTAs on

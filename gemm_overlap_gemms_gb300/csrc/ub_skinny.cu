@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_skinny_kernel(const __grid
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    pdl_wait();
+    if (!p.after_gather) pdl_wait();
     pdl_trigger();
 
     if (warp == 0 && lane == 0) {
@@ -539,6 +539,7 @@ __global__ void __launch_bounds__(THREADS, 1) ub_gemm_skinny_kernel(const __grid
         tc_fence_after();
         tmem_dealloc(tmem_base, tmem_cols);
     }
+    if (p.after_gather && threadIdx.x == 0) pdl_wait();  // complete only after the gather
 }
 
 // Calibration read: each CTA streams one contiguous share of the bytes through a ring of

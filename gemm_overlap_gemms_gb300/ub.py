@@ -29,7 +29,7 @@ ERRORS = {
 CODES = {v: k for k, v in ERRORS.items()}
 OPTIONS = {"sm_margin": 1, "timeout_ns": 2, "self_rank": 3, "drop_flag": 4, "profile": 5,
            "cta_pair": 6, "streamk": 7, "copy_streams": 8, "gather_kernel": 9, "skinny": 10, "pdl": 11,
-           "bulk_beside": 12}
+           "bulk_beside": 12, "gather_chain": 13}
 OPS = {"ag": 0, "rs": 1, "ag_swiglu": 2, "ag_kn": 3, "rs_kn": 4, "wgrad": 5, "reduce_scatter": 6}
 MAX_TP = 8
 EXPORTS = [

@@ -113,9 +113,16 @@ enum {
                               kernel lets the next one launch only after its own wait for the
                               grid before it, so a grid launched early finds every earlier
                               grid on the stream complete */
-    UB_OPT_BULK_BESIDE = 12 /* 1: ub_allgather and ub_reduce_scatter run beside the kernel
+    UB_OPT_BULK_BESIDE = 12, /* 1: ub_allgather and ub_reduce_scatter run beside the kernel
                               issued just before them on their stream (see ub_allgather);
                               0 (default): they wait for the work before them, as any call */
+    UB_OPT_GATHER_CHAIN = 13 /* when an AG call's gather is the one-launch gather kernel:
+                              1 (default, with UB_OPT_PDL = 1): the kernel runs on the call's
+                              stream and the GEMM is launched as its programmatic dependent,
+                              starting once every gather CTA holds its SM (the chunk flags the
+                              GEMM waits on are then certain to come) and completing only
+                              after the gather; 0: the kernel runs on the handle's side
+                              stream, forked from and joined back into the call's stream */
 };
 
 /* Operation ids for ub_kernel_time. */
@@ -186,9 +193,10 @@ int ub_buffer(ub_handle_t h, void **dev_ptr, size_t *bytes);
  * three gathers (UB_OPT_GATHER_KERNEL): cudaMemcpyAsync calls on the handle's side
  * streams (the stand-in for copy-engine send/recv; on GB300 the driver runs a
  * same-device copy as a kernel on SMs, next to the GEMM, whose CTAs leave room for it),
- * each followed by a readiness-flag write; one gather kernel on the side stream
- * (default for the few-token kernel, and for the tile kernels at T <= 512 or when the
- * tiles fit one wave, so that the gather's CTAs run on the SMs no tile holds); or the
+ * each followed by a readiness-flag write; one gather kernel (default for the few-token
+ * kernel, and for the tile kernels at T <= 512 or when the tiles fit one wave, so that
+ * the gather's CTAs run on the SMs no tile holds), on `stream` with the GEMM launched as
+ * its programmatic dependent (UB_OPT_GATHER_CHAIN) or on the side stream; or the
  * GEMM kernel's own epilogue warps before their first tile (default for tile-kernel
  * calls of more than one wave). One persistent GEMM kernel on `stream` walks the chunks in
  * ring order starting at UB_OPT_SELF_RANK (whose chunk it reads in place, without

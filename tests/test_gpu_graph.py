@@ -80,9 +80,10 @@ def test_captured_step_replays_with_new_inputs(T, H, N, streamk):
 
 
 # T = 64: few-token kernel (SwiGLU and RS); T = 512: single-CTA SwiGLU epilogue with the
-# one-launch gather; T = 2048 with the gather inside the GEMM (UB_OPT_GATHER_KERNEL = 2).
-@pytest.mark.parametrize("T,gather", [(64, -1), (512, -1), (2048, 2)])
-def test_captured_mlp_forward_and_backward_replay(T, gather):
+# one-launch gather (chained on the call's stream, or on the side stream: chain 0);
+# T = 2048 with the gather inside the GEMM (UB_OPT_GATHER_KERNEL = 2).
+@pytest.mark.parametrize("T,gather,chain", [(64, -1, 1), (64, -1, 0), (512, -1, 1), (512, -1, 0), (2048, 2, 1)])
+def test_captured_mlp_forward_and_backward_replay(T, gather, chain):
     """fc1 AG + SwiGLU, the K x N input-gradient GEMM-RS and the weight gradient from the
     gathered buffer, captured once and replayed with new activations."""
     tp, H, F = 4, 512, 256
@@ -112,6 +113,7 @@ def test_captured_mlp_forward_and_backward_replay(T, gather):
     with ub.UserBuffer([T, H], tp) as buf:
         buf.set_active_shape([T, H])
         buf.set_option("gather_kernel", gather)
+        buf.set_option("gather_chain", chain)
         s = torch.cuda.Stream(d)
         refill()
         torch.cuda.synchronize()

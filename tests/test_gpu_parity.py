@@ -50,8 +50,18 @@ def test_tiny_workload_ag_and_rs():
 
 SWEEP_C = [1, 2, 127, 128, 129, 255, 300]
 
+# The gather forms (UB_OPT_GATHER_KERNEL, UB_OPT_GATHER_CHAIN): 0 driver copies, 1 the
+# gather kernel chained on the call's stream (the GEMM its programmatic dependent), 2
+# inside the GEMM, 3 the gather kernel on the handle's side stream.
+GATHER_FORMS = [0, 1, 2, 3]
 
-@pytest.mark.parametrize("gather", [0, 1, 2])
+
+def set_gather(buf, form):
+    buf.set_option("gather_kernel", 1 if form == 3 else form)
+    buf.set_option("gather_chain", 0 if form == 3 else 1)
+
+
+@pytest.mark.parametrize("gather", GATHER_FORMS)
 @pytest.mark.parametrize("pair", [1, 0])
 @pytest.mark.parametrize("tp", [1, 2, 4])
 def test_ag_active_T_sweep(tp, pair, gather):
@@ -61,7 +71,7 @@ def test_ag_active_T_sweep(tp, pair, gather):
     Wt = synth.normal_bf16((N, H), H ** -0.5, g)
     with ub.UserBuffer([cap, H], tp) as buf:
         buf.set_option("cta_pair", pair)
-        buf.set_option("gather_kernel", gather)
+        set_gather(buf, gather)
         for c in SWEEP_C + [cap // tp]:
             T = c * tp
             buf.buffer().view(torch.int16).fill_(-1)
@@ -236,7 +246,7 @@ def test_rejects_misaligned_and_wrong_shapes():
 
 # ------------------------------------------------------------------ bounded waits
 
-@pytest.mark.parametrize("gather", [0, 1, 2])
+@pytest.mark.parametrize("gather", GATHER_FORMS)
 @pytest.mark.parametrize("pair", [1, 0])
 def test_dropped_flag_times_out_and_the_handle_recovers(pair, gather):
     """Fault injected on the host: the readiness flag of chunk 1 is never written. The
@@ -248,7 +258,7 @@ def test_dropped_flag_times_out_and_the_handle_recovers(pair, gather):
     shards, Wt = synth.ag_inputs(T, H, N, tp, g)
     with ub.UserBuffer([T, H], tp) as buf:
         buf.set_option("cta_pair", pair)
-        buf.set_option("gather_kernel", gather)
+        set_gather(buf, gather)
         buf.set_option("timeout_ns", 20_000_000)
         buf.set_option("drop_flag", 1)
         run_ag(buf, shards, Wt)
@@ -262,7 +272,7 @@ def test_dropped_flag_times_out_and_the_handle_recovers(pair, gather):
     assert_close(Y, Yref, "AG after recovery")
 
 
-@pytest.mark.parametrize("gather", [0, 1, 2])
+@pytest.mark.parametrize("gather", GATHER_FORMS)
 @pytest.mark.parametrize("op", ["ag", "rs", "ag_swiglu"])
 def test_back_to_back_calls_at_full_hidden(op, gather):
     """Ten calls in a row on one handle at hidden 4096 without synchronising in
@@ -276,7 +286,7 @@ def test_back_to_back_calls_at_full_hidden(op, gather):
     c = T // tp
     shards = [X[r * c:(r + 1) * c] for r in range(tp)]
     with ub.UserBuffer([T, H], tp) as buf:
-        buf.set_option("gather_kernel", gather)
+        set_gather(buf, gather)
         outs = []
         for _ in range(10):
             if op == "ag":

@@ -28,19 +28,21 @@ def _make_buf(T, H, tp, skinny=1, extra=8):
 
 # (tp, c, H, N): chunks of 1..64 rows (token sub-tiles of 16..64 columns), one or many
 # weight tiles, N not a multiple of 128, K of 2..64 k-blocks (split into pieces or not).
-@pytest.mark.parametrize("gather", [-1, 2])
+@pytest.mark.parametrize("gather", [-1, 2, 3])
 @pytest.mark.parametrize("tp,c,H,N", [(4, 1, 256, 384), (4, 16, 256, 136), (4, 63, 512, 264),
                                       (2, 100, 256, 392), (1, 200, 320, 128), (8, 32, 1024, 1000),
                                       (4, 64, 4096, 3072), (1, 1, 72, 8)])
 def test_skinny_ag_matches_oracle(tp, c, H, N, gather):
-    """gather -1: the one-launch gather kernel; 2: the kernel's epilogue warps gather,
-    each chunk by its own group of CTAs (N tiles fewer than the chunks included)."""
+    """gather -1: the one-launch gather kernel, chained on the call's stream; 3: the same
+    kernel on the handle's side stream; 2: the kernel's epilogue warps gather, each chunk
+    by its own group of CTAs (N tiles fewer than the chunks included)."""
     T = c * tp
     g = synth.generator(seed=101)
     shards = [synth.normal_bf16((c, H), 1.0, g) for _ in range(tp)]
     Wt = synth.normal_bf16((N, H), 1.0 / math.sqrt(H), g)
     with _make_buf(T, H, tp) as buf:
-        buf.set_option("gather_kernel", gather)
+        buf.set_option("gather_kernel", -1 if gather == 3 else gather)
+        buf.set_option("gather_chain", 0 if gather == 3 else 1)
         Y = run_ag(buf, shards, Wt, y_rows=T + 5)
         assert buf.query_status() == ub.UB_OK
         G = buf.buffer()[:T].cpu()
