@@ -50,9 +50,9 @@ KERNEL_SRC = [os.path.join(ROOT, "gemm_overlap_gemms_gb300", "csrc", f) for f in
 # per active token of the captured launch, and the kernel source they were taken on.
 # Traffic is reported as null once the kernel source no longer matches.
 NCU_TRAFFIC = {
-    "rs": {"sha256_16": "3c6d7d174032b015", "bytes": 1154.37e6, "T": 8192,
+    "rs": {"sha256_16": "06f91ffb7fa6d3ab", "bytes": 1175.07e6, "T": 8192,
            "source": "profiles/ub_gemm_pair_kernel_rs_swiglu_fc2_T8192.md"},
-    "ag_swiglu": {"sha256_16": "3c6d7d174032b015", "bytes": 482.46e6, "T": 8192,
+    "ag_swiglu": {"sha256_16": "06f91ffb7fa6d3ab", "bytes": 484.33e6, "T": 8192,
                   "source": "profiles/ub_gemm_pair_kernel_ag_glu_swiglu_fc1_T8192.md"},
 }
 
