@@ -98,7 +98,11 @@ __device__ __forceinline__ void fence_proxy_async_shared()
 // both are no-ops. Every kernel here runs its prologue (barriers, TMEM, tensor-map
 // prefetch), waits, and only then triggers: a grid launched on the trigger finds every
 // earlier grid on the stream complete, which a bulk collective launched beside a GEMM
-// (ub_bulk.cu, no wait of its own at entry) relies on for its inputs.
+// (ub_bulk.cu, no wait of its own at entry) relies on for its inputs. Two kinds of
+// launch skip the entry wait and trigger at once, each waiting for the grid before it
+// at exit instead (so that it still completes after that grid): a bulk collective in
+// beside mode, and an AG-GEMM launched behind its own gather kernel (p.after_gather),
+// whose reads of the gathered buffer the chunk flags order.
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
