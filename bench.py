@@ -50,9 +50,9 @@ KERNEL_SRC = [os.path.join(ROOT, "gemm_overlap_gemms_gb300", "csrc", f) for f in
 # per active token of the captured launch, and the kernel source they were taken on.
 # Traffic is reported as null once the kernel source no longer matches.
 NCU_TRAFFIC = {
-    "rs": {"sha256_16": "06f91ffb7fa6d3ab", "bytes": 1175.07e6, "T": 8192,
+    "rs": {"sha256_16": "35740635591b15c9", "bytes": 1154.08e6, "T": 8192,
            "source": "profiles/ub_gemm_pair_kernel_rs_swiglu_fc2_T8192.md"},
-    "ag_swiglu": {"sha256_16": "06f91ffb7fa6d3ab", "bytes": 484.33e6, "T": 8192,
+    "ag_swiglu": {"sha256_16": "35740635591b15c9", "bytes": 484.22e6, "T": 8192,
                   "source": "profiles/ub_gemm_pair_kernel_ag_glu_swiglu_fc1_T8192.md"},
 }
 
@@ -713,7 +713,7 @@ def bulk_measure(wl, stream, T=4096, reps=20):
     GEMM's stream right after it, launched once the GEMM's CTAs hold their SMs);
     `two_streams_overlapped_ms`: the collective on a second stream, the GEMM issued
     first. Times are ms per pair of operations (20 back to back per timing), each the
-    median of three timings interleaved with the others'."""
+    median of five timings interleaved with the others'."""
     w = wl.w
     H, F, tp = w.hidden, w.rs_k[0], w.tp
     dev = wl.W1.device
@@ -759,10 +759,10 @@ def bulk_measure(wl, stream, T=4096, reps=20):
             buf.set_option("bulk_beside", 0)
 
     def medians(*fns):
-        # the timings interleaved, three rounds, the median of each: single timings of a
+        # the timings interleaved, five rounds, the median of each: single timings of a
         # pair of kernels vary by several us, and a GEMM's time drifts with the clocks
         # over a run, which would bias whichever timing came first
-        rounds = [[f() for f in fns] for _ in range(3)]
+        rounds = [[f() for f in fns] for _ in range(5)]
         return [float(np.median([r[i] for r in rounds])) for i in range(len(fns))]
 
     dgrad = lambda: buf.gemm_rs_kn(dZ, Wt, outs, stream=stream)
