@@ -704,6 +704,31 @@ def padded_measure(wl, steps, warmup, stream, world):
     return ms
 
 
+def interleaved_medians(fns, rounds=5):
+    """Each timing function called once per round, in turn, for `rounds` rounds; the
+    median of each one's results. Single timings of a pair of kernels vary by several us,
+    and a GEMM's time drifts with the clocks over a run, which would bias whichever
+    timing came first if each were repeated on its own."""
+    results = [[f() for f in fns] for _ in range(rounds)]
+    return [float(np.median([r[i] for r in results])) for i in range(len(fns))]
+
+
+def split_around(steps: int):
+    """The steps of the per-kernel event regions before and after the headline region:
+    half each (the extra one after)."""
+    return steps // 2, steps - steps // 2
+
+
+def median_region(times_ms, steps: int):
+    """The median of several timed regions of `steps` steps each, and a note listing them
+    per step (the end-to-end measurement: the host link and the issuing thread see other
+    work on the machine, so one region can be slow for reasons outside the step)."""
+    med = float(np.median(times_ms))
+    note = "median of %d regions of %d steps each: %s ms per step" % (
+        len(times_ms), steps, ", ".join("%.2f" % (t / steps) for t in times_ms))
+    return med, note
+
+
 def bulk_measure(wl, stream, T=4096, reps=20):
     """The "bulk" method at one microbatch of the workload: an independent collective
     beside an unrelated GEMM. fc1 backward: its input-gradient GEMM (gemm_rs_kn over
@@ -758,13 +783,6 @@ def bulk_measure(wl, stream, T=4096, reps=20):
         finally:
             buf.set_option("bulk_beside", 0)
 
-    def medians(*fns):
-        # the timings interleaved, five rounds, the median of each: single timings of a
-        # pair of kernels vary by several us, and a GEMM's time drifts with the clocks
-        # over a run, which would bias whichever timing came first
-        rounds = [[f() for f in fns] for _ in range(5)]
-        return [float(np.median([r[i] for r in rounds])) for i in range(len(fns))]
-
     dgrad = lambda: buf.gemm_rs_kn(dZ, Wt, outs, stream=stream)
     ag_side = lambda: buf.allgather(shards, stream=side)
     ag_alone = lambda: buf.allgather(shards, stream=stream)
@@ -775,9 +793,9 @@ def bulk_measure(wl, stream, T=4096, reps=20):
     for name, gemm, coll_side, coll_alone, coll_bytes in (
             ("allgather_beside_dgrad", dgrad, ag_side, ag_alone, 2 * T * H * 2),
             ("reduce_scatter_beside_wgrad", wgrad, rs_side, rs_alone, (tp + 1) * T * H * 2)):
-        t_g, t_c, t_b, t_2 = medians(lambda: timed(gemm), lambda: timed(coll_alone),
-                                     lambda: timed_beside(beside(gemm, coll_alone)),
-                                     lambda: timed(both(gemm, coll_side)))
+        t_g, t_c, t_b, t_2 = interleaved_medians([lambda: timed(gemm), lambda: timed(coll_alone),
+                                                  lambda: timed_beside(beside(gemm, coll_alone)),
+                                                  lambda: timed(both(gemm, coll_side))])
         hidden = lambda t: (t_g + t_c - t) / t_c if t_c > 0 else None
         res[name] = {"gemm_ms": t_g, "collective_ms": t_c, "sequential_ms": t_g + t_c,
                      "overlapped_ms": t_b, "hidden_fraction": hidden(t_b),
@@ -851,8 +869,7 @@ def run_ours(args):
     # so the events stay out of the headline region; they run in two halves, just before
     # and just after it, so that their kernels see the GPU's clocks and power state on
     # both sides of the headline (under the power cap, the clocks drift over a run).
-    k_before = args.steps // 2
-    k_after = args.steps - k_before
+    k_before, k_after = split_around(args.steps)
     ag_ms = rs_ms = ms_events = 0.0
     ag_n = rs_n = 0
     clocks.start()
@@ -907,12 +924,10 @@ def run_ours(args):
         e_steps = max(2, min(args.steps, 10))
         e_all, h2d, d2h = e2e_measure(wl, e_steps, max(3, args.warmup), stream, world)
         e_all = [max_over_ranks(t, world) for t in e_all]
-        e_ms = float(np.median(e_all))
+        e_ms, e_note = median_region(e_all, e_steps)
         e2e = {"value": flops * e_steps * world / (e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": e_ms / e_steps,
-               "timed_regions": "median of %d regions of %d steps each: %s ms per step" % (
-                   len(e_all), e_steps, ", ".join("%.2f" % (t / e_steps) for t in e_all))}
+               "ms_per_step": e_ms / e_steps, "timed_regions": e_note}
 
     padded = None
     if not args.no_padded:

@@ -106,3 +106,37 @@ def test_default_sweep_covers_the_metric_ladder():
         w = synth.WORKLOADS[dict((a, b) for a, b, _, _ in bench.DEFAULT_SWEEP)[n]]
         assert all(T % w.tp == 0 and w.tp <= T <= w.max_tokens for T in Ts), n
     assert min(names["fc2_rs"]) == 4 and max(names["large_rs_k3584"]) == 16384
+
+
+def test_interleaved_medians_take_turns_and_return_each_ones_median():
+    """The bulk-overlap timings: one call of each timing function per round, in turn,
+    so that a drift over the run (clocks under the power cap) reaches all of them alike;
+    the result is each function's own median, not a pooled one."""
+    calls = []
+
+    def fake(name, values):
+        it = iter(values)
+
+        def f():
+            calls.append(name)
+            return next(it)
+        return f
+
+    a = fake("a", [5.0, 1.0, 3.0, 9.0, 7.0])
+    b = fake("b", [10.0, 30.0, 20.0, 50.0, 40.0])
+    assert bench.interleaved_medians([a, b], rounds=5) == [5.0, 30.0]
+    assert calls == ["a", "b"] * 5
+
+
+def test_event_regions_split_around_the_headline():
+    assert bench.split_around(20) == (10, 10)
+    assert bench.split_around(5) == (2, 3)
+    assert bench.split_around(1) == (0, 1)
+
+
+def test_median_region_ignores_one_slow_region():
+    """The end-to-end figure: one region slowed by the host does not move the median,
+    and every region is listed per step."""
+    med, note = bench.median_region([114.6, 209.2, 114.7], 10)
+    assert med == 114.7
+    assert note == "median of 3 regions of 10 steps each: 11.46, 20.92, 11.47 ms per step"
