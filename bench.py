@@ -585,7 +585,7 @@ def default_sweep(stream):
             "seconds": time.perf_counter() - t_start}
 
 
-def e2e_measure(wl, steps, warmup, stream, world, reps=3):
+def e2e_measure(wl, steps, warmup, stream, world, reps=5):
     """Same step, with each microbatch's activations copied in from pinned host memory
     and its outputs copied back, inside the timed region. Copies run on their own
     streams so that microbatch i+1's inputs and microbatch i-1's outputs move while
@@ -595,8 +595,9 @@ def e2e_measure(wl, steps, warmup, stream, world, reps=3):
     loop's prefetch would; no copy of the timed steps starts before the timer's start
     event, and the timer stops after the last output has landed in host memory. The
     timed region runs `reps` times (ms of each returned): the host link and the host
-    thread that issues the copies see other work on the machine, so one region can be
-    slow for reasons outside the step."""
+    thread that issues the copies see other work on the machine, so a region can be
+    slow for reasons outside the step (on GB300 machines about one region in three took
+    ~1.8x the others, at any position in the run)."""
     fused = MLP == "fused"
     a0 = 1 if fused else 0      # fused: A[i][0] is produced on the device by fc1
     hX = [x.cpu().pin_memory() for x in wl.X]
