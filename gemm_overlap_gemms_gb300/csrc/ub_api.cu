@@ -914,6 +914,14 @@ int64_t ub_plan_ag_self_head(int64_t T, int tp, int self, int64_t n_tiles, int64
     return self_head_for(T, T / tp, self, n_tiles, pairs);
 }
 
+int ub_plan_ag_group_m(int64_t T, int tp, int self, int64_t n_tiles, int64_t pairs)
+{
+    if (tp < 1 || tp > UB_MAX_TP || T < tp || T % tp != 0 || self < 0 || self >= tp || n_tiles < 1 || pairs < 1)
+        return fail(UB_ERR_ARG, "ub_plan_ag_group_m: invalid shape");
+    const int64_t c = T / tp;
+    return ag_group_m(c, ceil_div(self_head_for(T, c, self, n_tiles, pairs), ubk::PAIR_BM) * n_tiles, pairs);
+}
+
 // AG-GEMM, optionally with the SwiGLU epilogue (glu_f > 0: Wt is [2 * glu_f, hidden],
 // gate rows first, and Y receives [T, glu_f]), or with the weight stored hidden x N
 // (b_kn: the tensor core reads it MN-major).

@@ -40,6 +40,7 @@ EXPORTS = [
     "ag_gemm_noalloc", "ag_gemm_swiglu", "ag_gemm_kn", "gemm_rs_kn", "ub_wgrad",
     "ub_allgather", "ub_reduce_scatter", "ub_plan_tail_split", "ub_plan_path",
     "ub_plan_ag_self_head", "ag_gemm_from_buffer", "ub_plan_gather_parts", "ub_stream_read",
+    "ub_plan_ag_group_m",
 ]
 NOALLOC_MAX_ELEMS = 16 * 1024 * 1024
 
@@ -108,6 +109,7 @@ def load():
         "ub_plan_tail_split": [I64, I64, I64, I, I],
         "ub_plan_path": [I64, I64, I64, I64, I64, I, I, I, ctypes.POINTER(I), ctypes.POINTER(I)],
         "ub_plan_ag_self_head": [I64, I, I, I64, I64],
+        "ub_plan_ag_group_m": [I64, I, I, I64, I64],
         "ub_plan_gather_parts": [I, I, I64, I64, ctypes.POINTER(I), ctypes.POINTER(I64), ctypes.POINTER(I64),
                                  ctypes.POINTER(I)],
     }
@@ -168,6 +170,11 @@ def plan_gather_parts(tp: int, self_rank: int, c: int, head: int) -> list:
 def plan_ag_self_head(T: int, tp: int, self_rank: int, n_tiles: int, pairs: int) -> int:
     """Rows of the self chunk the CTA-pair AG kernel reads in place."""
     return _plan_check(load().ub_plan_ag_self_head(T, tp, self_rank, n_tiles, pairs))
+
+
+def plan_ag_group_m(T: int, tp: int, self_rank: int, n_tiles: int, pairs: int) -> int:
+    """Tile rows per group of a CTA-pair AG call's tile order (0: N fastest)."""
+    return _plan_check(load().ub_plan_ag_group_m(T, tp, self_rank, n_tiles, pairs))
 
 
 def _check(rc: int):

@@ -468,11 +468,18 @@ int ag_gemm_noalloc(const void *const *shards, int tp, int64_t T, int64_t hidden
  * flag): all c = T / tp rows, or only its whole 256-row tiles where that saves a wave of
  * `pairs` pairs over `n_tiles` N tiles (self: the ring's start rank). Returns the row
  * count, or UB_ERR_ARG for an invalid shape.
+ *
+ * ub_plan_ag_group_m: the tile order of a CTA-pair AG call: tile rows walked in groups of
+ * the returned count, rows fastest inside a group (0: N fastest). Groups of 8 when the
+ * first wave of `pairs` pairs reads only the self chunk's in-place rows (n_tiles N tiles
+ * per tile row); else groups of one chunk's tile rows, 0 below two. Returns the count,
+ * or UB_ERR_ARG for an invalid shape.
  */
 int64_t ub_plan_tail_split(int64_t tiles, int64_t pairs, int64_t k_blocks, int widest, int gathered);
 int ub_plan_path(int64_t single_tiles, int64_t pair_tiles, int64_t k_blocks, int64_t slots, int64_t pairs,
                  int cta_pair, int streamk, int gathered, int *pair, int *split);
 int64_t ub_plan_ag_self_head(int64_t T, int tp, int self, int64_t n_tiles, int64_t pairs);
+int ub_plan_ag_group_m(int64_t T, int tp, int self, int64_t n_tiles, int64_t pairs);
 
 /*
  * ub_plan_gather_parts: the copies of an ag_gemm gather by driver copies, in issue

@@ -192,3 +192,24 @@ def test_gather_parts_follow_the_planned_self_head():
     # QKV at T = 1140: the self chunk stays in place and is copied last
     head = ub.plan_ag_self_head(1140, 4, 0, 12, PAIRS)
     assert ub.plan_gather_parts(4, 0, 285, head)[-1] == (0, 0, 285, True)
+
+
+def test_ag_tile_order_groups_follow_the_first_wave():
+    """The CTA-pair AG tile order (76 pairs, tp 4): groups of 8 tile rows when the first
+    wave reads only the self chunk's in-place rows, else groups of one chunk's tile rows
+    (none below two), so that no group starts tiles of chunks late in the ring."""
+    # fc1 (28 N tiles): the self chunk's rows fill the first wave from T = 2280 (3 tile rows)
+    assert ub.plan_ag_group_m(4640, 4, 0, 28, 76) == 8
+    assert ub.plan_ag_group_m(2280, 4, 0, 28, 76) == 8
+    # below that, a chunk's tile rows: T = 2048 has 2 per chunk, T = 1140 fewer than 2
+    assert ub.plan_ag_group_m(2048, 4, 0, 28, 76) == 2
+    assert ub.plan_ag_group_m(1140, 4, 0, 28, 76) == 0
+    # 14 N tiles: the self chunk's 5 tile rows are 70 tiles, less than a wave
+    assert ub.plan_ag_group_m(4640, 4, 0, 14, 76) == 4
+    # QKV (12 N tiles): 4 tile rows per chunk at T = 4096, a whole first wave at 8192
+    assert ub.plan_ag_group_m(4096, 4, 0, 12, 76) == 4
+    assert ub.plan_ag_group_m(8192, 4, 0, 12, 76) == 8
+    # fewer pairs (an SM margin): the same self chunk fills the first wave sooner
+    assert ub.plan_ag_group_m(2048, 4, 0, 28, 50) == 8
+    with pytest.raises(ub.UbError):
+        ub.plan_ag_group_m(1023, 4, 0, 28, 76)
