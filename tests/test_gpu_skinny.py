@@ -215,3 +215,31 @@ def test_skinny_covers_every_T_up_to_its_limit_on_one_buffer():
             _, Rref = oracle.gemm_rs([_u16(a) for a in A], [_u16(b) for b in Bt])
             for r in range(tp):
                 assert_close(Ys[r], Rref[r], "RS T=%d block %d" % (T, r))
+
+
+@pytest.mark.parametrize("T", [64, 512])
+def test_chained_gather_with_per_launch_events(T):
+    """UB_OPT_PROFILE records a CUDA event before and after each GEMM launch; with the
+    gather kernel chained on the call's stream (the default) an event then stands between
+    the gather and its GEMM, so the GEMM runs after the gather instead of beside it. The
+    results must still match the oracle, the status stay clean, and every launch be
+    timed."""
+    tp, H, N = 4, 1024, 384
+    c = T // tp
+    g = synth.generator(seed=111)
+    shards = [synth.normal_bf16((c, H), 1.0, g) for _ in range(tp)]
+    Wt = synth.normal_bf16((N, H), 1.0 / math.sqrt(H), g)
+    with _make_buf(T, H, tp) as buf:
+        assert buf.get_option("gather_chain") == 1
+        buf.set_option("profile", 1)
+        for _ in range(3):
+            Y = run_ag(buf, shards, Wt, y_rows=T + 2)
+        assert ub.GATHERS[buf.counters()["last_gather"]] == "gather_kernel"
+        ms, n = buf.kernel_time("ag")
+        assert n == 3 and ms > 0
+        assert buf.query_status() == ub.UB_OK
+        G = buf.buffer()[:T].cpu()
+    Gref, Yref = oracle_ag(shards, Wt)
+    np.testing.assert_array_equal(_u16(G), Gref)
+    assert_close(Y[:T], Yref, "chained gather with events T=%d" % T)
+    assert is_sentinel(Y[T:])
