@@ -326,6 +326,27 @@ __device__ bool wait_flags(const uint32_t *flags, uint32_t mask, const WaitCtx &
 // The same for one chunk's flag.
 __device__ __forceinline__ bool wait_flag(const uint32_t *flag, const WaitCtx &w) { return wait_flags(flag, 1u, w); }
 
+// One look, without waiting, at the readiness flags in `mask` (at most UB_MAX_TP): the
+// loads are relaxed and issued together, so they are in flight at once; only when every
+// flag holds `epoch` does an acquire fence (with the proxy fence for the TMA reads that
+// follow) make the chunks' contents visible, as wait_flags' acquire loads do.
+__device__ __forceinline__ bool try_flags(const uint32_t *flags, uint32_t mask, uint32_t epoch)
+{
+    uint32_t v[UB_MAX_TP];
+#pragma unroll
+    for (int r = 0; r < UB_MAX_TP; ++r)
+        if ((mask >> r) & 1u) asm volatile("ld.relaxed.sys.global.u32 %0, [%1];" : "=r"(v[r]) : "l"(flags + r) : "memory");
+    bool all = true;
+#pragma unroll
+    for (int r = 0; r < UB_MAX_TP; ++r)
+        if ((mask >> r) & 1u) all = all && v[r] == epoch;
+    if (all) {
+        asm volatile("fence.acq_rel.sys;" ::: "memory");
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
+    return all;
+}
+
 __device__ __forceinline__ void st_release_u32(uint32_t *ptr, uint32_t v)
 {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
