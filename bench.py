@@ -50,9 +50,9 @@ KERNEL_SRC = [os.path.join(ROOT, "gemm_overlap_gemms_gb300", "csrc", f) for f in
 # per active token of the captured launch, and the kernel source they were taken on.
 # Traffic is reported as null once the kernel source no longer matches.
 NCU_TRAFFIC = {
-    "rs": {"sha256_16": "35740635591b15c9", "bytes": 1154.08e6, "T": 8192,
+    "rs": {"sha256_16": "87b9fffd489eae7b", "bytes": 1248.18e6, "T": 8192,
            "source": "profiles/ub_gemm_pair_kernel_rs_swiglu_fc2_T8192.md"},
-    "ag_swiglu": {"sha256_16": "35740635591b15c9", "bytes": 484.22e6, "T": 8192,
+    "ag_swiglu": {"sha256_16": "87b9fffd489eae7b", "bytes": 484.98e6, "T": 8192,
                   "source": "profiles/ub_gemm_pair_kernel_ag_glu_swiglu_fc1_T8192.md"},
 }
 
