@@ -23,6 +23,7 @@ of a longer ladder.
 from __future__ import annotations
 
 import argparse
+import gc
 import json
 import math
 import os
@@ -358,6 +359,25 @@ class SwigluWorkload:
             self.buf.gemm_rs(self.A[i], self.B, self.out_shards(i), stream=stream)
 
 
+class no_gc:
+    """Python's cyclic garbage collector run before a timed region and kept off during it:
+    a collection pauses the thread that issues the step's launches and copies, and the
+    GPU then runs out of queued work. Measured on GB300: about one end-to-end region in
+    three took ~1.8x the others (19.7-20.9 against 11.5 ms per step) with the collector
+    on; with it off, 15 regions of three runs all took 11.48-11.56 ms."""
+
+    def __enter__(self):
+        self.was = gc.isenabled()
+        gc.collect()
+        gc.disable()
+        return self
+
+    def __exit__(self, *exc):
+        if self.was:
+            gc.enable()
+        return False
+
+
 def time_steps(fn, steps, warmup, stream, world):
     for _ in range(warmup):
         fn()
@@ -366,11 +386,12 @@ def time_steps(fn, steps, warmup, stream, world):
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        fn()
-    e1.record(stream)
-    torch.cuda.synchronize()
+    with no_gc():
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
     barrier(world)
     return e0.elapsed_time(e1)  # ms
 
@@ -594,10 +615,9 @@ def e2e_measure(wl, steps, warmup, stream, world, reps=5):
     host link streams without a break from one timed step to the next, as a training
     loop's prefetch would; no copy of the timed steps starts before the timer's start
     event, and the timer stops after the last output has landed in host memory. The
-    timed region runs `reps` times (ms of each returned): the host link and the host
-    thread that issues the copies see other work on the machine, so a region can be
-    slow for reasons outside the step (on GB300 machines about one region in three took
-    ~1.8x the others, at any position in the run)."""
+    timed region runs `reps` times (ms of each returned), each with the garbage
+    collector off (no_gc): the host link and the host thread that issues the copies can
+    still see other work on the machine, which the median leaves out."""
     fused = MLP == "fused"
     a0 = 1 if fused else 0      # fused: A[i][0] is produced on the device by fc1
     hX = [x.cpu().pin_memory() for x in wl.X]
@@ -657,13 +677,14 @@ def e2e_measure(wl, steps, warmup, stream, world, reps=5):
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        s_in.wait_event(e0)            # nothing of the timed steps starts before the timer
-        for _ in range(steps):
-            step()
-        stream.wait_stream(s_out)      # the last outputs are in host memory
-        e1.record(stream)
-        torch.cuda.synchronize()
+        with no_gc():
+            e0.record(stream)
+            s_in.wait_event(e0)            # nothing of the timed steps starts before the timer
+            for _ in range(steps):
+                step()
+            stream.wait_stream(s_out)      # the last outputs are in host memory
+            e1.record(stream)
+            torch.cuda.synchronize()
         barrier(world)
         times.append(e0.elapsed_time(e1))
     return times, h2d, d2h

@@ -140,3 +140,18 @@ def test_median_region_ignores_one_slow_region():
     med, note = bench.median_region([114.6, 209.2, 114.7], 10)
     assert med == 114.7
     assert note == "median of 3 regions of 10 steps each: 11.46, 20.92, 11.47 ms per step"
+
+
+def test_no_gc_keeps_the_collector_off_inside_and_restores_it():
+    import gc
+    assert gc.isenabled()
+    with bench.no_gc():
+        assert not gc.isenabled()
+    assert gc.isenabled()
+    gc.disable()
+    try:
+        with bench.no_gc():
+            assert not gc.isenabled()
+        assert not gc.isenabled()      # left as it was found
+    finally:
+        gc.enable()
