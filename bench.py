@@ -360,16 +360,19 @@ class SwigluWorkload:
 
 
 class no_gc:
-    """Python's cyclic garbage collector run before a timed region and kept off during it:
-    a collection pauses the thread that issues the step's launches and copies, and the
-    GPU then runs out of queued work. Measured on GB300: about one end-to-end region in
-    three took ~1.8x the others (19.7-20.9 against 11.5 ms per step) with the collector
-    on; with it off, 15 regions of three runs all took 11.48-11.56 ms."""
+    """Python's cyclic garbage collector kept off across warm-up and timed regions: a
+    collection pauses the thread that issues the step's launches and copies, and the GPU
+    then runs out of queued work. Measured on GB300: about one end-to-end region in three
+    took ~1.8x the others (19.7-20.9 against 11.5 ms per step) with the collector on; with
+    it off, 15 regions of three runs all took 11.48-11.56 ms. Entered with the collector
+    on, it collects once and disables it (use it before the warm-up steps, so that the GPU
+    is busy again when the timer starts); entered with it off, it does nothing."""
 
     def __enter__(self):
         self.was = gc.isenabled()
-        gc.collect()
-        gc.disable()
+        if self.was:
+            gc.collect()
+            gc.disable()
         return self
 
     def __exit__(self, *exc):
@@ -379,20 +382,20 @@ class no_gc:
 
 
 def time_steps(fn, steps, warmup, stream, world):
-    for _ in range(warmup):
-        fn()
-    torch.cuda.synchronize()
-    barrier(world)
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
     with no_gc():
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(steps):
             fn()
         e1.record(stream)
         torch.cuda.synchronize()
-    barrier(world)
+        barrier(world)
     return e0.elapsed_time(e1)  # ms
 
 
@@ -666,6 +669,8 @@ def e2e_measure(wl, steps, warmup, stream, world, reps=5):
                 hY2[i].copy_(Y2[b][:T], non_blocking=True)
                 drained[b].record(s_out)
 
+    off = no_gc()
+    off.__enter__()                    # before the warm-up: the GPU is busy when timing starts
     for _ in range(warmup):
         s_in.wait_stream(stream)
         step()
@@ -677,16 +682,16 @@ def e2e_measure(wl, steps, warmup, stream, world, reps=5):
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        with no_gc():
-            e0.record(stream)
-            s_in.wait_event(e0)            # nothing of the timed steps starts before the timer
-            for _ in range(steps):
-                step()
-            stream.wait_stream(s_out)      # the last outputs are in host memory
-            e1.record(stream)
-            torch.cuda.synchronize()
+        e0.record(stream)
+        s_in.wait_event(e0)            # nothing of the timed steps starts before the timer
+        for _ in range(steps):
+            step()
+        stream.wait_stream(s_out)      # the last outputs are in host memory
+        e1.record(stream)
+        torch.cuda.synchronize()
         barrier(world)
         times.append(e0.elapsed_time(e1))
+    off.__exit__(None, None, None)
     return times, h2d, d2h
 
 
@@ -880,6 +885,8 @@ def run_ours(args):
         wl.step(stream)
 
     ag_op = "ag_swiglu" if MLP == "fused" else "ag"
+    off = no_gc()
+    off.__enter__()                    # before the warm-up, kept off through every region
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -913,6 +920,7 @@ def run_ours(args):
     ms = time_steps(step, args.steps, 0, stream, world)
     events_region(k_after)
     clk = clocks.stop()
+    off.__exit__(None, None, None)
     assert wl.buf.query_status() == ub.UB_OK, "device status %d" % wl.buf.query_status()
     ms = max_over_ranks(ms, world)
     total_flops = flops * args.steps * world

@@ -150,7 +150,7 @@ def test_no_gc_keeps_the_collector_off_inside_and_restores_it():
     assert gc.isenabled()
     gc.disable()
     try:
-        with bench.no_gc():
+        with bench.no_gc():            # already off: nothing collected, nothing changed
             assert not gc.isenabled()
         assert not gc.isenabled()      # left as it was found
     finally:
