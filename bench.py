@@ -669,29 +669,27 @@ def e2e_measure(wl, steps, warmup, stream, world, reps=5):
                 hY2[i].copy_(Y2[b][:T], non_blocking=True)
                 drained[b].record(s_out)
 
-    off = no_gc()
-    off.__enter__()                    # before the warm-up: the GPU is busy when timing starts
-    for _ in range(warmup):
-        s_in.wait_stream(stream)
-        step()
-        stream.wait_stream(s_out)
-    times = []
-    for _ in range(reps):
-        torch.cuda.synchronize()
-        barrier(world)
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        s_in.wait_event(e0)            # nothing of the timed steps starts before the timer
-        for _ in range(steps):
+    with no_gc():  # before the warm-up: the GPU is busy when timing starts
+        for _ in range(warmup):
+            s_in.wait_stream(stream)
             step()
-        stream.wait_stream(s_out)      # the last outputs are in host memory
-        e1.record(stream)
-        torch.cuda.synchronize()
-        barrier(world)
-        times.append(e0.elapsed_time(e1))
-    off.__exit__(None, None, None)
+            stream.wait_stream(s_out)
+        times = []
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            barrier(world)
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            s_in.wait_event(e0)            # nothing of the timed steps starts before the timer
+            for _ in range(steps):
+                step()
+            stream.wait_stream(s_out)      # the last outputs are in host memory
+            e1.record(stream)
+            torch.cuda.synchronize()
+            barrier(world)
+            times.append(e0.elapsed_time(e1))
     return times, h2d, d2h
 
 
@@ -885,42 +883,40 @@ def run_ours(args):
         wl.step(stream)
 
     ag_op = "ag_swiglu" if MLP == "fused" else "ag"
-    off = no_gc()
-    off.__enter__()                    # before the warm-up, kept off through every region
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    # The headline: K steps with nothing on the stream but the step's own work. The
-    # per-kernel durations for the roofline come from K more steps with a CUDA event
-    # recorded on the stream before and after every GEMM launch (UB_OPT_PROFILE). An event
-    # between two kernels removes their programmatic launch (the second kernel's launch
-    # and prologue no longer overlap the end of the first; ~1.5 % of the step on GB300),
-    # so the events stay out of the headline region; they run in two halves, just before
-    # and just after it, so that their kernels see the GPU's clocks and power state on
-    # both sides of the headline (under the power cap, the clocks drift over a run).
-    k_before, k_after = split_around(args.steps)
-    ag_ms = rs_ms = ms_events = 0.0
-    ag_n = rs_n = 0
-    clocks.start()
+    with no_gc():  # before the warm-up, kept off through every region
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        # The headline: K steps with nothing on the stream but the step's own work. The
+        # per-kernel durations for the roofline come from K more steps with a CUDA event
+        # recorded on the stream before and after every GEMM launch (UB_OPT_PROFILE). An event
+        # between two kernels removes their programmatic launch (the second kernel's launch
+        # and prologue no longer overlap the end of the first; ~1.5 % of the step on GB300),
+        # so the events stay out of the headline region; they run in two halves, just before
+        # and just after it, so that their kernels see the GPU's clocks and power state on
+        # both sides of the headline (under the power cap, the clocks drift over a run).
+        k_before, k_after = split_around(args.steps)
+        ag_ms = rs_ms = ms_events = 0.0
+        ag_n = rs_n = 0
+        clocks.start()
 
-    def events_region(k):
-        nonlocal ag_ms, rs_ms, ms_events, ag_n, rs_n
-        if k == 0:
-            return
-        wl.buf.set_option("profile", 1)
-        wl.buf.kernel_time(ag_op)
-        wl.buf.kernel_time("rs")
-        ms_events += max_over_ranks(time_steps(step, k, 0, stream, world), world)
-        a, an = wl.buf.kernel_time(ag_op)
-        r, rn = wl.buf.kernel_time("rs")
-        ag_ms, ag_n, rs_ms, rs_n = ag_ms + a, ag_n + an, rs_ms + r, rs_n + rn
-        wl.buf.set_option("profile", 0)
+        def events_region(k):
+            nonlocal ag_ms, rs_ms, ms_events, ag_n, rs_n
+            if k == 0:
+                return
+            wl.buf.set_option("profile", 1)
+            wl.buf.kernel_time(ag_op)
+            wl.buf.kernel_time("rs")
+            ms_events += max_over_ranks(time_steps(step, k, 0, stream, world), world)
+            a, an = wl.buf.kernel_time(ag_op)
+            r, rn = wl.buf.kernel_time("rs")
+            ag_ms, ag_n, rs_ms, rs_n = ag_ms + a, ag_n + an, rs_ms + r, rs_n + rn
+            wl.buf.set_option("profile", 0)
 
-    events_region(k_before)
-    ms = time_steps(step, args.steps, 0, stream, world)
-    events_region(k_after)
-    clk = clocks.stop()
-    off.__exit__(None, None, None)
+        events_region(k_before)
+        ms = time_steps(step, args.steps, 0, stream, world)
+        events_region(k_after)
+        clk = clocks.stop()
     assert wl.buf.query_status() == ub.UB_OK, "device status %d" % wl.buf.query_status()
     ms = max_over_ranks(ms, world)
     total_flops = flops * args.steps * world
