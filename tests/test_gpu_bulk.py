@@ -316,3 +316,35 @@ def test_gather_ahead_pipeline_matches_the_oracle(beside):
         assert_close(Z[i][ridx], oracle.swiglu(oracle.gemm_rows(Xu, synth.to_u16(W1), rows)), "fc1 mb %d" % i)
         ref = sum(oracle.gemm_rows(synth.to_u16(A[i][j]), synth.to_u16(Bt[j]), rows) for j in range(tp))
         assert_close(R[i][ridx], ref, "fc2 mb %d" % i)
+
+
+def test_beside_reduce_scatter_after_a_chained_ag_gemm():
+    """A few-token AG-GEMM whose gather kernel runs chained on the stream (the GEMM its
+    programmatic dependent, letting the next grid launch at entry), then a reduce-scatter
+    in beside mode on the same stream: the collective starts while the AG call may still
+    be running. Its inputs were written before the AG call, so both results must match
+    the oracle, and a kernel after the pair must see both."""
+    tp, H, N, T = 4, 1024, 512, 64
+    c = T // tp
+    g = synth.generator(seed=98)
+    shards = [synth.normal_bf16((c, H), 1.0, g) for _ in range(tp)]
+    Wt = synth.normal_bf16((N, H), 1.0 / math.sqrt(H), g)
+    P = [synth.small_int_bf16((T, H), -20, 20, g).to(dev()) for _ in range(tp)]
+    st = torch.cuda.Stream()
+    with ub.UserBuffer([T, H], tp) as buf:
+        buf.set_active_shape([T, H])
+        torch.cuda.synchronize()
+        Y = buf.ag_gemm([s.to(dev()) for s in shards], Wt.to(dev()), stream=st)
+        assert ub.GATHERS[buf.counters()["last_gather"]] == "gather_kernel"
+        buf.set_option("bulk_beside", 1)
+        Ys = buf.reduce_scatter(P, stream=st)
+        with torch.cuda.stream(st):
+            Y_after = Y.clone()
+            Ys_after = [y.clone() for y in Ys]
+        torch.cuda.synchronize()
+        assert buf.query_status() == ub.UB_OK
+    Gref, Yref = oracle.ag_gemm([_u16(s) for s in shards], _u16(Wt))
+    assert_close(Y_after, Yref, "AG before the beside reduce-scatter")
+    Rref = oracle.reduce_scatter([_u16(x) for x in P])
+    for r in range(tp):
+        np.testing.assert_array_equal(Ys_after[r].float().cpu().numpy(), Rref[r])
