@@ -364,7 +364,9 @@ class no_gc:
     collection pauses the thread that issues the step's launches and copies, and the GPU
     then runs out of queued work. Measured on GB300: about one end-to-end region in three
     took ~1.8x the others (19.7-20.9 against 11.5 ms per step) with the collector on; with
-    it off, 15 regions of three runs all took 11.48-11.56 ms. Entered with the collector
+    it off, 15 regions of three runs all took 11.48-11.56 ms (slow regions still come now
+    and then -- another run: 13.9 and 17.6 among five -- from outside the process, which
+    the median leaves out). Entered with the collector
     on, it collects once and disables it (use it before the warm-up steps, so that the GPU
     is busy again when the timer starts); entered with it off, it does nothing."""
 
