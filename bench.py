@@ -611,7 +611,7 @@ def default_sweep(stream):
             "seconds": time.perf_counter() - t_start}
 
 
-def e2e_measure(wl, steps, warmup, stream, world, reps=5):
+def e2e_measure(wl, steps, warmup, stream, world, reps=7):
     """Same step, with each microbatch's activations copied in from pinned host memory
     and its outputs copied back, inside the timed region. Copies run on their own
     streams so that microbatch i+1's inputs and microbatch i-1's outputs move while
